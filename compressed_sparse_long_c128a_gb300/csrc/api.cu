@@ -1,0 +1,230 @@
+// C ABI of libcsa: argument validation and kernel dispatch.  Every hot-path
+// entry point validates on the host, enqueues its kernels on the caller's
+// stream and returns without synchronising or allocating.
+
+#include <cmath>
+#include <cstring>
+
+#include "csa_kernels.h"
+
+using namespace csa;
+
+namespace {
+
+constexpr int32_t kVersion = 100;  // 0.1.0
+
+bool dtype_ok(int32_t dt) { return dt >= CSA_F32 && dt <= CSA_E2M1; }
+
+int check_paged(const csa_paged* c, int32_t dim, int32_t rows_per_block, unsigned allowed_dtypes) {
+  if (!c || !c->data || c->num_blocks <= 0) return CSA_ERR_INVALID_ARG;
+  if (!dtype_ok(c->dtype)) return CSA_ERR_INVALID_ARG;
+  if (!(allowed_dtypes & (1u << c->dtype))) return CSA_ERR_UNSUPPORTED;
+  if (c->dim != dim || c->rows_per_block != rows_per_block) return CSA_ERR_INVALID_ARG;
+  if ((c->dtype == CSA_E4M3 || c->dtype == CSA_E2M1) && !c->scales) return CSA_ERR_INVALID_ARG;
+  if (c->dtype == CSA_E2M1 && dim % 16) return CSA_ERR_INVALID_ARG;
+  return CSA_OK;
+}
+
+int check_bt(const csa_block_table* bt) {
+  if (!bt || !bt->table || bt->num_seqs <= 0 || bt->stride <= 0) return CSA_ERR_INVALID_ARG;
+  return CSA_OK;
+}
+
+int check_layer(const csa_layer* L) {
+  if (!L) return CSA_ERR_INVALID_ARG;
+  if (L->ratio <= 0 || L->window <= 0 || L->window > 256 || 256 % L->ratio) return CSA_ERR_INVALID_ARG;
+  if (L->dim <= 0 || L->dim % 2 || L->rope_dim < 0 || L->rope_dim % 2 || L->rope_dim > L->dim ||
+      L->rope_dim > 2 * kMaxRopePairs)
+    return CSA_ERR_INVALID_ARG;
+  if (L->heads <= 0 || L->swa <= 0 || L->swa > 256) return CSA_ERR_INVALID_ARG;
+  if (!(L->rope_theta > 0.f) || !(L->rms_eps >= 0.f) || !(L->scale > 0.f)) return CSA_ERR_INVALID_ARG;
+  return CSA_OK;
+}
+
+RopeTab make_rope(int32_t rope_dim, float theta) {
+  RopeTab t;
+  std::memset(&t, 0, sizeof(t));
+  t.rope_dim = rope_dim;
+  for (int k = 0; k < rope_dim / 2; ++k) t.inv_freq[k] = std::pow((double)theta, -2.0 * k / rope_dim);
+  return t;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA; }
+
+constexpr unsigned kF32 = 1u << CSA_F32, kBF16 = 1u << CSA_BF16, kE4M3 = 1u << CSA_E4M3,
+                   kE2M1 = 1u << CSA_E2M1;
+
+size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
+
+int attn_common(const csa_layer* L, const void* q, int32_t q_dtype, int32_t n_rows, const int32_t* seq_id,
+                const int32_t* pos, const csa_paged* comp, const csa_block_table* comp_bt, const int32_t* topk,
+                int32_t k, int32_t max_n, const csa_paged* swa, const csa_block_table* swa_bt, void* out,
+                int32_t out_dtype, float* out_scales, void* ws, size_t ws_bytes, int32_t* err,
+                csa_stream_t stream) {
+  int st = check_layer(L);
+  if (st) return st;
+  if (n_rows < 0 || max_n < 0 || (topk && k <= 0)) return CSA_ERR_INVALID_ARG;
+  if (n_rows == 0) return CSA_OK;
+  if (!q || !seq_id || !pos || !out || !err) return CSA_ERR_INVALID_ARG;
+  if (q_dtype != CSA_F32 && q_dtype != CSA_BF16) return CSA_ERR_UNSUPPORTED;
+  if (out_dtype != CSA_F32 && out_dtype != CSA_BF16 && out_dtype != CSA_E4M3) return CSA_ERR_UNSUPPORTED;
+  if (out_dtype == CSA_E4M3 && !out_scales) return CSA_ERR_INVALID_ARG;
+  if ((st = check_paged(comp, L->dim, 256 / L->ratio, kF32 | kBF16 | kE4M3))) return st;
+  if ((st = check_paged(swa, L->dim, 256, kF32 | kBF16 | kE4M3))) return st;
+  if ((st = check_bt(comp_bt)) || (st = check_bt(swa_bt))) return st;
+  if (L->dim % 32 || L->dim > 512 || L->heads % 8) return CSA_ERR_UNSUPPORTED;
+  const int32_t keys = (topk ? k : max_n) + L->swa;
+  AttnArgs a;
+  a.q = q;
+  a.q_dtype = q_dtype;
+  a.seq_id = seq_id;
+  a.pos = pos;
+  a.comp = *comp;
+  a.comp_bt = *comp_bt;
+  a.topk = topk;
+  a.k = topk ? k : 0;
+  a.swa = *swa;
+  a.swa_bt = *swa_bt;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.out_scales = out_scales;
+  a.heads = L->heads;
+  a.dim = L->dim;
+  a.ratio = L->ratio;
+  a.window = L->window;
+  a.swa_len = L->swa;
+  a.scale = L->scale;
+  a.rope = make_rope(L->rope_dim, L->rope_theta);
+  a.n_splits = attn_splits(n_rows, L->heads, keys);
+  const size_t need = attn_workspace_bytes(n_rows, L->heads, L->dim, a.n_splits);
+  if (need && (!ws || ws_bytes < need)) return CSA_ERR_WORKSPACE;
+  a.part_o = reinterpret_cast<float*>(ws);
+  a.part_ml = need ? a.part_o + (size_t)n_rows * L->heads * a.n_splits * L->dim : nullptr;
+  a.err = err;
+  return cuda_status(launch_attn(a, n_rows, keys, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int csa_compress_insert(const csa_layer* L, const void* kv, const void* gate, int32_t in_dtype, int32_t n_tok,
+                        const int32_t* seq_id, const int32_t* pos, const float* bias, const float* gamma_c,
+                        const float* gamma_swa, const csa_paged* state, const csa_block_table* state_bt,
+                        const csa_paged* swa, const csa_block_table* swa_bt, const csa_paged* comp,
+                        const csa_block_table* comp_bt, int32_t* err, csa_stream_t stream) {
+  int st = check_layer(L);
+  if (st) return st;
+  if (n_tok < 0) return CSA_ERR_INVALID_ARG;
+  if (n_tok == 0) return CSA_OK;
+  if (!kv || !gate || !seq_id || !pos || !bias || !gamma_c || !gamma_swa || !err) return CSA_ERR_INVALID_ARG;
+  if (in_dtype != CSA_F32 && in_dtype != CSA_BF16) return CSA_ERR_UNSUPPORTED;
+  if (L->dim > 4096) return CSA_ERR_UNSUPPORTED;
+  if ((st = check_paged(state, 2 * L->dim, 256, 1u << in_dtype))) return st;
+  if ((st = check_paged(swa, L->dim, 256, kF32 | kBF16 | kE4M3))) return st;
+  if ((st = check_paged(comp, L->dim, 256 / L->ratio, kF32 | kBF16 | kE4M3))) return st;
+  if ((st = check_bt(state_bt)) || (st = check_bt(swa_bt)) || (st = check_bt(comp_bt))) return st;
+  const RopeTab rt = make_rope(L->rope_dim, L->rope_theta);
+  IngestArgs ia{kv, gate, in_dtype, seq_id, pos, gamma_swa, *state, *state_bt, *swa, *swa_bt, L->dim, L->rms_eps,
+                rt, err};
+  cudaError_t e = launch_ingest(ia, n_tok, stream);
+  if (e != cudaSuccess) return CSA_ERR_CUDA;
+  EmitArgs ea{seq_id, pos, bias, gamma_c, *state, *state_bt, *comp, *comp_bt, L->dim, L->ratio, L->window,
+              L->rms_eps, rt, err};
+  return cuda_status(launch_emit(ea, n_tok, stream));
+}
+
+int csa_cache_store(const float* rows, int32_t n, const int32_t* seq_id, const int32_t* row_idx,
+                    const csa_paged* cache, const csa_block_table* bt, int32_t* err, csa_stream_t stream) {
+  if (n < 0) return CSA_ERR_INVALID_ARG;
+  if (n == 0) return CSA_OK;
+  if (!rows || !seq_id || !row_idx || !err || !cache) return CSA_ERR_INVALID_ARG;
+  int st = check_paged(cache, cache->dim, cache->rows_per_block, kF32 | kBF16 | kE4M3 | kE2M1);
+  if (st) return st;
+  if (cache->dim <= 0 || cache->rows_per_block <= 0 || cache->dim % 2) return CSA_ERR_INVALID_ARG;
+  if ((st = check_bt(bt))) return st;
+  StoreArgs a{rows, seq_id, row_idx, *cache, *bt, err};
+  return cuda_status(launch_store(a, n, stream));
+}
+
+size_t csa_indexer_topk_workspace_size(int32_t n_rows, int32_t max_n) {
+  if (n_rows <= 0 || max_n <= 0) return 0;
+  return align_up(sizeof(float) * (size_t)n_rows * max_n);
+}
+
+int csa_indexer_topk(const void* q_idx, int32_t q_dtype, const float* w, int32_t n_rows, int32_t idx_heads,
+                     int32_t idx_dim, const int32_t* seq_id, const int32_t* pos, int32_t ratio, int32_t window,
+                     const csa_paged* idx_cache, const csa_block_table* bt, int32_t k, int32_t max_n,
+                     int32_t* out_idx, void* ws, size_t ws_bytes, int32_t* err, csa_stream_t stream) {
+  if (n_rows < 0 || k <= 0 || max_n < 0 || idx_heads <= 0 || idx_dim <= 0) return CSA_ERR_INVALID_ARG;
+  if (ratio <= 0 || window <= 0 || 256 % ratio) return CSA_ERR_INVALID_ARG;
+  if (n_rows == 0) return CSA_OK;
+  if (!q_idx || !w || !seq_id || !pos || !out_idx || !err) return CSA_ERR_INVALID_ARG;
+  if (q_dtype != CSA_F32 && q_dtype != CSA_BF16) return CSA_ERR_UNSUPPORTED;
+  int st = check_paged(idx_cache, idx_dim, 256 / ratio, kF32 | kBF16 | kE2M1);
+  if (st) return st;
+  if ((st = check_bt(bt))) return st;
+  if ((size_t)idx_heads * idx_dim > 32768 || idx_dim > 256) return CSA_ERR_UNSUPPORTED;
+  const size_t need = csa_indexer_topk_workspace_size(n_rows, max_n);
+  if (need && (!ws || ws_bytes < need)) return CSA_ERR_WORKSPACE;
+  float* scores = reinterpret_cast<float*>(ws);
+  IndexerArgs ia{q_idx, q_dtype, w, seq_id, pos, *idx_cache, *bt, idx_heads, idx_dim, ratio, window, max_n,
+                 scores, err};
+  cudaError_t e = launch_indexer_scores(ia, n_rows, stream);
+  if (e != cudaSuccess) return CSA_ERR_CUDA;
+  TopkArgs ta{scores, pos, ratio, window, max_n, k, out_idx, err};
+  return cuda_status(launch_topk(ta, n_rows, stream));
+}
+
+size_t csa_sparse_attn_workspace_size(const csa_layer* L, int32_t n_rows, int32_t k_or_max_n) {
+  if (!L || n_rows <= 0 || L->heads <= 0 || L->dim <= 0) return 0;
+  const int32_t keys = k_or_max_n + L->swa;
+  const int32_t s = attn_splits(n_rows, L->heads, keys);
+  return align_up(attn_workspace_bytes(n_rows, L->heads, L->dim, s));
+}
+
+int csa_sparse_attn_decode(const csa_layer* L, const void* q, int32_t q_dtype, int32_t n_rows,
+                           const int32_t* seq_id, const int32_t* pos, const csa_paged* comp,
+                           const csa_block_table* comp_bt, const int32_t* topk, int32_t k, int32_t max_n,
+                           const csa_paged* swa, const csa_block_table* swa_bt, void* out, int32_t out_dtype,
+                           float* out_scales, void* ws, size_t ws_bytes, int32_t* err, csa_stream_t stream) {
+  return attn_common(L, q, q_dtype, n_rows, seq_id, pos, comp, comp_bt, topk, k, max_n, swa, swa_bt, out,
+                     out_dtype, out_scales, ws, ws_bytes, err, stream);
+}
+
+int csa_sparse_attn_prefill(const csa_layer* L, const void* q, int32_t q_dtype, int32_t n_rows,
+                            const int32_t* seq_id, const int32_t* pos, const csa_paged* comp,
+                            const csa_block_table* comp_bt, const int32_t* topk, int32_t k, int32_t max_n,
+                            const csa_paged* swa, const csa_block_table* swa_bt, void* out, int32_t out_dtype,
+                            float* out_scales, void* ws, size_t ws_bytes, int32_t* err, csa_stream_t stream) {
+  return attn_common(L, q, q_dtype, n_rows, seq_id, pos, comp, comp_bt, topk, k, max_n, swa, swa_bt, out,
+                     out_dtype, out_scales, ws, ws_bytes, err, stream);
+}
+
+int csa_read_status(int32_t* err, int32_t reset, csa_stream_t stream) {
+  if (!err) return CSA_ERR_INVALID_ARG;
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, err, sizeof(v), cudaMemcpyDeviceToHost, stream) != cudaSuccess) return CSA_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return CSA_ERR_CUDA;
+  if (reset && v != 0) {
+    if (cudaMemsetAsync(err, 0, sizeof(int32_t), stream) != cudaSuccess) return CSA_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return CSA_ERR_CUDA;
+  }
+  return v;
+}
+
+const char* csa_status_string(int32_t s) {
+  switch (s) {
+    case CSA_OK: return "ok";
+    case CSA_ERR_INVALID_ARG: return "invalid argument";
+    case CSA_ERR_UNSUPPORTED: return "unsupported combination";
+    case CSA_ERR_CUDA: return "CUDA error";
+    case CSA_ERR_DEVICE_BOUNDS: return "device: unmapped or out-of-range block or index";
+    case CSA_ERR_WORKSPACE: return "workspace too small";
+    default: return "unknown status";
+  }
+}
+
+int32_t csa_version(void) { return kVersion; }
+
+}  // extern "C"

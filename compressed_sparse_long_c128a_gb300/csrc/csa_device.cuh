@@ -1,0 +1,175 @@
+// Device-side helpers shared by the kernels of libcsa: error word, paging,
+// RoPE angles and the storage codecs (bf16, e4m3, e2m1).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "csa.h"
+
+namespace csa {
+
+constexpr int kMaxRopePairs = 64;  // rope_dim <= 128
+
+// pos * theta^(-2k/r) for the rotary pairs, filled on the host in double.
+struct RopeTab {
+  double inv_freq[kMaxRopePairs];
+  int32_t rope_dim;
+};
+
+__device__ __forceinline__ void record_error(int32_t* err, int32_t code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+// Physical row of logical row `lrow` of sequence `seq`, or -1 (and the error
+// word set) when the table or the cache has no such row.
+__device__ __forceinline__ int64_t phys_row(const csa_block_table& bt, const csa_paged& c, int seq,
+                                            int64_t lrow, int32_t* err) {
+  if (seq < 0 || seq >= bt.num_seqs || lrow < 0) {
+    record_error(err, CSA_ERR_DEVICE_BOUNDS);
+    return -1;
+  }
+  int64_t lb = lrow / c.rows_per_block;
+  if (lb >= bt.stride) {
+    record_error(err, CSA_ERR_DEVICE_BOUNDS);
+    return -1;
+  }
+  int32_t pb = bt.table[(int64_t)seq * bt.stride + lb];
+  if (pb < 0 || pb >= c.num_blocks) {
+    record_error(err, CSA_ERR_DEVICE_BOUNDS);
+    return -1;
+  }
+  return (int64_t)pb * c.rows_per_block + (lrow - lb * c.rows_per_block);
+}
+
+// Number of compressed entries visible to a query at p: entries whose last raw
+// token ratio*i+window-1 lies before p.
+__host__ __device__ __forceinline__ int32_t n_visible(int32_t p, int32_t ratio, int32_t window) {
+  return p < window ? 0 : (p - window) / ratio + 1;
+}
+
+// cos / sin of pos * inv_freq[k]; the product and its reduction to [-pi, pi]
+// are done in double so that positions near 2^20 keep a sub-microradian angle.
+__device__ __forceinline__ void rope_cs(const RopeTab& t, int k, int64_t pos, float& c, float& s) {
+  double a = (double)pos * t.inv_freq[k];
+  a -= 6.283185307179586476925 * rint(a * 0.15915494309189533577);
+  sincosf((float)a, &s, &c);
+}
+
+// ---------------------------------------------------------------- codecs
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) {
+  return __uint_as_float(((uint32_t)b) << 16);
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16(float x) {
+  __nv_bfloat16 h = __float2bfloat16_rn(x);
+  return *reinterpret_cast<uint16_t*>(&h);
+}
+
+// e4m3 (fn): sign | 4 exponent bits (bias 7) | 3 mantissa bits; exponent 0 is
+// subnormal (m * 2^-9); 0x7f / 0xff are NaN.
+__device__ __forceinline__ float e4m3_to_f32(uint8_t v) {
+  uint32_t s = (uint32_t)(v & 0x80) << 24;
+  uint32_t e = (v >> 3) & 0xF;
+  uint32_t m = v & 0x7;
+  if (e == 0) {
+    float f = (float)m * 0.001953125f;  // 2^-9
+    return __uint_as_float(__float_as_uint(f) | s);
+  }
+  if (e == 0xF && m == 0x7) return __uint_as_float(0x7FC00000u | s);
+  return __uint_as_float(s | ((e + 120u) << 23) | (m << 20));
+}
+
+// Round-to-nearest-even to e4m3 with saturation to +-448 (hardware cvt).
+__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;  // lo in bits 0..7, hi in bits 8..15
+}
+
+__device__ __forceinline__ uint8_t f32_to_e4m3(float x) {
+  return (uint8_t)(f32x2_to_e4m3x2(x, 0.0f) & 0xFF);
+}
+
+// e2m1: sign | 2 exponent bits (bias 1) | 1 mantissa bit; magnitudes
+// 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+__device__ __forceinline__ float e2m1_to_f32(uint32_t c) {
+  const float mag[8] = {0.f, 0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f};
+  float v = mag[c & 7];
+  return (c & 8) ? -v : v;
+}
+
+// Nearest e2m1 code, ties to the even code, saturating at 6.  Decision points
+// are the midpoints between neighbours; a midpoint goes to the neighbour whose
+// mantissa bit is 0.
+__device__ __forceinline__ uint32_t f32_to_e2m1(float x) {
+  float a = fabsf(x);
+  uint32_t m;
+  if (a <= 0.25f) m = 0;
+  else if (a < 0.75f) m = 1;
+  else if (a <= 1.25f) m = 2;
+  else if (a < 1.75f) m = 3;
+  else if (a <= 2.5f) m = 4;
+  else if (a < 3.5f) m = 5;
+  else if (a <= 5.0f) m = 6;
+  else m = 7;
+  return m | (signbit(x) ? 8u : 0u);
+}
+
+// ---------------------------------------------------------------- reductions
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Block-wide sum / max; `red` is shared scratch of >= 32 floats.  All threads
+// of the block must call it; blockDim.x is a multiple of 32.
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = warp_sum(v);
+  __syncthreads();
+  if (lane == 0) red[wid] = v;
+  __syncthreads();
+  float t = lane < nw ? red[lane] : 0.f;
+  return warp_sum(t);
+}
+
+__device__ __forceinline__ float block_max(float v, float* red) {
+  int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = warp_max(v);
+  __syncthreads();
+  if (lane == 0) red[wid] = v;
+  __syncthreads();
+  float t = lane < nw ? red[lane] : 0.f;
+  return warp_max(t);
+}
+
+// ---------------------------------------------------------------- row access
+
+// Element e of a row of a F32 / BF16 cache, or of an input array.
+__device__ __forceinline__ float load_elem(const void* base, int32_t dtype, int64_t idx) {
+  if (dtype == CSA_F32) return reinterpret_cast<const float*>(base)[idx];
+  return bf16_to_f32(reinterpret_cast<const uint16_t*>(base)[idx]);
+}
+
+__device__ __forceinline__ int64_t row_bytes(const csa_paged& c) {
+  switch (c.dtype) {
+    case CSA_F32: return (int64_t)c.dim * 4;
+    case CSA_BF16: return (int64_t)c.dim * 2;
+    case CSA_E4M3: return (int64_t)c.dim;
+    default: return (int64_t)c.dim / 2;
+  }
+}
+
+}  // namespace csa

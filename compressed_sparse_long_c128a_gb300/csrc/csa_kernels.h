@@ -1,0 +1,109 @@
+// Internal launch interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "csa_device.cuh"
+
+namespace csa {
+
+// ---- compressor (k_compress.cu)
+struct IngestArgs {
+  const void* kv;
+  const void* gate;
+  int32_t in_dtype;
+  const int32_t* seq_id;
+  const int32_t* pos;
+  const float* gamma_swa;
+  csa_paged state;
+  csa_block_table state_bt;
+  csa_paged swa;
+  csa_block_table swa_bt;
+  int32_t dim;
+  float eps;
+  RopeTab rope;
+  int32_t* err;
+};
+
+struct EmitArgs {
+  const int32_t* seq_id;
+  const int32_t* pos;
+  const float* bias;
+  const float* gamma_c;
+  csa_paged state;
+  csa_block_table state_bt;
+  csa_paged comp;
+  csa_block_table comp_bt;
+  int32_t dim, ratio, window;
+  float eps;
+  RopeTab rope;
+  int32_t* err;
+};
+
+cudaError_t launch_ingest(const IngestArgs& a, int32_t n_tok, cudaStream_t s);
+cudaError_t launch_emit(const EmitArgs& a, int32_t n_tok, cudaStream_t s);
+
+// ---- cache store (k_store.cu)
+struct StoreArgs {
+  const float* rows;
+  const int32_t* seq_id;
+  const int32_t* row_idx;
+  csa_paged cache;
+  csa_block_table bt;
+  int32_t* err;
+};
+cudaError_t launch_store(const StoreArgs& a, int32_t n, cudaStream_t s);
+
+// ---- indexer scores + top-k (k_indexer.cu, k_topk.cu)
+struct IndexerArgs {
+  const void* q_idx;
+  int32_t q_dtype;
+  const float* w;
+  const int32_t* seq_id;
+  const int32_t* pos;
+  csa_paged cache;
+  csa_block_table bt;
+  int32_t heads, dim, ratio, window;
+  int32_t max_n;    // row stride of the score buffer
+  float* scores;    // [n_rows][max_n]
+  int32_t* err;
+};
+cudaError_t launch_indexer_scores(const IndexerArgs& a, int32_t n_rows, cudaStream_t s);
+
+struct TopkArgs {
+  const float* scores;  // [n_rows][max_n]
+  const int32_t* pos;
+  int32_t ratio, window, max_n, k;
+  int32_t* out;  // [n_rows][k]
+  int32_t* err;
+};
+cudaError_t launch_topk(const TopkArgs& a, int32_t n_rows, cudaStream_t s);
+
+// ---- attention (k_attn.cu)
+struct AttnArgs {
+  const void* q;
+  int32_t q_dtype;
+  const int32_t* seq_id;
+  const int32_t* pos;
+  csa_paged comp;
+  csa_block_table comp_bt;
+  const int32_t* topk;  // nullptr: dense
+  int32_t k;
+  csa_paged swa;
+  csa_block_table swa_bt;
+  void* out;
+  int32_t out_dtype;
+  float* out_scales;
+  int32_t heads, dim, ratio, window, swa_len;
+  float scale;
+  RopeTab rope;
+  int32_t n_splits;
+  float* part_o;  // [n_rows][heads][n_splits][dim]
+  float* part_ml; // [n_rows][heads][n_splits][2]
+  int32_t* err;
+};
+int32_t attn_splits(int32_t n_rows, int32_t heads, int32_t keys_per_row);
+size_t attn_workspace_bytes(int32_t n_rows, int32_t heads, int32_t dim, int32_t n_splits);
+cudaError_t launch_attn(const AttnArgs& a, int32_t n_rows, int32_t keys_per_row, cudaStream_t s);
+
+}  // namespace csa

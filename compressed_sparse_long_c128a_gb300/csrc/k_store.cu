@@ -1,0 +1,74 @@
+// Quantising row insert into a paged cache (indexer-key insert, loading held entries).
+//
+// Pages: "vLLM解密：DeepSeek-V4本地部署為何如此困難" §3.2 first fusion (the
+// indexer K cache has its own insert kernel); "vLLM DeepSeek V4 Support",
+// "DeepSeek V4 Attention Architecture" last paragraph (fp4 indexer cache, fp8
+// attention cache).
+//   E4M3: scale = amax/448 per row; code = e4m3_rn_satfinite(x * (448/amax)).
+//   E2M1: per 16 elements, scale = e4m3_rn(amax16/6); code = e2m1_rn(x / scale).
+
+#include "csa_kernels.h"
+
+namespace csa {
+namespace {
+
+constexpr int kThreads = 128;
+
+__global__ void __launch_bounds__(kThreads) store_kernel(const StoreArgs a) {
+  __shared__ float red[32];
+  const int j = blockIdx.x;
+  const csa_paged& c = a.cache;
+  const int D = c.dim;
+  const int64_t prow = phys_row(a.bt, c, a.seq_id[j], a.row_idx[j], a.err);
+  if (prow < 0) return;  // block-uniform
+  const float* x = a.rows + (int64_t)j * D;
+
+  if (c.dtype == CSA_F32) {
+    float* row = reinterpret_cast<float*>(c.data) + prow * D;
+    for (int d = threadIdx.x; d < D; d += blockDim.x) row[d] = x[d];
+  } else if (c.dtype == CSA_BF16) {
+    uint16_t* row = reinterpret_cast<uint16_t*>(c.data) + prow * D;
+    for (int d = threadIdx.x; d < D; d += blockDim.x) row[d] = f32_to_bf16(x[d]);
+  } else if (c.dtype == CSA_E4M3) {
+    float am = 0.f;
+    for (int d = threadIdx.x; d < D; d += blockDim.x) am = fmaxf(am, fabsf(x[d]));
+    am = block_max(am, red);
+    const float inv = am > 0.f ? 448.0f / am : 0.0f;
+    uint8_t* row = reinterpret_cast<uint8_t*>(c.data) + prow * D;
+    for (int pr = threadIdx.x; pr < D / 2; pr += blockDim.x)
+      *reinterpret_cast<uint16_t*>(row + 2 * pr) = f32x2_to_e4m3x2(x[2 * pr] * inv, x[2 * pr + 1] * inv);
+    if (threadIdx.x == 0) reinterpret_cast<float*>(c.scales)[prow] = am / 448.0f;
+  } else {  // E2M1, one thread per group of 16
+    uint8_t* row = reinterpret_cast<uint8_t*>(c.data) + prow * (D / 2);
+    uint8_t* srow = reinterpret_cast<uint8_t*>(c.scales) + prow * (D / 16);
+    for (int g = threadIdx.x; g < D / 16; g += blockDim.x) {
+      float v[16];
+      float am = 0.f;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        v[e] = x[g * 16 + e];
+        am = fmaxf(am, fabsf(v[e]));
+      }
+      const uint8_t sc = f32_to_e4m3(am / 6.0f);
+      const float s = e4m3_to_f32(sc);
+      uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const uint32_t code = s > 0.f ? f32_to_e2m1(v[e] / s) : 0u;
+        packed[e / 8] |= code << (4 * (e % 8));
+      }
+      *reinterpret_cast<uint2*>(row + g * 8) = make_uint2(packed[0], packed[1]);
+      srow[g] = sc;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_store(const StoreArgs& a, int32_t n, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  store_kernel<<<n, kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace csa

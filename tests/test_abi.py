@@ -1,0 +1,122 @@
+"""The C-ABI library builds, loads and exports every symbol its header declares;
+host-side validation answers without touching a GPU (CPU only)."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import compressed_sparse_long_c128a_gb300 as csa
+from compressed_sparse_long_c128a_gb300 import build as csa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "csa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    csa_build.build()
+    return csa.lib()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(csa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_hot_path():
+    names = _declared()
+    for n in ("csa_compress_insert", "csa_indexer_topk", "csa_sparse_attn_decode", "csa_sparse_attn_prefill",
+              "csa_cache_store", "csa_read_status"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", csa_build.LIB], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (csa_\w+)", out))
+    assert set(_declared()) == exported  # nothing undeclared leaks out either
+    assert set(csa.EXPORTED) == exported
+
+
+def test_version_and_status_strings(lib):
+    assert csa.version() == 100
+    assert csa.status_string(csa.OK) == "ok"
+    assert "workspace" in csa.status_string(csa.ERR_WORKSPACE)
+    assert csa.status_string(12345) == "unknown status"
+
+
+def test_library_refuses_to_load_when_missing(tmp_path, monkeypatch):
+    monkeypatch.setattr(csa, "LIB_PATH", str(tmp_path / "absent.so"))
+    monkeypatch.setattr(csa, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        csa.lib()
+
+
+def _paged(dtype=csa.BF16, rows=64, dim=512):
+    return csa.Paged(0x1000, 0x2000, dtype, 10, rows, dim)
+
+
+def _bt():
+    return csa.BlockTableC(0x3000, 2, 4)
+
+
+def test_host_validation_rejects_bad_arguments(lib):
+    L = csa.make_layer(4, 8, 512, 64, 64)
+    P, B = _paged(), _bt()
+    st, sw = _paged(csa.BF16, 256, 1024), _paged(csa.BF16, 256, 512)
+    # null kv
+    r = lib.csa_compress_insert(ctypes.byref(L), None, 0x10, csa.BF16, 4, 0x10, 0x10, 0x10, 0x10, 0x10,
+                                ctypes.byref(st), ctypes.byref(B), ctypes.byref(sw), ctypes.byref(B),
+                                ctypes.byref(P), ctypes.byref(B), 0x10, None)
+    assert r == csa.ERR_INVALID_ARG
+    # state dtype must equal the input dtype
+    st32 = _paged(csa.F32, 256, 1024)
+    r = lib.csa_compress_insert(ctypes.byref(L), 0x10, 0x10, csa.BF16, 4, 0x10, 0x10, 0x10, 0x10, 0x10,
+                                ctypes.byref(st32), ctypes.byref(B), ctypes.byref(sw), ctypes.byref(B),
+                                ctypes.byref(P), ctypes.byref(B), 0x10, None)
+    assert r == csa.ERR_UNSUPPORTED
+    # compressed cache must have 256/ratio rows per block
+    bad = _paged(csa.BF16, 32, 512)
+    r = lib.csa_compress_insert(ctypes.byref(L), 0x10, 0x10, csa.BF16, 4, 0x10, 0x10, 0x10, 0x10, 0x10,
+                                ctypes.byref(st), ctypes.byref(B), ctypes.byref(sw), ctypes.byref(B),
+                                ctypes.byref(bad), ctypes.byref(B), 0x10, None)
+    assert r == csa.ERR_INVALID_ARG
+    # zero tokens is a no-op
+    r = lib.csa_compress_insert(ctypes.byref(L), None, None, csa.BF16, 0, None, None, None, None, None,
+                                ctypes.byref(st), ctypes.byref(B), ctypes.byref(sw), ctypes.byref(B),
+                                ctypes.byref(P), ctypes.byref(B), None, None)
+    assert r == csa.OK
+    # bad layer: ratio that does not divide 256
+    L2 = csa.make_layer(3, 8, 512, 64, 64)
+    r = lib.csa_compress_insert(ctypes.byref(L2), 0x10, 0x10, csa.BF16, 4, 0x10, 0x10, 0x10, 0x10, 0x10,
+                                ctypes.byref(st), ctypes.byref(B), ctypes.byref(sw), ctypes.byref(B),
+                                ctypes.byref(P), ctypes.byref(B), 0x10, None)
+    assert r == csa.ERR_INVALID_ARG
+
+
+def test_workspace_checks(lib):
+    L = csa.make_layer(4, 8, 512, 64, 64)
+    need = csa.indexer_topk_workspace_size(4, 262143)
+    assert need >= 4 * 262143 * 4
+    idx = _paged(csa.E2M1, 64, 128)
+    r = lib.csa_indexer_topk(0x10, csa.BF16, 0x10, 4, 64, 128, 0x10, 0x10, 4, 8, ctypes.byref(idx),
+                             ctypes.byref(_bt()), 512, 262143, 0x10, 0x10, need - 1, 0x10, None)
+    assert r == csa.ERR_WORKSPACE
+    # attention with many splits needs a workspace; a small row count needs one
+    ws = csa.sparse_attn_workspace_size(L, 4, 512)
+    assert ws > 0
+    P, S = _paged(csa.E4M3, 64, 512), _paged(csa.E4M3, 256, 512)
+    r = lib.csa_sparse_attn_decode(ctypes.byref(L), 0x10, csa.BF16, 4, 0x10, 0x10, ctypes.byref(P),
+                                   ctypes.byref(_bt()), 0x10, 512, 262143, ctypes.byref(S), ctypes.byref(_bt()),
+                                   0x10, csa.E4M3, 0x10, None, 0, 0x10, None)
+    assert r == csa.ERR_WORKSPACE
+    # e4m3 output needs a scale buffer
+    r = lib.csa_sparse_attn_decode(ctypes.byref(L), 0x10, csa.BF16, 4, 0x10, 0x10, ctypes.byref(P),
+                                   ctypes.byref(_bt()), 0x10, 512, 262143, ctypes.byref(S), ctypes.byref(_bt()),
+                                   0x10, csa.E4M3, None, 0x10, ws, 0x10, None)
+    assert r == csa.ERR_INVALID_ARG
