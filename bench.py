@@ -58,6 +58,8 @@ def _args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--load-seconds", type=float, default=1.5,
+                    help="untimed graph replays before the timed steps, so the clock sampler sees load")
     return ap.parse_args()
 
 
@@ -75,6 +77,22 @@ def _peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def max_over_ranks(x: float, world: int, device="cuda") -> float:
+    """The largest value of x over all ranks (every rank gets it)."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_throughput(units_per_rank: int, steps: int, world: int, ms_max: float) -> float:
+    """Units all ranks processed per second, timed by the slowest rank."""
+    return units_per_rank * steps * world / (ms_max / 1e3)
 
 
 # ---------------------------------------------------------------- byte accounting
@@ -319,10 +337,10 @@ def run_csa(args):
 
     clocks = Clocks(local)
     clocks.start()
-    # keep the GPU loaded for ~1.5 s so the clock sampler sees it under load
+    # keep the GPU loaded for a while so the clock sampler sees it under load
     t_load = time.perf_counter()
     i = 0
-    while time.perf_counter() - t_load < 1.5:
+    while time.perf_counter() - t_load < args.load_seconds:
         graphs[i % replicas].replay()
         i += 1
         if i % 256 == 0:
@@ -343,13 +361,9 @@ def run_csa(args):
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
-    ms_total = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([ms_total], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(t_start.elapsed_time(t_end), world)
     rows_per_step = sum(ld.n_rows for ld in base)
-    value = rows_per_step * args.steps * world / (ms_total / 1e3)
+    value = weak_throughput(rows_per_step, args.steps, world, ms_total)
     wd.check("timed steps")
 
     # dominant kernel: sparse attention of the first layer, event-timed per launch
@@ -433,12 +447,8 @@ def _e2e(args, reps, graphs, stream, rows_per_step, world):
             stream.synchronize()  # the host reads the step's result
     t1.record(stream)
     torch.cuda.synchronize()
-    ms = t0.elapsed_time(t1)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    return {"value": rows_per_step * k_steps * world / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": bi,
+    ms = max_over_ranks(t0.elapsed_time(t1), world)
+    return {"value": weak_throughput(rows_per_step, k_steps, world, ms), "unit": UNIT, "h2d_bytes_per_step": bi,
             "d2h_bytes_per_step": bo, "steps": k_steps}
 
 

@@ -95,13 +95,14 @@ int attn_common(const csa_layer* L, const void* q, int32_t q_dtype, int32_t n_ro
   a.swa_len = L->swa;
   a.scale = L->scale;
   a.rope = make_rope(L->rope_dim, L->rope_theta);
-  a.n_splits = attn_splits(n_rows, L->heads, keys);
+  const bool tc = attn_tc_eligible(a);
+  a.n_splits = tc ? attn_tc_splits(n_rows, keys) : attn_splits(n_rows, L->heads, keys);
   const size_t need = attn_workspace_bytes(n_rows, L->heads, L->dim, a.n_splits);
   if (need && (!ws || ws_bytes < need)) return CSA_ERR_WORKSPACE;
   a.part_o = reinterpret_cast<float*>(ws);
   a.part_ml = need ? a.part_o + (size_t)n_rows * L->heads * a.n_splits * L->dim : nullptr;
   a.err = err;
-  return cuda_status(launch_attn(a, n_rows, keys, stream));
+  return cuda_status(tc ? launch_attn_tc(a, n_rows, stream) : launch_attn(a, n_rows, keys, stream));
 }
 
 }  // namespace
@@ -178,9 +179,13 @@ int csa_indexer_topk(const void* q_idx, int32_t q_dtype, const float* w, int32_t
 
 size_t csa_sparse_attn_workspace_size(const csa_layer* L, int32_t n_rows, int32_t k_or_max_n) {
   if (!L || n_rows <= 0 || L->heads <= 0 || L->dim <= 0) return 0;
+  // the cache dtype decides between the two kernels; size for the larger
   const int32_t keys = k_or_max_n + L->swa;
   const int32_t s = attn_splits(n_rows, L->heads, keys);
-  return align_up(attn_workspace_bytes(n_rows, L->heads, L->dim, s));
+  const int32_t s_tc = attn_tc_splits(n_rows, keys);
+  const size_t a = attn_workspace_bytes(n_rows, L->heads, L->dim, s);
+  const size_t b = attn_workspace_bytes(n_rows, L->heads, L->dim, s_tc);
+  return align_up(a > b ? a : b);
 }
 
 int csa_sparse_attn_decode(const csa_layer* L, const void* q, int32_t q_dtype, int32_t n_rows,
@@ -221,6 +226,7 @@ const char* csa_status_string(int32_t s) {
     case CSA_ERR_CUDA: return "CUDA error";
     case CSA_ERR_DEVICE_BOUNDS: return "device: unmapped or out-of-range block or index";
     case CSA_ERR_WORKSPACE: return "workspace too small";
+    case CSA_ERR_TIMEOUT: return "device: a bounded wait gave up";
     default: return "unknown status";
   }
 }

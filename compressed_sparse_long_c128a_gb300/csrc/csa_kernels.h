@@ -105,5 +105,11 @@ struct AttnArgs {
 int32_t attn_splits(int32_t n_rows, int32_t heads, int32_t keys_per_row);
 size_t attn_workspace_bytes(int32_t n_rows, int32_t heads, int32_t dim, int32_t n_splits);
 cudaError_t launch_attn(const AttnArgs& a, int32_t n_rows, int32_t keys_per_row, cudaStream_t s);
+cudaError_t launch_attn_merge(const AttnArgs& a, int32_t n_rows, cudaStream_t s);
+
+// ---- tensor-core attention, D = 512 and H = 64 (k_attn_tc.cu)
+bool attn_tc_eligible(const AttnArgs& a);
+int32_t attn_tc_splits(int32_t n_rows, int32_t keys_per_row);
+cudaError_t launch_attn_tc(const AttnArgs& a, int32_t n_rows, cudaStream_t s);
 
 }  // namespace csa

@@ -23,11 +23,6 @@ constexpr int kThreads = 32 * kHeadsPerCta;
 constexpr int kKeyTile = 32;
 constexpr int kMaxDim = 512;
 
-struct KeyRef {
-  const csa_paged* cache;
-  int64_t prow;  // -1: masked
-};
-
 // Dequantised element d of physical row prow of cache c.
 __device__ __forceinline__ float cache_elem(const csa_paged& c, int64_t prow, int d) {
   if (c.dtype == CSA_F32) return reinterpret_cast<const float*>(c.data)[prow * c.dim + d];
@@ -256,6 +251,10 @@ cudaError_t launch_attn(const AttnArgs& a, int32_t n_rows, int32_t keys_per_row,
   attn_kernel<<<dim3(n_rows, a.heads / kHeadsPerCta, a.n_splits), kThreads, smem, s>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess || a.n_splits == 1) return e;
+  return launch_attn_merge(a, n_rows, s);
+}
+
+cudaError_t launch_attn_merge(const AttnArgs& a, int32_t n_rows, cudaStream_t s) {
   merge_kernel<<<dim3(n_rows, a.heads), 32, 0, s>>>(a);
   return cudaGetLastError();
 }

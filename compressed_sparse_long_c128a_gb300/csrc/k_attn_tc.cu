@@ -1,0 +1,532 @@
+// Shared-K=V sparse attention on the sm_103a tensor cores (tcgen05 + TMEM).
+//
+// Pages: "vLLM DeepSeek V4 Support", "DeepSeek V4 Attention Architecture"
+// (one shared key/value vector per entry, inverse RoPE on the output, DSA
+// top-k plus a 128-token raw window under one softmax);
+// "vLLM解密：DeepSeek-V4本地部署為何如此困難" §3.2 second fusion (inverse
+// RoPE fused with the fp8 quantisation of the output).
+//
+// Shape: D = 512, H = 64 query heads sharing every key (MQA).  One CTA takes
+// one query row and a contiguous slice of its key list (selected entries, then
+// window rows), in tiles of 128 keys.  Keys are the M dimension of the MMAs,
+// so every accumulator has the plain 128-lane TMEM layout:
+//
+//   S^T [128 keys x 64 heads]  = K_tile [128 x 512] . Q^T [512 x 64]
+//   O^T [512 dims x 64 heads] += K_tile^T [512 x 128] . P^T [128 x 64]   (4 chunks of 128 dims)
+//
+// The key tile sits in shared memory once, 128B-swizzled with keys as rows:
+// read K-major it is the A operand of S^T; read MN-major it is the A operand of
+// O^T (values = keys).  Q^T (pre-rotated, pre-scaled by scale*log2 e) and P^T
+// are the B operands.  TMEM: S^T in columns 0..63, O^T chunk c in 64+64c.
+//
+// Warp roles: warps 0-3 own TMEM lanes (thread t <-> key t of the tile for the
+// softmax, dim t of a chunk in the epilogue); warps 4-6 gather the tile's rows
+// from the paged caches (cp.async for bf16, load + convert for e4m3, whose
+// per-row scale is folded into the logits and into P); warp 7 allocates TMEM
+// and one lane issues the MMAs.  Eight warps leave 255 registers per thread.  The running per-head max is only raised when
+// a logit exceeds it by more than 2^8; raising it rescales O^T in TMEM.
+//
+// With one split the epilogue normalises, rotates back and stores; with
+// several, each split stores (m, l, o) and the generic merge kernel finishes.
+
+#include "csa_kernels.h"
+#include "tc_ptx.cuh"
+
+namespace csa {
+namespace {
+
+using namespace tc;
+
+constexpr int kD = 512, kH = 64, kTile = 128, kChunks = 4;
+constexpr int kSoftmax = 128, kProducers = 96;
+constexpr int kThreads = kSoftmax + kProducers + 32;
+constexpr uint32_t kQBytes = kH * kD * 2;             // 64 KB
+constexpr uint32_t kChunkBytes = kTile * 128 * 2;     // 32 KB: 128 keys x 128 dims
+constexpr uint32_t kAtomBytes = kTile * 128;          // 16 KB: 128 keys x 64 dims
+constexpr uint32_t kPBytes = kTile * kH * 2;          // 16 KB
+constexpr uint32_t kOffQ = 0, kOffK = kQBytes, kOffP = kOffK + kChunks * kChunkBytes;
+constexpr uint32_t kOffMisc = kOffP + kPBytes;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0, kColO = 64;
+constexpr float kRescaleMargin = 8.0f;  // log2 units
+
+struct Misc {
+  uint64_t kfull[kChunks], kfree[kChunks], s_full, p_full, p_free;
+  uint32_t tmem_base;
+  int32_t abort;
+  float M[kH];          // running per-head max (log2 domain), shared by the softmax threads
+  float red[4][kH];     // per-warp reductions
+  float alpha[kH];      // rescale factor of the last max raise
+  float L[kH];          // softmax denominators of the slice
+  float kscale[2][kTile];
+  int8_t kvalid[2][kTile];
+  const uint8_t* rowptr[kTile];
+};
+constexpr uint32_t kSmemBytes = kOffMisc + sizeof(Misc) + 1024;
+
+struct Geo {
+  int seq;
+  int64_t p, w_lo;
+  int32_t n_vis, n_sel, j0, j1, n_tiles;
+};
+
+__device__ __forceinline__ Geo row_geometry(const AttnArgs& a, int r, int split, int S) {
+  Geo g;
+  g.seq = a.seq_id[r];
+  g.p = a.pos[r];
+  g.n_vis = n_visible((int32_t)g.p, a.ratio, a.window);
+  g.n_sel = a.topk ? a.k : g.n_vis;
+  g.w_lo = g.p - a.swa_len + 1 > 0 ? g.p - a.swa_len + 1 : 0;
+  const int32_t n_keys = g.n_sel + (int32_t)(g.p - g.w_lo + 1);
+  const int32_t per = (n_keys + S - 1) / S;
+  g.j0 = min(n_keys, split * per);
+  g.j1 = min(n_keys, g.j0 + per);
+  g.n_tiles = (g.j1 - g.j0 + kTile - 1) / kTile;
+  return g;
+}
+
+// Bounded wait; after the first timeout in the CTA every later wait returns at
+// once, so all roles run to the end and TMEM is released.
+__device__ __forceinline__ bool wait_or_abort(Misc& ms, uint64_t* bar, uint32_t parity, int32_t* err) {
+  if (*reinterpret_cast<volatile int32_t*>(&ms.abort)) return false;
+  if (mbar_wait(bar, parity)) return true;
+  *reinterpret_cast<volatile int32_t*>(&ms.abort) = 1;
+  record_error(err, CSA_ERR_TIMEOUT);
+  return false;
+}
+
+// ------------------------------------------------------------------ producers
+
+__device__ void producer_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Misc& ms, int pt) {
+  const bool fp8 = a.comp.dtype == CSA_E4M3;
+  const uint32_t kbase = smem_u32(smem + kOffK);
+  for (int t = 0; t < g.n_tiles; ++t) {
+    const int par = t & 1;
+    // key metadata of the tile's 128 slots
+    for (int slot = pt; slot < kTile; slot += kProducers) {
+      const int32_t j = g.j0 + t * kTile + slot;
+      const uint8_t* rp = nullptr;
+      float sc = 1.f;
+      if (j < g.j1) {
+        const csa_paged* c = nullptr;
+        int64_t prow = -1;
+        if (j < g.n_sel) {
+          const int32_t idx = a.topk ? a.topk[(int64_t)blockIdx.x * a.k + j] : j;
+          if (idx >= 0) {
+            if (idx >= g.n_vis) {
+              record_error(a.err, CSA_ERR_DEVICE_BOUNDS);
+            } else {
+              c = &a.comp;
+              prow = phys_row(a.comp_bt, a.comp, g.seq, idx, a.err);
+            }
+          }
+        } else {
+          c = &a.swa;
+          prow = phys_row(a.swa_bt, a.swa, g.seq, g.w_lo + (j - g.n_sel), a.err);
+        }
+        if (prow >= 0) {
+          rp = reinterpret_cast<const uint8_t*>(c->data) + prow * (int64_t)kD * (fp8 ? 1 : 2);
+          if (fp8) sc = reinterpret_cast<const float*>(c->scales)[prow];
+        }
+      }
+      ms.rowptr[slot] = rp;
+      ms.kvalid[par][slot] = rp != nullptr;
+      ms.kscale[par][slot] = sc;
+    }
+    named_bar(2, kProducers);
+    for (int c = 0; c < kChunks; ++c) {
+      if (t > 0) wait_or_abort(ms, &ms.kfree[c], (t - 1) & 1, a.err);
+      const uint32_t cbase = kbase + c * kChunkBytes;
+      if (!fp8) {
+        // 16 consecutive threads per key row: 256 contiguous bytes = dims [128c, 128c+128)
+        for (int x = pt; x < kTile * 16; x += kProducers) {
+          const uint32_t key = x >> 4, piece = x & 15;
+          const uint8_t* rp = ms.rowptr[key];
+          const uint32_t dst = cbase + (piece >> 3) * kAtomBytes + (key >> 3) * 1024 + (key & 7) * 128 +
+                               (((piece & 7) ^ (key & 7)) << 4);
+          cp_async16(dst, rp ? rp + c * 256 + piece * 16 : a.comp.data, rp ? 16u : 0u);
+        }
+        cp_async_commit();
+      } else {
+        // 8 consecutive threads per key row: 128 code bytes -> 128 bf16 (exact)
+        constexpr int kIters = (kTile * 8 + kProducers - 1) / kProducers;
+        uint4 raw[kIters];
+#pragma unroll
+        for (int it = 0; it < kIters; ++it) {
+          const int x = pt + it * kProducers;
+          raw[it] = make_uint4(0, 0, 0, 0);
+          if (x < kTile * 8) {
+            const uint8_t* rp = ms.rowptr[x >> 3];
+            if (rp) raw[it] = __ldg(reinterpret_cast<const uint4*>(rp + c * 128 + (x & 7) * 16));
+          }
+        }
+#pragma unroll
+        for (int it = 0; it < kIters; ++it) {
+          const int x = pt + it * kProducers;
+          if (x >= kTile * 8) break;
+          const uint32_t key = x >> 3, q8 = x & 7;
+          const uint32_t w[4] = {raw[it].x, raw[it].y, raw[it].z, raw[it].w};
+          uint32_t outw[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const uint32_t b0 = (w[e >> 1] >> ((e & 1) * 16)) & 0xFF, b1 = (w[e >> 1] >> ((e & 1) * 16 + 8)) & 0xFF;
+            outw[e] = (uint32_t)f32_to_bf16(e4m3_to_f32((uint8_t)b0)) |
+                      ((uint32_t)f32_to_bf16(e4m3_to_f32((uint8_t)b1)) << 16);
+          }
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const uint32_t piece = q8 * 2 + half;  // 16-byte piece of the 256-byte bf16 chunk
+            uint8_t* dst = smem + kOffK + c * kChunkBytes + (piece >> 3) * kAtomBytes + (key >> 3) * 1024 +
+                           (key & 7) * 128 + (((piece & 7) ^ (key & 7)) << 4);
+            *reinterpret_cast<uint4*>(dst) =
+                make_uint4(outw[half * 4], outw[half * 4 + 1], outw[half * 4 + 2], outw[half * 4 + 3]);
+          }
+        }
+      }
+    }
+    if (!fp8) {
+      cp_async_wait<3>();
+      fence_proxy_async();
+      mbar_arrive(&ms.kfull[0]);
+      cp_async_wait<2>();
+      fence_proxy_async();
+      mbar_arrive(&ms.kfull[1]);
+      cp_async_wait<1>();
+      fence_proxy_async();
+      mbar_arrive(&ms.kfull[2]);
+      cp_async_wait<0>();
+      fence_proxy_async();
+      mbar_arrive(&ms.kfull[3]);
+    } else {
+      fence_proxy_async();
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) mbar_arrive(&ms.kfull[c]);
+    }
+    named_bar(2, kProducers);  // rowptr is rewritten for the next tile
+  }
+  cp_async_wait<0>();
+}
+
+// ------------------------------------------------------------------ MMA issuer
+
+__device__ void mma_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Misc& ms, uint32_t tmem) {
+  constexpr uint32_t idesc_s = idesc_bf16(128, kH, 0, 0);
+  constexpr uint32_t idesc_o = idesc_bf16(128, kH, 1, 1);
+  const uint32_t kbase = smem_u32(smem + kOffK), qbase = smem_u32(smem + kOffQ), pbase = smem_u32(smem + kOffP);
+  for (int t = 0; t < g.n_tiles; ++t) {
+    const uint32_t par = t & 1;
+    for (int c = 0; c < kChunks; ++c) {
+      wait_or_abort(ms, &ms.kfull[c], par, a.err);
+      tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t k0 = c * 128 + ks * 16;  // first dim of this K step
+        const uint64_t ad = sdesc_sw128(kbase + c * kChunkBytes + (ks >> 2) * kAtomBytes + (ks & 3) * 32, 16, 1024);
+        const uint64_t bd = sdesc_sw128(qbase + (k0 >> 6) * (kH * 128) + (k0 & 63) * 2, 16, 1024);
+        mma_bf16(tmem + kColS, ad, bd, idesc_s, (c | ks) != 0);
+      }
+    }
+    mma_commit(&ms.s_full);
+    wait_or_abort(ms, &ms.p_full, par, a.err);
+    tc_fence_after();
+    for (int c = 0; c < kChunks; ++c) {
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {  // 16 keys per step: two 8-key groups of 1 KB
+        const uint64_t ad = sdesc_sw128(kbase + c * kChunkBytes + ks * 2048, kAtomBytes, 1024);
+        const uint64_t bd = sdesc_sw128(pbase + ks * 2048, kAtomBytes, 1024);
+        mma_bf16(tmem + kColO + 64 * c, ad, bd, idesc_o, (t > 0 || ks > 0) ? 1u : 0u);
+      }
+      mma_commit(&ms.kfree[c]);
+    }
+    mma_commit(&ms.p_free);
+  }
+}
+
+// ------------------------------------------------------------------ softmax + epilogue
+
+// Per-warp max (or sum) of v[h] over the warp's 32 keys, for all 64 heads,
+// into ms.red[warp][h]; the caller synchronises before reading ms.red.
+template <bool kMax>
+__device__ __forceinline__ void warp_reduce64(const float* v, Misc& ms, int st) {
+  const int lane = st & 31, w = st >> 5;
+#pragma unroll
+  for (int h = 0; h < kH; ++h) {
+    float x = v[h];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float y = __shfl_xor_sync(0xffffffffu, x, o);
+      x = kMax ? fmaxf(x, y) : x + y;
+    }
+    if (lane == 0) ms.red[w][h] = x;
+  }
+}
+
+__device__ void softmax_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Misc& ms, uint32_t tmem, int st) {
+  const int w = st >> 5;
+  const uint32_t lane_addr = tmem + ((uint32_t)(w * 32) << 16);
+  float lsum[kH];
+#pragma unroll
+  for (int h = 0; h < kH; ++h) lsum[h] = 0.f;
+  uint8_t* prow = smem + kOffP + (st >> 3) * 1024 + (st & 7) * 128;
+
+  for (int t = 0; t < g.n_tiles; ++t) {
+    const uint32_t par = t & 1;
+    wait_or_abort(ms, &ms.s_full, par, a.err);
+    tc_fence_after();
+    float x[kH];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) tmem_ld16(lane_addr + kColS + 16 * i, x + 16 * i);
+    tmem_wait_ld();
+    const bool valid = ms.kvalid[par][st] != 0;
+    const float ksc = ms.kscale[par][st];
+    bool need = false;
+#pragma unroll
+    for (int h = 0; h < kH; ++h) {
+      x[h] = valid ? x[h] * ksc : -INFINITY;
+      need |= x[h] > ms.M[h] + kRescaleMargin;
+    }
+    if (named_bar_or(1, kSoftmax, need)) {
+      // raise the running max: thread h < 64 owns head h
+      warp_reduce64<true>(x, ms, st);
+      named_bar(1, kSoftmax);
+      if (st < kH) {
+        const float mo = ms.M[st];
+        const float mn = fmaxf(fmaxf(mo, fmaxf(ms.red[0][st], ms.red[1][st])), fmaxf(ms.red[2][st], ms.red[3][st]));
+        ms.alpha[st] = mo == -INFINITY ? 0.f : exp2f(mo - mn);
+        ms.M[st] = mn;
+      }
+      named_bar(1, kSoftmax);
+      if (t > 0) {
+        // O^T of the previous tiles is complete (the S^T commit of this tile follows it)
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float o[16];
+            tmem_ld16(lane_addr + kColO + 64 * c + 16 * i, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) o[j] *= ms.alpha[16 * i + j];
+            tmem_st16(lane_addr + kColO + 64 * c + 16 * i, o);
+          }
+        }
+        tmem_wait_st();
+      }
+#pragma unroll
+      for (int h = 0; h < kH; ++h) lsum[h] *= ms.alpha[h];
+    }
+    // P buffer free: O^T of the previous tile has consumed it (already complete
+    // here, since the tensor pipe ran it before this tile's S^T)
+    if (t > 0) wait_or_abort(ms, &ms.p_free, (t - 1) & 1, a.err);
+    // probabilities of this key for every head, 8 heads per 16-byte piece of the
+    // key's 128-byte P^T row; P carries the key's dequant scale
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      uint32_t w4[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int h = 8 * c + 2 * e;
+        const float m0 = ms.M[h], m1 = ms.M[h + 1];
+        const float p0 = (x[h] == -INFINITY || m0 == -INFINITY) ? 0.f : exp2f(x[h] - m0);
+        const float p1 = (x[h + 1] == -INFINITY || m1 == -INFINITY) ? 0.f : exp2f(x[h + 1] - m1);
+        lsum[h] += p0;
+        lsum[h + 1] += p1;
+        w4[e] = (uint32_t)f32_to_bf16(p0 * ksc) | ((uint32_t)f32_to_bf16(p1 * ksc) << 16);
+      }
+      *reinterpret_cast<uint4*>(prow + ((c ^ (st & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    mbar_arrive(&ms.p_full);
+  }
+
+  // ---- epilogue
+  if (g.n_tiles > 0) wait_or_abort(ms, &ms.p_free, (g.n_tiles - 1) & 1, a.err);
+  tc_fence_after();
+  warp_reduce64<false>(lsum, ms, st);
+  named_bar(1, kSoftmax);
+  if (st < kH) ms.L[st] = (ms.red[0][st] + ms.red[1][st]) + (ms.red[2][st] + ms.red[3][st]);
+  named_bar(1, kSoftmax);  // ms.L[h] = sum over the slice's keys of 2^(x - M[h])
+  const int S = gridDim.y;
+  const int r = blockIdx.x;
+  if (S > 1) {
+    const int64_t hb = (int64_t)r * a.heads * S + blockIdx.y;
+    for (int c = 0; c < kChunks; ++c) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float o[16];
+        if (g.n_tiles > 0) {
+          tmem_ld16(lane_addr + kColO + 64 * c + 16 * i, o);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) o[j] = 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) a.part_o[(hb + (int64_t)(16 * i + j) * S) * kD + 128 * c + st] = o[j];
+      }
+    }
+    if (st < kH) {
+      const float m = ms.M[st];
+      a.part_ml[(hb + (int64_t)st * S) * 2] = m == -INFINITY ? -INFINITY : m * 0.69314718055994531f;
+      a.part_ml[(hb + (int64_t)st * S) * 2 + 1] = ms.L[st];
+    }
+    return;
+  }
+  // one split: normalise into a [64][512] fp32 staging area (the key tile buffer is idle now)
+  float* stage = reinterpret_cast<float*>(smem + kOffK);
+  for (int c = 0; c < kChunks; ++c) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float o[16];
+      tmem_ld16(lane_addr + kColO + 64 * c + 16 * i, o);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int h = 16 * i + j;
+        const float L = ms.L[h];
+        stage[h * kD + 128 * c + st] = L > 0.f ? o[j] / L : 0.f;
+      }
+    }
+  }
+  named_bar(1, kSoftmax);
+  // each warp finishes 16 heads; lane l holds dims [16l, 16l+16)
+  const int lane = st & 31;
+  const int R = a.rope.rope_dim;
+  for (int hh = 0; hh < 16; ++hh) {
+    const int h = w * 16 + hh;
+    float v[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) v[e] = stage[h * kD + 16 * lane + e];
+#pragma unroll
+    for (int e = 0; e < 16; e += 2) {
+      const int d = 16 * lane + e;
+      if (d >= kD - R) {
+        float cs, sn;
+        rope_cs(a.rope, (d - (kD - R)) / 2, g.p, cs, sn);
+        const float x0 = v[e], x1 = v[e + 1];
+        v[e] = x0 * cs + x1 * sn;
+        v[e + 1] = -x0 * sn + x1 * cs;
+      }
+    }
+    const int64_t ob = ((int64_t)r * a.heads + h) * kD + 16 * lane;
+    if (a.out_dtype == CSA_E4M3) {
+      float am = 0.f;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) am = fmaxf(am, fabsf(v[e]));
+      am = warp_max(am);
+      const float inv = am > 0.f ? 448.0f / am : 0.0f;
+      uint32_t wv[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        wv[q] = (uint32_t)f32x2_to_e4m3x2(v[4 * q] * inv, v[4 * q + 1] * inv) |
+                ((uint32_t)f32x2_to_e4m3x2(v[4 * q + 2] * inv, v[4 * q + 3] * inv) << 16);
+      *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(a.out) + ob) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+      if (lane == 0) a.out_scales[(int64_t)r * a.heads + h] = am / 448.0f;
+    } else if (a.out_dtype == CSA_BF16) {
+      uint32_t wv[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        wv[q] = (uint32_t)f32_to_bf16(v[2 * q]) | ((uint32_t)f32_to_bf16(v[2 * q + 1]) << 16);
+      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + ob);
+      dst[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+      dst[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+    } else {
+      float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + ob);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Misc& ms = *reinterpret_cast<Misc*>(smem + kOffMisc);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int r = blockIdx.x;
+  const Geo g = row_geometry(a, r, blockIdx.y, gridDim.y);
+
+  if (tid == 0) {
+    for (int c = 0; c < kChunks; ++c) {
+      mbar_init(&ms.kfull[c], kProducers);
+      mbar_init(&ms.kfree[c], 1);
+    }
+    mbar_init(&ms.s_full, 1);
+    mbar_init(&ms.p_full, kSoftmax);
+    mbar_init(&ms.p_free, 1);
+    mbar_init_fence();
+    ms.abort = 0;
+  }
+  if (tid < kH) ms.M[tid] = -INFINITY;
+  if (warp == 7) tmem_alloc(&ms.tmem_base, kTmemCols);
+  // Q^T: rotated, scaled by scale * log2(e), bf16, 128B-swizzled K-major (rows = heads)
+  if (tid < kSoftmax + kProducers) {
+    const float qs = a.scale * 1.4426950408889634f;
+    const int R = a.rope.rope_dim;
+    for (int x = tid; x < kH * kD / 2; x += kSoftmax + kProducers) {
+      const int h = x / (kD / 2), d = 2 * (x % (kD / 2));
+      const int64_t qb = ((int64_t)r * a.heads + h) * kD + d;
+      float q0 = load_elem(a.q, a.q_dtype, qb), q1 = load_elem(a.q, a.q_dtype, qb + 1);
+      if (d >= kD - R) {
+        float cs, sn;
+        rope_cs(a.rope, (d - (kD - R)) / 2, g.p, cs, sn);
+        const float t0 = q0 * cs - q1 * sn;
+        q1 = q0 * sn + q1 * cs;
+        q0 = t0;
+      }
+      const uint32_t v = (uint32_t)f32_to_bf16(q0 * qs) | ((uint32_t)f32_to_bf16(q1 * qs) << 16);
+      *reinterpret_cast<uint32_t*>(smem + kOffQ + sw128_offset(h, d, kH)) = v;
+    }
+    fence_proxy_async();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ms.tmem_base;
+
+  if (warp < 4) {
+    softmax_role(a, g, smem, ms, tmem, tid);
+  } else if (warp < 7) {
+    producer_role(a, g, smem, ms, tid - kSoftmax);
+  } else if ((tid & 31) == 0) {
+    mma_role(a, g, smem, ms, tmem);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 7) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+bool attn_tc_eligible(const AttnArgs& a) {
+  return a.dim == kD && a.heads == kH && a.comp.dtype == a.swa.dtype &&
+         (a.comp.dtype == CSA_BF16 || a.comp.dtype == CSA_E4M3) && a.rope.rope_dim <= 128;
+}
+
+int32_t attn_tc_splits(int32_t n_rows, int32_t keys_per_row) {
+  int32_t s = n_rows > 0 ? 148 / n_rows : 1;
+  const int32_t tiles = (keys_per_row + kTile - 1) / kTile;
+  if (s > tiles) s = tiles;
+  if (s > 8) s = 8;
+  if (s < 1) s = 1;
+  return s;
+}
+
+cudaError_t launch_attn_tc(const AttnArgs& a, int32_t n_rows, cudaStream_t s) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  attn_tc_kernel<<<dim3(n_rows, a.n_splits), kThreads, kSmemBytes, s>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || a.n_splits == 1) return e;
+  return launch_attn_merge(a, n_rows, s);
+}
+
+}  // namespace csa

@@ -55,7 +55,8 @@ typedef enum {
   CSA_ERR_UNSUPPORTED = -2,   /* a valid combination this build has no kernel for */
   CSA_ERR_CUDA = -3,          /* a CUDA runtime call or launch failed */
   CSA_ERR_DEVICE_BOUNDS = -4, /* device: unmapped / out-of-range block or index */
-  CSA_ERR_WORKSPACE = -5      /* workspace smaller than the matching *_workspace_size */
+  CSA_ERR_WORKSPACE = -5,     /* workspace smaller than the matching *_workspace_size */
+  CSA_ERR_TIMEOUT = -6        /* device: a bounded wait inside a kernel gave up */
 } csa_status;
 
 typedef enum {
