@@ -56,7 +56,7 @@ _SIGS = {
     "csa_cache_store": (_I32, [_VP, _I32, _VP, _VP, _PP, _PB, _VP, _VP]),
     "csa_indexer_topk": (_I32, [_VP, _I32, _VP, _I32, _I32, _I32, _VP, _VP, _I32, _I32, _PP, _PB, _I32, _I32, _VP,
                                 _VP, _SZ, _VP, _VP]),
-    "csa_indexer_topk_workspace_size": (_SZ, [_I32, _I32]),
+    "csa_indexer_topk_workspace_size": (_SZ, [_I32, _I32, _I32]),
     "csa_sparse_attn_decode": (_I32, [_PL, _VP, _I32, _I32, _VP, _VP, _PP, _PB, _VP, _I32, _I32, _PP, _PB, _VP, _I32,
                                       _VP, _VP, _SZ, _VP, _VP]),
     "csa_sparse_attn_prefill": (_I32, [_PL, _VP, _I32, _I32, _VP, _VP, _PP, _PB, _VP, _I32, _I32, _PP, _PB, _VP,
@@ -194,8 +194,8 @@ def cache_store(rows, seq_id, row_idx, cache: PagedCache, bt, err, stream=None):
     _check(st, "csa_cache_store")
 
 
-def indexer_topk_workspace_size(n_rows: int, max_n: int) -> int:
-    return int(lib().csa_indexer_topk_workspace_size(n_rows, max_n))
+def indexer_topk_workspace_size(n_rows: int, max_n: int, k: int) -> int:
+    return int(lib().csa_indexer_topk_workspace_size(n_rows, max_n, k))
 
 
 def indexer_topk(q_idx, w, seq_id, pos, ratio: int, window: int, idx_cache: PagedCache, bt, k: int, max_n: int,

@@ -148,9 +148,9 @@ int csa_cache_store(const float* rows, int32_t n, const int32_t* seq_id, const i
   return cuda_status(launch_store(a, n, stream));
 }
 
-size_t csa_indexer_topk_workspace_size(int32_t n_rows, int32_t max_n) {
-  if (n_rows <= 0 || max_n <= 0) return 0;
-  return align_up(sizeof(float) * (size_t)n_rows * max_n);
+size_t csa_indexer_topk_workspace_size(int32_t n_rows, int32_t max_n, int32_t k) {
+  if (n_rows <= 0 || max_n <= 0 || k <= 0) return 0;
+  return align_up(sizeof(float) * (size_t)n_rows * max_n) + align_up(topk_candidate_bytes(n_rows, max_n, k));
 }
 
 int csa_indexer_topk(const void* q_idx, int32_t q_dtype, const float* w, int32_t n_rows, int32_t idx_heads,
@@ -166,15 +166,19 @@ int csa_indexer_topk(const void* q_idx, int32_t q_dtype, const float* w, int32_t
   if (st) return st;
   if ((st = check_bt(bt))) return st;
   if ((size_t)idx_heads * idx_dim > 32768 || idx_dim > 256) return CSA_ERR_UNSUPPORTED;
-  const size_t need = csa_indexer_topk_workspace_size(n_rows, max_n);
+  const size_t need = csa_indexer_topk_workspace_size(n_rows, max_n, k);
   if (need && (!ws || ws_bytes < need)) return CSA_ERR_WORKSPACE;
   float* scores = reinterpret_cast<float*>(ws);
+  void* cand = topk_candidate_bytes(n_rows, max_n, k)
+                   ? reinterpret_cast<uint8_t*>(ws) + align_up(sizeof(float) * (size_t)n_rows * max_n)
+                   : nullptr;
   IndexerArgs ia{q_idx, q_dtype, w, seq_id, pos, *idx_cache, *bt, idx_heads, idx_dim, ratio, window, max_n,
                  scores, err};
-  cudaError_t e = launch_indexer_scores(ia, n_rows, stream);
+  cudaError_t e = indexer_tc_eligible(ia) ? launch_indexer_tc(ia, n_rows, stream)
+                                           : launch_indexer_scores(ia, n_rows, stream);
   if (e != cudaSuccess) return CSA_ERR_CUDA;
   TopkArgs ta{scores, pos, ratio, window, max_n, k, out_idx, err};
-  return cuda_status(launch_topk(ta, n_rows, stream));
+  return cuda_status(launch_topk(ta, n_rows, cand, stream));
 }
 
 size_t csa_sparse_attn_workspace_size(const csa_layer* L, int32_t n_rows, int32_t k_or_max_n) {

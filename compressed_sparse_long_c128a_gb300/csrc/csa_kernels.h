@@ -69,6 +69,9 @@ struct IndexerArgs {
   int32_t* err;
 };
 cudaError_t launch_indexer_scores(const IndexerArgs& a, int32_t n_rows, cudaStream_t s);
+// tensor-core scores, 64 heads x 128 dims, bf16 or e2m1 keys (k_indexer_tc.cu)
+bool indexer_tc_eligible(const IndexerArgs& a);
+cudaError_t launch_indexer_tc(const IndexerArgs& a, int32_t n_rows, cudaStream_t s);
 
 struct TopkArgs {
   const float* scores;  // [n_rows][max_n]
@@ -77,7 +80,9 @@ struct TopkArgs {
   int32_t* out;  // [n_rows][k]
   int32_t* err;
 };
-cudaError_t launch_topk(const TopkArgs& a, int32_t n_rows, cudaStream_t s);
+// `cand`: topk_candidate_bytes() of scratch for the two-stage path (nullptr: one CTA per row)
+size_t topk_candidate_bytes(int32_t n_rows, int32_t max_n, int32_t k);
+cudaError_t launch_topk(const TopkArgs& a, int32_t n_rows, void* cand, cudaStream_t s);
 
 // ---- attention (k_attn.cu)
 struct AttnArgs {

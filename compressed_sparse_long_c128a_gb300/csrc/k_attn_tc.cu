@@ -26,8 +26,12 @@
 // and one lane issues the MMAs.  Eight warps leave 255 registers per thread.  The running per-head max is only raised when
 // a logit exceeds it by more than 2^8; raising it rescales O^T in TMEM.
 //
-// With one split the epilogue normalises, rotates back and stores; with
-// several, each split stores (m, l, o) and the generic merge kernel finishes.
+// A row's key list may be split over S = 1, 2, 4 or 8 CTAs launched as one
+// cluster.  Each CTA stages its unnormalised O (fp32, [64 heads][512]) with its
+// per-head max and denominator in its own shared memory; after a cluster
+// barrier CTA r merges heads [r*64/S, (r+1)*64/S) by reading the others'
+// staging through distributed shared memory, normalises, rotates back and
+// stores.  No partial result goes through global memory.
 
 #include "csa_kernels.h"
 #include "tc_ptx.cuh"
@@ -347,95 +351,102 @@ __device__ void softmax_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mis
   named_bar(1, kSoftmax);
   if (st < kH) ms.L[st] = (ms.red[0][st] + ms.red[1][st]) + (ms.red[2][st] + ms.red[3][st]);
   named_bar(1, kSoftmax);  // ms.L[h] = sum over the slice's keys of 2^(x - M[h])
-  const int S = gridDim.y;
-  const int r = blockIdx.x;
-  if (S > 1) {
-    const int64_t hb = (int64_t)r * a.heads * S + blockIdx.y;
-    for (int c = 0; c < kChunks; ++c) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float o[16];
-        if (g.n_tiles > 0) {
-          tmem_ld16(lane_addr + kColO + 64 * c + 16 * i, o);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) o[j] = 0.f;
-        }
-#pragma unroll
-        for (int j = 0; j < 16; ++j) a.part_o[(hb + (int64_t)(16 * i + j) * S) * kD + 128 * c + st] = o[j];
-      }
-    }
-    if (st < kH) {
-      const float m = ms.M[st];
-      a.part_ml[(hb + (int64_t)st * S) * 2] = m == -INFINITY ? -INFINITY : m * 0.69314718055994531f;
-      a.part_ml[(hb + (int64_t)st * S) * 2 + 1] = ms.L[st];
-    }
-    return;
-  }
-  // one split: normalise into a [64][512] fp32 staging area (the key tile buffer is idle now)
+  // stage the slice's unnormalised O^T as [64 heads][512 dims] fp32 in the idle key buffer
   float* stage = reinterpret_cast<float*>(smem + kOffK);
   for (int c = 0; c < kChunks; ++c) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       float o[16];
-      tmem_ld16(lane_addr + kColO + 64 * c + 16 * i, o);
-      tmem_wait_ld();
+      if (g.n_tiles > 0) {
+        tmem_ld16(lane_addr + kColO + 64 * c + 16 * i, o);
+        tmem_wait_ld();
+      } else {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int h = 16 * i + j;
-        const float L = ms.L[h];
-        stage[h * kD + 128 * c + st] = L > 0.f ? o[j] / L : 0.f;
+        for (int j = 0; j < 16; ++j) o[j] = 0.f;
       }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) stage[(16 * i + j) * kD + 128 * c + st] = o[j];
     }
   }
-  named_bar(1, kSoftmax);
-  // each warp finishes 16 heads; lane l holds dims [16l, 16l+16)
-  const int lane = st & 31;
+}
+
+// Inverse rotation at p and store of head h of row r; lane holds dims [16 lane, 16 lane + 16).
+__device__ void store_head16(const AttnArgs& a, int r, int h, int64_t p, float* v, int lane) {
   const int R = a.rope.rope_dim;
-  for (int hh = 0; hh < 16; ++hh) {
-    const int h = w * 16 + hh;
+#pragma unroll
+  for (int e = 0; e < 16; e += 2) {
+    const int d = 16 * lane + e;
+    if (d >= kD - R) {
+      float cs, sn;
+      rope_cs(a.rope, (d - (kD - R)) / 2, p, cs, sn);
+      const float x0 = v[e], x1 = v[e + 1];
+      v[e] = x0 * cs + x1 * sn;
+      v[e + 1] = -x0 * sn + x1 * cs;
+    }
+  }
+  const int64_t ob = ((int64_t)r * a.heads + h) * kD + 16 * lane;
+  if (a.out_dtype == CSA_E4M3) {
+    float am = 0.f;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) am = fmaxf(am, fabsf(v[e]));
+    am = warp_max(am);
+    const float inv = am > 0.f ? 448.0f / am : 0.0f;
+    uint32_t wv[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      wv[q] = (uint32_t)f32x2_to_e4m3x2(v[4 * q] * inv, v[4 * q + 1] * inv) |
+              ((uint32_t)f32x2_to_e4m3x2(v[4 * q + 2] * inv, v[4 * q + 3] * inv) << 16);
+    *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(a.out) + ob) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+    if (lane == 0) a.out_scales[(int64_t)r * a.heads + h] = am / 448.0f;
+  } else if (a.out_dtype == CSA_BF16) {
+    uint32_t wv[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) wv[q] = (uint32_t)f32_to_bf16(v[2 * q]) | ((uint32_t)f32_to_bf16(v[2 * q + 1]) << 16);
+    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + ob);
+    dst[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+    dst[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+  } else {
+    float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + ob);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  }
+}
+
+// All 8 warps: merge this CTA's share of the heads over the S CTAs of the cluster.
+__device__ void merge_role(const AttnArgs& a, uint8_t* smem, Misc& ms, int64_t p) {
+  const int S = gridDim.y;
+  const uint32_t rank = S > 1 ? cluster_rank() : 0;
+  const int per = kH / S;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float* stage = reinterpret_cast<const float*>(smem + kOffK);
+  for (int hh = warp; hh < per; hh += kThreads / 32) {
+    const int h = (int)rank * per + hh;
+    float mg = -INFINITY;
+    for (int s = 0; s < S; ++s) mg = fmaxf(mg, S > 1 ? ld_cluster_f32(map_shared(&ms.M[h], s)) : ms.M[h]);
     float v[16];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) v[e] = stage[h * kD + 16 * lane + e];
+    for (int e = 0; e < 16; ++e) v[e] = 0.f;
+    float lg = 0.f;
+    for (int s = 0; s < S; ++s) {
+      const float ms_ = S > 1 ? ld_cluster_f32(map_shared(&ms.M[h], s)) : ms.M[h];
+      if (ms_ == -INFINITY) continue;
+      const float f = exp2f(ms_ - mg);
+      lg += f * (S > 1 ? ld_cluster_f32(map_shared(&ms.L[h], s)) : ms.L[h]);
+      const float* src = stage + h * kD + 16 * lane;
 #pragma unroll
-    for (int e = 0; e < 16; e += 2) {
-      const int d = 16 * lane + e;
-      if (d >= kD - R) {
-        float cs, sn;
-        rope_cs(a.rope, (d - (kD - R)) / 2, g.p, cs, sn);
-        const float x0 = v[e], x1 = v[e + 1];
-        v[e] = x0 * cs + x1 * sn;
-        v[e + 1] = -x0 * sn + x1 * cs;
+      for (int q = 0; q < 4; ++q) {
+        const float4 x = S > 1 ? ld_cluster_f32x4(map_shared(src + 4 * q, s))
+                               : *reinterpret_cast<const float4*>(src + 4 * q);
+        v[4 * q] = fmaf(f, x.x, v[4 * q]);
+        v[4 * q + 1] = fmaf(f, x.y, v[4 * q + 1]);
+        v[4 * q + 2] = fmaf(f, x.z, v[4 * q + 2]);
+        v[4 * q + 3] = fmaf(f, x.w, v[4 * q + 3]);
       }
     }
-    const int64_t ob = ((int64_t)r * a.heads + h) * kD + 16 * lane;
-    if (a.out_dtype == CSA_E4M3) {
-      float am = 0.f;
+    const float inv = lg > 0.f ? 1.0f / lg : 0.f;
 #pragma unroll
-      for (int e = 0; e < 16; ++e) am = fmaxf(am, fabsf(v[e]));
-      am = warp_max(am);
-      const float inv = am > 0.f ? 448.0f / am : 0.0f;
-      uint32_t wv[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        wv[q] = (uint32_t)f32x2_to_e4m3x2(v[4 * q] * inv, v[4 * q + 1] * inv) |
-                ((uint32_t)f32x2_to_e4m3x2(v[4 * q + 2] * inv, v[4 * q + 3] * inv) << 16);
-      *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(a.out) + ob) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-      if (lane == 0) a.out_scales[(int64_t)r * a.heads + h] = am / 448.0f;
-    } else if (a.out_dtype == CSA_BF16) {
-      uint32_t wv[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        wv[q] = (uint32_t)f32_to_bf16(v[2 * q]) | ((uint32_t)f32_to_bf16(v[2 * q + 1]) << 16);
-      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + ob);
-      dst[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-      dst[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
-    } else {
-      float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + ob);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-    }
+    for (int e = 0; e < 16; ++e) v[e] *= inv;
+    store_head16(a, blockIdx.x, h, p, v, lane);
   }
 }
 
@@ -498,6 +509,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnArgs a) 
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  // every CTA's staging, M and L are complete before anyone reads them
+  if (gridDim.y > 1) cluster_sync();
+  merge_role(a, smem, ms, g.p);
+  if (gridDim.y > 1) cluster_sync();  // keep this CTA's shared memory alive until its peers are done
 }
 
 }  // namespace
@@ -508,11 +523,10 @@ bool attn_tc_eligible(const AttnArgs& a) {
 }
 
 int32_t attn_tc_splits(int32_t n_rows, int32_t keys_per_row) {
-  int32_t s = n_rows > 0 ? 148 / n_rows : 1;
+  // a power of two <= 8 (one cluster per row), about one CTA per SM in all
   const int32_t tiles = (keys_per_row + kTile - 1) / kTile;
-  if (s > tiles) s = tiles;
-  if (s > 8) s = 8;
-  if (s < 1) s = 1;
+  int32_t s = 1;
+  while (s < 8 && 2 * s * n_rows <= 148 && 2 * s <= tiles) s *= 2;
   return s;
 }
 
@@ -521,12 +535,23 @@ cudaError_t launch_attn_tc(const AttnArgs& a, int32_t n_rows, cudaStream_t s) {
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+    if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  attn_tc_kernel<<<dim3(n_rows, a.n_splits), kThreads, kSmemBytes, s>>>(a);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || a.n_splits == 1) return e;
-  return launch_attn_merge(a, n_rows, s);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_rows, a.n_splits, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = a.n_splits;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_tc_kernel, a);
 }
 
 }  // namespace csa

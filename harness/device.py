@@ -160,7 +160,7 @@ class LayerDev:
             self.io["q_idx"] = _dev(host["q_idx"], dt, d)
             self.io["w"] = _dev(host["w"], torch.float32, d)
             self.io["topk"] = torch.full((self.n_rows, L.topk), -1, dtype=torch.int32, device=d)
-            n = csa.indexer_topk_workspace_size(self.n_rows, max(self.max_n, 1))
+            n = csa.indexer_topk_workspace_size(self.n_rows, max(self.max_n, 1), L.topk)
             self.ws_idx = torch.empty(max(n, 1), dtype=torch.uint8, device=d)
         if L.out_dtype == "e4m3":
             self.io["out"] = torch.zeros((self.n_rows, L.heads, L.dim), dtype=torch.uint8, device=d)
@@ -185,10 +185,22 @@ class LayerDev:
 
     # ------------------------------------------------------------------ the hot path
 
-    def step(self, stream=None, topk_override=None):
-        """compress_insert -> (indexer_topk) -> sparse attention, all on `stream`."""
+    def step(self, stream=None, topk_override=None, side_stream=None):
+        """compress_insert -> (indexer_topk) -> sparse attention.
+
+        With `side_stream`, the indexer pipeline of a c4a layer runs on it in
+        parallel with compress_insert on `stream` and is joined before the
+        attention (the indexer reads only the indexer cache and the step's
+        indexer queries, nothing compress_insert writes)."""
         L, io = self.L, self.io
-        self.compress_insert(io["kv"], io["gate"], io["seq_id"], io["pos"], stream)
+        main = torch.cuda.current_stream() if stream is None else stream
+        use_side = side_stream is not None and L.has_indexer and topk_override is None
+        if use_side:
+            fork = torch.cuda.Event()
+            fork.record(main)
+            side_stream.wait_event(fork)
+        else:
+            self.compress_insert(io["kv"], io["gate"], io["seq_id"], io["pos"], main)
         topk, k = None, 0
         if L.has_indexer:
             k = L.topk
@@ -197,8 +209,14 @@ class LayerDev:
             else:
                 csa.indexer_topk(io["q_idx"], io["w"], io["seq_id"], io["pos"], L.ratio, L.window, self.idx,
                                  self.tables["idx"], k, max(self.max_n, 1), io["topk"], self.ws_idx, self.err,
-                                 stream)
+                                 side_stream if use_side else main)
                 topk = io["topk"]
+        if use_side:
+            self.compress_insert(io["kv"], io["gate"], io["seq_id"], io["pos"], main)
+            join = torch.cuda.Event()
+            join.record(side_stream)
+            main.wait_event(join)
+        stream = main
         attn = csa.sparse_attn_prefill if self.prefill else csa.sparse_attn_decode
         attn(self.c_layer, io["q"], io["seq_id"], io["pos"], self.comp, self.tables["comp"], topk, k,
              max(self.max_n, 1), self.swa, self.tables["swa"], io["out"], csa.DTYPES[L.out_dtype],
@@ -264,9 +282,9 @@ class WorkloadDev:
             ld.stage_step()
         torch.cuda.synchronize()
 
-    def step(self, stream=None):
+    def step(self, stream=None, side_stream=None):
         for ld in self.layers:
-            ld.step(stream)
+            ld.step(stream, side_stream=side_stream)
 
     def check(self, what="step"):
         for ld in self.layers:

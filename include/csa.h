@@ -172,15 +172,16 @@ CSA_API int csa_cache_store(const float* rows, int32_t n, const int32_t* seq_id,
  *   w         [n_rows][idx_heads] float
  *   idx_cache F32 / BF16 / E2M1, rows_per_block 256/ratio, dim idx_dim
  *   out_idx   [n_rows][k] int32
- *   ws        workspace of at least csa_indexer_topk_workspace_size(n_rows, max_n)
- *             bytes, max_n >= every row's n.  Contents are scratch.
+ *   ws        workspace of at least csa_indexer_topk_workspace_size(n_rows, max_n, k)
+ *             bytes, max_n >= every row's n.  Contents are scratch (the rows'
+ *             scores and each 8192-entry chunk's top-k candidates).
  */
 CSA_API int csa_indexer_topk(const void* q_idx, int32_t q_dtype, const float* w, int32_t n_rows,
                      int32_t idx_heads, int32_t idx_dim, const int32_t* seq_id, const int32_t* pos,
                      int32_t ratio, int32_t window, const csa_paged* idx_cache,
                      const csa_block_table* bt, int32_t k, int32_t max_n, int32_t* out_idx,
                      void* ws, size_t ws_bytes, int32_t* err, csa_stream_t stream);
-CSA_API size_t csa_indexer_topk_workspace_size(int32_t n_rows, int32_t max_n);
+CSA_API size_t csa_indexer_topk_workspace_size(int32_t n_rows, int32_t max_n, int32_t k);
 
 /*
  * csa_sparse_attn_decode -- shared-K=V attention of query rows over their

@@ -101,7 +101,7 @@ def test_host_validation_rejects_bad_arguments(lib):
 
 def test_workspace_checks(lib):
     L = csa.make_layer(4, 8, 512, 64, 64)
-    need = csa.indexer_topk_workspace_size(4, 262143)
+    need = csa.indexer_topk_workspace_size(4, 262143, 512)
     assert need >= 4 * 262143 * 4
     idx = _paged(csa.E2M1, 64, 128)
     r = lib.csa_indexer_topk(0x10, csa.BF16, 0x10, 4, 64, 128, 0x10, 0x10, 4, 8, ctypes.byref(idx),
