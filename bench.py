@@ -340,11 +340,12 @@ def run_csa(args):
     # keep the GPU loaded for a while so the clock sampler sees it under load
     t_load = time.perf_counter()
     i = 0
-    while time.perf_counter() - t_load < args.load_seconds:
-        graphs[i % replicas].replay()
-        i += 1
-        if i % 256 == 0:
-            stream.synchronize()
+    with torch.cuda.stream(stream):  # a graph replays on the current stream
+        while time.perf_counter() - t_load < args.load_seconds:
+            graphs[i % replicas].replay()
+            i += 1
+            if i % 256 == 0:
+                stream.synchronize()
     stream.synchronize()
 
     def barrier():
@@ -354,10 +355,11 @@ def run_csa(args):
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
-    t_start.record(stream)
-    for k in range(args.steps):
-        graphs[k % replicas].replay()
-    t_end.record(stream)
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for k in range(args.steps):
+            graphs[k % replicas].replay()
+        t_end.record(stream)
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()

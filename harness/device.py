@@ -34,7 +34,8 @@ def n_visible(p: int, ratio: int, window: int) -> int:
 
 
 def _dev(x, dtype=None, device="cuda"):
-    t = torch.from_numpy(np.ascontiguousarray(x))
+    x = np.ascontiguousarray(x)
+    t = torch.from_numpy(x if x.flags.writeable else x.copy())
     if dtype is not None:
         t = t.to(dtype)
     return t.to(device, non_blocking=False)

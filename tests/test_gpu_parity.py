@@ -88,8 +88,10 @@ def _assert_values(got, want, dtype, what, scale=None):
         sc = np.broadcast_to(np.asarray(scale, np.float64).reshape(-1, *([1] * (got.ndim - 1))), got.shape)
         step = np.maximum(_e4m3_step(want, sc), _e4m3_step(got, sc))
         assert np.all(diff <= step * 1.0001 + 1e-12), f"{what}: beyond one e4m3 step"
-        frac = np.mean(diff > 1e-12)
-        assert frac <= 1e-3, f"{what}: {frac:.2%} of elements differ"
+        # a different code moves the value by a full step; the per-row fp32 scale
+        # (amax/448 of slightly different fp32 rows) only moves it by scale ulps
+        frac = np.mean(diff > 0.25 * step)
+        assert frac <= 1e-3, f"{what}: {frac:.2%} of elements on a different code"
     else:
         raise ValueError(dtype)
 
@@ -274,8 +276,10 @@ def test_device_bounds_are_reported_not_faulted():
     bad = ld.tables["comp"].clone()
     bad[0, 1] = -1
     io = ld.io
+    ws = torch.empty(max(1, csa.sparse_attn_workspace_size(ld.c_layer, ld.n_rows, ld.max_n)), dtype=torch.uint8,
+                     device="cuda")
     csa.sparse_attn_decode(ld.c_layer, io["q"], io["seq_id"], io["pos"], ld.comp, bad, None, 0, ld.max_n,
-                           ld.swa, ld.tables["swa"], io["out"], csa.F32, None, ld.ws_attn, ld.err)
+                           ld.swa, ld.tables["swa"], io["out"], csa.F32, None, ws, ld.err)
     assert csa.read_status(ld.err) == csa.ERR_DEVICE_BOUNDS
     sel = torch.full((ld.n_rows, L.topk), -1, dtype=torch.int32, device="cuda")
     sel[:, 0] = 10 ** 6  # far beyond the visible entries
