@@ -45,7 +45,13 @@ RopeTab make_rope(int32_t rope_dim, float theta) {
   RopeTab t;
   std::memset(&t, 0, sizeof(t));
   t.rope_dim = rope_dim;
-  for (int k = 0; k < rope_dim / 2; ++k) t.inv_freq[k] = std::pow((double)theta, -2.0 * k / rope_dim);
+  for (int k = 0; k < rope_dim / 2; ++k) {
+    const double f = std::pow((double)theta, -2.0 * k / rope_dim) / (2.0 * 3.14159265358979323846);  // turns / pos
+    // f < 1: its 2^64 fixed-point form is an exact product of the double with 2^64, split in halves
+    const double hi = std::floor(std::ldexp(f, 32));
+    const double lo = std::ldexp(f, 64) - std::ldexp(hi, 32);
+    t.turns[k] = ((uint64_t)hi << 32) + (uint64_t)std::llround(lo);
+  }
   return t;
 }
 

@@ -13,9 +13,13 @@ namespace csa {
 
 constexpr int kMaxRopePairs = 64;  // rope_dim <= 128
 
-// pos * theta^(-2k/r) for the rotary pairs, filled on the host in double.
+// Rotary frequencies as turn fractions: turns[k] = round(2^64 * theta^(-2k/r) / (2 pi)),
+// filled on the host in double.  The angle of position p is then
+// (p * turns[k] mod 2^64) / 2^64 turns: one exact wrapping 64-bit integer
+// multiply gives the reduced angle, with an error of about p * 2^-53 turns,
+// far below a microradian at p ~ 2^20 (an fp32 product would be off by 0.06 rad).
 struct RopeTab {
-  double inv_freq[kMaxRopePairs];
+  uint64_t turns[kMaxRopePairs];
   int32_t rope_dim;
 };
 
@@ -50,12 +54,11 @@ __host__ __device__ __forceinline__ int32_t n_visible(int32_t p, int32_t ratio, 
   return p < window ? 0 : (p - window) / ratio + 1;
 }
 
-// cos / sin of pos * inv_freq[k]; the product and its reduction to [-pi, pi]
-// are done in double so that positions near 2^20 keep a sub-microradian angle.
+// cos / sin of the rotary angle of pair k at position pos, reduced to [-pi, pi).
 __device__ __forceinline__ void rope_cs(const RopeTab& t, int k, int64_t pos, float& c, float& s) {
-  double a = (double)pos * t.inv_freq[k];
-  a -= 6.283185307179586476925 * rint(a * 0.15915494309189533577);
-  sincosf((float)a, &s, &c);
+  const int64_t frac = (int64_t)((uint64_t)pos * t.turns[k]);  // signed turns * 2^64, |.| <= 1/2 turn
+  const float a = (float)frac * 3.4061215800865545e-19f;      // 2 pi / 2^64
+  sincosf(a, &s, &c);
 }
 
 // ---------------------------------------------------------------- codecs

@@ -64,7 +64,8 @@ struct Misc {
   float L[kH];          // softmax denominators of the slice
   float kscale[2][kTile];
   int8_t kvalid[2][kTile];
-  const uint8_t* rowptr[kTile];
+  const uint8_t* rowptr[2][kTile];  // producer-private, by tile parity
+  float rowscale[2][kTile];
 };
 constexpr uint32_t kSmemBytes = kOffMisc + sizeof(Misc) + 1024;
 
@@ -101,41 +102,49 @@ __device__ __forceinline__ bool wait_or_abort(Misc& ms, uint64_t* bar, uint32_t 
 
 // ------------------------------------------------------------------ producers
 
+// Row address (and e4m3 scale) of key slot `slot` of tile t, or nullptr if masked.
+__device__ __forceinline__ const uint8_t* key_row(const AttnArgs& a, const Geo& g, int t, int slot, bool fp8,
+                                                  float& sc) {
+  const int32_t j = g.j0 + t * kTile + slot;
+  sc = 1.f;
+  if (j >= g.j1) return nullptr;
+  const csa_paged* c = nullptr;
+  int64_t prow = -1;
+  if (j < g.n_sel) {
+    const int32_t idx = a.topk ? a.topk[(int64_t)blockIdx.x * a.k + j] : j;
+    if (idx < 0) return nullptr;
+    if (idx >= g.n_vis) {
+      record_error(a.err, CSA_ERR_DEVICE_BOUNDS);
+      return nullptr;
+    }
+    c = &a.comp;
+    prow = phys_row(a.comp_bt, a.comp, g.seq, idx, a.err);
+  } else {
+    c = &a.swa;
+    prow = phys_row(a.swa_bt, a.swa, g.seq, g.w_lo + (j - g.n_sel), a.err);
+  }
+  if (prow < 0) return nullptr;
+  if (fp8) sc = reinterpret_cast<const float*>(c->scales)[prow];
+  return reinterpret_cast<const uint8_t*>(c->data) + prow * (int64_t)kD * (fp8 ? 1 : 2);
+}
+
 __device__ void producer_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Misc& ms, int pt) {
   const bool fp8 = a.comp.dtype == CSA_E4M3;
   const uint32_t kbase = smem_u32(smem + kOffK);
+  const uint32_t row_bytes = fp8 ? kD : 2 * kD;
   for (int t = 0; t < g.n_tiles; ++t) {
     const int par = t & 1;
-    // key metadata of the tile's 128 slots
+    // row addresses of this tile (tile 0) and of the next one, whose rows are
+    // prefetched into L2 while this tile is gathered and computed
     for (int slot = pt; slot < kTile; slot += kProducers) {
-      const int32_t j = g.j0 + t * kTile + slot;
-      const uint8_t* rp = nullptr;
-      float sc = 1.f;
-      if (j < g.j1) {
-        const csa_paged* c = nullptr;
-        int64_t prow = -1;
-        if (j < g.n_sel) {
-          const int32_t idx = a.topk ? a.topk[(int64_t)blockIdx.x * a.k + j] : j;
-          if (idx >= 0) {
-            if (idx >= g.n_vis) {
-              record_error(a.err, CSA_ERR_DEVICE_BOUNDS);
-            } else {
-              c = &a.comp;
-              prow = phys_row(a.comp_bt, a.comp, g.seq, idx, a.err);
-            }
-          }
-        } else {
-          c = &a.swa;
-          prow = phys_row(a.swa_bt, a.swa, g.seq, g.w_lo + (j - g.n_sel), a.err);
-        }
-        if (prow >= 0) {
-          rp = reinterpret_cast<const uint8_t*>(c->data) + prow * (int64_t)kD * (fp8 ? 1 : 2);
-          if (fp8) sc = reinterpret_cast<const float*>(c->scales)[prow];
-        }
+      if (t == 0) ms.rowptr[0][slot] = key_row(a, g, 0, slot, fp8, ms.rowscale[0][slot]);
+      if (t + 1 < g.n_tiles) {
+        const uint8_t* nx = key_row(a, g, t + 1, slot, fp8, ms.rowscale[par ^ 1][slot]);
+        ms.rowptr[par ^ 1][slot] = nx;
+        if (nx) prefetch_l2(nx, row_bytes);
       }
-      ms.rowptr[slot] = rp;
-      ms.kvalid[par][slot] = rp != nullptr;
-      ms.kscale[par][slot] = sc;
+      ms.kvalid[par][slot] = ms.rowptr[par][slot] != nullptr;
+      ms.kscale[par][slot] = ms.rowscale[par][slot];
     }
     named_bar(2, kProducers);
     for (int c = 0; c < kChunks; ++c) {
@@ -145,7 +154,7 @@ __device__ void producer_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mi
         // 16 consecutive threads per key row: 256 contiguous bytes = dims [128c, 128c+128)
         for (int x = pt; x < kTile * 16; x += kProducers) {
           const uint32_t key = x >> 4, piece = x & 15;
-          const uint8_t* rp = ms.rowptr[key];
+          const uint8_t* rp = ms.rowptr[par][key];
           const uint32_t dst = cbase + (piece >> 3) * kAtomBytes + (key >> 3) * 1024 + (key & 7) * 128 +
                                (((piece & 7) ^ (key & 7)) << 4);
           cp_async16(dst, rp ? rp + c * 256 + piece * 16 : a.comp.data, rp ? 16u : 0u);
@@ -160,7 +169,7 @@ __device__ void producer_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mi
           const int x = pt + it * kProducers;
           raw[it] = make_uint4(0, 0, 0, 0);
           if (x < kTile * 8) {
-            const uint8_t* rp = ms.rowptr[x >> 3];
+            const uint8_t* rp = ms.rowptr[par][x >> 3];
             if (rp) raw[it] = __ldg(reinterpret_cast<const uint4*>(rp + c * 128 + (x & 7) * 16));
           }
         }
@@ -413,34 +422,58 @@ __device__ void store_head16(const AttnArgs& a, int r, int h, int64_t p, float* 
 }
 
 // All 8 warps: merge this CTA's share of the heads over the S CTAs of the cluster.
+// Every peer's M, L and staged O are read through generic cluster pointers,
+// all loads of a head issued before any is used.
 __device__ void merge_role(const AttnArgs& a, uint8_t* smem, Misc& ms, int64_t p) {
   const int S = gridDim.y;
   const uint32_t rank = S > 1 ? cluster_rank() : 0;
   const int per = kH / S;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* stage = reinterpret_cast<const float*>(smem + kOffK);
+  const float* Mp[8];
+  const float* Lp[8];
+  const float* Sp[8];
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const uint32_t rk = s < S ? (uint32_t)s : 0u;
+    Mp[s] = S > 1 ? map_shared_ptr(ms.M, rk) : ms.M;
+    Lp[s] = S > 1 ? map_shared_ptr(ms.L, rk) : ms.L;
+    Sp[s] = S > 1 ? map_shared_ptr(stage, rk) : stage;
+  }
   for (int hh = warp; hh < per; hh += kThreads / 32) {
     const int h = (int)rank * per + hh;
+    float m[8], l[8];
+    float4 x[8][4];
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      if (s < S) {
+        m[s] = Mp[s][h];
+        l[s] = Lp[s][h];
+        const float4* src = reinterpret_cast<const float4*>(Sp[s] + h * kD + 16 * lane);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) x[s][q] = src[q];
+      }
+    }
     float mg = -INFINITY;
-    for (int s = 0; s < S; ++s) mg = fmaxf(mg, S > 1 ? ld_cluster_f32(map_shared(&ms.M[h], s)) : ms.M[h]);
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+      if (s < S) mg = fmaxf(mg, m[s]);
     float v[16];
 #pragma unroll
     for (int e = 0; e < 16; ++e) v[e] = 0.f;
     float lg = 0.f;
-    for (int s = 0; s < S; ++s) {
-      const float ms_ = S > 1 ? ld_cluster_f32(map_shared(&ms.M[h], s)) : ms.M[h];
-      if (ms_ == -INFINITY) continue;
-      const float f = exp2f(ms_ - mg);
-      lg += f * (S > 1 ? ld_cluster_f32(map_shared(&ms.L[h], s)) : ms.L[h]);
-      const float* src = stage + h * kD + 16 * lane;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 x = S > 1 ? ld_cluster_f32x4(map_shared(src + 4 * q, s))
-                               : *reinterpret_cast<const float4*>(src + 4 * q);
-        v[4 * q] = fmaf(f, x.x, v[4 * q]);
-        v[4 * q + 1] = fmaf(f, x.y, v[4 * q + 1]);
-        v[4 * q + 2] = fmaf(f, x.z, v[4 * q + 2]);
-        v[4 * q + 3] = fmaf(f, x.w, v[4 * q + 3]);
+    for (int s = 0; s < 8; ++s) {
+      if (s < S && m[s] != -INFINITY) {
+        const float f = exp2f(m[s] - mg);
+        lg += f * l[s];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          v[4 * q] = fmaf(f, x[s][q].x, v[4 * q]);
+          v[4 * q + 1] = fmaf(f, x[s][q].y, v[4 * q + 1]);
+          v[4 * q + 2] = fmaf(f, x[s][q].z, v[4 * q + 2]);
+          v[4 * q + 3] = fmaf(f, x[s][q].w, v[4 * q + 3]);
+        }
       }
     }
     const float inv = lg > 0.f ? 1.0f / lg : 0.f;

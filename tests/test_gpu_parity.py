@@ -15,8 +15,9 @@ GPU produced.  Per workload:
 
 Tolerances: fp32 workload 1e-4 max-abs; bf16 2e-2 max-abs and 1e-2 rel-L2
 against the unrounded fp64 oracle; e4m3 caches within one e4m3 step of the
-oracle's code for every element and at most 0.1% of elements off at all;
-e4m3 output within one e4m3 step and 6e-2 max-abs / 3e-2 rel-L2.
+oracle's code for every element and at most 0.1% of elements on another code;
+e4m3 output 6e-2 max-abs / 3e-2 rel-L2, each element within one e4m3 step plus
+1% of its head's amax, scales within 1%.
 """
 
 import math
@@ -203,9 +204,12 @@ def _compare_out(ld, got_all, codes, scales, row, res, what, e2e=False):
         diff = np.abs(got - want)
         rel = np.linalg.norm(got - want) / np.linalg.norm(want)
         assert diff.max() <= 6e-2 and rel <= 3e-2, f"{what}: max-abs {diff.max():.3g} rel {rel:.3g}"
+        # one e4m3 step of rounding, plus the error of the bf16 operands the tensor
+        # cores take (q and p rounded to bf16): absolute, about 1% of the head's amax
         sc = scales[row][:, None]
         step = np.maximum(_e4m3_step(want, sc), _e4m3_step(got, sc))
-        assert np.all(diff <= step * 1.0001 + 1e-7), f"{what}: beyond one e4m3 step"
+        amax = np.abs(want).max(axis=1, keepdims=True)
+        assert np.all(diff <= step * 1.0001 + 1e-2 * amax), f"{what}: beyond one e4m3 step + 1% of amax"
         np.testing.assert_allclose(scales[row], res["out_scale"], rtol=1e-2)
     else:
         _assert_values(got, res["out"], L.out_dtype, what)
