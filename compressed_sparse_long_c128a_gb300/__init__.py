@@ -62,6 +62,8 @@ _SIGS = {
     "csa_sparse_attn_prefill": (_I32, [_PL, _VP, _I32, _I32, _VP, _VP, _PP, _PB, _VP, _I32, _I32, _PP, _PB, _VP,
                                        _I32, _VP, _VP, _SZ, _VP, _VP]),
     "csa_sparse_attn_workspace_size": (_SZ, [_PL, _I32, _I32]),
+    "csa_indexer_topk_noalloc": (_I32, [_VP, _I32, _VP, _I32, _I32, _I32, _VP, _VP, _I32, _I32, _PP, _PB, _I32,
+                                        _I32, _VP, _VP, _VP]),
     "csa_read_status": (_I32, [_VP, _I32, _VP]),
     "csa_status_string": (ctypes.c_char_p, [_I32]),
     "csa_version": (_I32, []),
@@ -206,6 +208,20 @@ def indexer_topk(q_idx, w, seq_id, pos, ratio: int, window: int, idx_cache: Page
                                 _ptr(out_idx), _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
                                 _ptr(err), _stream(stream))
     _check(st, "csa_indexer_topk")
+
+
+def indexer_topk_noalloc(q_idx, w, seq_id, pos, ratio: int, window: int, idx_cache: PagedCache, bt, k: int,
+                         max_n: int, out_idx, err, stream=None):
+    """indexer_topk without a workspace, for callers that cannot allocate device
+    memory: its scratch is a fixed 8 MiB array inside the library, shared by
+    every call (calls that may overlap on the GPU race; the first call on a
+    device should come before any stream capture)."""
+    n_rows, heads, dim = q_idx.shape
+    st = lib().csa_indexer_topk_noalloc(_ptr(q_idx), _tdtype(q_idx), _ptr(w), n_rows, heads, dim, _ptr(seq_id),
+                                        _ptr(pos), ratio, window, ctypes.byref(idx_cache.c()),
+                                        ctypes.byref(block_table(bt)), k, max_n, _ptr(out_idx), _ptr(err),
+                                        _stream(stream))
+    _check(st, "csa_indexer_topk_noalloc")
 
 
 def sparse_attn_workspace_size(layer: Layer, n_rows: int, k_or_max_n: int) -> int:

@@ -225,6 +225,33 @@ CSA_API int csa_sparse_attn_prefill(const csa_layer* layer, const void* q, int32
                             size_t ws_bytes, int32_t* err, csa_stream_t stream);
 CSA_API size_t csa_sparse_attn_workspace_size(const csa_layer* layer, int32_t n_rows, int32_t k_or_max_n);
 
+/*
+ * csa_indexer_topk_noalloc -- csa_indexer_topk for callers that cannot
+ * allocate device memory.  The pages have no counterpart: this is a calling
+ * convention of this library, not part of the method.
+ *
+ * Some callers cannot pass a workspace: a plugin inside a host runtime that
+ * owns all device memory and gives its extensions no allocator, or a serving
+ * loop that may not allocate on its hot path (an allocation can wait for the
+ * whole device or fail under memory pressure).  This variant computes exactly
+ * what csa_indexer_topk computes, with the same arguments minus the workspace,
+ * and keeps its scratch in a fixed 8 MiB array of device memory defined inside
+ * the library (held on every GPU that loads the library until the process
+ * exits).  It calls no allocator.
+ *   - A request whose scratch (csa_indexer_topk_workspace_size(n_rows, max_n,
+ *     k)) exceeds 8 MiB returns CSA_ERR_WORKSPACE and enqueues nothing.
+ *   - All calls share the one array: calls that can run at the same time on
+ *     the GPU (different streams, no ordering between them) race.  Calls on one
+ *     stream are safe; no scratch byte needs to start at zero.
+ *   - The first call on a device resolves the array's device address with
+ *     that device current; make that first call before any stream capture.
+ */
+CSA_API int csa_indexer_topk_noalloc(const void* q_idx, int32_t q_dtype, const float* w, int32_t n_rows,
+                                     int32_t idx_heads, int32_t idx_dim, const int32_t* seq_id,
+                                     const int32_t* pos, int32_t ratio, int32_t window,
+                                     const csa_paged* idx_cache, const csa_block_table* bt, int32_t k,
+                                     int32_t max_n, int32_t* out_idx, int32_t* err, csa_stream_t stream);
+
 /* Copy the device error word to the host (synchronises `stream`); if `reset`, zero it
  * afterwards.  Returns the recorded csa_status (CSA_OK if none) or CSA_ERR_CUDA. */
 CSA_API int csa_read_status(int32_t* err, int32_t reset, csa_stream_t stream);
