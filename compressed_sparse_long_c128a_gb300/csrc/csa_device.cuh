@@ -23,6 +23,18 @@ struct RopeTab {
   int32_t rope_dim;
 };
 
+// Programmatic dependent launch.  Every kernel of the library is launched so
+// that it may start while the previous kernel of the stream is finishing:
+// pdl_trigger() lets the next kernel launch; pdl_wait() blocks until the
+// previous kernel has completed and its writes are visible.  A kernel calls
+// pdl_wait() before it touches a cache, a workspace or an output (anything an
+// earlier kernel may write or read); reading the caller's inputs before it is
+// safe, since those were complete before the library's first kernel started.
+// Every CTA passes pdl_wait() before it exits, so a grid completes only after
+// its predecessor did and completion stays transitive along the stream.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void record_error(int32_t* err, int32_t code) {
   if (err) atomicCAS(err, 0, code);
 }
@@ -55,9 +67,14 @@ __host__ __device__ __forceinline__ int32_t n_visible(int32_t p, int32_t ratio, 
 }
 
 // cos / sin of the rotary angle of pair k at position pos, reduced to [-pi, pi).
+// Only the top 32 bits of the wrapped 64-bit product are needed (an angle
+// step of 2 pi / 2^32), and they come from 32-bit integer multiplies.
 __device__ __forceinline__ void rope_cs(const RopeTab& t, int k, int64_t pos, float& c, float& s) {
-  const int64_t frac = (int64_t)((uint64_t)pos * t.turns[k]);  // signed turns * 2^64, |.| <= 1/2 turn
-  const float a = (float)frac * 3.4061215800865545e-19f;      // 2 pi / 2^64
+  const uint32_t p = (uint32_t)pos;
+  const uint64_t f = t.turns[k];
+  const uint32_t lo_hi = __umulhi(p, (uint32_t)f);           // bits 32..63 of p * f_lo
+  const uint32_t top = lo_hi + p * (uint32_t)(f >> 32);      // bits 32..63 of p * f, mod 2^32
+  const float a = (float)(int32_t)top * 1.4629180792671596e-9f;  // 2 pi / 2^32
   sincosf(a, &s, &c);
 }
 
@@ -123,6 +140,13 @@ __device__ __forceinline__ uint32_t f32_to_e2m1(float x) {
 }
 
 // ---------------------------------------------------------------- reductions
+
+// 2^x with the special-function unit (about 2 ulp); the softmax weights need no more.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

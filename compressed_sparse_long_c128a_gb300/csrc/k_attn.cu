@@ -85,6 +85,8 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnArgs a) {
   __shared__ int64_t prow_s[kKeyTile];
   __shared__ int8_t which_s[kKeyTile];   // 0: comp, 1: swa, -1: masked
 
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x, hg = blockIdx.y, split = blockIdx.z;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int h = hg * kHeadsPerCta + warp;
@@ -198,6 +200,8 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnArgs a) {
 
 // One warp per (row, head): combine the splits' (m, l, o), normalise, rotate back, store.
 __global__ void __launch_bounds__(32) merge_kernel(const AttnArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x, h = blockIdx.y, lane = threadIdx.x;
   const int S = a.n_splits, D = a.dim;
   const int64_t hb = ((int64_t)r * a.heads + h) * S;
@@ -248,15 +252,13 @@ cudaError_t launch_attn(const AttnArgs& a, int32_t n_rows, int32_t keys_per_row,
   const size_t smem = sizeof(float) * ((size_t)kHeadsPerCta * a.dim + (size_t)kKeyTile * (a.dim + 1));
   cudaError_t e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  attn_kernel<<<dim3(n_rows, a.heads / kHeadsPerCta, a.n_splits), kThreads, smem, s>>>(a);
-  e = cudaGetLastError();
+  e = launch_k(attn_kernel, dim3(n_rows, a.heads / kHeadsPerCta, a.n_splits), dim3(kThreads), smem, s, 0, a);
   if (e != cudaSuccess || a.n_splits == 1) return e;
   return launch_attn_merge(a, n_rows, s);
 }
 
 cudaError_t launch_attn_merge(const AttnArgs& a, int32_t n_rows, cudaStream_t s) {
-  merge_kernel<<<dim3(n_rows, a.heads), 32, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_k(merge_kernel, dim3(n_rows, a.heads), dim3(32), 0, s, 0, a);
 }
 
 }  // namespace csa

@@ -55,13 +55,14 @@ constexpr uint32_t kColS = 0, kColO = 64;
 constexpr float kRescaleMargin = 8.0f;  // log2 units
 
 struct Misc {
-  uint64_t kfull[kChunks], kfree[kChunks], s_full, p_full, p_free;
+  uint64_t kfull[kChunks], kfree[kChunks], s_full, p_full, p_free, q_full;
   uint32_t tmem_base;
   int32_t abort;
   float M[kH];          // running per-head max (log2 domain), shared by the softmax threads
   float red[4][kH];     // per-warp reductions
   float alpha[kH];      // rescale factor of the last max raise
   float L[kH];          // softmax denominators of the slice
+  float rc[kMaxRopePairs], rs[kMaxRopePairs];  // cos / sin of each rotary pair at the row's position
   float kscale[2][kTile];
   int8_t kvalid[2][kTile];
   const uint8_t* rowptr[2][kTile];  // producer-private, by tile parity
@@ -132,21 +133,16 @@ __device__ void producer_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mi
   const bool fp8 = a.comp.dtype == CSA_E4M3;
   const uint32_t kbase = smem_u32(smem + kOffK);
   const uint32_t row_bytes = fp8 ? kD : 2 * kD;
+  // row addresses of tile 0; later tiles' addresses are looked up one tile ahead
+  for (int slot = pt; slot < kTile; slot += kProducers)
+    ms.rowptr[0][slot] = g.n_tiles > 0 ? key_row(a, g, 0, slot, fp8, ms.rowscale[0][slot]) : nullptr;
+  named_bar(2, kProducers);
   for (int t = 0; t < g.n_tiles; ++t) {
     const int par = t & 1;
-    // row addresses of this tile (tile 0) and of the next one, whose rows are
-    // prefetched into L2 while this tile is gathered and computed
     for (int slot = pt; slot < kTile; slot += kProducers) {
-      if (t == 0) ms.rowptr[0][slot] = key_row(a, g, 0, slot, fp8, ms.rowscale[0][slot]);
-      if (t + 1 < g.n_tiles) {
-        const uint8_t* nx = key_row(a, g, t + 1, slot, fp8, ms.rowscale[par ^ 1][slot]);
-        ms.rowptr[par ^ 1][slot] = nx;
-        if (nx) prefetch_l2(nx, row_bytes);
-      }
       ms.kvalid[par][slot] = ms.rowptr[par][slot] != nullptr;
       ms.kscale[par][slot] = ms.rowscale[par][slot];
     }
-    named_bar(2, kProducers);
     for (int c = 0; c < kChunks; ++c) {
       if (t > 0) wait_or_abort(ms, &ms.kfree[c], (t - 1) & 1, a.err);
       const uint32_t cbase = kbase + c * kChunkBytes;
@@ -197,6 +193,14 @@ __device__ void producer_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mi
         }
       }
     }
+    // while tile t is in flight: the next tile's row addresses, and its rows into L2
+    if (t + 1 < g.n_tiles) {
+      for (int slot = pt; slot < kTile; slot += kProducers) {
+        const uint8_t* nx = key_row(a, g, t + 1, slot, fp8, ms.rowscale[par ^ 1][slot]);
+        ms.rowptr[par ^ 1][slot] = nx;
+        if (nx) prefetch_l2(nx, row_bytes);
+      }
+    }
     if (!fp8) {
       cp_async_wait<3>();
       fence_proxy_async();
@@ -226,6 +230,7 @@ __device__ void mma_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Misc& m
   constexpr uint32_t idesc_s = idesc_bf16(128, kH, 0, 0);
   constexpr uint32_t idesc_o = idesc_bf16(128, kH, 1, 1);
   const uint32_t kbase = smem_u32(smem + kOffK), qbase = smem_u32(smem + kOffQ), pbase = smem_u32(smem + kOffP);
+  wait_or_abort(ms, &ms.q_full, 0, a.err);
   for (int t = 0; t < g.n_tiles; ++t) {
     const uint32_t par = t & 1;
     for (int c = 0; c < kChunks; ++c) {
@@ -274,7 +279,64 @@ __device__ __forceinline__ void warp_reduce64(const float* v, Misc& ms, int st) 
   }
 }
 
+// Q^T operand: the row's 64 heads rotated at p, scaled by scale * log2(e),
+// rounded to bf16, 128B-swizzled K-major (rows = heads).  The 128 softmax
+// threads fill it with 16-byte loads while the producers gather the first
+// key tile, then release the MMA issuer through q_full.
+__device__ void fill_q(const AttnArgs& a, const Geo& g, uint8_t* smem, Misc& ms, int st) {
+  const float qs = a.scale * 1.4426950408889634f;
+  const int R = a.rope.rope_dim;
+  const int64_t rb = (int64_t)blockIdx.x * a.heads * kD;
+  constexpr int kPieces = kH * (kD / 8);  // 16-byte pieces of bf16 (8 dims each)
+  constexpr int kBatch = 8;               // loads in flight per thread
+  for (int x0 = st; x0 < kPieces; x0 += kSoftmax * kBatch) {
+    float q[kBatch][8];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int x = x0 + u * kSoftmax;
+      const int h = x / (kD / 8), d0 = 8 * (x % (kD / 8));
+      if (a.q_dtype == CSA_BF16) {
+        const uint4 v =
+            __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q) + rb + h * kD + d0));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          q[u][2 * e] = bf16_to_f32((uint16_t)(w[e] & 0xFFFF));
+          q[u][2 * e + 1] = bf16_to_f32((uint16_t)(w[e] >> 16));
+        }
+      } else {
+        const float4* src = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.q) + rb + h * kD + d0);
+        const float4 v0 = __ldg(src), v1 = __ldg(src + 1);
+        q[u][0] = v0.x; q[u][1] = v0.y; q[u][2] = v0.z; q[u][3] = v0.w;
+        q[u][4] = v1.x; q[u][5] = v1.y; q[u][6] = v1.z; q[u][7] = v1.w;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int x = x0 + u * kSoftmax;
+      const int h = x / (kD / 8), d0 = 8 * (x % (kD / 8));
+      uint32_t o[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float q0 = q[u][2 * e], q1 = q[u][2 * e + 1];
+        const int d = d0 + 2 * e;
+        if (d >= kD - R) {
+          const float cs = ms.rc[(d - (kD - R)) / 2], sn = ms.rs[(d - (kD - R)) / 2];
+          const float t0 = q0 * cs - q1 * sn;
+          q1 = q0 * sn + q1 * cs;
+          q0 = t0;
+        }
+        o[e] = (uint32_t)f32_to_bf16(q0 * qs) | ((uint32_t)f32_to_bf16(q1 * qs) << 16);
+      }
+      *reinterpret_cast<uint4*>(smem + kOffQ + sw128_offset(h, d0, kH)) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+  fence_proxy_async();
+  mbar_arrive(&ms.q_full);
+}
+
 __device__ void softmax_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Misc& ms, uint32_t tmem, int st) {
+  fill_q(a, g, smem, ms, st);
   const int w = st >> 5;
   const uint32_t lane_addr = tmem + ((uint32_t)(w * 32) << 16);
   float lsum[kH];
@@ -340,8 +402,8 @@ __device__ void softmax_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mis
       for (int e = 0; e < 4; ++e) {
         const int h = 8 * c + 2 * e;
         const float m0 = ms.M[h], m1 = ms.M[h + 1];
-        const float p0 = (x[h] == -INFINITY || m0 == -INFINITY) ? 0.f : exp2f(x[h] - m0);
-        const float p1 = (x[h + 1] == -INFINITY || m1 == -INFINITY) ? 0.f : exp2f(x[h + 1] - m1);
+        const float p0 = (x[h] == -INFINITY || m0 == -INFINITY) ? 0.f : fast_exp2(x[h] - m0);
+        const float p1 = (x[h + 1] == -INFINITY || m1 == -INFINITY) ? 0.f : fast_exp2(x[h + 1] - m1);
         lsum[h] += p0;
         lsum[h + 1] += p1;
         w4[e] = (uint32_t)f32_to_bf16(p0 * ksc) | ((uint32_t)f32_to_bf16(p1 * ksc) << 16);
@@ -380,14 +442,13 @@ __device__ void softmax_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mis
 }
 
 // Inverse rotation at p and store of head h of row r; lane holds dims [16 lane, 16 lane + 16).
-__device__ void store_head16(const AttnArgs& a, int r, int h, int64_t p, float* v, int lane) {
+__device__ void store_head16(const AttnArgs& a, const Misc& ms, int r, int h, float* v, int lane) {
   const int R = a.rope.rope_dim;
 #pragma unroll
   for (int e = 0; e < 16; e += 2) {
     const int d = 16 * lane + e;
     if (d >= kD - R) {
-      float cs, sn;
-      rope_cs(a.rope, (d - (kD - R)) / 2, p, cs, sn);
+      const float cs = ms.rc[(d - (kD - R)) / 2], sn = ms.rs[(d - (kD - R)) / 2];
       const float x0 = v[e], x1 = v[e + 1];
       v[e] = x0 * cs + x1 * sn;
       v[e + 1] = -x0 * sn + x1 * cs;
@@ -479,7 +540,7 @@ __device__ void merge_role(const AttnArgs& a, uint8_t* smem, Misc& ms, int64_t p
     const float inv = lg > 0.f ? 1.0f / lg : 0.f;
 #pragma unroll
     for (int e = 0; e < 16; ++e) v[e] *= inv;
-    store_head16(a, blockIdx.x, h, p, v, lane);
+    store_head16(a, ms, blockIdx.x, h, v, lane);
   }
 }
 
@@ -490,6 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnArgs a) 
   const int tid = threadIdx.x, warp = tid >> 5;
   const int r = blockIdx.x;
   const Geo g = row_geometry(a, r, blockIdx.y, gridDim.y);
+  pdl_trigger();
 
   if (tid == 0) {
     for (int c = 0; c < kChunks; ++c) {
@@ -499,31 +561,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnArgs a) 
     mbar_init(&ms.s_full, 1);
     mbar_init(&ms.p_full, kSoftmax);
     mbar_init(&ms.p_free, 1);
+    mbar_init(&ms.q_full, kSoftmax);
     mbar_init_fence();
     ms.abort = 0;
   }
   if (tid < kH) ms.M[tid] = -INFINITY;
+  if (tid < a.rope.rope_dim / 2) rope_cs(a.rope, tid, g.p, ms.rc[tid], ms.rs[tid]);
   if (warp == 7) tmem_alloc(&ms.tmem_base, kTmemCols);
-  // Q^T: rotated, scaled by scale * log2(e), bf16, 128B-swizzled K-major (rows = heads)
-  if (tid < kSoftmax + kProducers) {
-    const float qs = a.scale * 1.4426950408889634f;
-    const int R = a.rope.rope_dim;
-    for (int x = tid; x < kH * kD / 2; x += kSoftmax + kProducers) {
-      const int h = x / (kD / 2), d = 2 * (x % (kD / 2));
-      const int64_t qb = ((int64_t)r * a.heads + h) * kD + d;
-      float q0 = load_elem(a.q, a.q_dtype, qb), q1 = load_elem(a.q, a.q_dtype, qb + 1);
-      if (d >= kD - R) {
-        float cs, sn;
-        rope_cs(a.rope, (d - (kD - R)) / 2, g.p, cs, sn);
-        const float t0 = q0 * cs - q1 * sn;
-        q1 = q0 * sn + q1 * cs;
-        q0 = t0;
-      }
-      const uint32_t v = (uint32_t)f32_to_bf16(q0 * qs) | ((uint32_t)f32_to_bf16(q1 * qs) << 16);
-      *reinterpret_cast<uint32_t*>(smem + kOffQ + sw128_offset(h, d, kH)) = v;
-    }
-    fence_proxy_async();
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -532,6 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnArgs a) 
   if (warp < 4) {
     softmax_role(a, g, smem, ms, tmem, tid);
   } else if (warp < 7) {
+    pdl_wait();  // caches and selections are complete only after the previous launch
     producer_role(a, g, smem, ms, tid - kSoftmax);
   } else if ((tid & 31) == 0) {
     mma_role(a, g, smem, ms, tmem);
@@ -572,19 +617,7 @@ cudaError_t launch_attn_tc(const AttnArgs& a, int32_t n_rows, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(n_rows, a.n_splits, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = a.n_splits;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_tc_kernel, a);
+  return launch_k(attn_tc_kernel, dim3(n_rows, a.n_splits), dim3(kThreads), kSmemBytes, s, a.n_splits, a);
 }
 
 }  // namespace csa

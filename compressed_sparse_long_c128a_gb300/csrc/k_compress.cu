@@ -72,6 +72,8 @@ __device__ void norm_rope_inplace(float* y, int D, float inv_rms, const float* g
 __global__ void __launch_bounds__(kThreads) ingest_kernel(const IngestArgs a) {
   extern __shared__ float y[];
   __shared__ float red[32];
+  pdl_trigger();
+  pdl_wait();
   const int j = blockIdx.x;
   const int D = a.dim;
   const int seq = a.seq_id[j];
@@ -107,6 +109,11 @@ __global__ void __launch_bounds__(kThreads) emit_kernel(const EmitArgs a) {
   const int j = blockIdx.x;
   const int64_t t = a.pos[j];
   const int W = a.window, Rt = a.ratio, D = a.dim;
+  pdl_trigger();
+  // every CTA waits, even one with nothing to emit: this grid may only complete
+  // after the ingest launch has, so later launches that wait on this one also
+  // see ingest's writes
+  pdl_wait();
   if (t < W - 1 || (t - W + 1) % Rt) return;  // no window closes at this token
   const int64_t i = (t - W + 1) / Rt;
   const int64_t base = i * Rt;  // first raw position = anchor
@@ -174,14 +181,12 @@ __global__ void __launch_bounds__(kThreads) emit_kernel(const EmitArgs a) {
 
 cudaError_t launch_ingest(const IngestArgs& a, int32_t n_tok, cudaStream_t s) {
   if (n_tok == 0) return cudaSuccess;
-  ingest_kernel<<<n_tok, kThreads, a.dim * sizeof(float), s>>>(a);
-  return cudaGetLastError();
+  return launch_k(ingest_kernel, dim3(n_tok), dim3(kThreads), a.dim * sizeof(float), s, 0, a);
 }
 
 cudaError_t launch_emit(const EmitArgs& a, int32_t n_tok, cudaStream_t s) {
   if (n_tok == 0) return cudaSuccess;
-  emit_kernel<<<n_tok, kThreads, a.dim * sizeof(float), s>>>(a);
-  return cudaGetLastError();
+  return launch_k(emit_kernel, dim3(n_tok), dim3(kThreads), a.dim * sizeof(float), s, 0, a);
 }
 
 }  // namespace csa

@@ -34,6 +34,8 @@ __global__ void __launch_bounds__(kThreads) indexer_scores_kernel(const IndexerA
   float* part = ks + kTile * ld;     // [kQuarters][kTile]
   __shared__ int64_t prow_s[kTile];
 
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x;
   const int32_t p = a.pos[r];
   const int seq = a.seq_id[r];
@@ -95,8 +97,7 @@ cudaError_t launch_indexer_scores(const IndexerArgs& a, int32_t n_rows, cudaStre
   int gy = (2 * 152 * 2 + n_rows - 1) / n_rows;  // about four CTAs per SM in all
   if (gy > tiles) gy = tiles;
   if (gy < 1) gy = 1;
-  indexer_scores_kernel<<<dim3(n_rows, gy), kThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_k(indexer_scores_kernel, dim3(n_rows, gy), dim3(kThreads), smem, s, 0, a);
 }
 
 }  // namespace csa

@@ -35,14 +35,15 @@ constexpr uint32_t kRawBytes = kRawCodes + kRawScales;
 constexpr uint32_t kOffQ = 0, kOffStage = kQBytes, kOffRaw = kOffStage + kStages * kStageBytes;
 constexpr uint32_t kOffMisc = kOffRaw + kStages * kRawBytes;
 constexpr uint32_t kTmemCols = 128;
+constexpr int kRowsPerBlock = 64;  // entries per 256-position block (c4a)
+constexpr int kTblMax = 1024;      // block-table entries a CTA caches (= 512 tiles)
 
 struct Misc {
   uint64_t full[kStages], empty[kStages], tfull[2], tempty[2];
   uint32_t tmem_base;
   int32_t abort;
   float w[kHI];
-  const uint8_t* rowptr[kTile];   // codes (or bf16 row) of each entry of the tile being issued
-  const uint8_t* sclptr[kTile];   // e2m1 scale bytes of each entry
+  int32_t tbl[kTblMax];  // physical blocks of the CTA's entry range (-1: unmapped / out of range)
 };
 constexpr uint32_t kSmemBytes = kOffMisc + sizeof(Misc) + 1024;
 
@@ -79,61 +80,63 @@ __device__ __forceinline__ uint32_t e2m1_bf16(uint32_t code, float scale) {
   return f32_to_bf16(e2m1_to_f32(code) * scale);
 }
 
+// Physical row of entry e of this CTA's range, from the cached block table; -1 if unmapped.
+__device__ __forceinline__ int64_t entry_row(const Misc& ms, int32_t blk0, int32_t e) {
+  const int32_t j = (e / kRowsPerBlock) - blk0;
+  if (j < 0 || j >= kTblMax) return -1;  // the launcher keeps every CTA's range inside the cache
+  const int32_t pb = ms.tbl[j];
+  return pb < 0 ? -1 : (int64_t)pb * kRowsPerBlock + (e % kRowsPerBlock);
+}
+
+// Each thread derives its own rows' addresses from the cached table, so issuing
+// a tile needs no barrier; e2m1 tiles need one before the conversion reads
+// bytes other threads copied.
 __device__ void producer_role(const IndexerArgs& a, const Range& g, uint8_t* smem, Misc& ms, int pt) {
   const bool fp4 = a.cache.dtype == CSA_E2M1;
   const uint32_t stage0 = smem_u32(smem + kOffStage), raw0 = smem_u32(smem + kOffRaw);
+  const int32_t blk0 = g.t0 * kTile / kRowsPerBlock;
+  const uint8_t* base = reinterpret_cast<const uint8_t*>(a.cache.data);
+  const uint8_t* sbase = reinterpret_cast<const uint8_t*>(a.cache.scales);
   for (int i = 0; i < g.nt + 2; ++i) {
     if (i < g.nt) {
       const int s = i % kStages;
       if (i >= kStages) wait_or_abort(ms, &ms.empty[s], ((i / kStages) - 1) & 1, a.err);
       const int32_t e0 = (g.t0 + i) * kTile;
-      for (int slot = pt; slot < kTile; slot += kProd) {
-        const int32_t e = e0 + slot;
-        const uint8_t* rp = nullptr;
-        const uint8_t* sp = nullptr;
-        if (e < g.n) {
-          const int64_t prow = phys_row(a.bt, a.cache, g.seq, e, a.err);
-          if (prow >= 0) {
-            rp = reinterpret_cast<const uint8_t*>(a.cache.data) + prow * (fp4 ? kDI / 2 : kDI * 2);
-            if (fp4) sp = reinterpret_cast<const uint8_t*>(a.cache.scales) + prow * (kDI / 16);
-          }
-        }
-        ms.rowptr[slot] = rp;
-        ms.sclptr[slot] = sp;
-      }
-      named_bar(2, kProd);
       if (!fp4) {
         // 16 consecutive threads per 256-byte row
         const uint32_t sb = stage0 + s * kStageBytes;
         for (int x = pt; x < kTile * 16; x += kProd) {
           const uint32_t key = x >> 4, piece = x & 15;
-          const uint8_t* rp = ms.rowptr[key];
+          const int32_t e = e0 + (int32_t)key;
+          const int64_t pr = e < g.n ? entry_row(ms, blk0, e) : -1;
           const uint32_t dst = sb + (piece >> 3) * kAtomBytes + (key >> 3) * 1024 + (key & 7) * 128 +
                                (((piece & 7) ^ (key & 7)) << 4);
-          cp_async16(dst, rp ? rp + piece * 16 : a.cache.data, rp ? 16u : 0u);
+          cp_async16(dst, pr >= 0 ? base + pr * (kDI * 2) + piece * 16 : base, pr >= 0 ? 16u : 0u);
         }
       } else {
         // raw ring: [128 rows][64 code bytes] then [128 rows][8 scale bytes]
         const uint32_t rb = raw0 + s * kRawBytes;
         for (int x = pt; x < kTile * 4; x += kProd) {
           const uint32_t key = x >> 2, piece = x & 3;
-          const uint8_t* rp = ms.rowptr[key];
-          cp_async16(rb + key * 64 + piece * 16, rp ? rp + piece * 16 : a.cache.data, rp ? 16u : 0u);
+          const int32_t e = e0 + (int32_t)key;
+          const int64_t pr = e < g.n ? entry_row(ms, blk0, e) : -1;
+          cp_async16(rb + key * 64 + piece * 16, pr >= 0 ? base + pr * (kDI / 2) + piece * 16 : base,
+                     pr >= 0 ? 16u : 0u);
         }
-        for (int x = pt; x < kTile / 2; x += kProd) {  // two rows' 8 scale bytes per 16-byte piece
-          const uint8_t* s0 = ms.sclptr[2 * x];
-          const uint8_t* s1 = ms.sclptr[2 * x + 1];
-          if (s0 && s1 && s1 == s0 + 8) {
-            cp_async16(rb + kRawCodes + x * 16, s0, 16u);
+        // two entries' 8 scale bytes per 16-byte piece; entries 2x, 2x+1 share a block
+        for (int x = pt; x < kTile / 2; x += kProd) {
+          const int32_t e = e0 + 2 * x;
+          const int64_t pr = e < g.n ? entry_row(ms, blk0, e) : -1;
+          const bool both = e + 1 < g.n;
+          if (pr >= 0 && both) {
+            cp_async16(rb + kRawCodes + x * 16, sbase + pr * (kDI / 16), 16u);
           } else {
-            uint2 v0 = s0 ? *reinterpret_cast<const uint2*>(s0) : make_uint2(0, 0);
-            uint2 v1 = s1 ? *reinterpret_cast<const uint2*>(s1) : make_uint2(0, 0);
+            const uint2 v0 = pr >= 0 ? *reinterpret_cast<const uint2*>(sbase + pr * (kDI / 16)) : make_uint2(0, 0);
             *reinterpret_cast<uint4*>(smem + kOffRaw + s * kRawBytes + kRawCodes + x * 16) =
-                make_uint4(v0.x, v0.y, v1.x, v1.y);
+                make_uint4(v0.x, v0.y, 0u, 0u);
           }
         }
       }
-      named_bar(2, kProd);  // rowptr / sclptr are rewritten for the next tile
     }
     cp_async_commit();
     if (i >= 2) {
@@ -166,6 +169,7 @@ __device__ void producer_role(const IndexerArgs& a, const Range& g, uint8_t* sme
                                       (((piece & 7) ^ (key & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
           }
         }
+        named_bar(2, kProd);  // the raw stage may be refilled only after everyone converted
       }
       fence_proxy_async();
       mbar_arrive(&ms.full[s]);
@@ -238,16 +242,54 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(const IndexerAr
     ms.abort = 0;
   }
   if (tid < kHI) ms.w[tid] = a.w[(int64_t)r * kHI + tid];
+  {
+    // block-table slice of the CTA's entry range
+    const int32_t blk0 = g.t0 * kTile / kRowsPerBlock;
+    const int32_t nblk = min(kTblMax, (g.nt * kTile + kRowsPerBlock - 1) / kRowsPerBlock);
+    for (int j = tid; j < nblk; j += kThreads) {
+      const int32_t lb = blk0 + j;
+      int32_t pb = -1;
+      if (g.seq >= 0 && g.seq < a.bt.num_seqs && lb < a.bt.stride) {
+        pb = a.bt.table[(int64_t)g.seq * a.bt.stride + lb];
+        if (pb >= a.cache.num_blocks) pb = -1;
+      }
+      if (pb < 0 && lb * kRowsPerBlock < g.n) record_error(a.err, CSA_ERR_DEVICE_BOUNDS);
+      ms.tbl[j] = pb;
+    }
+  }
   if (warp == 7) tmem_alloc(&ms.tmem_base, kTmemCols);
-  // Q_idx^T: bf16, 128B-swizzled K-major, rows = heads
-  for (int x = tid; x < kHI * kDI / 2; x += kThreads) {
-    const int h = x / (kDI / 2), d = 2 * (x % (kDI / 2));
-    const int64_t qb = ((int64_t)r * kHI + h) * kDI + d;
-    const uint32_t v = (uint32_t)f32_to_bf16(load_elem(a.q_idx, a.q_dtype, qb)) |
-                       ((uint32_t)f32_to_bf16(load_elem(a.q_idx, a.q_dtype, qb + 1)) << 16);
-    *reinterpret_cast<uint32_t*>(smem + kOffQ + sw128_offset(h, d, kHI)) = v;
+  // Q_idx^T: bf16, 128B-swizzled K-major, rows = heads; 8 dims per 16-byte
+  // piece, every thread's loads issued before its stores
+  {
+    constexpr int kPieces = kHI * kDI / 8;
+    constexpr int kPer = kPieces / kThreads;
+    uint32_t w[kPer][4];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int x = tid + u * kThreads;
+      const int64_t qb = (int64_t)r * kHI * kDI + 8 * x;
+      if (a.q_dtype == CSA_BF16) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q_idx) + qb));
+        w[u][0] = v.x; w[u][1] = v.y; w[u][2] = v.z; w[u][3] = v.w;
+      } else {
+        const float4* src = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.q_idx) + qb);
+        const float4 v0 = __ldg(src), v1 = __ldg(src + 1);
+        w[u][0] = (uint32_t)f32_to_bf16(v0.x) | ((uint32_t)f32_to_bf16(v0.y) << 16);
+        w[u][1] = (uint32_t)f32_to_bf16(v0.z) | ((uint32_t)f32_to_bf16(v0.w) << 16);
+        w[u][2] = (uint32_t)f32_to_bf16(v1.x) | ((uint32_t)f32_to_bf16(v1.y) << 16);
+        w[u][3] = (uint32_t)f32_to_bf16(v1.z) | ((uint32_t)f32_to_bf16(v1.w) << 16);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int x = tid + u * kThreads;
+      const int h = x / (kDI / 8), d0 = 8 * (x % (kDI / 8));
+      *reinterpret_cast<uint4*>(smem + kOffQ + sw128_offset(h, d0, kHI)) = make_uint4(w[u][0], w[u][1], w[u][2], w[u][3]);
+    }
   }
   fence_proxy_async();
+  pdl_trigger();
+  pdl_wait();  // caches and the score scratch may be in use by the previous launch until here
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -284,9 +326,12 @@ cudaError_t launch_indexer_tc(const IndexerArgs& a, int32_t n_rows, cudaStream_t
   const int32_t tiles = (a.max_n + kTile - 1) / kTile;
   int32_t splits = n_rows > 0 ? (148 + n_rows - 1) / n_rows : 1;
   if (splits > tiles) splits = tiles;
+  // every CTA's range must fit the cached block-table slice (kTblMax blocks)
+  const int32_t tiles_per_cta_max = kTblMax * kRowsPerBlock / kTile;
+  const int32_t min_splits = (tiles + tiles_per_cta_max - 1) / tiles_per_cta_max;
+  if (splits < min_splits) splits = min_splits;
   if (splits < 1) splits = 1;
-  indexer_tc_kernel<<<dim3(n_rows, splits), kThreads, kSmemBytes, s>>>(a);
-  return cudaGetLastError();
+  return launch_k(indexer_tc_kernel, dim3(n_rows, splits), dim3(kThreads), kSmemBytes, s, 0, a);
 }
 
 }  // namespace csa

@@ -16,6 +16,8 @@ constexpr int kThreads = 128;
 
 __global__ void __launch_bounds__(kThreads) store_kernel(const StoreArgs a) {
   __shared__ float red[32];
+  pdl_trigger();
+  pdl_wait();
   const int j = blockIdx.x;
   const csa_paged& c = a.cache;
   const int D = c.dim;
@@ -67,8 +69,7 @@ __global__ void __launch_bounds__(kThreads) store_kernel(const StoreArgs a) {
 
 cudaError_t launch_store(const StoreArgs& a, int32_t n, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
-  store_kernel<<<n, kThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_k(store_kernel, dim3(n), dim3(kThreads), 0, s, 0, a);
 }
 
 }  // namespace csa

@@ -34,6 +34,8 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
   __shared__ uint32_t sh_digit, sh_rem, sh_eq_base;
   __shared__ int out_ctr;
 
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x;
   int n = n_visible(a.pos[r], a.ratio, a.window);
   if (n > a.max_n) {
@@ -236,6 +238,8 @@ __global__ void __launch_bounds__(kChunkThreads) topk_chunk_kernel(const TopkArg
                                                                     int32_t* cand_idx, int32_t* cand_cnt,
                                                                     int n_chunks) {
   __shared__ uint32_t keys[kChunk];
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x, c = blockIdx.y;
   int n = n_visible(a.pos[r], a.ratio, a.window);
   if (n > a.max_n) {
@@ -268,6 +272,8 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(const TopkArg
   uint32_t* keys = msm;                                            // [n_chunks * k]
   int32_t* idx = reinterpret_cast<int32_t*>(msm + n_chunks * a.k);  // [n_chunks * k]
   __shared__ int32_t off[65];
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x;
   if (threadIdx.x == 0) {
     int32_t t = 0;
@@ -312,15 +318,13 @@ size_t topk_candidate_bytes(int32_t n_rows, int32_t max_n, int32_t k) {
 cudaError_t launch_topk(const TopkArgs& a, int32_t n_rows, void* cand, cudaStream_t s) {
   if (n_rows == 0 || a.k == 0) return cudaSuccess;
   if (!topk_two_stage(a.max_n, a.k) || cand == nullptr) {
-    topk_kernel<<<n_rows, kThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_k(topk_kernel, dim3(n_rows), dim3(kThreads), 0, s, 0, a);
   }
   const int32_t nc = topk_chunks(a.max_n);
   uint32_t* ck = reinterpret_cast<uint32_t*>(cand);
   int32_t* ci = reinterpret_cast<int32_t*>(ck + (size_t)n_rows * nc * a.k);
   int32_t* cc = ci + (size_t)n_rows * nc * a.k;
-  topk_chunk_kernel<<<dim3(n_rows, nc), kChunkThreads, 0, s>>>(a, ck, ci, cc, nc);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_k(topk_chunk_kernel, dim3(n_rows, nc), dim3(kChunkThreads), 0, s, 0, a, ck, ci, cc, nc);
   if (e != cudaSuccess) return e;
   const size_t smem = (size_t)nc * a.k * 8;
   static size_t smem_set = 0;
@@ -329,8 +333,8 @@ cudaError_t launch_topk(const TopkArgs& a, int32_t n_rows, void* cand, cudaStrea
     if (e != cudaSuccess) return e;
     smem_set = smem;
   }
-  topk_merge_kernel<<<n_rows, kMergeThreads, smem, s>>>(a, ck, ci, cc, nc);
-  return cudaGetLastError();
+  return launch_k(topk_merge_kernel, dim3(n_rows), dim3(kMergeThreads), smem, s, 0, a, (const uint32_t*)ck,
+                  (const int32_t*)ci, (const int32_t*)cc, nc);
 }
 
 }  // namespace csa
