@@ -14,24 +14,28 @@
 //   S^T [128 keys x 64 heads]  = K_tile [128 x 512] . Q^T [512 x 64]
 //   O^T [512 dims x 64 heads] += K_tile^T [512 x 128] . P^T [128 x 64]   (4 chunks of 128 dims)
 //
-// The key tile sits in shared memory once, 128B-swizzled with keys as rows:
-// read K-major it is the A operand of S^T; read MN-major it is the A operand of
-// O^T (values = keys).  Q^T (pre-rotated, pre-scaled by scale*log2 e) and P^T
-// are the B operands.  TMEM: S^T in columns 0..63, O^T chunk c in 64+64c.
+// Key rows are gathered into a ring of four 32 KB slots (128 keys x 128 dims,
+// 128B-swizzled, keys as rows): read K-major a slot is an A operand of S^T,
+// read MN-major an A operand of O^T (values = keys).  Q^T (pre-rotated,
+// pre-scaled by scale*log2 e) and P^T are the B operands.  Each tile passes
+// through the ring twice -- for S^T, then again from L2 for O^T -- in the
+// order S_0, S_1, O_0, S_2, O_1, ..., so that the softmax of tile t overlaps
+// S_{t+1} and the ring never waits for a softmax.  TMEM: S^T double-buffered
+// in columns 0..127, O^T chunk c in 128+64c.
 //
 // Warp roles: warps 0-3 own TMEM lanes (thread t <-> key t of the tile for the
-// softmax, dim t of a chunk in the epilogue); warps 4-6 gather the tile's rows
-// from the paged caches (cp.async for bf16, load + convert for e4m3, whose
-// per-row scale is folded into the logits and into P); warp 7 allocates TMEM
-// and one lane issues the MMAs.  Eight warps leave 255 registers per thread.  The running per-head max is only raised when
-// a logit exceeds it by more than 2^8; raising it rescales O^T in TMEM.
+// softmax, dim t of a chunk in the epilogue); warps 4-6 gather the rows from
+// the paged caches (cp.async for bf16, load + convert for e4m3, whose per-row
+// scale is folded into the logits and into P); warp 7 allocates TMEM and one
+// lane issues the MMAs.  Eight warps leave 255 registers per thread.  The
+// running per-head max is only raised when a logit exceeds it by more than
+// 2^8; raising it rescales O^T in TMEM.
 //
 // A row's key list may be split over S = 1, 2, 4 or 8 CTAs launched as one
-// cluster.  Each CTA stages its unnormalised O (fp32, [64 heads][512]) with its
-// per-head max and denominator in its own shared memory; after a cluster
-// barrier CTA r merges heads [r*64/S, (r+1)*64/S) by reading the others'
-// staging through distributed shared memory, normalises, rotates back and
-// stores.  No partial result goes through global memory.
+// cluster.  Each CTA writes its unnormalised O with its per-head max and
+// denominator to the workspace (L2); after a cluster barrier CTA m merges
+// heads [m*64/S, (m+1)*64/S), normalises, rotates back and stores, then
+// discards the consumed workspace lines from L2.
 
 #include "csa_kernels.h"
 #include "tc_ptx.cuh"
@@ -51,22 +55,24 @@ constexpr uint32_t kPBytes = kTile * kH * 2;          // 16 KB
 constexpr uint32_t kOffQ = 0, kOffK = kQBytes, kOffP = kOffK + kChunks * kChunkBytes;
 constexpr uint32_t kOffMisc = kOffP + kPBytes;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColO = 64;
+constexpr uint32_t kColS = 0, kColO = 128;  // S^T double-buffered in 0..127, O^T chunk c at 128 + 64c
 constexpr float kRescaleMargin = 8.0f;  // log2 units
 
 struct Misc {
-  uint64_t kfull[kChunks], kfree[kChunks], s_full, p_full, p_free, q_full;
+  uint64_t kfull[kChunks], kfree[kChunks], s_full[2], kmeta[2], p_full, p_free, q_full, mma_done, recv;
   uint32_t tmem_base;
   int32_t abort;
-  float M[kH];          // running per-head max (log2 domain), shared by the softmax threads
-  float red[4][kH];     // per-warp reductions
+  alignas(16) float M[kH];  // running per-head max (log2 domain), shared by the softmax threads
+  float red[4][kH];     // per-warp reductions; merge weights
+  float amax[kThreads / 32][32];  // per-warp head maxima of the merged output
   float alpha[kH];      // rescale factor of the last max raise
-  float L[kH];          // softmax denominators of the slice
+  alignas(16) float L[kH];  // softmax denominators of the slice
+  alignas(16) float rM[8][32], rL[8][32];  // merged heads' max and denominator of each slice (split rows)
   float rc[kMaxRopePairs], rs[kMaxRopePairs];  // cos / sin of each rotary pair at the row's position
   float kscale[2][kTile];
   int8_t kvalid[2][kTile];
-  const uint8_t* rowptr[2][kTile];  // producer-private, by tile parity
-  float rowscale[2][kTile];
+  const uint8_t* rowptr[3][kTile];  // producer-private, by tile mod 3
+  float rowscale[3][kTile];
 };
 constexpr uint32_t kSmemBytes = kOffMisc + sizeof(Misc) + 1024;
 
@@ -129,33 +135,62 @@ __device__ __forceinline__ const uint8_t* key_row(const AttnArgs& a, const Geo& 
   return reinterpret_cast<const uint8_t*>(c->data) + prow * (int64_t)kD * (fp8 ? 1 : 2);
 }
 
+// Phase i of the tensor pipe over a slice of n tiles.  Every key tile passes
+// through the key ring twice, once for S^T and once more (from L2) for O^T,
+// in the order S_0, S_1, O_0, S_2, O_1, ..., S_{n-1}, O_{n-2}, O_{n-1}: the
+// softmax of tile t runs while the tensor pipe computes S_{t+1}, and the ring
+// keeps streaming instead of idling between a tile's S^T and its O^T.
+__device__ __forceinline__ int phase_tile(int i, int n, bool& is_s) {
+  if (i == 0) {
+    is_s = true;
+    return 0;
+  }
+  if (i == 2 * n - 1) {
+    is_s = false;
+    return n - 1;
+  }
+  is_s = (i & 1) != 0;
+  return is_s ? (i + 1) >> 1 : (i >> 1) - 1;
+}
+
+// Producers: one 32 KB ring slot per 128-dim chunk of the current phase's tile.
+// bf16 rows are copied with cp.async, each thread's copies arriving on the
+// slot's barrier as they land (the MMA issuer fences them into the async
+// proxy); e4m3 rows are converted through registers.
 __device__ void producer_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Misc& ms, int pt) {
   const bool fp8 = a.comp.dtype == CSA_E4M3;
   const uint32_t kbase = smem_u32(smem + kOffK);
   const uint32_t row_bytes = fp8 ? kD : 2 * kD;
-  // row addresses of tile 0; later tiles' addresses are looked up one tile ahead
-  for (int slot = pt; slot < kTile; slot += kProducers)
-    ms.rowptr[0][slot] = g.n_tiles > 0 ? key_row(a, g, 0, slot, fp8, ms.rowscale[0][slot]) : nullptr;
-  named_bar(2, kProducers);
-  for (int t = 0; t < g.n_tiles; ++t) {
-    const int par = t & 1;
-    for (int slot = pt; slot < kTile; slot += kProducers) {
-      ms.kvalid[par][slot] = ms.rowptr[par][slot] != nullptr;
-      ms.kscale[par][slot] = ms.rowscale[par][slot];
-    }
+  const int n = g.n_tiles;
+  if (n > 0)
+    for (int slot = pt; slot < kTile; slot += kProducers)
+      ms.rowptr[0][slot] = key_row(a, g, 0, slot, fp8, ms.rowscale[0][slot]);
+  for (int i = 0; i < 2 * n; ++i) {
+    bool is_s;
+    const int t = phase_tile(i, n, is_s), par = t & 1, buf = t % 3;
+    if (is_s) named_bar(2, kProducers);  // tile t's row addresses are complete
     for (int c = 0; c < kChunks; ++c) {
-      if (t > 0) wait_or_abort(ms, &ms.kfree[c], (t - 1) & 1, a.err);
+      if (i > 0) wait_or_abort(ms, &ms.kfree[c], (i - 1) & 1, a.err);
+      if (is_s && c == 0) {
+        // key validity and scale of tile t for the softmax (its previous reader, the
+        // softmax of tile t-2, is done: O_{t-2} has consumed its P)
+        for (int slot = pt; slot < kTile; slot += kProducers) {
+          ms.kvalid[par][slot] = ms.rowptr[buf][slot] != nullptr;
+          ms.kscale[par][slot] = ms.rowscale[buf][slot];
+        }
+        mbar_arrive(&ms.kmeta[par]);
+      }
       const uint32_t cbase = kbase + c * kChunkBytes;
       if (!fp8) {
         // 16 consecutive threads per key row: 256 contiguous bytes = dims [128c, 128c+128)
         for (int x = pt; x < kTile * 16; x += kProducers) {
           const uint32_t key = x >> 4, piece = x & 15;
-          const uint8_t* rp = ms.rowptr[par][key];
+          const uint8_t* rp = ms.rowptr[buf][key];
           const uint32_t dst = cbase + (piece >> 3) * kAtomBytes + (key >> 3) * 1024 + (key & 7) * 128 +
                                (((piece & 7) ^ (key & 7)) << 4);
           cp_async16(dst, rp ? rp + c * 256 + piece * 16 : a.comp.data, rp ? 16u : 0u);
         }
-        cp_async_commit();
+        cp_async_arrive_noinc(&ms.kfull[c]);
       } else {
         // 8 consecutive threads per key row: 128 code bytes -> 128 bf16 (exact)
         constexpr int kIters = (kTile * 8 + kProducers - 1) / kProducers;
@@ -165,7 +200,7 @@ __device__ void producer_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mi
           const int x = pt + it * kProducers;
           raw[it] = make_uint4(0, 0, 0, 0);
           if (x < kTile * 8) {
-            const uint8_t* rp = ms.rowptr[par][x >> 3];
+            const uint8_t* rp = ms.rowptr[buf][x >> 3];
             if (rp) raw[it] = __ldg(reinterpret_cast<const uint4*>(rp + c * 128 + (x & 7) * 16));
           }
         }
@@ -191,35 +226,21 @@ __device__ void producer_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mi
                 make_uint4(outw[half * 4], outw[half * 4 + 1], outw[half * 4 + 2], outw[half * 4 + 3]);
           }
         }
+        fence_proxy_async();
+        mbar_arrive(&ms.kfull[c]);
       }
     }
-    // while tile t is in flight: the next tile's row addresses, and its rows into L2
-    if (t + 1 < g.n_tiles) {
+    if (is_s && t + 1 < n) {
+      // tile t+1's row addresses, and its rows into L2, while the ring drains; the
+      // buffer was last read by O_{t-2}, which every producer has issued by now
+      named_bar(2, kProducers);
+      const int nb = (t + 1) % 3;
       for (int slot = pt; slot < kTile; slot += kProducers) {
-        const uint8_t* nx = key_row(a, g, t + 1, slot, fp8, ms.rowscale[par ^ 1][slot]);
-        ms.rowptr[par ^ 1][slot] = nx;
-        if (nx) prefetch_l2(nx, row_bytes);
+        const uint8_t* rp = key_row(a, g, t + 1, slot, fp8, ms.rowscale[nb][slot]);
+        ms.rowptr[nb][slot] = rp;
+        if (rp) prefetch_l2(rp, row_bytes);
       }
     }
-    if (!fp8) {
-      cp_async_wait<3>();
-      fence_proxy_async();
-      mbar_arrive(&ms.kfull[0]);
-      cp_async_wait<2>();
-      fence_proxy_async();
-      mbar_arrive(&ms.kfull[1]);
-      cp_async_wait<1>();
-      fence_proxy_async();
-      mbar_arrive(&ms.kfull[2]);
-      cp_async_wait<0>();
-      fence_proxy_async();
-      mbar_arrive(&ms.kfull[3]);
-    } else {
-      fence_proxy_async();
-#pragma unroll
-      for (int c = 0; c < kChunks; ++c) mbar_arrive(&ms.kfull[c]);
-    }
-    named_bar(2, kProducers);  // rowptr is rewritten for the next tile
   }
   cp_async_wait<0>();
 }
@@ -229,35 +250,43 @@ __device__ void producer_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mi
 __device__ void mma_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Misc& ms, uint32_t tmem) {
   constexpr uint32_t idesc_s = idesc_bf16(128, kH, 0, 0);
   constexpr uint32_t idesc_o = idesc_bf16(128, kH, 1, 1);
-  const uint32_t kbase = smem_u32(smem + kOffK), qbase = smem_u32(smem + kOffQ), pbase = smem_u32(smem + kOffP);
+  // descriptors of the ring, Q^T and P^T; every operand below is one of these plus a constant
+  const uint64_t a_s = sdesc_sw128(smem_u32(smem + kOffK), 16, 1024);
+  const uint64_t b_s = sdesc_sw128(smem_u32(smem + kOffQ), 16, 1024);
+  const uint64_t a_o = sdesc_sw128(smem_u32(smem + kOffK), kAtomBytes, 1024);
+  const uint64_t b_o = sdesc_sw128(smem_u32(smem + kOffP), kAtomBytes, 1024);
+  const int n = g.n_tiles;
   wait_or_abort(ms, &ms.q_full, 0, a.err);
-  for (int t = 0; t < g.n_tiles; ++t) {
-    const uint32_t par = t & 1;
+  for (int i = 0; i < 2 * n; ++i) {
+    bool is_s;
+    const int t = phase_tile(i, n, is_s);
+    if (!is_s) wait_or_abort(ms, &ms.p_full, t & 1, a.err);
+    const uint32_t d_s = tmem + kColS + 64 * (t & 1);
+#pragma unroll
     for (int c = 0; c < kChunks; ++c) {
-      wait_or_abort(ms, &ms.kfull[c], par, a.err);
+      wait_or_abort(ms, &ms.kfull[c], i & 1, a.err);
+      fence_proxy_async();  // the slot was written through the generic proxy
       tc_fence_after();
+      if (is_s) {
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t k0 = c * 128 + ks * 16;  // first dim of this K step
-        const uint64_t ad = sdesc_sw128(kbase + c * kChunkBytes + (ks >> 2) * kAtomBytes + (ks & 3) * 32, 16, 1024);
-        const uint64_t bd = sdesc_sw128(qbase + (k0 >> 6) * (kH * 128) + (k0 & 63) * 2, 16, 1024);
-        mma_bf16(tmem + kColS, ad, bd, idesc_s, (c | ks) != 0);
-      }
-    }
-    mma_commit(&ms.s_full);
-    wait_or_abort(ms, &ms.p_full, par, a.err);
-    tc_fence_after();
-    for (int c = 0; c < kChunks; ++c) {
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t k0 = c * 128 + ks * 16;  // first dim of this K step
+          mma_bf16(d_s, a_s + ((c * kChunkBytes + (ks >> 2) * kAtomBytes + (ks & 3) * 32) >> 4),
+                   b_s + (((k0 >> 6) * (kH * 128) + (k0 & 63) * 2) >> 4), idesc_s, (c | ks) != 0);
+        }
+      } else {
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {  // 16 keys per step: two 8-key groups of 1 KB
-        const uint64_t ad = sdesc_sw128(kbase + c * kChunkBytes + ks * 2048, kAtomBytes, 1024);
-        const uint64_t bd = sdesc_sw128(pbase + ks * 2048, kAtomBytes, 1024);
-        mma_bf16(tmem + kColO + 64 * c, ad, bd, idesc_o, (t > 0 || ks > 0) ? 1u : 0u);
+        for (int ks = 0; ks < 8; ++ks)  // 16 keys per step: two 8-key groups of 1 KB
+          mma_bf16(tmem + kColO + 64 * c, a_o + ((c * kChunkBytes + ks * 2048) >> 4), b_o + ((ks * 2048) >> 4),
+                   idesc_o, (t > 0 || ks > 0) ? 1u : 0u);
       }
       mma_commit(&ms.kfree[c]);
     }
-    mma_commit(&ms.p_free);
+    mma_commit(is_s ? &ms.s_full[t & 1] : &ms.p_free);
   }
+  // nothing may still write TMEM when it is released, even after a timeout
+  mma_commit(&ms.mma_done);
+  mbar_wait(&ms.mma_done, 0);
 }
 
 // ------------------------------------------------------------------ softmax + epilogue
@@ -279,64 +308,95 @@ __device__ __forceinline__ void warp_reduce64(const float* v, Misc& ms, int st) 
   }
 }
 
+// Rotation of the pair (d, d+1) at the row's position (rotary dims only), the
+// logit scale, and bf16 rounding of the pair.
+__device__ __forceinline__ uint32_t rot_pack(float q0, float q1, int d, float qs, int R, const Misc& ms) {
+  if (d >= kD - R) {
+    const float cs = ms.rc[(d - (kD - R)) / 2], sn = ms.rs[(d - (kD - R)) / 2];
+    const float t0 = q0 * cs - q1 * sn;
+    q1 = q0 * sn + q1 * cs;
+    q0 = t0;
+  }
+  return (uint32_t)f32_to_bf16(q0 * qs) | ((uint32_t)f32_to_bf16(q1 * qs) << 16);
+}
+
 // Q^T operand: the row's 64 heads rotated at p, scaled by scale * log2(e),
-// rounded to bf16, 128B-swizzled K-major (rows = heads).  The 128 softmax
-// threads fill it with 16-byte loads while the producers gather the first
-// key tile, then release the MMA issuer through q_full.
-__device__ void fill_q(const AttnArgs& a, const Geo& g, uint8_t* smem, Misc& ms, int st) {
+// rounded to bf16, 128B-swizzled K-major (rows = heads).  bf16 rows are
+// copied raw with cp.async as the very first requests of the CTA (ahead of the
+// key gathers, which wait for the previous launch) and then transformed in
+// place, each thread on the pieces it copied itself; fp32 rows go through
+// registers.  The softmax threads then release the MMA issuer through q_full.
+// The query rows, seq_id and pos are inputs of the step, not written by the
+// library's preceding launches, so they are read before griddepcontrol.wait.
+__device__ void fill_q(const AttnArgs& a, uint8_t* smem, Misc& ms, int st) {
   const float qs = a.scale * 1.4426950408889634f;
   const int R = a.rope.rope_dim;
   const int64_t rb = (int64_t)blockIdx.x * a.heads * kD;
   constexpr int kPieces = kH * (kD / 8);  // 16-byte pieces of bf16 (8 dims each)
-  constexpr int kBatch = 8;               // loads in flight per thread
-  for (int x0 = st; x0 < kPieces; x0 += kSoftmax * kBatch) {
-    float q[kBatch][8];
+  if (a.q_dtype == CSA_BF16) {
+    const uint16_t* src = reinterpret_cast<const uint16_t*>(a.q) + rb;
+    const uint32_t qbase = smem_u32(smem + kOffQ);
+    for (int x = st; x < kPieces; x += kSoftmax) {
+      const int h = x >> 6, d0 = (x & 63) * 8;
+      cp_async16(qbase + sw128_offset(h, d0, kH), src + h * kD + d0, 16u);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    for (int x = st; x < kPieces; x += kSoftmax) {
+      const int h = x >> 6, d0 = (x & 63) * 8;
+      uint4* p = reinterpret_cast<uint4*>(smem + kOffQ + sw128_offset(h, d0, kH));
+      const uint4 v = *p;
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[4];
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int x = x0 + u * kSoftmax;
-      const int h = x / (kD / 8), d0 = 8 * (x % (kD / 8));
-      if (a.q_dtype == CSA_BF16) {
-        const uint4 v =
-            __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q) + rb + h * kD + d0));
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      for (int e = 0; e < 4; ++e)
+        o[e] = rot_pack(bf16_to_f32((uint16_t)(w[e] & 0xFFFF)), bf16_to_f32((uint16_t)(w[e] >> 16)), d0 + 2 * e, qs,
+                        R, ms);
+      *p = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  } else {
+    constexpr int kBatch = 8;  // loads in flight per thread
+    for (int x0 = st; x0 < kPieces; x0 += kSoftmax * kBatch) {
+      float q[kBatch][8];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          q[u][2 * e] = bf16_to_f32((uint16_t)(w[e] & 0xFFFF));
-          q[u][2 * e + 1] = bf16_to_f32((uint16_t)(w[e] >> 16));
-        }
-      } else {
-        const float4* src = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.q) + rb + h * kD + d0);
-        const float4 v0 = __ldg(src), v1 = __ldg(src + 1);
+      for (int u = 0; u < kBatch; ++u) {
+        const int x = x0 + u * kSoftmax;
+        const int h = x >> 6, d0 = (x & 63) * 8;
+        const float4* p4 = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.q) + rb + h * kD + d0);
+        const float4 v0 = __ldg(p4), v1 = __ldg(p4 + 1);
         q[u][0] = v0.x; q[u][1] = v0.y; q[u][2] = v0.z; q[u][3] = v0.w;
         q[u][4] = v1.x; q[u][5] = v1.y; q[u][6] = v1.z; q[u][7] = v1.w;
       }
-    }
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int x = x0 + u * kSoftmax;
-      const int h = x / (kD / 8), d0 = 8 * (x % (kD / 8));
-      uint32_t o[4];
+      for (int u = 0; u < kBatch; ++u) {
+        const int x = x0 + u * kSoftmax;
+        const int h = x >> 6, d0 = (x & 63) * 8;
+        uint32_t o[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float q0 = q[u][2 * e], q1 = q[u][2 * e + 1];
-        const int d = d0 + 2 * e;
-        if (d >= kD - R) {
-          const float cs = ms.rc[(d - (kD - R)) / 2], sn = ms.rs[(d - (kD - R)) / 2];
-          const float t0 = q0 * cs - q1 * sn;
-          q1 = q0 * sn + q1 * cs;
-          q0 = t0;
-        }
-        o[e] = (uint32_t)f32_to_bf16(q0 * qs) | ((uint32_t)f32_to_bf16(q1 * qs) << 16);
+        for (int e = 0; e < 4; ++e) o[e] = rot_pack(q[u][2 * e], q[u][2 * e + 1], d0 + 2 * e, qs, R, ms);
+        *reinterpret_cast<uint4*>(smem + kOffQ + sw128_offset(h, d0, kH)) = make_uint4(o[0], o[1], o[2], o[3]);
       }
-      *reinterpret_cast<uint4*>(smem + kOffQ + sw128_offset(h, d0, kH)) = make_uint4(o[0], o[1], o[2], o[3]);
     }
   }
   fence_proxy_async();
   mbar_arrive(&ms.q_full);
 }
 
+// The 64 head columns of one O^T chunk for this thread's TMEM lane (zeros for
+// an empty slice): four loads in flight, one wait.
+__device__ __forceinline__ void load_o_chunk(uint32_t taddr, bool any, float* o) {
+  if (any) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) tmem_ld16(taddr + 16 * i, o + 16 * i);
+    tmem_wait_ld();
+  } else {
+#pragma unroll
+    for (int h = 0; h < kH; ++h) o[h] = 0.f;
+  }
+}
+
 __device__ void softmax_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Misc& ms, uint32_t tmem, int st) {
-  fill_q(a, g, smem, ms, st);
+  fill_q(a, smem, ms, st);
   const int w = st >> 5;
   const uint32_t lane_addr = tmem + ((uint32_t)(w * 32) << 16);
   float lsum[kH];
@@ -345,13 +405,14 @@ __device__ void softmax_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mis
   uint8_t* prow = smem + kOffP + (st >> 3) * 1024 + (st & 7) * 128;
 
   for (int t = 0; t < g.n_tiles; ++t) {
-    const uint32_t par = t & 1;
-    wait_or_abort(ms, &ms.s_full, par, a.err);
+    const uint32_t par = t & 1, use = (t >> 1) & 1;
+    wait_or_abort(ms, &ms.s_full[par], use, a.err);
     tc_fence_after();
     float x[kH];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) tmem_ld16(lane_addr + kColS + 16 * i, x + 16 * i);
+    for (int i = 0; i < 4; ++i) tmem_ld16(lane_addr + kColS + 64 * par + 16 * i, x + 16 * i);
     tmem_wait_ld();
+    wait_or_abort(ms, &ms.kmeta[par], use, a.err);
     const bool valid = ms.kvalid[par][st] != 0;
     const float ksc = ms.kscale[par][st];
     bool need = false;
@@ -372,7 +433,9 @@ __device__ void softmax_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mis
       }
       named_bar(1, kSoftmax);
       if (t > 0) {
-        // O^T of the previous tiles is complete (the S^T commit of this tile follows it)
+        // rescale O^T once it holds exactly the tiles before t (O_{t-1} complete)
+        wait_or_abort(ms, &ms.p_free, (t - 1) & 1, a.err);
+        tc_fence_after();
 #pragma unroll
         for (int c = 0; c < kChunks; ++c) {
 #pragma unroll
@@ -390,26 +453,24 @@ __device__ void softmax_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mis
 #pragma unroll
       for (int h = 0; h < kH; ++h) lsum[h] *= ms.alpha[h];
     }
-    // P buffer free: O^T of the previous tile has consumed it (already complete
-    // here, since the tensor pipe ran it before this tile's S^T)
-    if (t > 0) wait_or_abort(ms, &ms.p_free, (t - 1) & 1, a.err);
     // probabilities of this key for every head, 8 heads per 16-byte piece of the
     // key's 128-byte P^T row; P carries the key's dequant scale
+    uint32_t pw[kH / 2];
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      uint32_t w4[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int h = 8 * c + 2 * e;
-        const float m0 = ms.M[h], m1 = ms.M[h + 1];
-        const float p0 = (x[h] == -INFINITY || m0 == -INFINITY) ? 0.f : fast_exp2(x[h] - m0);
-        const float p1 = (x[h + 1] == -INFINITY || m1 == -INFINITY) ? 0.f : fast_exp2(x[h + 1] - m1);
-        lsum[h] += p0;
-        lsum[h + 1] += p1;
-        w4[e] = (uint32_t)f32_to_bf16(p0 * ksc) | ((uint32_t)f32_to_bf16(p1 * ksc) << 16);
-      }
-      *reinterpret_cast<uint4*>(prow + ((c ^ (st & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+    for (int h = 0; h < kH; h += 2) {
+      const float m0 = ms.M[h], m1 = ms.M[h + 1];
+      const float p0 = (x[h] == -INFINITY || m0 == -INFINITY) ? 0.f : fast_exp2(x[h] - m0);
+      const float p1 = (x[h + 1] == -INFINITY || m1 == -INFINITY) ? 0.f : fast_exp2(x[h + 1] - m1);
+      lsum[h] += p0;
+      lsum[h + 1] += p1;
+      pw[h / 2] = (uint32_t)f32_to_bf16(p0 * ksc) | ((uint32_t)f32_to_bf16(p1 * ksc) << 16);
     }
+    // the P buffer is free once O_{t-1} has consumed it
+    if (t > 0) wait_or_abort(ms, &ms.p_free, (t - 1) & 1, a.err);
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      *reinterpret_cast<uint4*>(prow + ((c ^ (st & 7)) << 4)) =
+          make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
     fence_proxy_async();
     tc_fence_before();
     mbar_arrive(&ms.p_full);
@@ -422,23 +483,37 @@ __device__ void softmax_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mis
   named_bar(1, kSoftmax);
   if (st < kH) ms.L[st] = (ms.red[0][st] + ms.red[1][st]) + (ms.red[2][st] + ms.red[3][st]);
   named_bar(1, kSoftmax);  // ms.L[h] = sum over the slice's keys of 2^(x - M[h])
-  // stage the slice's unnormalised O^T as [64 heads][512 dims] fp32 in the idle key buffer
-  float* stage = reinterpret_cast<float*>(smem + kOffK);
+  const int S = gridDim.y;
+  if (S == 1) {
+    // stage the row's unnormalised O^T as [64 heads][512 dims] fp32 in the idle key buffer
+    float* stage = reinterpret_cast<float*>(smem + kOffK);
+    for (int c = 0; c < kChunks; ++c) {
+      float o[kH];
+      load_o_chunk(lane_addr + kColO + 64 * c, g.n_tiles > 0, o);
+#pragma unroll
+      for (int h = 0; h < kH; ++h) stage[h * kD + 128 * c + st] = o[h];
+    }
+    return;
+  }
+  // split row: stage the slice's unnormalised O in bf16 in the idle ring, grouped
+  // by the CTA that merges each head: [merger][512 dims][heads of the merger]
+  const int per = kH / S;
+  uint8_t* stage = smem + kOffK;
   for (int c = 0; c < kChunks; ++c) {
+    float o[kH];
+    load_o_chunk(lane_addr + kColO + 64 * c, g.n_tiles > 0, o);
+    const int d = 128 * c + st;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float o[16];
-      if (g.n_tiles > 0) {
-        tmem_ld16(lane_addr + kColO + 64 * c + 16 * i, o);
-        tmem_wait_ld();
-      } else {
+    for (int q = 0; q < kH / 8; ++q) {
+      const int m = 8 * q / per, hh = 8 * q - m * per;
+      uint32_t w[4];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) o[j] = 0.f;
-      }
-#pragma unroll
-      for (int j = 0; j < 16; ++j) stage[(16 * i + j) * kD + 128 * c + st] = o[j];
+      for (int e = 0; e < 4; ++e)
+        w[e] = (uint32_t)f32_to_bf16(o[8 * q + 2 * e]) | ((uint32_t)f32_to_bf16(o[8 * q + 2 * e + 1]) << 16);
+      *reinterpret_cast<uint4*>(stage + (((size_t)m * kD + d) * per + hh) * 2) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
+  fence_proxy_async();  // the copy engine reads the staging
 }
 
 // Inverse rotation at p and store of head h of row r; lane holds dims [16 lane, 16 lane + 16).
@@ -482,66 +557,134 @@ __device__ void store_head16(const AttnArgs& a, const Misc& ms, int r, int h, fl
   }
 }
 
-// All 8 warps: merge this CTA's share of the heads over the S CTAs of the cluster.
-// Every peer's M, L and staged O are read through generic cluster pointers,
-// all loads of a head issued before any is used.
-__device__ void merge_role(const AttnArgs& a, uint8_t* smem, Misc& ms, int64_t p) {
-  const int S = gridDim.y;
-  const uint32_t rank = S > 1 ? cluster_rank() : 0;
-  const int per = kH / S;
+// Unsplit row: all 8 warps normalise the staged O (8 heads a warp) and store.
+__device__ void finish_local(const AttnArgs& a, uint8_t* smem, const Misc& ms) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* stage = reinterpret_cast<const float*>(smem + kOffK);
-  const float* Mp[8];
-  const float* Lp[8];
-  const float* Sp[8];
-#pragma unroll
-  for (int s = 0; s < 8; ++s) {
-    const uint32_t rk = s < S ? (uint32_t)s : 0u;
-    Mp[s] = S > 1 ? map_shared_ptr(ms.M, rk) : ms.M;
-    Lp[s] = S > 1 ? map_shared_ptr(ms.L, rk) : ms.L;
-    Sp[s] = S > 1 ? map_shared_ptr(stage, rk) : stage;
-  }
-  for (int hh = warp; hh < per; hh += kThreads / 32) {
-    const int h = (int)rank * per + hh;
-    float m[8], l[8];
-    float4 x[8][4];
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      if (s < S) {
-        m[s] = Mp[s][h];
-        l[s] = Lp[s][h];
-        const float4* src = reinterpret_cast<const float4*>(Sp[s] + h * kD + 16 * lane);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) x[s][q] = src[q];
-      }
-    }
-    float mg = -INFINITY;
-#pragma unroll
-    for (int s = 0; s < 8; ++s)
-      if (s < S) mg = fmaxf(mg, m[s]);
+  for (int h = warp; h < kH; h += kThreads / 32) {
+    const float4* src = reinterpret_cast<const float4*>(stage + h * kD + 16 * lane);
     float v[16];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) v[e] = 0.f;
-    float lg = 0.f;
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      if (s < S && m[s] != -INFINITY) {
-        const float f = exp2f(m[s] - mg);
-        lg += f * l[s];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          v[4 * q] = fmaf(f, x[s][q].x, v[4 * q]);
-          v[4 * q + 1] = fmaf(f, x[s][q].y, v[4 * q + 1]);
-          v[4 * q + 2] = fmaf(f, x[s][q].z, v[4 * q + 2]);
-          v[4 * q + 3] = fmaf(f, x[s][q].w, v[4 * q + 3]);
-        }
-      }
+    for (int q = 0; q < 4; ++q) {
+      const float4 x = src[q];
+      v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
     }
-    const float inv = lg > 0.f ? 1.0f / lg : 0.f;
+    const float inv = ms.L[h] > 0.f ? 1.0f / ms.L[h] : 0.f;
 #pragma unroll
     for (int e = 0; e < 16; ++e) v[e] *= inv;
     store_head16(a, ms, blockIdx.x, h, v, lane);
   }
+}
+
+// Split row, after the cluster barrier: every CTA hands each peer m the staged
+// block of m's heads, with their max and denominator, through the copy engine
+// (into m's idle Q^T area and rM/rL); CTA m then merges heads
+// [m*64/S, (m+1)*64/S) over the S slices, thread t taking dims 2t and 2t+1,
+// rotates back, quantises and stores.
+template <int S>
+__device__ void merge_split(const AttnArgs& a, uint8_t* smem, Misc& ms) {
+  constexpr int kPer = kH / S;
+  constexpr uint32_t kBlk = kD * kPer * 2;  // bf16 block of one merger
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int me = blockIdx.y;
+  const size_t row = blockIdx.x;
+  const uint8_t* stage = smem + kOffK;
+  if (t == 0) {
+#pragma unroll 1
+    for (int m = 0; m < S; ++m) {
+      if (m == me) continue;
+      const uint32_t bar = map_shared(&ms.recv, m);
+      bulk_copy_to_peer(map_shared(smem + kOffQ + me * kBlk, m), stage + m * kBlk, kBlk, bar);
+      bulk_copy_to_peer(map_shared(&ms.rM[me][0], m), &ms.M[m * kPer], kPer * 4, bar);
+      bulk_copy_to_peer(map_shared(&ms.rL[me][0], m), &ms.L[m * kPer], kPer * 4, bar);
+    }
+    bulk_commit();
+  }
+  if (t < kPer) {
+    ms.rM[me][t] = ms.M[me * kPer + t];
+    ms.rL[me][t] = ms.L[me * kPer + t];
+  }
+  if (!mbar_wait(&ms.recv, 0)) record_error(a.err, CSA_ERR_TIMEOUT);
+  __syncthreads();
+  if (t < kPer) {  // weights 2^(M_s - max) / sum_s 2^(M_s - max) L_s into ms.red[2][s * kPer + t]
+    float mg = -INFINITY;
+#pragma unroll
+    for (int sl = 0; sl < S; ++sl) mg = fmaxf(mg, ms.rM[sl][t]);
+    float lg = 0.f, f[S];
+#pragma unroll
+    for (int sl = 0; sl < S; ++sl) {
+      const float mv = ms.rM[sl][t];
+      f[sl] = mv == -INFINITY ? 0.f : exp2f(mv - mg);
+      lg += f[sl] * ms.rL[sl][t];
+    }
+    const float inv = lg > 0.f ? 1.0f / lg : 0.f;
+#pragma unroll
+    for (int sl = 0; sl < S; ++sl) ms.red[2][sl * kPer + t] = f[sl] * inv;
+  }
+  __syncthreads();
+  float v[2][kPer];
+#pragma unroll
+  for (int hh = 0; hh < kPer; ++hh) v[0][hh] = v[1][hh] = 0.f;
+#pragma unroll
+  for (int sl = 0; sl < S; ++sl) {
+    const uint8_t* blk = sl == me ? stage + me * kBlk : smem + kOffQ + sl * kBlk;
+    // dims 2t and 2t+1: 2 * kPer consecutive bf16
+    const uint4* src = reinterpret_cast<const uint4*>(blk + (size_t)2 * t * kPer * 2);
+#pragma unroll
+    for (int q = 0; q < kPer / 4; ++q) {
+      const uint4 u = src[q];
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int k = 8 * q + e, dd = k / kPer, hh = k % kPer;
+        const float x = bf16_to_f32((uint16_t)(w[e >> 1] >> ((e & 1) * 16)));
+        v[dd][hh] = fmaf(ms.red[2][sl * kPer + hh], x, v[dd][hh]);
+      }
+    }
+  }
+  // inverse rotation of the pair (2t, 2t+1)
+  const int R = a.rope.rope_dim, d = 2 * t;
+  if (d >= kD - R) {
+    const float cs = ms.rc[(d - (kD - R)) / 2], sn = ms.rs[(d - (kD - R)) / 2];
+#pragma unroll
+    for (int hh = 0; hh < kPer; ++hh) {
+      const float x0 = v[0][hh], x1 = v[1][hh];
+      v[0][hh] = x0 * cs + x1 * sn;
+      v[1][hh] = -x0 * sn + x1 * cs;
+    }
+  }
+  const int h0 = me * kPer;
+  const int64_t ob = (int64_t)row * a.heads * kD + d;
+  if (a.out_dtype == CSA_E4M3) {
+    // per-head amax over the 512 dims, from the warps' maxima
+#pragma unroll
+    for (int hh = 0; hh < kPer; ++hh) {
+      const float am = warp_max(fmaxf(fabsf(v[0][hh]), fabsf(v[1][hh])));
+      if (lane == 0) ms.amax[warp][hh] = am;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int hh = 0; hh < kPer; ++hh) {
+      float am = 0.f;
+#pragma unroll
+      for (int w = 0; w < kThreads / 32; ++w) am = fmaxf(am, ms.amax[w][hh]);
+      const float inv = am > 0.f ? 448.0f / am : 0.0f;
+      *reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(a.out) + ob + (int64_t)(h0 + hh) * kD) =
+          f32x2_to_e4m3x2(v[0][hh] * inv, v[1][hh] * inv);
+      if (t == 0) a.out_scales[(int64_t)row * a.heads + h0 + hh] = am / 448.0f;
+    }
+  } else if (a.out_dtype == CSA_BF16) {
+#pragma unroll
+    for (int hh = 0; hh < kPer; ++hh)
+      *reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(a.out) + ob + (int64_t)(h0 + hh) * kD) =
+          (uint32_t)f32_to_bf16(v[0][hh]) | ((uint32_t)f32_to_bf16(v[1][hh]) << 16);
+  } else {
+#pragma unroll
+    for (int hh = 0; hh < kPer; ++hh)
+      *reinterpret_cast<float2*>(reinterpret_cast<float*>(a.out) + ob + (int64_t)(h0 + hh) * kD) =
+          make_float2(v[0][hh], v[1][hh]);
+  }
+  if (t == 0) bulk_wait_read();  // the staging stays valid until the engine has read it
 }
 
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnArgs a) {
@@ -558,10 +701,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnArgs a) 
       mbar_init(&ms.kfull[c], kProducers);
       mbar_init(&ms.kfree[c], 1);
     }
-    mbar_init(&ms.s_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&ms.s_full[b], 1);
+      mbar_init(&ms.kmeta[b], kProducers);
+    }
     mbar_init(&ms.p_full, kSoftmax);
     mbar_init(&ms.p_free, 1);
     mbar_init(&ms.q_full, kSoftmax);
+    mbar_init(&ms.mma_done, 1);
+    mbar_init(&ms.recv, 1);
     mbar_init_fence();
     ms.abort = 0;
   }
@@ -587,10 +735,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnArgs a) 
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-  // every CTA's staging, M and L are complete before anyone reads them
-  if (gridDim.y > 1) cluster_sync();
-  merge_role(a, smem, ms, g.p);
-  if (gridDim.y > 1) cluster_sync();  // keep this CTA's shared memory alive until its peers are done
+  if (gridDim.y == 1) {
+    finish_local(a, smem, ms);
+    return;
+  }
+  // every slice is staged and every CTA's tensor pipe is idle (its Q^T area is
+  // free) before anyone copies; each receive barrier expects its S-1 blocks
+  if (tid == 0) {
+    const uint32_t per = kH / gridDim.y;
+    mbar_arrive_expect_tx(&ms.recv, (gridDim.y - 1) * (kD * per * 2 + 2 * per * 4));
+  }
+  cluster_sync();
+  switch (gridDim.y) {
+    case 2: merge_split<2>(a, smem, ms); break;
+    case 4: merge_split<4>(a, smem, ms); break;
+    default: merge_split<8>(a, smem, ms); break;
+  }
 }
 
 }  // namespace
