@@ -57,9 +57,10 @@ constexpr uint32_t kOffMisc = kOffP + kPBytes;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColO = 128;  // S^T double-buffered in 0..127, O^T chunk c at 128 + 64c
 constexpr float kRescaleMargin = 8.0f;  // log2 units
+constexpr int kRowBufs = 4;             // tiles whose row addresses are known ahead
 
 struct Misc {
-  uint64_t kfull[kChunks], kfree[kChunks], s_full[2], kmeta[2], p_full, p_free, q_full, mma_done, recv;
+  uint64_t kfull[kChunks], kfree[kChunks], s_full[2], rows_ready[kRowBufs], p_full, p_free, q_full, mma_done, recv;
   uint32_t tmem_base;
   int32_t abort;
   alignas(16) float M[kH];  // running per-head max (log2 domain), shared by the softmax threads
@@ -69,10 +70,11 @@ struct Misc {
   alignas(16) float L[kH];  // softmax denominators of the slice
   alignas(16) float rM[8][32], rL[8][32];  // merged heads' max and denominator of each slice (split rows)
   float rc[kMaxRopePairs], rs[kMaxRopePairs];  // cos / sin of each rotary pair at the row's position
-  float kscale[2][kTile];
-  int8_t kvalid[2][kTile];
-  const uint8_t* rowptr[3][kTile];  // producer-private, by tile mod 3
-  float rowscale[3][kTile];
+  // by tile mod kRowBufs: row addresses (written by the softmax threads, read by
+  // the producers), and each key's validity and e4m3 scale (softmax-private)
+  const uint8_t* rowptr[kRowBufs][kTile];
+  float kscale[kRowBufs][kTile];
+  int8_t kvalid[kRowBufs][kTile];
 };
 constexpr uint32_t kSmemBytes = kOffMisc + sizeof(Misc) + 1024;
 
@@ -80,6 +82,7 @@ struct Geo {
   int seq;
   int64_t p, w_lo;
   int32_t n_vis, n_sel, j0, j1, n_tiles;
+  __device__ __forceinline__ int keys(int t) const { return min(kTile, j1 - j0 - t * kTile); }
 };
 
 __device__ __forceinline__ Geo row_geometry(const AttnArgs& a, int r, int split, int S) {
@@ -160,35 +163,37 @@ __device__ __forceinline__ int phase_tile(int i, int n, bool& is_s) {
 __device__ void producer_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Misc& ms, int pt) {
   const bool fp8 = a.comp.dtype == CSA_E4M3;
   const uint32_t kbase = smem_u32(smem + kOffK);
-  const uint32_t row_bytes = fp8 ? kD : 2 * kD;
   const int n = g.n_tiles;
-  if (n > 0)
-    for (int slot = pt; slot < kTile; slot += kProducers)
-      ms.rowptr[0][slot] = key_row(a, g, 0, slot, fp8, ms.rowscale[0][slot]);
+  // bf16 gathers: thread pt copies 16-byte piece (pt & 15) of keys 6j + (pt >> 4);
+  // the piece's swizzled offset inside a key's 128-byte row segment is fixed per key
+  constexpr int kGroups = kProducers / 16, kPerThr = (kTile + kGroups - 1) / kGroups;
+  const int kg = pt >> 4, piece = pt & 15;
+  const uint32_t poff = (piece >> 3) * kAtomBytes;
   for (int i = 0; i < 2 * n; ++i) {
     bool is_s;
-    const int t = phase_tile(i, n, is_s), par = t & 1, buf = t % 3;
-    if (is_s) named_bar(2, kProducers);  // tile t's row addresses are complete
+    const int t = phase_tile(i, n, is_s), buf = t % kRowBufs;
+    if (is_s) wait_or_abort(ms, &ms.rows_ready[buf], (t / kRowBufs) & 1, a.err);
+    // keys past the slice are skipped; for O^T the last 16-key step is completed with zeros
+    const int nk = g.keys(t), lim = is_s ? nk : (nk + 15) & ~15;
+    const uint8_t* rps[kPerThr];
+    if (!fp8) {
+#pragma unroll
+      for (int j = 0; j < kPerThr; ++j) {
+        const int k = kGroups * j + kg;
+        rps[j] = k < lim ? ms.rowptr[buf][k] : nullptr;
+      }
+    }
     for (int c = 0; c < kChunks; ++c) {
       if (i > 0) wait_or_abort(ms, &ms.kfree[c], (i - 1) & 1, a.err);
-      if (is_s && c == 0) {
-        // key validity and scale of tile t for the softmax (its previous reader, the
-        // softmax of tile t-2, is done: O_{t-2} has consumed its P)
-        for (int slot = pt; slot < kTile; slot += kProducers) {
-          ms.kvalid[par][slot] = ms.rowptr[buf][slot] != nullptr;
-          ms.kscale[par][slot] = ms.rowscale[buf][slot];
-        }
-        mbar_arrive(&ms.kmeta[par]);
-      }
-      const uint32_t cbase = kbase + c * kChunkBytes;
+      const uint32_t cbase = kbase + c * kChunkBytes + poff;
       if (!fp8) {
-        // 16 consecutive threads per key row: 256 contiguous bytes = dims [128c, 128c+128)
-        for (int x = pt; x < kTile * 16; x += kProducers) {
-          const uint32_t key = x >> 4, piece = x & 15;
-          const uint8_t* rp = ms.rowptr[buf][key];
-          const uint32_t dst = cbase + (piece >> 3) * kAtomBytes + (key >> 3) * 1024 + (key & 7) * 128 +
-                               (((piece & 7) ^ (key & 7)) << 4);
-          cp_async16(dst, rp ? rp + c * 256 + piece * 16 : a.comp.data, rp ? 16u : 0u);
+#pragma unroll
+        for (int j = 0; j < kPerThr; ++j) {
+          const int k = kGroups * j + kg;
+          if (k < lim) {
+            const uint32_t dst = cbase + (k >> 3) * 1024 + (k & 7) * 128 + (((piece & 7) ^ (k & 7)) << 4);
+            cp_async16(dst, rps[j] ? rps[j] + c * 256 + piece * 16 : a.comp.data, rps[j] ? 16u : 0u);
+          }
         }
         cp_async_arrive_noinc(&ms.kfull[c]);
       } else {
@@ -199,7 +204,7 @@ __device__ void producer_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mi
         for (int it = 0; it < kIters; ++it) {
           const int x = pt + it * kProducers;
           raw[it] = make_uint4(0, 0, 0, 0);
-          if (x < kTile * 8) {
+          if (x < lim * 8) {
             const uint8_t* rp = ms.rowptr[buf][x >> 3];
             if (rp) raw[it] = __ldg(reinterpret_cast<const uint4*>(rp + c * 128 + (x & 7) * 16));
           }
@@ -207,7 +212,7 @@ __device__ void producer_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mi
 #pragma unroll
         for (int it = 0; it < kIters; ++it) {
           const int x = pt + it * kProducers;
-          if (x >= kTile * 8) break;
+          if (x >= lim * 8) break;
           const uint32_t key = x >> 3, q8 = x & 7;
           const uint32_t w[4] = {raw[it].x, raw[it].y, raw[it].z, raw[it].w};
           uint32_t outw[8];
@@ -228,17 +233,6 @@ __device__ void producer_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mi
         }
         fence_proxy_async();
         mbar_arrive(&ms.kfull[c]);
-      }
-    }
-    if (is_s && t + 1 < n) {
-      // tile t+1's row addresses, and its rows into L2, while the ring drains; the
-      // buffer was last read by O_{t-2}, which every producer has issued by now
-      named_bar(2, kProducers);
-      const int nb = (t + 1) % 3;
-      for (int slot = pt; slot < kTile; slot += kProducers) {
-        const uint8_t* rp = key_row(a, g, t + 1, slot, fp8, ms.rowscale[nb][slot]);
-        ms.rowptr[nb][slot] = rp;
-        if (rp) prefetch_l2(rp, row_bytes);
       }
     }
   }
@@ -275,10 +269,12 @@ __device__ void mma_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Misc& m
                    b_s + (((k0 >> 6) * (kH * 128) + (k0 & 63) * 2) >> 4), idesc_s, (c | ks) != 0);
         }
       } else {
+        const int ksteps = (g.keys(t) + 15) >> 4;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)  // 16 keys per step: two 8-key groups of 1 KB
-          mma_bf16(tmem + kColO + 64 * c, a_o + ((c * kChunkBytes + ks * 2048) >> 4), b_o + ((ks * 2048) >> 4),
-                   idesc_o, (t > 0 || ks > 0) ? 1u : 0u);
+          if (ks < ksteps)
+            mma_bf16(tmem + kColO + 64 * c, a_o + ((c * kChunkBytes + ks * 2048) >> 4), b_o + ((ks * 2048) >> 4),
+                     idesc_o, (t > 0 || ks > 0) ? 1u : 0u);
       }
       mma_commit(&ms.kfree[c]);
     }
@@ -323,24 +319,28 @@ __device__ __forceinline__ uint32_t rot_pack(float q0, float q1, int d, float qs
 // Q^T operand: the row's 64 heads rotated at p, scaled by scale * log2(e),
 // rounded to bf16, 128B-swizzled K-major (rows = heads).  bf16 rows are
 // copied raw with cp.async as the very first requests of the CTA (ahead of the
-// key gathers, which wait for the previous launch) and then transformed in
+// key lookups, which wait for the previous launch) and then transformed in
 // place, each thread on the pieces it copied itself; fp32 rows go through
 // registers.  The softmax threads then release the MMA issuer through q_full.
 // The query rows, seq_id and pos are inputs of the step, not written by the
 // library's preceding launches, so they are read before griddepcontrol.wait.
-__device__ void fill_q(const AttnArgs& a, uint8_t* smem, Misc& ms, int st) {
+__device__ __forceinline__ void fill_q_issue(const AttnArgs& a, uint8_t* smem, int st) {
+  if (a.q_dtype != CSA_BF16) return;
+  constexpr int kPieces = kH * (kD / 8);  // 16-byte pieces of bf16 (8 dims each)
+  const uint16_t* src = reinterpret_cast<const uint16_t*>(a.q) + (int64_t)blockIdx.x * a.heads * kD;
+  const uint32_t qbase = smem_u32(smem + kOffQ);
+  for (int x = st; x < kPieces; x += kSoftmax) {
+    const int h = x >> 6, d0 = (x & 63) * 8;
+    cp_async16(qbase + sw128_offset(h, d0, kH), src + h * kD + d0, 16u);
+  }
+  cp_async_commit();
+}
+
+__device__ void fill_q_finish(const AttnArgs& a, uint8_t* smem, Misc& ms, int st) {
   const float qs = a.scale * 1.4426950408889634f;
   const int R = a.rope.rope_dim;
-  const int64_t rb = (int64_t)blockIdx.x * a.heads * kD;
-  constexpr int kPieces = kH * (kD / 8);  // 16-byte pieces of bf16 (8 dims each)
+  constexpr int kPieces = kH * (kD / 8);
   if (a.q_dtype == CSA_BF16) {
-    const uint16_t* src = reinterpret_cast<const uint16_t*>(a.q) + rb;
-    const uint32_t qbase = smem_u32(smem + kOffQ);
-    for (int x = st; x < kPieces; x += kSoftmax) {
-      const int h = x >> 6, d0 = (x & 63) * 8;
-      cp_async16(qbase + sw128_offset(h, d0, kH), src + h * kD + d0, 16u);
-    }
-    cp_async_commit();
     cp_async_wait<0>();
     for (int x = st; x < kPieces; x += kSoftmax) {
       const int h = x >> 6, d0 = (x & 63) * 8;
@@ -355,6 +355,7 @@ __device__ void fill_q(const AttnArgs& a, uint8_t* smem, Misc& ms, int st) {
       *p = make_uint4(o[0], o[1], o[2], o[3]);
     }
   } else {
+    const int64_t rb = (int64_t)blockIdx.x * a.heads * kD;
     constexpr int kBatch = 8;  // loads in flight per thread
     for (int x0 = st; x0 < kPieces; x0 += kSoftmax * kBatch) {
       float q[kBatch][8];
@@ -382,6 +383,21 @@ __device__ void fill_q(const AttnArgs& a, uint8_t* smem, Misc& ms, int st) {
   mbar_arrive(&ms.q_full);
 }
 
+// Softmax thread st looks up key st of tile u: row address for the producers
+// (released through rows_ready), and its own validity flag and e4m3 scale.
+// (An L2 prefetch of the rows here measured slower: each prefetch instruction
+// occupies the SM's TMA unit for about as long as a 1 KB row takes to stream.)
+__device__ __forceinline__ void lookup_keys(const AttnArgs& a, const Geo& g, Misc& ms, int u, int st) {
+  const bool fp8 = a.comp.dtype == CSA_E4M3;
+  const int b = u % kRowBufs;
+  float sc;
+  const uint8_t* rp = key_row(a, g, u, st, fp8, sc);
+  ms.rowptr[b][st] = rp;
+  ms.kvalid[b][st] = rp != nullptr;
+  ms.kscale[b][st] = sc;
+  mbar_arrive(&ms.rows_ready[b]);
+}
+
 // The 64 head columns of one O^T chunk for this thread's TMEM lane (zeros for
 // an empty slice): four loads in flight, one wait.
 __device__ __forceinline__ void load_o_chunk(uint32_t taddr, bool any, float* o) {
@@ -396,7 +412,11 @@ __device__ __forceinline__ void load_o_chunk(uint32_t taddr, bool any, float* o)
 }
 
 __device__ void softmax_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Misc& ms, uint32_t tmem, int st) {
-  fill_q(a, smem, ms, st);
+  fill_q_issue(a, smem, st);
+  pdl_wait();  // selections and caches are complete only after the previous launch
+  if (g.n_tiles > 0) lookup_keys(a, g, ms, 0, st);
+  fill_q_finish(a, smem, ms, st);
+  for (int u = 1; u < min(g.n_tiles, kRowBufs - 1); ++u) lookup_keys(a, g, ms, u, st);
   const int w = st >> 5;
   const uint32_t lane_addr = tmem + ((uint32_t)(w * 32) << 16);
   float lsum[kH];
@@ -412,9 +432,8 @@ __device__ void softmax_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mis
 #pragma unroll
     for (int i = 0; i < 4; ++i) tmem_ld16(lane_addr + kColS + 64 * par + 16 * i, x + 16 * i);
     tmem_wait_ld();
-    wait_or_abort(ms, &ms.kmeta[par], use, a.err);
-    const bool valid = ms.kvalid[par][st] != 0;
-    const float ksc = ms.kscale[par][st];
+    const bool valid = ms.kvalid[t % kRowBufs][st] != 0;
+    const float ksc = ms.kscale[t % kRowBufs][st];
     bool need = false;
 #pragma unroll
     for (int h = 0; h < kH; ++h) {
@@ -474,6 +493,8 @@ __device__ void softmax_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mis
     fence_proxy_async();
     tc_fence_before();
     mbar_arrive(&ms.p_full);
+    // tile t-1 is done with its address buffer (O_{t-1} is complete): look ahead
+    if (t + kRowBufs - 1 < g.n_tiles) lookup_keys(a, g, ms, t + kRowBufs - 1, st);
   }
 
   // ---- epilogue
@@ -701,10 +722,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnArgs a) 
       mbar_init(&ms.kfull[c], kProducers);
       mbar_init(&ms.kfree[c], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&ms.s_full[b], 1);
-      mbar_init(&ms.kmeta[b], kProducers);
-    }
+    for (int b = 0; b < 2; ++b) mbar_init(&ms.s_full[b], 1);
+    for (int b = 0; b < kRowBufs; ++b) mbar_init(&ms.rows_ready[b], kSoftmax);
     mbar_init(&ms.p_full, kSoftmax);
     mbar_init(&ms.p_free, 1);
     mbar_init(&ms.q_full, kSoftmax);
