@@ -8,34 +8,34 @@
 //
 // Shape: D = 512, H = 64 query heads sharing every key (MQA).  One CTA takes
 // one query row and a contiguous slice of its key list (selected entries, then
-// window rows), in tiles of 128 keys.  Keys are the M dimension of the MMAs,
-// so every accumulator has the plain 128-lane TMEM layout:
+// window rows), in tiles of 64 keys:
 //
-//   S^T [128 keys x 64 heads]  = K_tile [128 x 512] . Q^T [512 x 64]
-//   O^T [512 dims x 64 heads] += K_tile^T [512 x 128] . P^T [128 x 64]   (4 chunks of 128 dims)
+//   S   [64 heads x 64 keys]    = Q [64 x 512] . K_tile^T [512 x 64]        (M = 64)
+//   O^T [512 dims x 64 heads]  += K_tile^T [512 x 64] . P^T [64 x 64]        (4 chunks of 128 dims)
 //
-// Key rows are gathered into a ring of four 32 KB slots (128 keys x 128 dims,
-// 128B-swizzled, keys as rows): read K-major a slot is an A operand of S^T,
-// read MN-major an A operand of O^T (values = keys).  Q^T (pre-rotated,
-// pre-scaled by scale*log2 e) and P^T are the B operands.  Each tile passes
-// through the ring twice -- for S^T, then again from L2 for O^T -- in the
-// order S_0, S_1, O_0, S_2, O_1, ..., so that the softmax of tile t overlaps
-// S_{t+1} and the ring never waits for a softmax.  TMEM: S^T double-buffered
-// in columns 0..127, O^T chunk c in 128+64c.
+// Shared memory holds Q (64 KB, pre-rotated, pre-scaled by scale*log2 e), a
+// ring of two 64 KB key tiles and two P buffers.  A key tile is gathered once,
+// 128B-swizzled with keys as rows: read K-major it is the B operand of S, read
+// MN-major the A operand of O^T (values = keys).  While one tile is in use the
+// next is being gathered; the tensor pipe runs S_0, S_1, O_0, S_2, O_1, ...,
+// so the softmax of tile t overlaps S_{t+1}.  TMEM: S double-buffered in
+// columns 0..127 (M = 64 layout: head h in lane 32*(h/16) + h%16), O^T chunk c
+// in 128+64c.
 //
-// Warp roles: warps 0-3 own TMEM lanes (thread t <-> key t of the tile for the
-// softmax, dim t of a chunk in the epilogue); warps 4-6 gather the rows from
-// the paged caches (cp.async for bf16, load + convert for e4m3, whose per-row
-// scale is folded into the logits and into P); warp 7 allocates TMEM and one
-// lane issues the MMAs.  Eight warps leave 255 registers per thread.  The
-// running per-head max is only raised when a logit exceeds it by more than
-// 2^8; raising it rescales O^T in TMEM.
+// Warp roles: warps 0-3 are the softmax (lanes 0-15 own one head each: the
+// row max and the denominator stay in a register) and the epilogue (thread t
+// owns TMEM lane t: dim t of an O^T chunk); they also look the tile's row
+// addresses up three tiles ahead.  Warps 4-6 gather the rows from the paged
+// caches (cp.async for bf16, load + convert for e4m3, whose per-row scale is
+// folded into the logits and into P).  Warp 7 allocates TMEM and one lane
+// issues the MMAs.  The running per-head max is only raised when a logit
+// exceeds it by more than 2^8; raising it rescales O^T in TMEM.
 //
 // A row's key list may be split over S = 1, 2, 4 or 8 CTAs launched as one
-// cluster.  Each CTA writes its unnormalised O with its per-head max and
-// denominator to the workspace (L2); after a cluster barrier CTA m merges
-// heads [m*64/S, (m+1)*64/S), normalises, rotates back and stores, then
-// discards the consumed workspace lines from L2.
+// cluster.  Each CTA stages its unnormalised O (bf16) in its idle ring; after
+// a cluster barrier the copy engine hands each peer m the block of the heads
+// m merges, with their max and denominator, into m's idle Q area; CTA m then
+// merges heads [m*64/S, (m+1)*64/S), normalises, rotates back and stores.
 
 #include "csa_kernels.h"
 #include "tc_ptx.cuh"
@@ -45,36 +45,39 @@ namespace {
 
 using namespace tc;
 
-constexpr int kD = 512, kH = 64, kTile = 128, kChunks = 4;
+constexpr int kD = 512, kH = 64, kTile = 64, kChunks = 4;
 constexpr int kSoftmax = 128, kProducers = 96;
 constexpr int kThreads = kSoftmax + kProducers + 32;
 constexpr uint32_t kQBytes = kH * kD * 2;             // 64 KB
-constexpr uint32_t kChunkBytes = kTile * 128 * 2;     // 32 KB: 128 keys x 128 dims
-constexpr uint32_t kAtomBytes = kTile * 128;          // 16 KB: 128 keys x 64 dims
-constexpr uint32_t kPBytes = kTile * kH * 2;          // 16 KB
-constexpr uint32_t kOffQ = 0, kOffK = kQBytes, kOffP = kOffK + kChunks * kChunkBytes;
-constexpr uint32_t kOffMisc = kOffP + kPBytes;
+constexpr uint32_t kChunkBytes = kTile * 128 * 2;     // 16 KB: 64 keys x 128 dims
+constexpr uint32_t kAtomBytes = kTile * 128;          // 8 KB: 64 keys x 64 dims
+constexpr uint32_t kTileBytes = kChunks * kChunkBytes;  // 64 KB
+constexpr uint32_t kPBytes = kH * kTile * 2;          // 8 KB: 64 heads x 64 keys
+constexpr uint32_t kOffQ = 0, kOffK = kQBytes, kOffP = kOffK + 2 * kTileBytes;
+constexpr uint32_t kOffMisc = kOffP + 2 * kPBytes;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColO = 128;  // S^T double-buffered in 0..127, O^T chunk c at 128 + 64c
-constexpr float kRescaleMargin = 8.0f;  // log2 units
-constexpr int kRowBufs = 4;             // tiles whose row addresses are known ahead
+constexpr uint32_t kColS = 0, kColO = 128;  // S double-buffered in 0..127, O^T chunk c at 128 + 64c
+constexpr float kRescaleMargin = 8.0f;       // log2 units
+constexpr int kRowBufs = 4;                  // tiles whose row addresses are known ahead
 
 struct Misc {
-  uint64_t kfull[kChunks], kfree[kChunks], s_full[2], rows_ready[kRowBufs], p_full, p_free, q_full, mma_done, recv;
+  uint64_t kfull[2][kChunks];  // tile slot, chunk
+  uint64_t o_done[2];          // O^T of the slot's tile complete: slot and P buffer free
+  uint64_t s_full[2], p_full[2], rows_ready[kRowBufs], q_full, mma_done, recv;
   uint32_t tmem_base;
   int32_t abort;
-  alignas(16) float M[kH];  // running per-head max (log2 domain), shared by the softmax threads
-  float red[4][kH];     // per-warp reductions; merge weights
-  float amax[kThreads / 32][32];  // per-warp head maxima of the merged output
-  float alpha[kH];      // rescale factor of the last max raise
+  alignas(16) float M[kH];  // per-head max (log2 domain) of the slice, for the merge
   alignas(16) float L[kH];  // softmax denominators of the slice
+  float red[4][kH];         // merge weights
+  float amax[kThreads / 32][32];  // per-warp head maxima of the merged output
+  float alpha[kH];          // rescale factor of the last max raise
   alignas(16) float rM[8][32], rL[8][32];  // merged heads' max and denominator of each slice (split rows)
   float rc[kMaxRopePairs], rs[kMaxRopePairs];  // cos / sin of each rotary pair at the row's position
-  // by tile mod kRowBufs: row addresses (written by the softmax threads, read by
-  // the producers), and each key's validity and e4m3 scale (softmax-private)
+  // by tile mod kRowBufs (released through rows_ready): row addresses for the
+  // producers, and each key's validity and e4m3 scale for the softmax
   const uint8_t* rowptr[kRowBufs][kTile];
-  float kscale[kRowBufs][kTile];
-  int8_t kvalid[kRowBufs][kTile];
+  alignas(16) float kscale[kRowBufs][kTile];
+  alignas(16) int8_t kvalid[kRowBufs][kTile];
 };
 constexpr uint32_t kSmemBytes = kOffMisc + sizeof(Misc) + 1024;
 
@@ -138,55 +141,34 @@ __device__ __forceinline__ const uint8_t* key_row(const AttnArgs& a, const Geo& 
   return reinterpret_cast<const uint8_t*>(c->data) + prow * (int64_t)kD * (fp8 ? 1 : 2);
 }
 
-// Phase i of the tensor pipe over a slice of n tiles.  Every key tile passes
-// through the key ring twice, once for S^T and once more (from L2) for O^T,
-// in the order S_0, S_1, O_0, S_2, O_1, ..., S_{n-1}, O_{n-2}, O_{n-1}: the
-// softmax of tile t runs while the tensor pipe computes S_{t+1}, and the ring
-// keeps streaming instead of idling between a tile's S^T and its O^T.
-__device__ __forceinline__ int phase_tile(int i, int n, bool& is_s) {
-  if (i == 0) {
-    is_s = true;
-    return 0;
-  }
-  if (i == 2 * n - 1) {
-    is_s = false;
-    return n - 1;
-  }
-  is_s = (i & 1) != 0;
-  return is_s ? (i + 1) >> 1 : (i >> 1) - 1;
-}
-
-// Producers: one 32 KB ring slot per 128-dim chunk of the current phase's tile.
-// bf16 rows are copied with cp.async, each thread's copies arriving on the
-// slot's barrier as they land (the MMA issuer fences them into the async
-// proxy); e4m3 rows are converted through registers.
+// Producers: tile t goes to ring slot t & 1 once O^T of tile t-2 has released
+// it, one 16 KB chunk (128 dims) at a time.  bf16 rows are copied with
+// cp.async, each thread's copies arriving on the chunk's barrier as they land
+// (the MMA issuer fences them into the async proxy); e4m3 rows are converted
+// through registers.  Keys past the slice are not loaded; the rest of the last
+// 16-key step of O^T is filled with zeros.
 __device__ void producer_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Misc& ms, int pt) {
   const bool fp8 = a.comp.dtype == CSA_E4M3;
-  const uint32_t kbase = smem_u32(smem + kOffK);
   const int n = g.n_tiles;
-  // bf16 gathers: thread pt copies 16-byte piece (pt & 15) of keys 6j + (pt >> 4);
-  // the piece's swizzled offset inside a key's 128-byte row segment is fixed per key
+  // bf16: thread pt copies 16-byte piece (pt & 15) of keys 6j + (pt >> 4)
   constexpr int kGroups = kProducers / 16, kPerThr = (kTile + kGroups - 1) / kGroups;
   const int kg = pt >> 4, piece = pt & 15;
-  const uint32_t poff = (piece >> 3) * kAtomBytes;
-  for (int i = 0; i < 2 * n; ++i) {
-    bool is_s;
-    const int t = phase_tile(i, n, is_s), buf = t % kRowBufs;
-    if (is_s) wait_or_abort(ms, &ms.rows_ready[buf], (t / kRowBufs) & 1, a.err);
-    // keys past the slice are skipped; for O^T the last 16-key step is completed with zeros
-    const int nk = g.keys(t), lim = is_s ? nk : (nk + 15) & ~15;
-    const uint8_t* rps[kPerThr];
+  for (int t = 0; t < n; ++t) {
+    const int slot = t & 1, buf = t % kRowBufs;
+    wait_or_abort(ms, &ms.rows_ready[buf], (t / kRowBufs) & 1, a.err);
+    if (t >= 2) wait_or_abort(ms, &ms.o_done[slot], ((t - 2) >> 1) & 1, a.err);
+    const int lim = min(kTile, (g.keys(t) + 15) & ~15);
+    const uint32_t tbase = smem_u32(smem + kOffK) + slot * kTileBytes;
     if (!fp8) {
+      const uint8_t* rps[kPerThr];
 #pragma unroll
       for (int j = 0; j < kPerThr; ++j) {
         const int k = kGroups * j + kg;
         rps[j] = k < lim ? ms.rowptr[buf][k] : nullptr;
       }
-    }
-    for (int c = 0; c < kChunks; ++c) {
-      if (i > 0) wait_or_abort(ms, &ms.kfree[c], (i - 1) & 1, a.err);
-      const uint32_t cbase = kbase + c * kChunkBytes + poff;
-      if (!fp8) {
+      const uint32_t poff = (piece >> 3) * kAtomBytes;
+      for (int c = 0; c < kChunks; ++c) {
+        const uint32_t cbase = tbase + c * kChunkBytes + poff;
 #pragma unroll
         for (int j = 0; j < kPerThr; ++j) {
           const int k = kGroups * j + kg;
@@ -195,10 +177,12 @@ __device__ void producer_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mi
             cp_async16(dst, rps[j] ? rps[j] + c * 256 + piece * 16 : a.comp.data, rps[j] ? 16u : 0u);
           }
         }
-        cp_async_arrive_noinc(&ms.kfull[c]);
-      } else {
-        // 8 consecutive threads per key row: 128 code bytes -> 128 bf16 (exact)
-        constexpr int kIters = (kTile * 8 + kProducers - 1) / kProducers;
+        cp_async_arrive_noinc(&ms.kfull[slot][c]);
+      }
+    } else {
+      // 8 consecutive threads per key row: 128 code bytes -> 128 bf16 (exact)
+      constexpr int kIters = (kTile * 8 + kProducers - 1) / kProducers;
+      for (int c = 0; c < kChunks; ++c) {
         uint4 raw[kIters];
 #pragma unroll
         for (int it = 0; it < kIters; ++it) {
@@ -224,15 +208,15 @@ __device__ void producer_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mi
           }
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
-            const uint32_t piece = q8 * 2 + half;  // 16-byte piece of the 256-byte bf16 chunk
-            uint8_t* dst = smem + kOffK + c * kChunkBytes + (piece >> 3) * kAtomBytes + (key >> 3) * 1024 +
-                           (key & 7) * 128 + (((piece & 7) ^ (key & 7)) << 4);
+            const uint32_t pc = q8 * 2 + half;  // 16-byte piece of the 256-byte bf16 chunk
+            uint8_t* dst = smem + kOffK + slot * kTileBytes + c * kChunkBytes + (pc >> 3) * kAtomBytes +
+                           (key >> 3) * 1024 + (key & 7) * 128 + (((pc & 7) ^ (key & 7)) << 4);
             *reinterpret_cast<uint4*>(dst) =
                 make_uint4(outw[half * 4], outw[half * 4 + 1], outw[half * 4 + 2], outw[half * 4 + 3]);
           }
         }
         fence_proxy_async();
-        mbar_arrive(&ms.kfull[c]);
+        mbar_arrive(&ms.kfull[slot][c]);
       }
     }
   }
@@ -241,44 +225,66 @@ __device__ void producer_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mi
 
 // ------------------------------------------------------------------ MMA issuer
 
+// Phase i of the tensor pipe over n tiles: S_0, S_1, O_0, S_2, O_1, ..., S_{n-1}, O_{n-2}, O_{n-1}.
+__device__ __forceinline__ int phase_tile(int i, int n, bool& is_s) {
+  if (i == 0) {
+    is_s = true;
+    return 0;
+  }
+  if (i == 2 * n - 1) {
+    is_s = false;
+    return n - 1;
+  }
+  is_s = (i & 1) != 0;
+  return is_s ? (i + 1) >> 1 : (i >> 1) - 1;
+}
+
 __device__ void mma_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Misc& ms, uint32_t tmem) {
-  constexpr uint32_t idesc_s = idesc_bf16(128, kH, 0, 0);
-  constexpr uint32_t idesc_o = idesc_bf16(128, kH, 1, 1);
-  // descriptors of the ring, Q^T and P^T; every operand below is one of these plus a constant
-  const uint64_t a_s = sdesc_sw128(smem_u32(smem + kOffK), 16, 1024);
-  const uint64_t b_s = sdesc_sw128(smem_u32(smem + kOffQ), 16, 1024);
-  const uint64_t a_o = sdesc_sw128(smem_u32(smem + kOffK), kAtomBytes, 1024);
-  const uint64_t b_o = sdesc_sw128(smem_u32(smem + kOffP), kAtomBytes, 1024);
+  constexpr uint32_t idesc_s = idesc_bf16(64, kTile, 0, 0);   // A = Q (K-major), B = key tile (K-major)
+  constexpr uint32_t idesc_o = idesc_bf16(128, kH, 1, 0);     // A = key tile^T (MN-major), B = P (K-major)
+  // every operand below is one of these descriptors plus a constant
+  const uint64_t d_q = sdesc_sw128(smem_u32(smem + kOffQ), 16, 1024);
+  const uint64_t d_ks = sdesc_sw128(smem_u32(smem + kOffK), 16, 1024);
+  const uint64_t d_ko = sdesc_sw128(smem_u32(smem + kOffK), kAtomBytes, 1024);
+  const uint64_t d_p = sdesc_sw128(smem_u32(smem + kOffP), 16, 1024);
   const int n = g.n_tiles;
   wait_or_abort(ms, &ms.q_full, 0, a.err);
   for (int i = 0; i < 2 * n; ++i) {
     bool is_s;
-    const int t = phase_tile(i, n, is_s);
-    if (!is_s) wait_or_abort(ms, &ms.p_full, t & 1, a.err);
-    const uint32_t d_s = tmem + kColS + 64 * (t & 1);
+    const int t = phase_tile(i, n, is_s), slot = t & 1;
+    const uint32_t use = (t >> 1) & 1;
+    const uint32_t toff = (slot * kTileBytes) >> 4;
+    if (is_s) {
+      const uint32_t d_s = tmem + kColS + 64 * slot;
 #pragma unroll
-    for (int c = 0; c < kChunks; ++c) {
-      wait_or_abort(ms, &ms.kfull[c], i & 1, a.err);
-      fence_proxy_async();  // the slot was written through the generic proxy
-      tc_fence_after();
-      if (is_s) {
+      for (int c = 0; c < kChunks; ++c) {
+        wait_or_abort(ms, &ms.kfull[slot][c], use, a.err);
+        fence_proxy_async();  // the chunk was written through the generic proxy
+        tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t k0 = c * 128 + ks * 16;  // first dim of this K step
-          mma_bf16(d_s, a_s + ((c * kChunkBytes + (ks >> 2) * kAtomBytes + (ks & 3) * 32) >> 4),
-                   b_s + (((k0 >> 6) * (kH * 128) + (k0 & 63) * 2) >> 4), idesc_s, (c | ks) != 0);
+          mma_bf16(d_s, d_q + (((k0 >> 6) * (kH * 128) + (k0 & 63) * 2) >> 4),
+                   d_ks + toff + ((c * kChunkBytes + (ks >> 2) * kAtomBytes + (ks & 3) * 32) >> 4), idesc_s,
+                   (c | ks) != 0);
         }
-      } else {
-        const int ksteps = (g.keys(t) + 15) >> 4;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)  // 16 keys per step: two 8-key groups of 1 KB
-          if (ks < ksteps)
-            mma_bf16(tmem + kColO + 64 * c, a_o + ((c * kChunkBytes + ks * 2048) >> 4), b_o + ((ks * 2048) >> 4),
-                     idesc_o, (t > 0 || ks > 0) ? 1u : 0u);
       }
-      mma_commit(&ms.kfree[c]);
+      mma_commit(&ms.s_full[slot]);
+    } else {
+      wait_or_abort(ms, &ms.p_full[slot], use, a.err);
+      tc_fence_after();
+      const int ksteps = (g.keys(t) + 15) >> 4;
+      const uint32_t poff = (slot * kPBytes) >> 4;
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) {
+#pragma unroll
+        for (int ks = 0; ks < kTile / 16; ++ks)  // 16 keys per step: two 8-key groups of 1 KB
+          if (ks < ksteps)
+            mma_bf16(tmem + kColO + 64 * c, d_ko + toff + ((c * kChunkBytes + ks * 2048) >> 4),
+                     d_p + poff + ((ks * 32) >> 4), idesc_o, (t > 0 || ks > 0) ? 1u : 0u);
+      }
+      mma_commit(&ms.o_done[slot]);
     }
-    mma_commit(is_s ? &ms.s_full[t & 1] : &ms.p_free);
   }
   // nothing may still write TMEM when it is released, even after a timeout
   mma_commit(&ms.mma_done);
@@ -286,23 +292,6 @@ __device__ void mma_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Misc& m
 }
 
 // ------------------------------------------------------------------ softmax + epilogue
-
-// Per-warp max (or sum) of v[h] over the warp's 32 keys, for all 64 heads,
-// into ms.red[warp][h]; the caller synchronises before reading ms.red.
-template <bool kMax>
-__device__ __forceinline__ void warp_reduce64(const float* v, Misc& ms, int st) {
-  const int lane = st & 31, w = st >> 5;
-#pragma unroll
-  for (int h = 0; h < kH; ++h) {
-    float x = v[h];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float y = __shfl_xor_sync(0xffffffffu, x, o);
-      x = kMax ? fmaxf(x, y) : x + y;
-    }
-    if (lane == 0) ms.red[w][h] = x;
-  }
-}
 
 // Rotation of the pair (d, d+1) at the row's position (rotary dims only), the
 // logit scale, and bf16 rounding of the pair.
@@ -316,7 +305,7 @@ __device__ __forceinline__ uint32_t rot_pack(float q0, float q1, int d, float qs
   return (uint32_t)f32_to_bf16(q0 * qs) | ((uint32_t)f32_to_bf16(q1 * qs) << 16);
 }
 
-// Q^T operand: the row's 64 heads rotated at p, scaled by scale * log2(e),
+// Q operand: the row's 64 heads rotated at p, scaled by scale * log2(e),
 // rounded to bf16, 128B-swizzled K-major (rows = heads).  bf16 rows are
 // copied raw with cp.async as the very first requests of the CTA (ahead of the
 // key lookups, which wait for the previous launch) and then transformed in
@@ -383,18 +372,20 @@ __device__ void fill_q_finish(const AttnArgs& a, uint8_t* smem, Misc& ms, int st
   mbar_arrive(&ms.q_full);
 }
 
-// Softmax thread st looks up key st of tile u: row address for the producers
-// (released through rows_ready), and its own validity flag and e4m3 scale.
-// (An L2 prefetch of the rows here measured slower: each prefetch instruction
-// occupies the SM's TMA unit for about as long as a 1 KB row takes to stream.)
+// Softmax threads st < 64 look up key st of tile u: row address for the
+// producers, validity and e4m3 scale for the softmax; all 128 release the
+// buffer through rows_ready.  (An L2 prefetch of the rows here measured
+// slower: each prefetch instruction holds the SM's TMA unit about as long as a
+// 1 KB row takes to stream.)
 __device__ __forceinline__ void lookup_keys(const AttnArgs& a, const Geo& g, Misc& ms, int u, int st) {
-  const bool fp8 = a.comp.dtype == CSA_E4M3;
   const int b = u % kRowBufs;
-  float sc;
-  const uint8_t* rp = key_row(a, g, u, st, fp8, sc);
-  ms.rowptr[b][st] = rp;
-  ms.kvalid[b][st] = rp != nullptr;
-  ms.kscale[b][st] = sc;
+  if (st < kTile) {
+    float sc;
+    const uint8_t* rp = key_row(a, g, u, st, a.comp.dtype == CSA_E4M3, sc);
+    ms.rowptr[b][st] = rp;
+    ms.kvalid[b][st] = rp != nullptr;
+    ms.kscale[b][st] = sc;
+  }
   mbar_arrive(&ms.rows_ready[b]);
 }
 
@@ -417,102 +408,109 @@ __device__ void softmax_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mis
   if (g.n_tiles > 0) lookup_keys(a, g, ms, 0, st);
   fill_q_finish(a, smem, ms, st);
   for (int u = 1; u < min(g.n_tiles, kRowBufs - 1); ++u) lookup_keys(a, g, ms, u, st);
-  const int w = st >> 5;
+  const int w = st >> 5, l = st & 31;
+  const bool owner = l < 16;         // lanes 0-15 of each warp own a head of S
+  const int h = 16 * w + (l & 15);   // the head (owners only)
   const uint32_t lane_addr = tmem + ((uint32_t)(w * 32) << 16);
-  float lsum[kH];
-#pragma unroll
-  for (int h = 0; h < kH; ++h) lsum[h] = 0.f;
-  uint8_t* prow = smem + kOffP + (st >> 3) * 1024 + (st & 7) * 128;
+  float m_run = -INFINITY, l_run = 0.f;  // this head's running max and denominator
 
   for (int t = 0; t < g.n_tiles; ++t) {
-    const uint32_t par = t & 1, use = (t >> 1) & 1;
-    wait_or_abort(ms, &ms.s_full[par], use, a.err);
+    const int slot = t & 1, b = t % kRowBufs;
+    const uint32_t use = (t >> 1) & 1;
+    wait_or_abort(ms, &ms.s_full[slot], use, a.err);
     tc_fence_after();
-    float x[kH];
+    float x[kTile];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) tmem_ld16(lane_addr + kColS + 64 * par + 16 * i, x + 16 * i);
+    for (int i = 0; i < 4; ++i) tmem_ld16(lane_addr + kColS + 64 * slot + 16 * i, x + 16 * i);
     tmem_wait_ld();
-    const bool valid = ms.kvalid[t % kRowBufs][st] != 0;
-    const float ksc = ms.kscale[t % kRowBufs][st];
-    bool need = false;
+    wait_or_abort(ms, &ms.rows_ready[b], (t / kRowBufs) & 1, a.err);
+    float mt = -INFINITY;
 #pragma unroll
-    for (int h = 0; h < kH; ++h) {
-      x[h] = valid ? x[h] * ksc : -INFINITY;
-      need |= x[h] > ms.M[h] + kRescaleMargin;
+    for (int k4 = 0; k4 < kTile / 4; ++k4) {
+      const float4 sc = *reinterpret_cast<const float4*>(&ms.kscale[b][4 * k4]);
+      const uint32_t vb = *reinterpret_cast<const uint32_t*>(&ms.kvalid[b][4 * k4]);
+      const float s4[4] = {sc.x, sc.y, sc.z, sc.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int k = 4 * k4 + e;
+        x[k] = ((vb >> (8 * e)) & 0xFF) ? x[k] * s4[e] : -INFINITY;
+        mt = fmaxf(mt, x[k]);
+      }
     }
+    const bool need = owner && mt > m_run + kRescaleMargin;
     if (named_bar_or(1, kSoftmax, need)) {
-      // raise the running max: thread h < 64 owns head h
-      warp_reduce64<true>(x, ms, st);
-      named_bar(1, kSoftmax);
-      if (st < kH) {
-        const float mo = ms.M[st];
-        const float mn = fmaxf(fmaxf(mo, fmaxf(ms.red[0][st], ms.red[1][st])), fmaxf(ms.red[2][st], ms.red[3][st]));
-        ms.alpha[st] = mo == -INFINITY ? 0.f : exp2f(mo - mn);
-        ms.M[st] = mn;
+      // raise every head's max to its current maximum; rescale O^T and the denominator
+      if (owner) {
+        const float mn = fmaxf(m_run, mt);
+        ms.alpha[h] = m_run == -INFINITY ? 0.f : exp2f(m_run - mn);
+        l_run *= ms.alpha[h];
+        m_run = mn;
       }
       named_bar(1, kSoftmax);
       if (t > 0) {
-        // rescale O^T once it holds exactly the tiles before t (O_{t-1} complete)
-        wait_or_abort(ms, &ms.p_free, (t - 1) & 1, a.err);
+        // O^T holds exactly the tiles before t once O_{t-1} is complete
+        wait_or_abort(ms, &ms.o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, a.err);
         tc_fence_after();
+        const uint32_t my_lane = tmem + ((uint32_t)(w * 32) << 16);
 #pragma unroll
         for (int c = 0; c < kChunks; ++c) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             float o[16];
-            tmem_ld16(lane_addr + kColO + 64 * c + 16 * i, o);
+            tmem_ld16(my_lane + kColO + 64 * c + 16 * i, o);
             tmem_wait_ld();
 #pragma unroll
             for (int j = 0; j < 16; ++j) o[j] *= ms.alpha[16 * i + j];
-            tmem_st16(lane_addr + kColO + 64 * c + 16 * i, o);
+            tmem_st16(my_lane + kColO + 64 * c + 16 * i, o);
           }
         }
         tmem_wait_st();
       }
-#pragma unroll
-      for (int h = 0; h < kH; ++h) lsum[h] *= ms.alpha[h];
     }
-    // probabilities of this key for every head, 8 heads per 16-byte piece of the
-    // key's 128-byte P^T row; P carries the key's dequant scale
-    uint32_t pw[kH / 2];
+    // probabilities of this head for the tile's keys: one 128-byte P row,
+    // 8 keys per 16-byte piece; P carries each key's dequant scale
+    uint32_t pw[kTile / 2];
 #pragma unroll
-    for (int h = 0; h < kH; h += 2) {
-      const float m0 = ms.M[h], m1 = ms.M[h + 1];
-      const float p0 = (x[h] == -INFINITY || m0 == -INFINITY) ? 0.f : fast_exp2(x[h] - m0);
-      const float p1 = (x[h + 1] == -INFINITY || m1 == -INFINITY) ? 0.f : fast_exp2(x[h + 1] - m1);
-      lsum[h] += p0;
-      lsum[h + 1] += p1;
-      pw[h / 2] = (uint32_t)f32_to_bf16(p0 * ksc) | ((uint32_t)f32_to_bf16(p1 * ksc) << 16);
+    for (int k = 0; k < kTile; k += 2) {
+      const float p0 = (x[k] == -INFINITY || m_run == -INFINITY) ? 0.f : fast_exp2(x[k] - m_run);
+      const float p1 = (x[k + 1] == -INFINITY || m_run == -INFINITY) ? 0.f : fast_exp2(x[k + 1] - m_run);
+      l_run += p0 + p1;
+      pw[k / 2] = (uint32_t)f32_to_bf16(p0 * ms.kscale[b][k]) | ((uint32_t)f32_to_bf16(p1 * ms.kscale[b][k + 1]) << 16);
     }
-    // the P buffer is free once O_{t-1} has consumed it
-    if (t > 0) wait_or_abort(ms, &ms.p_free, (t - 1) & 1, a.err);
+    // the P buffer is free once O_{t-2} has consumed it
+    if (t >= 2) wait_or_abort(ms, &ms.o_done[slot], ((t - 2) >> 1) & 1, a.err);
+    if (owner) {
+      uint8_t* prow = smem + kOffP + slot * kPBytes + (h >> 3) * 1024 + (h & 7) * 128;
 #pragma unroll
-    for (int c = 0; c < 8; ++c)
-      *reinterpret_cast<uint4*>(prow + ((c ^ (st & 7)) << 4)) =
-          make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(prow + ((c ^ (h & 7)) << 4)) =
+            make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
+    }
     fence_proxy_async();
     tc_fence_before();
-    mbar_arrive(&ms.p_full);
-    // tile t-1 is done with its address buffer (O_{t-1} is complete): look ahead
+    mbar_arrive(&ms.p_full[slot]);
+    // tile t-1 is done with its address buffer: look ahead
     if (t + kRowBufs - 1 < g.n_tiles) lookup_keys(a, g, ms, t + kRowBufs - 1, st);
   }
 
   // ---- epilogue
-  if (g.n_tiles > 0) wait_or_abort(ms, &ms.p_free, (g.n_tiles - 1) & 1, a.err);
+  if (g.n_tiles > 0) wait_or_abort(ms, &ms.o_done[(g.n_tiles - 1) & 1], ((g.n_tiles - 1) >> 1) & 1, a.err);
   tc_fence_after();
-  warp_reduce64<false>(lsum, ms, st);
+  if (owner) {
+    ms.M[h] = m_run;
+    ms.L[h] = l_run;  // sum over the slice's keys of 2^(x - M[h])
+  }
   named_bar(1, kSoftmax);
-  if (st < kH) ms.L[st] = (ms.red[0][st] + ms.red[1][st]) + (ms.red[2][st] + ms.red[3][st]);
-  named_bar(1, kSoftmax);  // ms.L[h] = sum over the slice's keys of 2^(x - M[h])
   const int S = gridDim.y;
+  const uint32_t my_lane = tmem + ((uint32_t)(w * 32) << 16);
   if (S == 1) {
-    // stage the row's unnormalised O^T as [64 heads][512 dims] fp32 in the idle key buffer
+    // stage the row's unnormalised O^T as [64 heads][512 dims] fp32 in the idle key ring
     float* stage = reinterpret_cast<float*>(smem + kOffK);
     for (int c = 0; c < kChunks; ++c) {
       float o[kH];
-      load_o_chunk(lane_addr + kColO + 64 * c, g.n_tiles > 0, o);
+      load_o_chunk(my_lane + kColO + 64 * c, g.n_tiles > 0, o);
 #pragma unroll
-      for (int h = 0; h < kH; ++h) stage[h * kD + 128 * c + st] = o[h];
+      for (int hh = 0; hh < kH; ++hh) stage[hh * kD + 128 * c + st] = o[hh];
     }
     return;
   }
@@ -522,16 +520,16 @@ __device__ void softmax_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mis
   uint8_t* stage = smem + kOffK;
   for (int c = 0; c < kChunks; ++c) {
     float o[kH];
-    load_o_chunk(lane_addr + kColO + 64 * c, g.n_tiles > 0, o);
+    load_o_chunk(my_lane + kColO + 64 * c, g.n_tiles > 0, o);
     const int d = 128 * c + st;
 #pragma unroll
     for (int q = 0; q < kH / 8; ++q) {
       const int m = 8 * q / per, hh = 8 * q - m * per;
-      uint32_t w[4];
+      uint32_t wv[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e)
-        w[e] = (uint32_t)f32_to_bf16(o[8 * q + 2 * e]) | ((uint32_t)f32_to_bf16(o[8 * q + 2 * e + 1]) << 16);
-      *reinterpret_cast<uint4*>(stage + (((size_t)m * kD + d) * per + hh) * 2) = make_uint4(w[0], w[1], w[2], w[3]);
+        wv[e] = (uint32_t)f32_to_bf16(o[8 * q + 2 * e]) | ((uint32_t)f32_to_bf16(o[8 * q + 2 * e + 1]) << 16);
+      *reinterpret_cast<uint4*>(stage + (((size_t)m * kD + d) * per + hh) * 2) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
     }
   }
   fence_proxy_async();  // the copy engine reads the staging
@@ -718,14 +716,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnArgs a) 
   pdl_trigger();
 
   if (tid == 0) {
-    for (int c = 0; c < kChunks; ++c) {
-      mbar_init(&ms.kfull[c], kProducers);
-      mbar_init(&ms.kfree[c], 1);
+    for (int b = 0; b < 2; ++b) {
+      for (int c = 0; c < kChunks; ++c) mbar_init(&ms.kfull[b][c], kProducers);
+      mbar_init(&ms.o_done[b], 1);
+      mbar_init(&ms.s_full[b], 1);
+      mbar_init(&ms.p_full[b], kSoftmax);
     }
-    for (int b = 0; b < 2; ++b) mbar_init(&ms.s_full[b], 1);
     for (int b = 0; b < kRowBufs; ++b) mbar_init(&ms.rows_ready[b], kSoftmax);
-    mbar_init(&ms.p_full, kSoftmax);
-    mbar_init(&ms.p_free, 1);
     mbar_init(&ms.q_full, kSoftmax);
     mbar_init(&ms.mma_done, 1);
     mbar_init(&ms.recv, 1);
@@ -780,8 +777,9 @@ bool attn_tc_eligible(const AttnArgs& a) {
 }
 
 int32_t attn_tc_splits(int32_t n_rows, int32_t keys_per_row) {
-  // a power of two <= 8 (one cluster per row), about one CTA per SM in all
-  const int32_t tiles = (keys_per_row + kTile - 1) / kTile;
+  // a power of two <= 8 (one cluster per row), about one CTA per SM in all, and
+  // at least 256 keys per CTA
+  const int32_t tiles = (keys_per_row + 127) / 128;
   int32_t s = 1;
   while (s < 8 && 2 * s * n_rows <= 148 && 2 * s <= tiles) s *= 2;
   return s;
