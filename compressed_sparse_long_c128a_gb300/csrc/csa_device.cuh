@@ -89,6 +89,13 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float x) {
   return *reinterpret_cast<uint16_t*>(&h);
 }
 
+// Two floats rounded to bf16 (nearest even) in one instruction: lo in bits 0..15, hi in 16..31.
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 // e4m3 (fn): sign | 4 exponent bits (bias 7) | 3 mantissa bits; exponent 0 is
 // subnormal (m * 2^-9); 0x7f / 0xff are NaN.
 __device__ __forceinline__ float e4m3_to_f32(uint8_t v) {

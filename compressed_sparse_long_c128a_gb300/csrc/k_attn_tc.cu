@@ -22,8 +22,8 @@
 // columns 0..127 (M = 64 layout: head h in lane 32*(h/16) + h%16), O^T chunk c
 // in 128+64c.
 //
-// Warp roles: warps 0-3 are the softmax (lanes 0-15 own one head each: the
-// row max and the denominator stay in a register) and the epilogue (thread t
+// Warp roles: warps 0-3 are the softmax (lanes l and l+16 share head 16w+l: the
+// row max and the denominator stay in registers) and the epilogue (thread t
 // owns TMEM lane t: dim t of an O^T chunk); they also look the tile's row
 // addresses up three tiles ahead.  Warps 4-6 gather the rows from the paged
 // caches (cp.async for bf16, load + convert for e4m3, whose per-row scale is
@@ -61,8 +61,9 @@ constexpr float kRescaleMargin = 8.0f;       // log2 units
 constexpr int kRowBufs = 4;                  // tiles whose row addresses are known ahead
 
 struct Misc {
-  uint64_t kfull[2][kChunks];  // tile slot, chunk
-  uint64_t o_done[2];          // O^T of the slot's tile complete: slot and P buffer free
+  uint64_t kfull[2][kChunks];  // tile slot, chunk: loaded
+  uint64_t kfree[2][kChunks];  // tile slot, chunk: consumed by O^T
+  uint64_t o_done[2];          // O^T of the slot's tile complete: P buffer free
   uint64_t s_full[2], p_full[2], rows_ready[kRowBufs], q_full, mma_done, recv;
   uint32_t tmem_base;
   int32_t abort;
@@ -141,8 +142,8 @@ __device__ __forceinline__ const uint8_t* key_row(const AttnArgs& a, const Geo& 
   return reinterpret_cast<const uint8_t*>(c->data) + prow * (int64_t)kD * (fp8 ? 1 : 2);
 }
 
-// Producers: tile t goes to ring slot t & 1 once O^T of tile t-2 has released
-// it, one 16 KB chunk (128 dims) at a time.  bf16 rows are copied with
+// Producers: tile t goes to ring slot t & 1, one 16 KB chunk (128 dims) at a
+// time, each chunk as soon as O^T of tile t-2 has released it.  bf16 rows are copied with
 // cp.async, each thread's copies arriving on the chunk's barrier as they land
 // (the MMA issuer fences them into the async proxy); e4m3 rows are converted
 // through registers.  Keys past the slice are not loaded; the rest of the last
@@ -156,7 +157,7 @@ __device__ void producer_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mi
   for (int t = 0; t < n; ++t) {
     const int slot = t & 1, buf = t % kRowBufs;
     wait_or_abort(ms, &ms.rows_ready[buf], (t / kRowBufs) & 1, a.err);
-    if (t >= 2) wait_or_abort(ms, &ms.o_done[slot], ((t - 2) >> 1) & 1, a.err);
+    const uint32_t prev = ((t - 2) >> 1) & 1;  // use of the slot by tile t-2
     const int lim = min(kTile, (g.keys(t) + 15) & ~15);
     const uint32_t tbase = smem_u32(smem + kOffK) + slot * kTileBytes;
     if (!fp8) {
@@ -168,6 +169,7 @@ __device__ void producer_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mi
       }
       const uint32_t poff = (piece >> 3) * kAtomBytes;
       for (int c = 0; c < kChunks; ++c) {
+        if (t >= 2) wait_or_abort(ms, &ms.kfree[slot][c], prev, a.err);
         const uint32_t cbase = tbase + c * kChunkBytes + poff;
 #pragma unroll
         for (int j = 0; j < kPerThr; ++j) {
@@ -183,6 +185,7 @@ __device__ void producer_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mi
       // 8 consecutive threads per key row: 128 code bytes -> 128 bf16 (exact)
       constexpr int kIters = (kTile * 8 + kProducers - 1) / kProducers;
       for (int c = 0; c < kChunks; ++c) {
+        if (t >= 2) wait_or_abort(ms, &ms.kfree[slot][c], prev, a.err);
         uint4 raw[kIters];
 #pragma unroll
         for (int it = 0; it < kIters; ++it) {
@@ -203,8 +206,7 @@ __device__ void producer_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mi
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const uint32_t b0 = (w[e >> 1] >> ((e & 1) * 16)) & 0xFF, b1 = (w[e >> 1] >> ((e & 1) * 16 + 8)) & 0xFF;
-            outw[e] = (uint32_t)f32_to_bf16(e4m3_to_f32((uint8_t)b0)) |
-                      ((uint32_t)f32_to_bf16(e4m3_to_f32((uint8_t)b1)) << 16);
+            outw[e] = f32x2_to_bf16x2(e4m3_to_f32((uint8_t)b0), e4m3_to_f32((uint8_t)b1));
           }
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
@@ -282,6 +284,7 @@ __device__ void mma_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Misc& m
           if (ks < ksteps)
             mma_bf16(tmem + kColO + 64 * c, d_ko + toff + ((c * kChunkBytes + ks * 2048) >> 4),
                      d_p + poff + ((ks * 32) >> 4), idesc_o, (t > 0 || ks > 0) ? 1u : 0u);
+        mma_commit(&ms.kfree[slot][c]);  // the chunk can take tile t+2's rows
       }
       mma_commit(&ms.o_done[slot]);
     }
@@ -302,7 +305,7 @@ __device__ __forceinline__ uint32_t rot_pack(float q0, float q1, int d, float qs
     q1 = q0 * sn + q1 * cs;
     q0 = t0;
   }
-  return (uint32_t)f32_to_bf16(q0 * qs) | ((uint32_t)f32_to_bf16(q1 * qs) << 16);
+  return f32x2_to_bf16x2(q0 * qs, q1 * qs);
 }
 
 // Q operand: the row's 64 heads rotated at p, scaled by scale * log2(e),
@@ -409,27 +412,41 @@ __device__ void softmax_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mis
   fill_q_finish(a, smem, ms, st);
   for (int u = 1; u < min(g.n_tiles, kRowBufs - 1); ++u) lookup_keys(a, g, ms, u, st);
   const int w = st >> 5, l = st & 31;
-  const bool owner = l < 16;         // lanes 0-15 of each warp own a head of S
-  const int h = 16 * w + (l & 15);   // the head (owners only)
+  // lanes l and l+16 of warp w share head 16w + l (lanes 0-15 hold its TMEM row):
+  // lane l takes keys [0, 32) of each tile, lane l+16 keys [32, 64)
+  const int hf = l >> 4, h = 16 * w + (l & 15);
+  const bool fp8 = a.comp.dtype == CSA_E4M3;
   const uint32_t lane_addr = tmem + ((uint32_t)(w * 32) << 16);
-  float m_run = -INFINITY, l_run = 0.f;  // this head's running max and denominator
+  float m_run = -INFINITY, l_run = 0.f;  // the head's running max; this half's denominator
 
   for (int t = 0; t < g.n_tiles; ++t) {
     const int slot = t & 1, b = t % kRowBufs;
     const uint32_t use = (t >> 1) & 1;
     wait_or_abort(ms, &ms.s_full[slot], use, a.err);
     tc_fence_after();
-    float x[kTile];
+    float x[kTile / 2];
+    {
+      float xt[kTile];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) tmem_ld16(lane_addr + kColS + 64 * slot + 16 * i, x + 16 * i);
-    tmem_wait_ld();
+      for (int i = 0; i < 4; ++i) tmem_ld16(lane_addr + kColS + 64 * slot + 16 * i, xt + 16 * i);
+      tmem_wait_ld();
+#pragma unroll
+      for (int k = 0; k < kTile / 2; ++k) {
+        const float hi = __shfl_sync(0xffffffffu, xt[kTile / 2 + k], l & 15);
+        x[k] = hf ? hi : xt[k];
+      }
+    }
     wait_or_abort(ms, &ms.rows_ready[b], (t / kRowBufs) & 1, a.err);
+    const int k0 = hf * (kTile / 2);
     float mt = -INFINITY;
 #pragma unroll
-    for (int k4 = 0; k4 < kTile / 4; ++k4) {
-      const float4 sc = *reinterpret_cast<const float4*>(&ms.kscale[b][4 * k4]);
-      const uint32_t vb = *reinterpret_cast<const uint32_t*>(&ms.kvalid[b][4 * k4]);
-      const float s4[4] = {sc.x, sc.y, sc.z, sc.w};
+    for (int k4 = 0; k4 < kTile / 8; ++k4) {
+      const uint32_t vb = *reinterpret_cast<const uint32_t*>(&ms.kvalid[b][k0 + 4 * k4]);
+      float s4[4] = {1.f, 1.f, 1.f, 1.f};
+      if (fp8) {
+        const float4 sc = *reinterpret_cast<const float4*>(&ms.kscale[b][k0 + 4 * k4]);
+        s4[0] = sc.x; s4[1] = sc.y; s4[2] = sc.z; s4[3] = sc.w;
+      }
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int k = 4 * k4 + e;
@@ -437,72 +454,79 @@ __device__ void softmax_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mis
         mt = fmaxf(mt, x[k]);
       }
     }
-    const bool need = owner && mt > m_run + kRescaleMargin;
-    if (named_bar_or(1, kSoftmax, need)) {
-      // raise every head's max to its current maximum; rescale O^T and the denominator
-      if (owner) {
-        const float mn = fmaxf(m_run, mt);
-        ms.alpha[h] = m_run == -INFINITY ? 0.f : exp2f(m_run - mn);
-        l_run *= ms.alpha[h];
-        m_run = mn;
-      }
+    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));  // the head's tile max
+    if (named_bar_or(1, kSoftmax, mt > m_run + kRescaleMargin)) {
+      // raise every head's max to its current maximum; rescale O^T and the denominators
+      const float mn = fmaxf(m_run, mt);
+      const float al = m_run == -INFINITY ? 0.f : exp2f(m_run - mn);
+      if (hf == 0) ms.alpha[h] = al;
+      l_run *= al;
+      m_run = mn;
       named_bar(1, kSoftmax);
       if (t > 0) {
         // O^T holds exactly the tiles before t once O_{t-1} is complete
         wait_or_abort(ms, &ms.o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, a.err);
         tc_fence_after();
-        const uint32_t my_lane = tmem + ((uint32_t)(w * 32) << 16);
 #pragma unroll
         for (int c = 0; c < kChunks; ++c) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             float o[16];
-            tmem_ld16(my_lane + kColO + 64 * c + 16 * i, o);
+            tmem_ld16(lane_addr + kColO + 64 * c + 16 * i, o);
             tmem_wait_ld();
 #pragma unroll
             for (int j = 0; j < 16; ++j) o[j] *= ms.alpha[16 * i + j];
-            tmem_st16(my_lane + kColO + 64 * c + 16 * i, o);
+            tmem_st16(lane_addr + kColO + 64 * c + 16 * i, o);
           }
         }
         tmem_wait_st();
       }
     }
-    // probabilities of this head for the tile's keys: one 128-byte P row,
-    // 8 keys per 16-byte piece; P carries each key's dequant scale
-    uint32_t pw[kTile / 2];
+    // probabilities of this head for this half of the tile's keys: 64 bytes of
+    // the head's P row, 8 keys per 16-byte piece; P carries each key's dequant scale
+    uint32_t pw[kTile / 4];
+    float ls[4] = {0.f, 0.f, 0.f, 0.f};
+    if (m_run == -INFINITY) {
 #pragma unroll
-    for (int k = 0; k < kTile; k += 2) {
-      const float p0 = (x[k] == -INFINITY || m_run == -INFINITY) ? 0.f : fast_exp2(x[k] - m_run);
-      const float p1 = (x[k + 1] == -INFINITY || m_run == -INFINITY) ? 0.f : fast_exp2(x[k + 1] - m_run);
-      l_run += p0 + p1;
-      pw[k / 2] = (uint32_t)f32_to_bf16(p0 * ms.kscale[b][k]) | ((uint32_t)f32_to_bf16(p1 * ms.kscale[b][k + 1]) << 16);
+      for (int k = 0; k < kTile / 4; ++k) pw[k] = 0u;
+    } else {
+#pragma unroll
+      for (int k = 0; k < kTile / 2; k += 2) {
+        float p0 = fast_exp2(x[k] - m_run), p1 = fast_exp2(x[k + 1] - m_run);  // exp2(-inf) = 0
+        ls[(k >> 1) & 3] += p0 + p1;
+        if (fp8) {
+          p0 *= ms.kscale[b][k0 + k];
+          p1 *= ms.kscale[b][k0 + k + 1];
+        }
+        pw[k / 2] = f32x2_to_bf16x2(p0, p1);
+      }
     }
+    l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
     // the P buffer is free once O_{t-2} has consumed it
     if (t >= 2) wait_or_abort(ms, &ms.o_done[slot], ((t - 2) >> 1) & 1, a.err);
-    if (owner) {
-      uint8_t* prow = smem + kOffP + slot * kPBytes + (h >> 3) * 1024 + (h & 7) * 128;
+    uint8_t* prow = smem + kOffP + slot * kPBytes + (h >> 3) * 1024 + (h & 7) * 128;
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(prow + ((c ^ (h & 7)) << 4)) =
-            make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
-    }
+    for (int c = 0; c < 4; ++c)
+      *reinterpret_cast<uint4*>(prow + (((4 * hf + c) ^ (h & 7)) << 4)) =
+          make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
     fence_proxy_async();
     tc_fence_before();
     mbar_arrive(&ms.p_full[slot]);
     // tile t-1 is done with its address buffer: look ahead
     if (t + kRowBufs - 1 < g.n_tiles) lookup_keys(a, g, ms, t + kRowBufs - 1, st);
   }
+  l_run += __shfl_xor_sync(0xffffffffu, l_run, 16);  // both halves of the head's keys
 
   // ---- epilogue
   if (g.n_tiles > 0) wait_or_abort(ms, &ms.o_done[(g.n_tiles - 1) & 1], ((g.n_tiles - 1) >> 1) & 1, a.err);
   tc_fence_after();
-  if (owner) {
+  if (hf == 0) {
     ms.M[h] = m_run;
     ms.L[h] = l_run;  // sum over the slice's keys of 2^(x - M[h])
   }
   named_bar(1, kSoftmax);
   const int S = gridDim.y;
-  const uint32_t my_lane = tmem + ((uint32_t)(w * 32) << 16);
+  const uint32_t my_lane = lane_addr;
   if (S == 1) {
     // stage the row's unnormalised O^T as [64 heads][512 dims] fp32 in the idle key ring
     float* stage = reinterpret_cast<float*>(smem + kOffK);
@@ -516,7 +540,7 @@ __device__ void softmax_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mis
   }
   // split row: stage the slice's unnormalised O in bf16 in the idle ring, grouped
   // by the CTA that merges each head: [merger][512 dims][heads of the merger]
-  const int per = kH / S;
+  const int per = kH / S, lper = __ffs(per) - 1;  // per is a power of two
   uint8_t* stage = smem + kOffK;
   for (int c = 0; c < kChunks; ++c) {
     float o[kH];
@@ -524,11 +548,10 @@ __device__ void softmax_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mis
     const int d = 128 * c + st;
 #pragma unroll
     for (int q = 0; q < kH / 8; ++q) {
-      const int m = 8 * q / per, hh = 8 * q - m * per;
+      const int m = (8 * q) >> lper, hh = (8 * q) & (per - 1);
       uint32_t wv[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        wv[e] = (uint32_t)f32_to_bf16(o[8 * q + 2 * e]) | ((uint32_t)f32_to_bf16(o[8 * q + 2 * e + 1]) << 16);
+      for (int e = 0; e < 4; ++e) wv[e] = f32x2_to_bf16x2(o[8 * q + 2 * e], o[8 * q + 2 * e + 1]);
       *reinterpret_cast<uint4*>(stage + (((size_t)m * kD + d) * per + hh) * 2) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
     }
   }
@@ -565,7 +588,7 @@ __device__ void store_head16(const AttnArgs& a, const Misc& ms, int r, int h, fl
   } else if (a.out_dtype == CSA_BF16) {
     uint32_t wv[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) wv[q] = (uint32_t)f32_to_bf16(v[2 * q]) | ((uint32_t)f32_to_bf16(v[2 * q + 1]) << 16);
+    for (int q = 0; q < 8; ++q) wv[q] = f32x2_to_bf16x2(v[2 * q], v[2 * q + 1]);
     uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + ob);
     dst[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
     dst[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
@@ -696,7 +719,7 @@ __device__ void merge_split(const AttnArgs& a, uint8_t* smem, Misc& ms) {
 #pragma unroll
     for (int hh = 0; hh < kPer; ++hh)
       *reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(a.out) + ob + (int64_t)(h0 + hh) * kD) =
-          (uint32_t)f32_to_bf16(v[0][hh]) | ((uint32_t)f32_to_bf16(v[1][hh]) << 16);
+          f32x2_to_bf16x2(v[0][hh], v[1][hh]);
   } else {
 #pragma unroll
     for (int hh = 0; hh < kPer; ++hh)
@@ -717,7 +740,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnArgs a) 
 
   if (tid == 0) {
     for (int b = 0; b < 2; ++b) {
-      for (int c = 0; c < kChunks; ++c) mbar_init(&ms.kfull[b][c], kProducers);
+      for (int c = 0; c < kChunks; ++c) {
+        mbar_init(&ms.kfull[b][c], kProducers);
+        mbar_init(&ms.kfree[b][c], 1);
+      }
       mbar_init(&ms.o_done[b], 1);
       mbar_init(&ms.s_full[b], 1);
       mbar_init(&ms.p_full[b], kSoftmax);
