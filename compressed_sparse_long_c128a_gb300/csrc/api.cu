@@ -62,6 +62,36 @@ constexpr unsigned kF32 = 1u << CSA_F32, kBF16 = 1u << CSA_BF16, kE4M3 = 1u << C
 
 size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
 
+// cuTensorMapEncodeTiled, fetched from the driver once.
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiled encode_tiled() {
+  static EncodeTiled fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<EncodeTiled>(p);
+  }();
+  return fn;
+}
+
+// The tensor-core attention's query tensor: n_rows*64 rows of 512 bf16, boxes of
+// 64 dims x 64 heads, 128-byte swizzle (the layout of its shared Q operand).
+bool encode_q_map(CUtensorMap* m, const void* q, int32_t n_rows) {
+  const EncodeTiled fn = encode_tiled();
+  if (!fn || (reinterpret_cast<uintptr_t>(q) & 15)) return false;
+  const cuuint64_t dims[2] = {512, (cuuint64_t)n_rows * 64};
+  const cuuint64_t strides[1] = {512 * 2};
+  const cuuint32_t box[2] = {64, 64};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int attn_common(const csa_layer* L, const void* q, int32_t q_dtype, int32_t n_rows, const int32_t* seq_id,
                 const int32_t* pos, const csa_paged* comp, const csa_block_table* comp_bt, const int32_t* topk,
                 int32_t k, int32_t max_n, const csa_paged* swa, const csa_block_table* swa_bt, void* out,
@@ -102,6 +132,8 @@ int attn_common(const csa_layer* L, const void* q, int32_t q_dtype, int32_t n_ro
   a.scale = L->scale;
   a.rope = make_rope(L->rope_dim, L->rope_theta);
   const bool tc = attn_tc_eligible(a);
+  std::memset(&a.q_map, 0, sizeof(a.q_map));
+  a.q_tma = tc && q_dtype == CSA_BF16 && encode_q_map(&a.q_map, q, n_rows);
   a.n_splits = tc ? attn_tc_splits(n_rows, keys) : attn_splits(n_rows, L->heads, keys);
   const size_t need = attn_workspace_bytes(n_rows, L->heads, L->dim, a.n_splits);
   if (need && (!ws || ws_bytes < need)) return CSA_ERR_WORKSPACE;

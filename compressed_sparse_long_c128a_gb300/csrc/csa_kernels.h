@@ -1,6 +1,7 @@
 // Internal launch interface between the C-ABI layer (api.cu) and the kernels.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (type only; the encoder is fetched at run time)
 #include <cuda_runtime.h>
 
 #include "csa_device.cuh"
@@ -133,6 +134,10 @@ struct AttnArgs {
   float* part_o;  // [n_rows][heads][n_splits][dim]
   float* part_ml; // [n_rows][heads][n_splits][2]
   int32_t* err;
+  // tensor-core path: bf16 query rows as a [rows*64][512] tensor, 64x64 boxes,
+  // 128-byte swizzle (q_tma = 0 when q cannot be described, e.g. unaligned)
+  CUtensorMap q_map;
+  int32_t q_tma;
 };
 int32_t attn_splits(int32_t n_rows, int32_t heads, int32_t keys_per_row);
 size_t attn_workspace_bytes(int32_t n_rows, int32_t heads, int32_t dim, int32_t n_splits);

@@ -17,17 +17,18 @@
 // ring of two 64 KB key tiles and two P buffers.  A key tile is gathered once,
 // 128B-swizzled with keys as rows: read K-major it is the B operand of S, read
 // MN-major the A operand of O^T (values = keys).  While one tile is in use the
-// next is being gathered; the tensor pipe runs S_0, S_1, O_0, S_2, O_1, ...,
-// so the softmax of tile t overlaps S_{t+1}.  TMEM: S double-buffered in
+// next is being gathered; the tensor pipe takes S chunks as their rows land
+// and O of a tile as soon as its P is written, so the softmax of tile t
+// overlaps S_{t+1}.  TMEM: S double-buffered in
 // columns 0..127 (M = 64 layout: head h in lane 32*(h/16) + h%16), O^T chunk c
 // in 128+64c.
 //
-// Warp roles: warps 0-3 are the softmax (lanes l and l+16 share head 16w+l: the
+// Warp roles (12 warps): warps 0-3 are the softmax (lanes l and l+16 share head 16w+l: the
 // row max and the denominator stay in registers) and the epilogue (thread t
 // owns TMEM lane t: dim t of an O^T chunk); they also look the tile's row
-// addresses up three tiles ahead.  Warps 4-6 gather the rows from the paged
+// addresses up three tiles ahead.  Warps 4-10 gather the rows from the paged
 // caches (cp.async for bf16, load + convert for e4m3, whose per-row scale is
-// folded into the logits and into P).  Warp 7 allocates TMEM and one lane
+// folded into the logits and into P).  Warp 11 allocates TMEM and one lane
 // issues the MMAs.  The running per-head max is only raised when a logit
 // exceeds it by more than 2^8; raising it rescales O^T in TMEM.
 //
@@ -46,8 +47,10 @@ namespace {
 using namespace tc;
 
 constexpr int kD = 512, kH = 64, kTile = 64, kChunks = 4;
-constexpr int kSoftmax = 128, kProducers = 96;
+constexpr int kSoftmax = 128, kProducers = 224;
 constexpr int kThreads = kSoftmax + kProducers + 32;
+constexpr int kMmaWarp = kThreads / 32 - 1;
+constexpr int kMergeThreads = 256;  // thread t of the merge takes dims 2t and 2t+1
 constexpr uint32_t kQBytes = kH * kD * 2;             // 64 KB
 constexpr uint32_t kChunkBytes = kTile * 128 * 2;     // 16 KB: 64 keys x 128 dims
 constexpr uint32_t kAtomBytes = kTile * 128;          // 8 KB: 64 keys x 64 dims
@@ -64,13 +67,13 @@ struct Misc {
   uint64_t kfull[2][kChunks];  // tile slot, chunk: loaded
   uint64_t kfree[2][kChunks];  // tile slot, chunk: consumed by O^T
   uint64_t o_done[2];          // O^T of the slot's tile complete: P buffer free
-  uint64_t s_full[2], p_full[2], rows_ready[kRowBufs], q_full, mma_done, recv;
+  uint64_t s_full[2], p_full[2], rows_ready[kRowBufs], q_raw, q_full, mma_done, recv;
   uint32_t tmem_base;
   int32_t abort;
   alignas(16) float M[kH];  // per-head max (log2 domain) of the slice, for the merge
   alignas(16) float L[kH];  // softmax denominators of the slice
   float red[4][kH];         // merge weights
-  float amax[kThreads / 32][32];  // per-warp head maxima of the merged output
+  float amax[kMergeThreads / 32][32];  // per-warp head maxima of the merged output
   float alpha[kH];          // rescale factor of the last max raise
   alignas(16) float rM[8][32], rL[8][32];  // merged heads' max and denominator of each slice (split rows)
   float rc[kMaxRopePairs], rs[kMaxRopePairs];  // cos / sin of each rotary pair at the row's position
@@ -227,20 +230,11 @@ __device__ void producer_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mi
 
 // ------------------------------------------------------------------ MMA issuer
 
-// Phase i of the tensor pipe over n tiles: S_0, S_1, O_0, S_2, O_1, ..., S_{n-1}, O_{n-2}, O_{n-1}.
-__device__ __forceinline__ int phase_tile(int i, int n, bool& is_s) {
-  if (i == 0) {
-    is_s = true;
-    return 0;
-  }
-  if (i == 2 * n - 1) {
-    is_s = false;
-    return n - 1;
-  }
-  is_s = (i & 1) != 0;
-  return is_s ? (i + 1) >> 1 : (i >> 1) - 1;
-}
-
+// One lane issues every MMA.  Work becomes ready in two streams: the S chunks
+// of tile t as its rows land (each also needs the S buffer free: O of tile
+// t-2 issued, i.e. its softmax done), and O of tile t once its P is written.
+// O is issued as soon as it is ready, ahead of the S chunks still waiting for
+// rows, because it releases the ring slot the next tile loads into.
 __device__ void mma_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Misc& ms, uint32_t tmem) {
   constexpr uint32_t idesc_s = idesc_bf16(64, kTile, 0, 0);   // A = Q (K-major), B = key tile (K-major)
   constexpr uint32_t idesc_o = idesc_bf16(128, kH, 1, 0);     // A = key tile^T (MN-major), B = P (K-major)
@@ -251,32 +245,15 @@ __device__ void mma_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Misc& m
   const uint64_t d_p = sdesc_sw128(smem_u32(smem + kOffP), 16, 1024);
   const int n = g.n_tiles;
   wait_or_abort(ms, &ms.q_full, 0, a.err);
-  for (int i = 0; i < 2 * n; ++i) {
-    bool is_s;
-    const int t = phase_tile(i, n, is_s), slot = t & 1;
-    const uint32_t use = (t >> 1) & 1;
-    const uint32_t toff = (slot * kTileBytes) >> 4;
-    if (is_s) {
-      const uint32_t d_s = tmem + kColS + 64 * slot;
-#pragma unroll
-      for (int c = 0; c < kChunks; ++c) {
-        wait_or_abort(ms, &ms.kfull[slot][c], use, a.err);
-        fence_proxy_async();  // the chunk was written through the generic proxy
-        tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t k0 = c * 128 + ks * 16;  // first dim of this K step
-          mma_bf16(d_s, d_q + (((k0 >> 6) * (kH * 128) + (k0 & 63) * 2) >> 4),
-                   d_ks + toff + ((c * kChunkBytes + (ks >> 2) * kAtomBytes + (ks & 3) * 32) >> 4), idesc_s,
-                   (c | ks) != 0);
-        }
-      }
-      mma_commit(&ms.s_full[slot]);
-    } else {
-      wait_or_abort(ms, &ms.p_full[slot], use, a.err);
+  int st_t = 0, st_c = 0, o_t = 0;  // next S chunk (tile, chunk); next O tile
+  int idle = 0;
+  while (o_t < n) {
+    if (*reinterpret_cast<volatile int32_t*>(&ms.abort)) break;
+    if (o_t < st_t && mbar_test(&ms.p_full[o_t & 1], (o_t >> 1) & 1)) {
+      const int t = o_t, slot = t & 1;
       tc_fence_after();
       const int ksteps = (g.keys(t) + 15) >> 4;
-      const uint32_t poff = (slot * kPBytes) >> 4;
+      const uint32_t toff = (slot * kTileBytes) >> 4, poff = (slot * kPBytes) >> 4;
 #pragma unroll
       for (int c = 0; c < kChunks; ++c) {
 #pragma unroll
@@ -287,6 +264,34 @@ __device__ void mma_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Misc& m
         mma_commit(&ms.kfree[slot][c]);  // the chunk can take tile t+2's rows
       }
       mma_commit(&ms.o_done[slot]);
+      ++o_t;
+      idle = 0;
+      continue;
+    }
+    if (st_t < n && st_t <= o_t + 1 && mbar_test(&ms.kfull[st_t & 1][st_c], (st_t >> 1) & 1)) {
+      const int t = st_t, slot = t & 1, c = st_c;
+      fence_proxy_async();  // the chunk was written through the generic proxy
+      tc_fence_after();
+      const uint32_t d_s = tmem + kColS + 64 * slot;
+      const uint32_t koff = (slot * kTileBytes + c * kChunkBytes) >> 4;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t k0 = c * 128 + ks * 16;  // first dim of this K step
+        mma_bf16(d_s, d_q + (((k0 >> 6) * (kH * 128) + (k0 & 63) * 2) >> 4),
+                 d_ks + koff + (((ks >> 2) * kAtomBytes + (ks & 3) * 32) >> 4), idesc_s, (c | ks) != 0);
+      }
+      if (++st_c == kChunks) {
+        mma_commit(&ms.s_full[slot]);
+        st_c = 0;
+        ++st_t;
+      }
+      idle = 0;
+      continue;
+    }
+    if (++idle > 4 * kSpinLimit) {
+      *reinterpret_cast<volatile int32_t*>(&ms.abort) = 1;
+      record_error(a.err, CSA_ERR_TIMEOUT);
+      break;
     }
   }
   // nothing may still write TMEM when it is released, even after a timeout
@@ -309,15 +314,24 @@ __device__ __forceinline__ uint32_t rot_pack(float q0, float q1, int d, float qs
 }
 
 // Q operand: the row's 64 heads rotated at p, scaled by scale * log2(e),
-// rounded to bf16, 128B-swizzled K-major (rows = heads).  bf16 rows are
-// copied raw with cp.async as the very first requests of the CTA (ahead of the
-// key lookups, which wait for the previous launch) and then transformed in
-// place, each thread on the pieces it copied itself; fp32 rows go through
-// registers.  The softmax threads then release the MMA issuer through q_full.
+// rounded to bf16, 128B-swizzled K-major (rows = heads).  bf16 rows arrive
+// raw as the CTA's first requests (eight TMA boxes of 64 dims x 64 heads, or
+// cp.async when the rows cannot be described by a tensor map), ahead of the
+// key lookups, which wait for the previous launch, and are then transformed
+// in place; fp32 rows go through registers.  The softmax threads then release the MMA issuer through q_full.
 // The query rows, seq_id and pos are inputs of the step, not written by the
 // library's preceding launches, so they are read before griddepcontrol.wait.
-__device__ __forceinline__ void fill_q_issue(const AttnArgs& a, uint8_t* smem, int st) {
+__device__ __forceinline__ void fill_q_issue(const AttnArgs& a, uint8_t* smem, Misc& ms, int st) {
   if (a.q_dtype != CSA_BF16) return;
+  if (a.q_tma) {
+    // eight 64-dim x 64-head boxes land already swizzled
+    if (st == 0) {
+      mbar_arrive_expect_tx(&ms.q_raw, kQBytes);
+      for (int at = 0; at < kD / 64; ++at)
+        tma_load_2d(smem + kOffQ + at * (kH * 128), &a.q_map, 64 * at, kH * blockIdx.x, &ms.q_raw);
+    }
+    return;
+  }
   constexpr int kPieces = kH * (kD / 8);  // 16-byte pieces of bf16 (8 dims each)
   const uint16_t* src = reinterpret_cast<const uint16_t*>(a.q) + (int64_t)blockIdx.x * a.heads * kD;
   const uint32_t qbase = smem_u32(smem + kOffQ);
@@ -333,7 +347,11 @@ __device__ void fill_q_finish(const AttnArgs& a, uint8_t* smem, Misc& ms, int st
   const int R = a.rope.rope_dim;
   constexpr int kPieces = kH * (kD / 8);
   if (a.q_dtype == CSA_BF16) {
-    cp_async_wait<0>();
+    if (a.q_tma) {
+      if (!mbar_wait(&ms.q_raw, 0)) record_error(a.err, CSA_ERR_TIMEOUT);
+    } else {
+      cp_async_wait<0>();
+    }
     for (int x = st; x < kPieces; x += kSoftmax) {
       const int h = x >> 6, d0 = (x & 63) * 8;
       uint4* p = reinterpret_cast<uint4*>(smem + kOffQ + sw128_offset(h, d0, kH));
@@ -406,7 +424,7 @@ __device__ __forceinline__ void load_o_chunk(uint32_t taddr, bool any, float* o)
 }
 
 __device__ void softmax_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Misc& ms, uint32_t tmem, int st) {
-  fill_q_issue(a, smem, st);
+  fill_q_issue(a, smem, ms, st);
   pdl_wait();  // selections and caches are complete only after the previous launch
   if (g.n_tiles > 0) lookup_keys(a, g, ms, 0, st);
   fill_q_finish(a, smem, ms, st);
@@ -647,7 +665,7 @@ __device__ void merge_split(const AttnArgs& a, uint8_t* smem, Misc& ms) {
     ms.rL[me][t] = ms.L[me * kPer + t];
   }
   if (!mbar_wait(&ms.recv, 0)) record_error(a.err, CSA_ERR_TIMEOUT);
-  __syncthreads();
+  named_bar(3, kMergeThreads);
   if (t < kPer) {  // weights 2^(M_s - max) / sum_s 2^(M_s - max) L_s into ms.red[2][s * kPer + t]
     float mg = -INFINITY;
 #pragma unroll
@@ -663,7 +681,7 @@ __device__ void merge_split(const AttnArgs& a, uint8_t* smem, Misc& ms) {
 #pragma unroll
     for (int sl = 0; sl < S; ++sl) ms.red[2][sl * kPer + t] = f[sl] * inv;
   }
-  __syncthreads();
+  named_bar(3, kMergeThreads);
   float v[2][kPer];
 #pragma unroll
   for (int hh = 0; hh < kPer; ++hh) v[0][hh] = v[1][hh] = 0.f;
@@ -704,12 +722,12 @@ __device__ void merge_split(const AttnArgs& a, uint8_t* smem, Misc& ms) {
       const float am = warp_max(fmaxf(fabsf(v[0][hh]), fabsf(v[1][hh])));
       if (lane == 0) ms.amax[warp][hh] = am;
     }
-    __syncthreads();
+    named_bar(3, kMergeThreads);
 #pragma unroll
     for (int hh = 0; hh < kPer; ++hh) {
       float am = 0.f;
 #pragma unroll
-      for (int w = 0; w < kThreads / 32; ++w) am = fmaxf(am, ms.amax[w][hh]);
+      for (int w = 0; w < kMergeThreads / 32; ++w) am = fmaxf(am, ms.amax[w][hh]);
       const float inv = am > 0.f ? 448.0f / am : 0.0f;
       *reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(a.out) + ob + (int64_t)(h0 + hh) * kD) =
           f32x2_to_e4m3x2(v[0][hh] * inv, v[1][hh] * inv);
@@ -729,7 +747,7 @@ __device__ void merge_split(const AttnArgs& a, uint8_t* smem, Misc& ms) {
   if (t == 0) bulk_wait_read();  // the staging stays valid until the engine has read it
 }
 
-__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Misc& ms = *reinterpret_cast<Misc*>(smem + kOffMisc);
@@ -749,6 +767,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnArgs a) 
       mbar_init(&ms.p_full[b], kSoftmax);
     }
     for (int b = 0; b < kRowBufs; ++b) mbar_init(&ms.rows_ready[b], kSoftmax);
+    mbar_init(&ms.q_raw, 1);
     mbar_init(&ms.q_full, kSoftmax);
     mbar_init(&ms.mma_done, 1);
     mbar_init(&ms.recv, 1);
@@ -757,7 +776,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnArgs a) 
   }
   if (tid < kH) ms.M[tid] = -INFINITY;
   if (tid < a.rope.rope_dim / 2) rope_cs(a.rope, tid, g.p, ms.rc[tid], ms.rs[tid]);
-  if (warp == 7) tmem_alloc(&ms.tmem_base, kTmemCols);
+  if (warp == kMmaWarp) tmem_alloc(&ms.tmem_base, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -765,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnArgs a) 
 
   if (warp < 4) {
     softmax_role(a, g, smem, ms, tmem, tid);
-  } else if (warp < 7) {
+  } else if (warp < kMmaWarp) {
     pdl_wait();  // caches and selections are complete only after the previous launch
     producer_role(a, g, smem, ms, tid - kSoftmax);
   } else if ((tid & 31) == 0) {
@@ -773,7 +792,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnArgs a) 
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 7) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -788,6 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnArgs a) 
     mbar_arrive_expect_tx(&ms.recv, (gridDim.y - 1) * (kD * per * 2 + 2 * per * 4));
   }
   cluster_sync();
+  if (tid >= kMergeThreads) return;
   switch (gridDim.y) {
     case 2: merge_split<2>(a, smem, ms); break;
     case 4: merge_split<4>(a, smem, ms); break;
