@@ -78,18 +78,27 @@ EncodeTiled encode_tiled() {
   return fn;
 }
 
+}  // namespace
+
+bool csa::encode_bf16_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t stride_bytes,
+                          uint32_t box_cols, uint32_t box_rows) {
+  const EncodeTiled fn = encode_tiled();
+  if (!fn || (reinterpret_cast<uintptr_t>(base) & 15) || (stride_bytes & 15) || rows == 0) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {stride_bytes};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
+
 // The tensor-core attention's query tensor: n_rows*64 rows of 512 bf16, boxes of
 // 64 dims x 64 heads, 128-byte swizzle (the layout of its shared Q operand).
 bool encode_q_map(CUtensorMap* m, const void* q, int32_t n_rows) {
-  const EncodeTiled fn = encode_tiled();
-  if (!fn || (reinterpret_cast<uintptr_t>(q) & 15)) return false;
-  const cuuint64_t dims[2] = {512, (cuuint64_t)n_rows * 64};
-  const cuuint64_t strides[1] = {512 * 2};
-  const cuuint32_t box[2] = {64, 64};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_bf16_map(m, q, 512, (uint64_t)n_rows * 64, 512 * 2, 64, 64);
 }
 
 int attn_common(const csa_layer* L, const void* q, int32_t q_dtype, int32_t n_rows, const int32_t* seq_id,

@@ -35,6 +35,12 @@ inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, siz
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// 2-D bf16 tensor map over `rows` rows of `cols` elements (row stride `stride_bytes`),
+// boxes of box_cols x box_rows, 128-byte swizzle; false if it cannot be encoded
+// (unaligned base or stride, or no driver entry point).  Defined in api.cu.
+bool encode_bf16_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t stride_bytes,
+                     uint32_t box_cols, uint32_t box_rows);
+
 // ---- compressor (k_compress.cu)
 struct IngestArgs {
   const void* kv;
@@ -95,6 +101,10 @@ struct IndexerArgs {
   int32_t max_n;    // row stride of the score buffer
   float* scores;    // [n_rows][max_n]
   int32_t* err;
+  // tensor-core path, bf16 cache: the cache as [blocks*64][128] rows, 64x64
+  // boxes, 128-byte swizzle (set by the launcher; k_tma = 0: cp.async gathers)
+  CUtensorMap k_map;
+  int32_t k_tma;
 };
 cudaError_t launch_indexer_scores(const IndexerArgs& a, int32_t n_rows, cudaStream_t s);
 // tensor-core scores, 64 heads x 128 dims, bf16 or e2m1 keys (k_indexer_tc.cu)

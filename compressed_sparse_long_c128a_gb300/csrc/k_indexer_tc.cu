@@ -7,10 +7,12 @@
 // contiguous range of 128-entry tiles.  Entries are the M dimension:
 //   S^T [128 entries x 64 heads] = K_idx [128 x 128] . Q_idx^T [128 x 64]
 // so thread t of the epilogue warps owns TMEM lane t = entry t, reads its 64
-// head dots, and writes one score.  Keys are gathered into a 4-stage ring of
-// 128B-swizzled K-major tiles: bf16 rows by cp.async; e2m1 rows (64 code bytes
-// + 8 e4m3 scale bytes) by cp.async into a raw ring, then dequantised to bf16
-// (exact: a 2-bit e2m1 significand times a 4-bit e4m3 one fits bf16).
+// head dots, and writes one score.  Keys go into a 4-stage ring of
+// 128B-swizzled K-major tiles.  A tile is two 64-entry paged blocks, 16 KB
+// each and contiguous in a bf16 cache, so bf16 tiles arrive as four TMA boxes
+// (64 dims x 64 entries); e2m1 rows (64 code bytes + 8 e4m3 scale bytes) come
+// by cp.async into a raw ring and are dequantised to bf16 (exact: a 2-bit
+// e2m1 significand times a 4-bit e4m3 one fits bf16).
 // TMEM holds two S^T buffers so the epilogue of tile i overlaps the MMA of i+1.
 //
 // Warps 0-3: epilogue; warps 4-6: producers; warp 7: TMEM allocation + MMA issue.
@@ -86,6 +88,35 @@ __device__ __forceinline__ int64_t entry_row(const Misc& ms, int32_t blk0, int32
   if (j < 0 || j >= kTblMax) return -1;  // the launcher keeps every CTA's range inside the cache
   const int32_t pb = ms.tbl[j];
   return pb < 0 ? -1 : (int64_t)pb * kRowsPerBlock + (e % kRowsPerBlock);
+}
+
+// bf16 with a tensor map: one thread issues each tile as up to four TMA boxes
+// (two blocks x two 64-dim atoms); a block that is unmapped or past the visible
+// entries is not loaded (its scores are not used).
+__device__ void producer_tma(const IndexerArgs& a, const Range& g, uint8_t* smem, Misc& ms) {
+  const int32_t blk0 = g.t0 * kTile / kRowsPerBlock;
+  for (int i = 0; i < g.nt; ++i) {
+    const int s = i % kStages;
+    if (i >= kStages) wait_or_abort(ms, &ms.empty[s], ((i / kStages) - 1) & 1, a.err);
+    const int32_t e0 = (g.t0 + i) * kTile;
+    int32_t pb[2];
+    uint32_t bytes = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int32_t e = e0 + h * kRowsPerBlock, j = e / kRowsPerBlock - blk0;
+      pb[h] = (e < g.n && j >= 0 && j < kTblMax) ? ms.tbl[j] : -1;
+      if (pb[h] >= 0) bytes += kRowsPerBlock * kDI * 2;
+    }
+    mbar_arrive_expect_tx(&ms.full[s], bytes);
+    uint8_t* sb = smem + kOffStage + s * kStageBytes;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      if (pb[h] >= 0)
+#pragma unroll
+        for (int at = 0; at < kDI / 64; ++at)
+          tma_load_2d(sb + at * kAtomBytes + h * (kRowsPerBlock * 128), &a.k_map, 64 * at, pb[h] * kRowsPerBlock,
+                      &ms.full[s]);
+  }
 }
 
 // Each thread derives its own rows' addresses from the cached table, so issuing
@@ -203,6 +234,7 @@ __device__ void epilogue_role(const IndexerArgs& a, const Range& g, Misc& ms, ui
 #pragma unroll
   for (int h = 0; h < kHI; ++h) w[h] = ms.w[h];
   float* out = a.scores + (int64_t)blockIdx.x * a.max_n;
+  const int32_t blk0 = g.t0 * kTile / kRowsPerBlock;
   for (int i = 0; i < g.nt; ++i) {
     const int b = i & 1;
     wait_or_abort(ms, &ms.tfull[b], (i >> 1) & 1, a.err);
@@ -216,12 +248,13 @@ __device__ void epilogue_role(const IndexerArgs& a, const Range& g, Misc& ms, ui
     float s = 0.f;
 #pragma unroll
     for (int h = 0; h < kHI; ++h) s = fmaf(w[h], fmaxf(v[h], 0.f), s);
-    const int32_t e = (g.t0 + i) * kTile + et;
-    if (e < g.n) out[e] = s;
+    const int32_t e = (g.t0 + i) * kTile + et, j = e / kRowsPerBlock - blk0;
+    // an unmapped block (reported when the table was cached) scores 0
+    if (e < g.n) out[e] = (j >= 0 && j < kTblMax && ms.tbl[j] >= 0) ? s : 0.f;
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(const IndexerArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(const __grid_constant__ IndexerArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Misc& ms = *reinterpret_cast<Misc*>(smem + kOffMisc);
@@ -230,8 +263,9 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(const IndexerAr
   const Range g = row_range(a, r);
 
   if (tid == 0) {
+    const bool tma = a.k_tma && a.cache.dtype == CSA_BF16;
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&ms.full[s], kProd);
+      mbar_init(&ms.full[s], tma ? 1 : kProd);
       mbar_init(&ms.empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -298,7 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(const IndexerAr
   if (warp < 4) {
     epilogue_role(a, g, ms, tmem, tid);
   } else if (warp < 7) {
-    producer_role(a, g, smem, ms, tid - kEpi);
+    if (!(a.k_tma && a.cache.dtype == CSA_BF16)) producer_role(a, g, smem, ms, tid - kEpi);
+    else if (tid == kEpi) producer_tma(a, g, smem, ms);
   } else if ((tid & 31) == 0) {
     mma_role(a, g, smem, ms, tmem);
   }
@@ -313,18 +348,29 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(const IndexerAr
 }  // namespace
 
 bool indexer_tc_eligible(const IndexerArgs& a) {
-  return a.heads == kHI && a.dim == kDI && (a.cache.dtype == CSA_BF16 || a.cache.dtype == CSA_E2M1);
+  return a.heads == kHI && a.dim == kDI && a.cache.rows_per_block == kRowsPerBlock &&
+         (a.cache.dtype == CSA_BF16 || a.cache.dtype == CSA_E2M1);
 }
 
-cudaError_t launch_indexer_tc(const IndexerArgs& a, int32_t n_rows, cudaStream_t s) {
+cudaError_t launch_indexer_tc(const IndexerArgs& args, int32_t n_rows, cudaStream_t s) {
   static bool attr_set = false;
+  static int n_sm = 0;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm <= 0)
+      n_sm = 148;
     attr_set = true;
   }
+  IndexerArgs a = args;
+  a.k_tma = a.cache.dtype == CSA_BF16 &&
+            encode_bf16_map(&a.k_map, a.cache.data, kDI, (uint64_t)a.cache.num_blocks * kRowsPerBlock, kDI * 2,
+                            64, kRowsPerBlock);
   const int32_t tiles = (a.max_n + kTile - 1) / kTile;
-  int32_t splits = n_rows > 0 ? (148 + n_rows - 1) / n_rows : 1;
+  // one CTA per SM: as many splits per row as fit in a single wave
+  int32_t splits = n_rows > 0 ? n_sm / n_rows : 1;
   if (splits > tiles) splits = tiles;
   // every CTA's range must fit the cached block-table slice (kTblMax blocks)
   const int32_t tiles_per_cta_max = kTblMax * kRowsPerBlock / kTile;
