@@ -392,7 +392,7 @@ def run_csa(args):
 
     e2e = None
     if not args.no_e2e:
-        e2e = _e2e(args, reps, graphs, stream, rows_per_step, world)
+        e2e = _e2e(args, reps, graphs, stream, rows_per_step, world, step)
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_total / args.steps, "higher_is_better": True,
@@ -400,7 +400,7 @@ def run_csa(args):
             "config": _config(wl, replicas),
             "achieved_gbs_step": step_bytes / (ms_total / args.steps / 1e3) / 1e9,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": None, "kernel": "sparse attention",
+                         "frac": achieved / peak, "traffic": _attn_traffic(wl.name), "kernel": "sparse attention",
                          "algorithmic_bytes_per_launch": att_bytes, "avg_launch_ms": att_avg_ms,
                          "peak_source": f"{peak_src} hbm_gbs (copy bandwidth, burst)"},
             "clocks": clk,
@@ -417,8 +417,36 @@ def run_csa(args):
         torch.distributed.destroy_process_group()
 
 
-def _e2e(args, reps, graphs, stream, rows_per_step, world):
-    """Same steps with inputs copied from pinned host memory and the output read back every step."""
+# DRAM bytes (read + write) of one attention launch from an ncu capture, keyed by
+# workload, valid only for the kernel source it was taken on (sha256 of
+# k_attn_tc.cu); see profiles/attn_tc_c128a_decode_b32.md.
+ATTN_TRAFFIC = {
+    "c128a_decode_b32_128k": (40027392 + 768, "c2649c649246d32f996d462908a44e4a6c7dab5bb4b687a4794092a98d9c1985"),
+}
+
+
+def _attn_traffic(workload_name):
+    """Measured DRAM traffic per attention launch, or None when absent or taken on other source."""
+    import hashlib
+    entry = ATTN_TRAFFIC.get(workload_name)
+    if entry is None:
+        return None
+    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "compressed_sparse_long_c128a_gb300", "csrc",
+                       "k_attn_tc.cu")
+    with open(src, "rb") as f:
+        digest = hashlib.sha256(f.read()).hexdigest()
+    return float(entry[0]) if digest == entry[1] else None
+
+
+def _e2e(args, reps, graphs, stream, rows_per_step, world, step):
+    """Same steps with inputs copied from pinned host memory and the output read back every step.
+
+    Each replica's step is captured once more as one CUDA graph that also holds
+    the host-to-device copies of the step's inputs and the device-to-host copy
+    of its output, as a serving loop would launch it; the host waits for every
+    step's result before launching the next.  If the copies cannot be captured,
+    they are issued around the replay of the kernel-only graph instead.
+    """
     import torch
     base = reps[0]
     host_in, host_out = [], []
@@ -432,26 +460,49 @@ def _e2e(args, reps, graphs, stream, rows_per_step, world):
         host_out.append(hout)
     bi = sum(t.numel() * t.element_size() for h in host_in for t in h.values())
     bo = sum(t.numel() * t.element_size() for h in host_out for t in h)
+
+    def copy_in():
+        for ld, hin in zip(base, host_in):  # replicas share the step's io buffers
+            for key, t in hin.items():
+                ld.io[key].copy_(t, non_blocking=True)
+
+    def copy_out():
+        for ld, hout in zip(base, host_out):
+            hout[0].copy_(ld.io["out"], non_blocking=True)
+            if len(hout) > 1:
+                hout[1].copy_(ld.io["out_scales"], non_blocking=True)
+
+    full = []
+    try:
+        for rep in reps:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                copy_in()
+                step(rep, stream)
+                copy_out()
+            full.append(g)
+        torch.cuda.synchronize()
+    except RuntimeError:
+        full = []
+        torch.cuda.synchronize()
     k_steps = min(args.steps, 200)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     t0.record(stream)
     with torch.cuda.stream(stream):
         for k in range(k_steps):
-            for ld, hin in zip(base, host_in):  # replicas share the step's io buffers
-                for key, t in hin.items():
-                    ld.io[key].copy_(t, non_blocking=True)
-            graphs[k % len(graphs)].replay()
-            for ld, hout in zip(base, host_out):
-                hout[0].copy_(ld.io["out"], non_blocking=True)
-                if len(hout) > 1:
-                    hout[1].copy_(ld.io["out_scales"], non_blocking=True)
+            if full:
+                full[k % len(full)].replay()
+            else:
+                copy_in()
+                graphs[k % len(graphs)].replay()
+                copy_out()
             stream.synchronize()  # the host reads the step's result
     t1.record(stream)
     torch.cuda.synchronize()
     ms = max_over_ranks(t0.elapsed_time(t1), world)
     return {"value": weak_throughput(rows_per_step, k_steps, world, ms), "unit": UNIT, "h2d_bytes_per_step": bi,
-            "d2h_bytes_per_step": bo, "steps": k_steps}
+            "d2h_bytes_per_step": bo, "steps": k_steps, "copies_in_graph": bool(full)}
 
 
 def main():
