@@ -84,24 +84,11 @@ __device__ __forceinline__ bool named_bar_or(int id, int count, bool v) {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
 // Shared::cluster address of the same shared variable in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t map_shared(const void* p, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
   return r;
-}
-// Generic pointer to the same shared variable in CTA `rank` of the cluster;
-// ordinary loads through it may be batched and overlapped by the compiler.
-template <typename T>
-__device__ __forceinline__ const T* map_shared_ptr(const T* p, uint32_t rank) {
-  uint64_t r;
-  asm("mapa.u64 %0, %1, %2;" : "=l"(r) : "l"(reinterpret_cast<uint64_t>(p)), "r"(rank));
-  return reinterpret_cast<const T*>(r);
 }
 
 // ---------------------------------------------------------------- TMEM
@@ -208,18 +195,7 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
-// Drop the 128-byte L2 line at p (128-byte aligned) without writing it back;
-// its contents become undefined.  For scratch that has been consumed.
-__device__ __forceinline__ void discard_l2(const void* p) {
-  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
-}
-
 // ---------------------------------------------------------------- cp.async
-
-// Ask for `bytes` (multiple of 16, 16-byte aligned) of global memory to be brought into L2.
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
 
 // 16-byte global -> shared copy; src_bytes = 0 writes zeros and reads nothing.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
