@@ -23,6 +23,14 @@
  *     atomicCAS from 0); the offending row or element is skipped, never read
  *     or written out of bounds.  No kernel traps or waits without a bound.
  *     csa_read_status() fetches and optionally clears the word.
+ *   - Kernels are launched with programmatic dependent launch: a kernel may
+ *     start while the previous launch on `stream` is still running, and waits
+ *     for it to complete before it reads a cache, a block table, the selected
+ *     indices or a scratch buffer.  The attention kernels read the query rows,
+ *     seq_id and pos before that wait, so these inputs must be complete when the
+ *     call is made, which holds for any producer except a kernel launched just
+ *     before on the same stream that itself signals programmatic completion
+ *     early.
  *   - Positions are 0-based.  Compressed entry i of a layer with stride
  *     `ratio` and window `window` sums raw tokens [ratio*i, ratio*i+window-1]
  *     and is anchored (rotated) at ratio*i ([延迟] "KV 缓存压缩").  A query at
@@ -174,7 +182,8 @@ CSA_API int csa_cache_store(const float* rows, int32_t n, const int32_t* seq_id,
  *   out_idx   [n_rows][k] int32
  *   ws        workspace of at least csa_indexer_topk_workspace_size(n_rows, max_n, k)
  *             bytes, max_n >= every row's n.  Contents are scratch (the rows'
- *             scores and each 8192-entry chunk's top-k candidates).
+ *             scores, and when max_n > 16384 each 16384-entry chunk's top-k
+ *             candidates).
  */
 CSA_API int csa_indexer_topk(const void* q_idx, int32_t q_dtype, const float* w, int32_t n_rows,
                      int32_t idx_heads, int32_t idx_dim, const int32_t* seq_id, const int32_t* pos,

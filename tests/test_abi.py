@@ -120,3 +120,17 @@ def test_workspace_checks(lib):
                                    ctypes.byref(_bt()), 0x10, 512, 262143, ctypes.byref(S), ctypes.byref(_bt()),
                                    0x10, csa.E4M3, None, 0x10, ws, 0x10, None)
     assert r == csa.ERR_INVALID_ARG
+
+
+def test_topk_scratch_sizes(lib):
+    """Rows of one 16384-entry chunk need only the score scratch; longer rows also
+    need each chunk's top-k candidates (key and index) and a count."""
+    def aligned(x):
+        return (x + 255) // 256 * 256
+
+    assert csa.indexer_topk_workspace_size(64, 16383, 512) == aligned(64 * 16383 * 4)
+    assert csa.indexer_topk_workspace_size(64, 16384, 512) == aligned(64 * 16384 * 4)
+    n = 262143
+    chunks = (n + 16383) // 16384
+    assert csa.indexer_topk_workspace_size(4, n, 512) == aligned(4 * n * 4) + aligned(4 * chunks * (512 * 8 + 4))
+    assert csa.indexer_topk_workspace_size(0, n, 512) == 0
