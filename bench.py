@@ -284,13 +284,21 @@ def _clone_layer(ld):
 
 
 def _launches_per_step(ld) -> int:
+    """Kernel launches of one layer step, following the library's dispatch rules."""
     import compressed_sparse_long_c128a_gb300 as csa
-    n = 2  # ingest + emit
-    if ld.L.has_indexer:
-        n += 2  # scores + top-k
-    kq = ld.L.topk if ld.L.has_indexer else ld.max_n
-    splits_ws = csa.sparse_attn_workspace_size(ld.c_layer, ld.n_rows, kq)
-    n += 2 if splits_ws > 0 else 1  # attention (+ split merge)
+    L = ld.L
+    n = 2  # compress_insert: ingest + emit
+    if L.has_indexer:
+        n += 1  # scores (tensor-core or generic)
+        chunks = -(-max(ld.max_n, 1) // 16384)  # top-k chunks of 16384 scores
+        two_stage = 2 <= chunks <= 64 and 4 * (chunks * L.topk + chunks * L.topk // 32 + 1 + chunks * L.topk) <= 200 * 1024
+        n += 2 if two_stage else 1  # chunk select (+ merge)
+    tc = L.dim == 512 and L.heads == 64 and L.cache_dtype in ("bf16", "e4m3") and L.rope_dim <= 128
+    if tc:
+        n += 1  # one launch; split rows merge inside it
+    else:
+        kq = L.topk if L.has_indexer else ld.max_n
+        n += 2 if csa.sparse_attn_workspace_size(ld.c_layer, ld.n_rows, kq) > 0 else 1  # (+ split merge)
     return n
 
 
