@@ -60,7 +60,7 @@ typedef struct CUstream_st* csa_stream_t; /* the same type as cudaStream_t */
 typedef enum {
   CSA_OK = 0,
   CSA_ERR_INVALID_ARG = -1,   /* null pointer, bad size, inconsistent shapes */
-  CSA_ERR_UNSUPPORTED = -2,   /* a valid combination this build has no kernel for */
+  CSA_ERR_UNSUPPORTED = -2,   /* a valid combination the library has no kernel for */
   CSA_ERR_CUDA = -3,          /* a CUDA runtime call or launch failed */
   CSA_ERR_DEVICE_BOUNDS = -4, /* device: unmapped / out-of-range block or index */
   CSA_ERR_WORKSPACE = -5,     /* workspace smaller than the matching *_workspace_size */
