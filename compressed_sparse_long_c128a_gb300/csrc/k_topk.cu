@@ -290,7 +290,19 @@ __global__ void __launch_bounds__(kChunkThreads) topk_chunk_kernel(const TopkArg
     return;
   }
   const float* s = a.scores + (int64_t)r * a.max_n + lo;
-  for (int i = threadIdx.x; i < len; i += kChunkThreads) keys[padded(i)] = order_key(s[i]);
+  // all of a thread's loads are issued before any is stored
+  constexpr int kLoads = kChunk / kChunkThreads;
+  float v[kLoads];
+#pragma unroll
+  for (int u = 0; u < kLoads; ++u) {
+    const int i = threadIdx.x + u * kChunkThreads;
+    v[u] = i < len ? s[i] : 0.f;
+  }
+#pragma unroll
+  for (int u = 0; u < kLoads; ++u) {
+    const int i = threadIdx.x + u * kChunkThreads;
+    if (i < len) keys[padded(i)] = order_key(v[u]);
+  }
   __syncthreads();
   if (final_out) {
     block_select<kChunkThreads>(keys, len, a.k, [&](int pos, uint32_t rank) { out[rank] = pos; });
