@@ -17,3 +17,35 @@ def test_attention_traffic_only_for_the_captured_source(monkeypatch):
 def test_weak_throughput_counts_all_ranks():
     # 32 rows a step, 10 steps, 2 ranks, 5 ms of wall time
     assert bench.weak_throughput(32, 10, 2, 5.0) == 32 * 10 * 2 / 5e-3
+
+
+def test_attention_bytes_match_the_closed_form():
+    """c128a dense decode, B = 32 at p = 131072: 1024 entries + 128 window rows of
+    1 KiB per row, plus 64 KiB of query and 64 KiB of output per row."""
+    import types
+
+    import numpy as np
+
+    import synth
+    wl = synth.workload(1)
+    L = wl.layers[0]
+    pos = np.array([s.first_new for s in wl.seqs], dtype=np.int64)
+    assert np.all(pos == 131072)
+    ld = types.SimpleNamespace(L=L, n_rows=len(pos), host={"pos": pos})
+    assert bench.attention_bytes(ld) == 32 * ((1024 + 128) * 1024 + 2 * 64 * 512 * 2)
+    assert bench.indexer_bytes(ld) == 0.0
+
+
+def test_indexer_bytes_count_every_visible_key():
+    import types
+
+    import numpy as np
+
+    import synth
+    wl = synth.workload(2)
+    L = wl.layers[0]
+    pos = np.array([s.first_new for s in wl.seqs], dtype=np.int64)
+    ld = types.SimpleNamespace(L=L, n_rows=len(pos), host={"pos": pos})
+    n = sum((int(p) - L.window) // L.ratio + 1 for p in pos)
+    q = len(pos) * L.idx_heads * (L.idx_dim * 2 + 4)
+    assert bench.indexer_bytes(ld) == n * L.idx_dim * 2 + q + len(pos) * L.topk * 4
