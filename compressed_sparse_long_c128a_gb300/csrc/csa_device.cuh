@@ -124,9 +124,11 @@ __device__ __forceinline__ uint8_t f32_to_e4m3(float x) {
 // e2m1: sign | 2 exponent bits (bias 1) | 1 mantissa bit; magnitudes
 // 0, 0.5, 1, 1.5, 2, 3, 4, 6.
 __device__ __forceinline__ float e2m1_to_f32(uint32_t c) {
-  const float mag[8] = {0.f, 0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f};
-  float v = mag[c & 7];
-  return (c & 8) ? -v : v;
+  // magnitude code m: exponent bits m>>1 (bias 1), mantissa bit m&1; exponent 0
+  // is the subnormal 0 / 0.5.  Built as fp32 bits (no table, no local memory).
+  const uint32_t m = c & 7;
+  const uint32_t mag = m >= 2 ? (((m >> 1) + 126u) << 23) | ((m & 1u) << 22) : (m ? 0x3F000000u : 0u);
+  return __uint_as_float(mag | ((c & 8u) << 28));
 }
 
 // Nearest e2m1 code, ties to the even code, saturating at 6.  Decision points

@@ -77,9 +77,10 @@ __device__ __forceinline__ Range row_range(const IndexerArgs& a, int r) {
   return g;
 }
 
-// e2m1 code -> bf16 bits of code * scale (exact)
-__device__ __forceinline__ uint32_t e2m1_bf16(uint32_t code, float scale) {
-  return f32_to_bf16(e2m1_to_f32(code) * scale);
+// Two e2m1 codes times one scale -> packed bf16 (lo in bits 0..15); exact, since a
+// 2-bit e2m1 significand times a 4-bit e4m3 one fits bf16's 8 bits.
+__device__ __forceinline__ uint32_t e2m1x2_bf16x2(uint32_t lo, uint32_t hi, float scale) {
+  return f32x2_to_bf16x2(e2m1_to_f32(lo) * scale, e2m1_to_f32(hi) * scale);
 }
 
 // Physical row of entry e of this CTA's range, from the cached block table; -1 if unmapped.
@@ -193,7 +194,7 @@ __device__ void producer_role(const IndexerArgs& a, const Range& g, uint8_t* sme
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const uint32_t lo = (word >> (8 * e)) & 0xF, hi = (word >> (8 * e + 4)) & 0xF;
-              o[e] = e2m1_bf16(lo, scl) | (e2m1_bf16(hi, scl) << 16);
+              o[e] = e2m1x2_bf16x2(lo, hi, scl);
             }
             const uint32_t piece = q * 4 + half;  // 0..15 over the 128 dims
             *reinterpret_cast<uint4*>(sb + (piece >> 3) * kAtomBytes + (key >> 3) * 1024 + (key & 7) * 128 +
