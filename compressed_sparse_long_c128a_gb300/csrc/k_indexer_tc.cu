@@ -15,7 +15,7 @@
 // e2m1 significand times a 4-bit e4m3 one fits bf16).
 // TMEM holds two S^T buffers so the epilogue of tile i overlaps the MMA of i+1.
 //
-// Warps 0-3: epilogue; warps 4-6: producers; warp 7: TMEM allocation + MMA issue.
+// Warps 0-3: epilogue; warps 4-10: producers; warp 11: TMEM allocation + MMA issue.
 
 #include "csa_kernels.h"
 #include "tc_ptx.cuh"
@@ -26,8 +26,9 @@ namespace {
 using namespace tc;
 
 constexpr int kHI = 64, kDI = 128, kTile = 128, kStages = 4;
-constexpr int kEpi = 128, kProd = 96;
+constexpr int kEpi = 128, kProd = 224;
 constexpr int kThreads = kEpi + kProd + 32;
+constexpr int kMmaWarp = (kEpi + kProd) / 32;
 constexpr uint32_t kQBytes = kHI * kDI * 2;         // 16 KB: 2 K-atoms of 64 rows x 128 B
 constexpr uint32_t kStageBytes = kTile * kDI * 2;   // 32 KB: 2 K-atoms of 128 rows x 128 B
 constexpr uint32_t kAtomBytes = kTile * 128;        // 16 KB
@@ -77,10 +78,41 @@ __device__ __forceinline__ Range row_range(const IndexerArgs& a, int r) {
   return g;
 }
 
-// Two e2m1 codes times one scale -> packed bf16 (lo in bits 0..15); exact, since a
-// 2-bit e2m1 significand times a 4-bit e4m3 one fits bf16's 8 bits.
-__device__ __forceinline__ uint32_t e2m1x2_bf16x2(uint32_t lo, uint32_t hi, float scale) {
-  return f32x2_to_bf16x2(e2m1_to_f32(lo) * scale, e2m1_to_f32(hi) * scale);
+// High and low bytes of the bf16 bits of the e2m1 magnitudes 0, 0.5, 1, 1.5, 2,
+// 3, 4, 6, as byte-permute tables indexed by the 3-bit magnitude code.
+constexpr uint32_t kMagHi03 = 0x3F3F3F00u, kMagHi47 = 0x40404040u;
+constexpr uint32_t kMagLo03 = 0xC0800000u, kMagLo47 = 0xC0804000u;
+
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// Eight e2m1 codes (nibble j of w is value j) times one scale (bf16, in both
+// halves of scale2) -> four bf16x2 words, word e holding values 2e and 2e+1.
+// The magnitudes come from byte-permute lookups, the signs from a permute of
+// the codes' sign bits.  The multiply is exact: a 2-bit e2m1 significand times
+// a 4-bit e4m3 one fits bf16's 8 bits, and the products stay in bf16's normal
+// range (2^-10 .. 2688).
+__device__ __forceinline__ void e2m1x8_bf16x2(uint32_t w, uint32_t scale2, uint32_t o[4]) {
+  const uint32_t mag = w & 0x77777777u;
+  const uint32_t sl = (w << 4) & 0x80808080u;  // sign of value 2e at bit 7 of byte e
+  const uint32_t sh = w & 0x80808080u;         // sign of value 2e+1 at bit 7 of byte e
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t sel = mag >> (16 * h);  // values 4h..4h+3 (the permute reads 4 nibbles)
+    const uint32_t hi = __byte_perm(kMagHi03, kMagHi47, sel) | __byte_perm(sl, sh, h ? 0x7362u : 0x5140u);
+    const uint32_t lo = __byte_perm(kMagLo03, kMagLo47, sel);
+    o[2 * h] = bf16x2_mul(__byte_perm(lo, hi, 0x5140u), scale2);
+    o[2 * h + 1] = bf16x2_mul(__byte_perm(lo, hi, 0x7362u), scale2);
+  }
+}
+
+// e4m3 scale -> its bf16 bits in both halves (exact: 4 significant bits)
+__device__ __forceinline__ uint32_t e4m3_bf16x2(uint8_t v) {
+  const uint32_t b = __float_as_uint(e4m3_to_f32(v)) >> 16;
+  return b | (b << 16);
 }
 
 // Physical row of entry e of this CTA's range, from the cached block table; -1 if unmapped.
@@ -184,18 +216,12 @@ __device__ void producer_role(const IndexerArgs& a, const Range& g, uint8_t* sme
           const uint32_t key = x >> 2, q = x & 3;
           const uint4 c4 = *reinterpret_cast<const uint4*>(rb + key * 64 + q * 16);
           const uint8_t* sc = rb + kRawCodes + key * 8 + q * 2;
-          const float s0 = e4m3_to_f32(sc[0]), s1 = e4m3_to_f32(sc[1]);
+          const uint32_t s0 = e4m3_bf16x2(sc[0]), s1 = e4m3_bf16x2(sc[1]);
           const uint32_t cw[4] = {c4.x, c4.y, c4.z, c4.w};
 #pragma unroll
           for (int half = 0; half < 4; ++half) {  // 8 values -> one 16-byte piece
-            const float scl = half < 2 ? s0 : s1;
-            const uint32_t word = cw[half];
             uint32_t o[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const uint32_t lo = (word >> (8 * e)) & 0xF, hi = (word >> (8 * e + 4)) & 0xF;
-              o[e] = e2m1x2_bf16x2(lo, hi, scl);
-            }
+            e2m1x8_bf16x2(cw[half], half < 2 ? s0 : s1, o);
             const uint32_t piece = q * 4 + half;  // 0..15 over the 128 dims
             *reinterpret_cast<uint4*>(sb + (piece >> 3) * kAtomBytes + (key >> 3) * 1024 + (key & 7) * 128 +
                                       (((piece & 7) ^ (key & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
@@ -292,16 +318,16 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(const __grid_co
       ms.tbl[j] = pb;
     }
   }
-  if (warp == 7) tmem_alloc(&ms.tmem_base, kTmemCols);
+  if (warp == kMmaWarp) tmem_alloc(&ms.tmem_base, kTmemCols);
   // Q_idx^T: bf16, 128B-swizzled K-major, rows = heads; 8 dims per 16-byte
   // piece, every thread's loads issued before its stores
   {
     constexpr int kPieces = kHI * kDI / 8;
-    constexpr int kPer = kPieces / kThreads;
+    constexpr int kPer = (kPieces + kThreads - 1) / kThreads;
     uint32_t w[kPer][4];
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
-      const int x = tid + u * kThreads;
+      const int x = min(tid + u * kThreads, kPieces - 1);  // clamped; stored below only when in range
       const int64_t qb = (int64_t)r * kHI * kDI + 8 * x;
       if (a.q_dtype == CSA_BF16) {
         const uint4 v = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q_idx) + qb));
@@ -318,6 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(const __grid_co
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
       const int x = tid + u * kThreads;
+      if (x >= kPieces) break;
       const int h = x / (kDI / 8), d0 = 8 * (x % (kDI / 8));
       *reinterpret_cast<uint4*>(smem + kOffQ + sw128_offset(h, d0, kHI)) = make_uint4(w[u][0], w[u][1], w[u][2], w[u][3]);
     }
@@ -332,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(const __grid_co
 
   if (warp < 4) {
     epilogue_role(a, g, ms, tmem, tid);
-  } else if (warp < 7) {
+  } else if (warp < kMmaWarp) {
     if (!(a.k_tma && a.cache.dtype == CSA_BF16)) producer_role(a, g, smem, ms, tid - kEpi);
     else if (tid == kEpi) producer_tma(a, g, smem, ms);
   } else if ((tid & 31) == 0) {
@@ -340,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(const __grid_co
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 7) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
