@@ -23,6 +23,10 @@ Under torchrun each rank runs its own replica of the workload on its own GPU
 (sequences are independent; no collective on the data path), so the scaling
 is weak and value = tokens of all ranks / max time.
 
+--side-stream runs each c4a layer's indexer and top-k on a second stream,
+forked from the step's stream before compress_insert and joined before the
+attention (both streams are captured into the same graph).
+
 --impl reference times the CPU oracle on this machine's host cores on the
 same workload, one bounded sample of rows per step.
 """
@@ -58,6 +62,8 @@ def _args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--side-stream", action="store_true",
+                    help="run each c4a layer's indexer + top-k on a second stream, beside compress_insert")
     ap.add_argument("--load-seconds", type=float, default=1.5,
                     help="untimed graph replays before the timed steps, so the clock sampler sees load")
     return ap.parse_args()
@@ -324,10 +330,11 @@ def run_csa(args):
     replicas = 1 if step_bytes > 2.5 * L2_BYTES else int(math.ceil(2.5 * L2_BYTES / step_bytes)) + 1
     reps = [base] + [[_clone_layer(ld) for ld in base] for _ in range(replicas - 1)]
     stream = torch.cuda.Stream()
+    side = torch.cuda.Stream() if args.side_stream else None
 
     def step(rep, s=None):
         for ld in rep:
-            ld.step(s)
+            ld.step(s, side_stream=side)
 
     with torch.cuda.stream(stream):
         for i in range(max(args.warmup, replicas)):
@@ -414,6 +421,8 @@ def run_csa(args):
             "clocks": clk,
             "gpu_launches": sum(_launches_per_step(ld) for ld in base) * args.steps,
             "e2e": e2e}
+    if side is not None:
+        line["config"]["indexer_stream"] = "side"
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n, dt = oracle_rows_per_second(wl, args.cpu_seconds)
         line["cpu_baseline"] = {"value": n / dt, "unit": UNIT, "cores": _cores(), "kind": "oracle",

@@ -269,6 +269,42 @@ def test_end_to_end(idx):
         assert compared >= len(rows) - max(1, len(rows) // 20)
 
 
+
+@pytest.mark.parametrize("idx", [0, 2, 4])
+def test_two_stream_step_matches_one_stream(idx):
+    """A c4a layer's indexer and top-k on a second stream, beside compress_insert
+    on the first and joined before the attention, write the same bytes as the
+    one-stream step: the launches are the same, only the order of independent
+    ones changes (the indexer reads nothing compress_insert writes)."""
+    wd = _dev(idx)
+    main, side = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def run(side_stream):
+        with torch.cuda.stream(main):
+            for ld in wd.layers:
+                ld.io["out"].zero_()
+                if "topk" in ld.io:
+                    ld.io["topk"].fill_(-2)
+            wd.step(main, side_stream=side_stream)
+        torch.cuda.synchronize()
+        wd.check("two-stream step" if side_stream is not None else "one-stream step")
+        snap = []
+        for ld in wd.layers:
+            t = {"out": ld.io["out"].clone(), "comp": ld.comp.data.clone(), "swa": ld.swa.data.clone()}
+            if ld.io["out_scales"] is not None:
+                t["out_scales"] = ld.io["out_scales"].clone()
+            if "topk" in ld.io:
+                t["topk"] = ld.io["topk"].clone()
+            snap.append(t)
+        return snap
+
+    one = run(None)
+    two = run(side)
+    for ld, a, b in zip(wd.layers, one, two):
+        assert a.keys() == b.keys()
+        for key in a:
+            assert torch.equal(a[key], b[key]), f"{ld.L.name}: {key} differs between one and two streams"
+
 def test_device_bounds_are_reported_not_faulted():
     """An unmapped block and an out-of-range selection set the error word; the kernels skip them."""
     import compressed_sparse_long_c128a_gb300 as csa
