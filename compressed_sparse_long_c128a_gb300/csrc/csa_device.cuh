@@ -199,13 +199,4 @@ __device__ __forceinline__ float load_elem(const void* base, int32_t dtype, int6
   return bf16_to_f32(reinterpret_cast<const uint16_t*>(base)[idx]);
 }
 
-__device__ __forceinline__ int64_t row_bytes(const csa_paged& c) {
-  switch (c.dtype) {
-    case CSA_F32: return (int64_t)c.dim * 4;
-    case CSA_BF16: return (int64_t)c.dim * 2;
-    case CSA_E4M3: return (int64_t)c.dim;
-    default: return (int64_t)c.dim / 2;
-  }
-}
-
 }  // namespace csa
