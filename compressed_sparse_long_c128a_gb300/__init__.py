@@ -178,11 +178,16 @@ def make_layer(ratio, window, dim, rope_dim, heads, swa=128, rope_theta=10000.0,
 
 
 def compress_insert(layer: Layer, kv, gate, seq_id, pos, bias, gamma_c, gamma_swa, state: PagedCache, state_bt,
-                    swa: PagedCache, swa_bt, comp: PagedCache, comp_bt, err, stream=None):
+                    swa: PagedCache | None, swa_bt, comp: PagedCache, comp_bt, err, stream=None):
+    """swa=None (swa_bt and gamma_swa then ignored) writes no sliding-window rows:
+    the indexer-key compressor, whose keys go to an indexer cache (comp may be E2M1)."""
+    no_swa = swa is None
     st = lib().csa_compress_insert(ctypes.byref(layer), _ptr(kv), _ptr(gate), _tdtype(kv), kv.shape[0],
-                                   _ptr(seq_id), _ptr(pos), _ptr(bias), _ptr(gamma_c), _ptr(gamma_swa),
+                                   _ptr(seq_id), _ptr(pos), _ptr(bias), _ptr(gamma_c),
+                                   None if no_swa else _ptr(gamma_swa),
                                    ctypes.byref(state.c()), ctypes.byref(block_table(state_bt)),
-                                   ctypes.byref(swa.c()), ctypes.byref(block_table(swa_bt)),
+                                   None if no_swa else ctypes.byref(swa.c()),
+                                   None if no_swa else ctypes.byref(block_table(swa_bt)),
                                    ctypes.byref(comp.c()), ctypes.byref(block_table(comp_bt)), _ptr(err),
                                    _stream(stream))
     _check(st, "csa_compress_insert")

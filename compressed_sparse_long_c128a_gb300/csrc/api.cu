@@ -165,16 +165,19 @@ int csa_compress_insert(const csa_layer* L, const void* kv, const void* gate, in
   if (st) return st;
   if (n_tok < 0) return CSA_ERR_INVALID_ARG;
   if (n_tok == 0) return CSA_OK;
-  if (!kv || !gate || !seq_id || !pos || !bias || !gamma_c || !gamma_swa || !err) return CSA_ERR_INVALID_ARG;
+  if (!kv || !gate || !seq_id || !pos || !bias || !gamma_c || !err) return CSA_ERR_INVALID_ARG;
+  if (swa && !gamma_swa) return CSA_ERR_INVALID_ARG;
   if (in_dtype != CSA_F32 && in_dtype != CSA_BF16) return CSA_ERR_UNSUPPORTED;
   if (L->dim > 4096) return CSA_ERR_UNSUPPORTED;
   if ((st = check_paged(state, 2 * L->dim, 256, 1u << in_dtype))) return st;
-  if ((st = check_paged(swa, L->dim, 256, kF32 | kBF16 | kE4M3))) return st;
-  if ((st = check_paged(comp, L->dim, 256 / L->ratio, kF32 | kBF16 | kE4M3))) return st;
-  if ((st = check_bt(state_bt)) || (st = check_bt(swa_bt)) || (st = check_bt(comp_bt))) return st;
+  if (swa && (st = check_paged(swa, L->dim, 256, kF32 | kBF16 | kE4M3))) return st;
+  if ((st = check_paged(comp, L->dim, 256 / L->ratio, kF32 | kBF16 | kE4M3 | kE2M1))) return st;
+  if ((st = check_bt(state_bt)) || (swa && (st = check_bt(swa_bt))) || (st = check_bt(comp_bt))) return st;
   const RopeTab rt = make_rope(L->rope_dim, L->rope_theta);
-  IngestArgs ia{kv, gate, in_dtype, seq_id, pos, gamma_swa, *state, *state_bt, *swa, *swa_bt, L->dim, L->rms_eps,
-                rt, err};
+  const csa_paged no_swa{};
+  const csa_block_table no_swa_bt{};
+  IngestArgs ia{kv, gate, in_dtype, seq_id, pos, gamma_swa, *state, *state_bt, swa ? *swa : no_swa,
+                swa ? *swa_bt : no_swa_bt, L->dim, L->rms_eps, rt, err};
   cudaError_t e = launch_ingest(ia, n_tok, stream);
   if (e != cudaSuccess) return CSA_ERR_CUDA;
   EmitArgs ea{seq_id, pos, bias, gamma_c, *state, *state_bt, *comp, *comp_bt, L->dim, L->ratio, L->window,

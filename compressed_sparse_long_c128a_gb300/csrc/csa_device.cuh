@@ -148,6 +148,26 @@ __device__ __forceinline__ uint32_t f32_to_e2m1(float x) {
   return m | (signbit(x) ? 8u : 0u);
 }
 
+// One group of 16 values -> 8 bytes of e2m1 codes (element e in nibble e of the
+// little-endian pair of words: element 2j in the low nibble of byte j) and the
+// group's e4m3 scale byte: scale = e4m3_rn(amax/6); code = e2m1_rn(v / scale);
+// a zero scale gives zero codes.  `v` may point to shared or local memory.
+__device__ __forceinline__ uint8_t quantize_e2m1_group(const float* v, uint2& packed) {
+  float am = 0.f;
+#pragma unroll
+  for (int e = 0; e < 16; ++e) am = fmaxf(am, fabsf(v[e]));
+  const uint8_t sc = f32_to_e4m3(am / 6.0f);
+  const float s = e4m3_to_f32(sc);
+  uint32_t w[2] = {0u, 0u};
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const uint32_t code = s > 0.f ? f32_to_e2m1(v[e] / s) : 0u;
+    w[e / 8] |= code << (4 * (e % 8));
+  }
+  packed = make_uint2(w[0], w[1]);
+  return sc;
+}
+
 // ---------------------------------------------------------------- reductions
 
 // 2^x with the special-function unit (about 2 ulp); the softmax weights need no more.

@@ -36,6 +36,14 @@ __device__ void store_row(const csa_paged& c, int64_t prow, const float* y, int 
     for (int pr = threadIdx.x; pr < D / 2; pr += blockDim.x)
       *reinterpret_cast<uint16_t*>(row + 2 * pr) = f32x2_to_e4m3x2(y[2 * pr] * inv, y[2 * pr + 1] * inv);
     if (threadIdx.x == 0) reinterpret_cast<float*>(c.scales)[prow] = scale;
+  } else if (c.dtype == CSA_E2M1) {  // one thread per group of 16 (D % 16 == 0)
+    uint8_t* row = reinterpret_cast<uint8_t*>(c.data) + prow * (int64_t)(D / 2);
+    uint8_t* srow = reinterpret_cast<uint8_t*>(c.scales) + prow * (int64_t)(D / 16);
+    for (int g = threadIdx.x; g < D / 16; g += blockDim.x) {
+      uint2 packed;
+      srow[g] = quantize_e2m1_group(y + 16 * g, packed);
+      *reinterpret_cast<uint2*>(row + g * 8) = packed;
+    }
   } else if (c.dtype == CSA_BF16) {
     uint16_t* row = reinterpret_cast<uint16_t*>(c.data) + prow * (int64_t)D;
     for (int pr = threadIdx.x; pr < D / 2; pr += blockDim.x) {
@@ -79,7 +87,7 @@ __global__ void __launch_bounds__(kThreads) ingest_kernel(const IngestArgs a) {
   const int seq = a.seq_id[j];
   const int64_t p = a.pos[j];
   const int64_t srow = phys_row(a.state_bt, a.state, seq, p, a.err);
-  const int64_t wrow = phys_row(a.swa_bt, a.swa, seq, p, a.err);
+  const int64_t wrow = a.swa.data ? phys_row(a.swa_bt, a.swa, seq, p, a.err) : -1;  // no window cache: state only
 
   float ss = 0.f;
   for (int d = threadIdx.x; d < D; d += blockDim.x) {

@@ -45,22 +45,11 @@ __global__ void __launch_bounds__(kThreads) store_kernel(const StoreArgs a) {
     uint8_t* srow = reinterpret_cast<uint8_t*>(c.scales) + prow * (D / 16);
     for (int g = threadIdx.x; g < D / 16; g += blockDim.x) {
       float v[16];
-      float am = 0.f;
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        v[e] = x[g * 16 + e];
-        am = fmaxf(am, fabsf(v[e]));
-      }
-      const uint8_t sc = f32_to_e4m3(am / 6.0f);
-      const float s = e4m3_to_f32(sc);
-      uint32_t packed[2] = {0u, 0u};
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const uint32_t code = s > 0.f ? f32_to_e2m1(v[e] / s) : 0u;
-        packed[e / 8] |= code << (4 * (e % 8));
-      }
-      *reinterpret_cast<uint2*>(row + g * 8) = make_uint2(packed[0], packed[1]);
-      srow[g] = sc;
+      for (int e = 0; e < 16; ++e) v[e] = x[g * 16 + e];
+      uint2 packed;
+      srow[g] = quantize_e2m1_group(v, packed);
+      *reinterpret_cast<uint2*>(row + g * 8) = packed;
     }
   }
 }

@@ -127,7 +127,7 @@ typedef struct {
  *
  * For each token j (position pos[j] of sequence seq_id[j]):
  *   state row (logical row pos[j]) := kv[j] | gate[j]            (raw, in_dtype)
- *   swa row   (logical row pos[j]) := RoPE(RMSNorm(kv[j]; gamma_swa), pos[j])
+ *   swa row   (logical row pos[j]) := RoPE(RMSNorm(kv[j]; gamma_swa), pos[j])  (if swa)
  * then, for each token whose position t satisfies t >= window-1 and
  * (t-window+1) % ratio == 0, entry i = (t-window+1)/ratio becomes
  *   c[d] = sum_{o<window} softmax_o(gate[o,d] + bias[o,d]) * kv[o,d]   (o = offset
@@ -141,8 +141,13 @@ typedef struct {
  *   seq_id,pos [n_tok] int32; (seq, pos) pairs must be distinct within a call
  *   bias       [window][D] float; gamma_c, gamma_swa [D] float
  *   state      dtype == in_dtype, rows_per_block 256, dim 2*D
- *   swa        F32 / BF16 / E4M3, rows_per_block 256, dim D
- *   comp       F32 / BF16 / E4M3, rows_per_block 256/ratio, dim D
+ *   swa        F32 / BF16 / E4M3, rows_per_block 256, dim D; or NULL, with
+ *              swa_bt and gamma_swa unused (may be NULL): no window rows are
+ *              written.  This is the indexer-key compressor ([部署] §3.2 first
+ *              fusion: the indexer K cache keeps its own compress + norm + RoPE
+ *              + insert), whose keys have no sliding window.
+ *   comp       F32 / BF16 / E4M3 / E2M1, rows_per_block 256/ratio, dim D.
+ *              E2M1 (D % 16 == 0) quantises as csa_cache_store does.
  *   err        device int32 error word
  */
 CSA_API int csa_compress_insert(const csa_layer* layer, const void* kv, const void* gate, int32_t in_dtype,

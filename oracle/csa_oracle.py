@@ -40,6 +40,10 @@ What the pages fix, and the readings taken where they leave a step open:
     (amax / 448); e2m1 with one e4m3 scale per 16 elements (amax16 / 6, rounded
     to e4m3).  The codec's rounding decisions are taken in fp32, the precision
     the kernels take them in.
+  * the indexer K cache has its own compress + RMSNorm + RoPE + insert kernel
+    ([部署] §3.2, first fusion).  Reading: the same compressor (c4a stride and
+    window) over the indexer's own raw streams at its dim, with its own bias and
+    gain, RoPE on its last 64 dims, no sliding window (`complete_entries`).
 """
 
 from __future__ import annotations
@@ -160,6 +164,21 @@ def compressed_entry(kv, gate, first_pos: int, i: int, ratio: int, window: int, 
     y = rms_norm(c, gamma_c, eps)
     return rope(y, lo, rope_dim, theta)
 
+
+
+def complete_entries(kv, gate, ratio: int, window: int, bias, gamma_c, eps: float, rope_dim: int,
+                     theta: float) -> np.ndarray:
+    """Every entry whose window lies inside the raw rows kv, gate (positions 0 .. n-1):
+    entries 0 .. (n - window) // ratio, each `compressed_entry`.  [D] rows, [0, D] if none.
+
+    The indexer's keys are this at the indexer's dim with their own gate, bias and
+    gain: [部署] §3.2 first fusion (compress, RMSNorm, RoPE and the write into the
+    attention or the indexer K cache; the indexer K cache keeps its own kernel).
+    """
+    n = len(kv)
+    m = (n - window) // ratio + 1 if n >= window else 0
+    rows = [compressed_entry(kv, gate, 0, i, ratio, window, bias, gamma_c, eps, rope_dim, theta) for i in range(m)]
+    return np.stack(rows) if rows else np.zeros((0, np.shape(kv)[1]))
 
 def swa_row(kv_t, t: int, gamma_swa, eps: float, rope_dim: int, theta: float) -> np.ndarray:
     """Sliding-window row of raw token t: RMSNorm with its own gain, RoPE at t.

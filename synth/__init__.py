@@ -16,6 +16,7 @@ from .workloads import (  # noqa: F401
     seq_raw,
     seq_history,
     seq_index_keys,
+    index_key_case,
     seq_queries,
     block_table,
     physical_row,

@@ -56,6 +56,7 @@ CACHE_KINDS = ("comp", "idx", "swa", "state")
 # seeding keys: (workload seed, tensor id, layer id, sequence, ...)
 _T_BIAS, _T_GAMMA_C, _T_GAMMA_SWA, _T_KV, _T_GATE, _T_HIST, _T_KIDX = 1, 2, 3, 4, 5, 6, 7
 _T_Q, _T_QIDX, _T_W, _T_LENGTHS, _T_TABLE, _T_SUBSET, _T_OFFSETS = 8, 9, 10, 11, 12, 13, 14
+_T_IK_KV, _T_IK_GATE, _T_IK_BIAS, _T_IK_GAMMA, _T_IK_TABLE = 15, 16, 17, 18, 19
 
 
 def _rng(*key) -> np.random.Generator:
@@ -290,3 +291,35 @@ def physical_row(table: np.ndarray, b: int, logical_row, rows_per_block: int):
     if np.any(blk < 0):
         raise IndexError("logical row maps to an unmapped block")
     return blk, logical_row % rows_per_block
+
+
+# ---------------------------------------------------------------- indexer-key compressor
+
+
+def index_key_case(seed: int, lengths, dim: int = 128, window: int = 8, in_dtype: str = "bf16") -> dict:
+    """Inputs of the indexer-key compressor for sequences of the given lengths.
+
+    Sequence b holds raw tokens at positions 0 .. lengths[b]-1: kv and gate
+    [lengths[b], dim] ~N(0,1) in `in_dtype`.  Learned parameters: offset bias
+    [window, dim] ~N(0, 0.1^2), gain [dim] ~1+N(0, 0.02^2).  Block tables map
+    the ceil(length/256) logical blocks of each sequence through one seeded
+    permutation per cache kind ("state": the compressor state, "idx": the
+    indexer cache), as the workloads' tables do.
+    """
+    kv = [_stored(_rng(seed, _T_IK_KV, b).standard_normal((n, dim), dtype=np.float32), in_dtype)
+          for b, n in enumerate(lengths)]
+    gate = [_stored(_rng(seed, _T_IK_GATE, b).standard_normal((n, dim), dtype=np.float32), in_dtype)
+            for b, n in enumerate(lengths)]
+    bias = _rng(seed, _T_IK_BIAS).normal(0.0, 0.1, size=(window, dim)).astype(np.float32)
+    gamma = (1.0 + _rng(seed, _T_IK_GAMMA).normal(0.0, 0.02, size=dim)).astype(np.float32)
+    blocks = [-(-n // BLOCK_POSITIONS) for n in lengths]
+    tables = {}
+    for kind in ("state", "idx"):
+        perm = _rng(seed, _T_IK_TABLE, CACHE_KINDS.index(kind)).permutation(sum(blocks)).astype(np.int32)
+        t = np.full((len(lengths), max(blocks)), -1, dtype=np.int32)
+        k = 0
+        for b, nb in enumerate(blocks):
+            t[b, :nb] = perm[k:k + nb]
+            k += nb
+        tables[kind] = t
+    return {"kv": kv, "gate": gate, "bias": bias, "gamma": gamma, "tables": tables, "n_blocks": sum(blocks)}

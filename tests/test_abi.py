@@ -99,6 +99,40 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert r == csa.ERR_INVALID_ARG
 
 
+
+def test_indexer_key_compressor_validation(lib):
+    """compress_insert without a window cache (the indexer-key compressor) and
+    into an e2m1 cache: the host checks that stop a call before any launch."""
+    L = csa.make_layer(4, 8, 128, 64, 64)
+    st, B = _paged(csa.BF16, 256, 256), _bt()
+    sw = _paged(csa.BF16, 256, 128)
+    idx = _paged(csa.E2M1, 64, 128)
+
+    def call(layer, swa, swa_bt, gamma_swa, comp):
+        return lib.csa_compress_insert(ctypes.byref(layer), 0x10, 0x10, csa.BF16, 4, 0x10, 0x10, 0x10, 0x10,
+                                       gamma_swa, ctypes.byref(st), ctypes.byref(B), swa, swa_bt,
+                                       ctypes.byref(comp), ctypes.byref(B), 0x10, None)
+
+    # a window cache needs its gains and its block table
+    assert call(L, ctypes.byref(sw), ctypes.byref(B), None, idx) == csa.ERR_INVALID_ARG
+    assert call(L, ctypes.byref(sw), None, 0x10, idx) == csa.ERR_INVALID_ARG
+    # e2m1 entries need the scale array and D % 16 == 0
+    no_scales = csa.Paged(0x1000, None, csa.E2M1, 10, 64, 128)
+    assert call(L, None, None, None, no_scales) == csa.ERR_INVALID_ARG
+    L24 = csa.make_layer(4, 8, 24, 8, 8)
+    st24 = _paged(csa.BF16, 256, 48)
+    r = lib.csa_compress_insert(ctypes.byref(L24), 0x10, 0x10, csa.BF16, 4, 0x10, 0x10, 0x10, 0x10, None,
+                                ctypes.byref(st24), ctypes.byref(B), None, None,
+                                ctypes.byref(_paged(csa.E2M1, 64, 24)), ctypes.byref(B), 0x10, None)
+    assert r == csa.ERR_INVALID_ARG
+    # the window cache stays limited to the dtypes attention reads
+    assert call(L, ctypes.byref(_paged(csa.E2M1, 256, 128)), ctypes.byref(B), 0x10, idx) == csa.ERR_UNSUPPORTED
+    # no tokens: a no-op with or without a window cache
+    r = lib.csa_compress_insert(ctypes.byref(L), None, None, csa.BF16, 0, None, None, None, None, None,
+                                ctypes.byref(st), ctypes.byref(B), None, None, ctypes.byref(idx),
+                                ctypes.byref(B), None, None)
+    assert r == csa.OK
+
 def test_workspace_checks(lib):
     L = csa.make_layer(4, 8, 512, 64, 64)
     need = csa.indexer_topk_workspace_size(4, 262143, 512)
