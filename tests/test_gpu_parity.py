@@ -270,7 +270,7 @@ def test_end_to_end(idx):
 
 
 
-@pytest.mark.parametrize("idx", [0, 2, 4])
+@pytest.mark.parametrize("idx", [4, 0, 2])  # 4 first: still resident from test_end_to_end
 def test_two_stream_step_matches_one_stream(idx):
     """A c4a layer's indexer and top-k on a second stream, beside compress_insert
     on the first and joined before the attention, write the same bytes as the
