@@ -180,6 +180,7 @@ def complete_entries(kv, gate, ratio: int, window: int, bias, gamma_c, eps: floa
     rows = [compressed_entry(kv, gate, 0, i, ratio, window, bias, gamma_c, eps, rope_dim, theta) for i in range(m)]
     return np.stack(rows) if rows else np.zeros((0, np.shape(kv)[1]))
 
+
 def swa_row(kv_t, t: int, gamma_swa, eps: float, rope_dim: int, theta: float) -> np.ndarray:
     """Sliding-window row of raw token t: RMSNorm with its own gain, RoPE at t.
     [部署] §3.2 third fusion (KV RoPE + K insert for the uncompressed window)."""
