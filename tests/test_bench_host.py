@@ -49,3 +49,28 @@ def test_indexer_bytes_count_every_visible_key():
     n = sum((int(p) - L.window) // L.ratio + 1 for p in pos)
     q = len(pos) * L.idx_heads * (L.idx_dim * 2 + 4)
     assert bench.indexer_bytes(ld) == n * L.idx_dim * 2 + q + len(pos) * L.topk * 4
+
+
+def _layer_stand_in(wl, L):
+    """What _launches_per_step reads of a device layer, without a device."""
+    import types
+
+    import compressed_sparse_long_c128a_gb300 as csa
+    from harness.device import n_visible
+
+    pos = [p for s in wl.seqs for p in range(s.first_new, s.end)]
+    return types.SimpleNamespace(L=L, n_rows=len(pos), max_n=max(n_visible(p, L.ratio, L.window) for p in pos),
+                                 c_layer=csa.make_layer(L.ratio, L.window, L.dim, L.rope_dim, L.heads, L.swa,
+                                                        L.theta, L.eps))
+
+
+def test_launch_count_matches_the_launch_lists():
+    """Kernel launches per step, from the dispatch rules, against what ncu listed per
+    step: c128a decode 3 (ingest, emit, attention), c4a decode 5 (+ indexer, one top-k
+    chunk launch), c4a at 2^20 with the fp4 indexer 6 (+ the top-k merge)."""
+    import synth
+
+    for idx, want in ((1, 3), (2, 5), (3, 6)):
+        wl = synth.workload(idx)
+        got = sum(bench._launches_per_step(_layer_stand_in(wl, L)) for L in wl.layers)
+        assert got == want, f"workload {idx}: {got} launches per step, the launch list shows {want}"
