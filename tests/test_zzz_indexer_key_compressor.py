@@ -78,9 +78,9 @@ def _read(t, case, b, ids):
 def _untouched(idx, case, b, m):
     n_rows = ROWS * int(np.sum(case["tables"]["idx"][b] >= 0))
     rest = np.arange(m, n_rows)
-    assert torch.count_nonzero(_read(idx.data, case, b, rest)) == 0, f"seq {b}: entries past the last window"
+    assert not bool((_read(idx.data, case, b, rest) != 0).any()), f"seq {b}: entries past the last window"
     if idx.scales is not None:
-        assert torch.count_nonzero(_read(idx.scales, case, b, rest)) == 0, f"seq {b}: scales past the last window"
+        assert not bool((_read(idx.scales, case, b, rest) != 0).any()), f"seq {b}: scales past the last window"
 
 
 def test_e2m1_indexer_keys():
