@@ -20,7 +20,6 @@ e4m3 output 6e-2 max-abs / 3e-2 rel-L2, each element within one e4m3 step plus
 1% of its head's amax, scales within 1%.
 """
 
-import math
 
 import numpy as np
 import pytest
