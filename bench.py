@@ -1,34 +1,40 @@
 #!/usr/bin/env python3
 """Throughput of the compressed sparse attention hot path on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 0..4] [--impl csa|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 0..4] [--extra 1,3,4|none]
+                    [--impl csa|reference]
 
-One step is one pass of the hot path over one batch of the workload: for
-every layer, csa_compress_insert of the step's new tokens, csa_indexer_topk
-(c4a layers) and the sparse attention call.  A token is one query row that
-completes that pass for one layer.  The default workload is c128a dense
-decode: 32 sequences at context 131072, D=512, H=64, bf16.
+One step is one pass of the hot path over one batch of a workload: for every
+layer, csa_compress_insert of the step's new tokens, csa_indexer_topk (c4a
+layers) and the sparse attention call.  A token is one query row that
+completes that pass for one layer.
+
+The headline workload is c4a DSA decode: 64 sequences at contexts uniform in
+[32768, 65536], D=512, H=64, indexer 64 heads x 128 dims, top-512, bf16.  The
+other full-size workloads are measured the same way and reported under
+"configs" (c128a dense decode at 131072; c4a decode at 2^20 with the fp8
+attention cache and fp4 indexer cache; mixed chunked prefill + decode with a
+c4a and a c128a layer).
 
 Timing: W eager warm-up steps, then K steps replayed from CUDA graphs (one
 graph per step) on one stream, bracketed by CUDA events with a device
 synchronise (and, under torchrun, a barrier) on both sides; the max over
-ranks is reported.  The step's working set is smaller than L2, so the steps
-rotate over R copies of every cache with R x (bytes a step touches) > 2.5 x
-L2; no step finds its inputs in L2.  The dominant kernel (sparse attention)
-is timed in a second event-timed pass of K launches over the same replicas.
-`e2e` repeats the step through the public API with its inputs copied from
-pinned host memory and its output read back to the host every step.
+ranks is reported.  When a step's working set is smaller than L2 the steps
+rotate over R copies of every cache with R x (bytes a step touches) >
+2.5 x L2, so no step finds its inputs in L2.  Each call of the step is then
+event-timed on its own over the same rotation, for the per-call roofline; the
+dominant call's (the longest) is the line's `roofline`.  `e2e` repeats the
+step with its inputs copied from pinned host memory and its output read back
+to the host every step.  `gpu_launches` counts the kernel nodes of the
+captured step graphs times the steps replayed.
 
 Under torchrun each rank runs its own replica of the workload on its own GPU
 (sequences are independent; no collective on the data path), so the scaling
 is weak and value = tokens of all ranks / max time.
 
---side-stream runs each c4a layer's indexer and top-k on a second stream,
-forked from the step's stream before compress_insert and joined before the
-attention (both streams are captured into the same graph).
-
---impl reference times the CPU oracle on this machine's host cores on the
-same workload, one bounded sample of rows per step.
+`cpu_baseline` and `--impl reference` time the CPU oracle (fp64 numpy) on
+this machine's host cores: a pool of one single-threaded worker process per
+core, each answering whole query rows of the same workload.
 """
 
 from __future__ import annotations
@@ -37,6 +43,7 @@ import argparse
 import json
 import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -50,23 +57,36 @@ if ROOT not in sys.path:
 METRIC = "c4a/c128a sparse decode attention tokens/s; achieved HBM GB/s vs ~8 TB/s"
 UNIT = "tokens/s"
 L2_BYTES = 129 * 2 ** 20
+HEADLINE = 2
+EXTRA = (1, 3, 4)
 
 
-def _args():
+def _args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", type=int, default=1)
+    ap.add_argument("--workload", type=int, default=HEADLINE)
+    ap.add_argument("--extra", default=",".join(str(i) for i in EXTRA),
+                    help="comma-separated workloads also measured and reported under 'configs', or 'none'")
+    ap.add_argument("--extra-steps", type=int, default=200, help="timed steps of each extra workload (at most K)")
     ap.add_argument("--impl", choices=["csa", "reference"], default="csa")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--reference-seconds", type=float, default=150.0,
+                    help="the reference arm stops after this many seconds of timed steps")
     ap.add_argument("--side-stream", action="store_true",
                     help="run each c4a layer's indexer + top-k on a second stream, beside compress_insert")
     ap.add_argument("--load-seconds", type=float, default=1.5,
                     help="untimed graph replays before the timed steps, so the clock sampler sees load")
-    return ap.parse_args()
+    return ap.parse_args(argv)
+
+
+def _extras(args):
+    if args.extra in ("", "none"):
+        return []
+    return [int(x) for x in args.extra.split(",") if int(x) != args.workload]
 
 
 def _dist():
@@ -77,12 +97,13 @@ def _dist():
 
 
 def _peaks():
+    """(HBM GB/s, bf16 dense TFLOP/s burst, source)."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
-    return 6800.0, "fallback"
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 1900.0)), "measured"
+    return 6800.0, 1900.0, "fallback"
 
 
 def max_over_ranks(x: float, world: int, device="cuda") -> float:
@@ -101,7 +122,7 @@ def weak_throughput(units_per_rank: int, steps: int, world: int, ms_max: float) 
     return units_per_rank * steps * world / (ms_max / 1e3)
 
 
-# ---------------------------------------------------------------- byte accounting
+# ---------------------------------------------------------------- algorithmic bytes and flops
 
 def _elem_bytes(dt: str) -> float:
     return {"f32": 4.0, "bf16": 2.0, "e4m3": 1.0, "e2m1": 0.5}[dt]
@@ -116,9 +137,7 @@ def _row_bytes(dt: str, dim: int) -> float:
     return b
 
 
-def attention_bytes(ld) -> float:
-    """Algorithmic bytes of one sparse-attention launch: every key row read once,
-    queries read once, outputs written once."""
+def _attended_keys(ld) -> int:
     from harness import n_visible
     L = ld.L
     keys = 0
@@ -126,32 +145,94 @@ def attention_bytes(ld) -> float:
         n = n_visible(int(p), L.ratio, L.window)
         sel = min(L.topk, n) if L.has_indexer else n
         keys += sel + min(L.swa, int(p) + 1)
+    return keys
+
+
+def attention_bytes(ld) -> float:
+    """Algorithmic bytes of one sparse-attention launch: every key row read once,
+    queries read once, outputs written once."""
+    L = ld.L
     q = ld.n_rows * L.heads * L.dim * _elem_bytes(L.in_dtype)
     out = ld.n_rows * L.heads * (L.dim * _elem_bytes(L.out_dtype) + (4 if L.out_dtype == "e4m3" else 0))
-    return keys * _row_bytes(L.cache_dtype, L.dim) + q + out
+    return _attended_keys(ld) * _row_bytes(L.cache_dtype, L.dim) + q + out
+
+
+def attention_flops(ld) -> float:
+    """q.k and p.v for every head over every attended key."""
+    L = ld.L
+    return 4.0 * L.heads * L.dim * _attended_keys(ld)
+
+
+def _visible_sum(ld) -> int:
+    from harness import n_visible
+    L = ld.L
+    return sum(n_visible(int(p), L.ratio, L.window) for p in ld.host["pos"])
 
 
 def indexer_bytes(ld) -> float:
-    from harness import n_visible
+    """Every visible indexer key read once, the indexer queries and weights read
+    once, the selection written once (score scratch not counted)."""
     L = ld.L
     if not L.has_indexer:
         return 0.0
-    n = sum(n_visible(int(p), L.ratio, L.window) for p in ld.host["pos"])
     q = ld.n_rows * L.idx_heads * (L.idx_dim * _elem_bytes(L.in_dtype) + 4)
-    return n * _row_bytes(L.idx_dtype, L.idx_dim) + q + ld.n_rows * L.topk * 4
+    return _visible_sum(ld) * _row_bytes(L.idx_dtype, L.idx_dim) + q + ld.n_rows * L.topk * 4
+
+
+def indexer_flops(ld) -> float:
+    L = ld.L
+    return 2.0 * L.idx_heads * L.idx_dim * _visible_sum(ld) if L.has_indexer else 0.0
 
 
 def compress_bytes(ld) -> float:
     """Raw rows in, state + window rows out, and for each closing window its
     state rows read and its entry written."""
     L = ld.L
-    from harness import n_visible  # noqa: F401
     n = ld.n_rows
     inb = n * 2 * L.dim * _elem_bytes(L.in_dtype)
     outb = n * (2 * L.dim * _elem_bytes(L.in_dtype) + _row_bytes(L.cache_dtype, L.dim))
     closing = sum(1 for p in ld.host["pos"] if p >= L.window - 1 and (p - L.window + 1) % L.ratio == 0)
     emit = closing * (L.window * 2 * L.dim * _elem_bytes(L.in_dtype) + _row_bytes(L.cache_dtype, L.dim))
     return inb + outb + emit
+
+
+def call_roofline(name: str, nbytes: float, flops: float, ms: float, hbm_gbs: float, tflops: float,
+                  traffic=None) -> dict:
+    """Roofline of one call: bound by HBM or by the tensor pipe, whichever takes longer at peak."""
+    t_hbm = nbytes / (hbm_gbs * 1e9)
+    t_tc = flops / (tflops * 1e12)
+    if t_tc > t_hbm:
+        achieved = flops / (ms / 1e3) / 1e12
+        return {"call": name, "bound": "tensor", "achieved": achieved, "peak": tflops, "unit": "TFLOP/s",
+                "frac": achieved / tflops, "traffic": traffic, "algorithmic_flops_per_launch": flops,
+                "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": ms}
+    achieved = nbytes / (ms / 1e3) / 1e9
+    return {"call": name, "bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+            "frac": achieved / hbm_gbs, "traffic": traffic, "algorithmic_bytes_per_launch": nbytes,
+            "algorithmic_flops_per_launch": flops, "avg_launch_ms": ms}
+
+
+# DRAM bytes (read + write) per launch of a call from an ncu capture, keyed by
+# (workload, call); valid only for the kernel source it was taken on (sha256 of
+# the call's kernel file).
+TRAFFIC = {}
+_CALL_SOURCE = {"attention": "k_attn_tc.cu", "indexer_topk": "k_indexer_tc.cu", "compress_insert": "k_compress.cu"}
+
+
+def _kernel_digest(name="k_attn_tc.cu"):
+    """sha256 of a kernel source file as it stands."""
+    import hashlib
+    src = os.path.join(ROOT, "compressed_sparse_long_c128a_gb300", "csrc", name)
+    with open(src, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def measured_traffic(workload_name: str, call: str):
+    """Measured DRAM traffic per launch, or None when absent or taken on another source."""
+    entry = TRAFFIC.get((workload_name, call))
+    if entry is None:
+        return None
+    return float(entry[0]) if _kernel_digest(_CALL_SOURCE[call]) == entry[1] else None
 
 
 # ---------------------------------------------------------------- clocks
@@ -204,17 +285,48 @@ class Clocks:
 
 # ---------------------------------------------------------------- CPU oracle timing
 
-def oracle_rows_per_second(wl, seconds: float, max_rows: int | None = None):
-    """Time the oracle on whole query rows of the workload (all layers per row)."""
-    from oracle import SequenceOracle
+def host_cpu() -> dict:
+    """The host's CPU model and core count (lscpu, else /proc/cpuinfo)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.TimeoutExpired):
+        pass
+    if model is None and os.path.exists("/proc/cpuinfo"):
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    return {"model": model or platform.processor() or "unknown", "machine": platform.machine(),
+            "logical_cpus": os.cpu_count() or 1}
+
+
+def _sample_rows(wl, n: int):
+    """An evenly spaced sample of n query rows (sequence, row) of the workload."""
     rows = [(b, r) for b, s in enumerate(wl.seqs) for r in range(s.n_new)]
-    stride = max(1, len(rows) // 64)
-    rows = rows[::stride]
-    done = 0
-    t0 = time.perf_counter()
+    stride = max(1, len(rows) // max(n, 1))
+    return rows[::stride][:n] if n else rows
+
+
+def _oracle_worker(job):
+    """One worker of the pool: answer query rows with the oracle until the deadline.
+
+    job = (workload index, [(sequence, row), ...], wall-clock deadline or None).
+    Returns the number of rows answered (every layer of each row)."""
+    wl_idx, rows, deadline = job
+    import synth
+    from oracle import SequenceOracle
+    wl = synth.workload(wl_idx)
     cache = {}
-    while time.perf_counter() - t0 < seconds and (max_rows is None or done < max_rows):
-        b, r = rows[done % len(rows)]
+    done = 0
+    for b, r in rows:
+        if deadline is not None and time.time() >= deadline:
+            break
         for L in wl.layers:
             key = (L.tid, b)
             if key not in cache:
@@ -222,15 +334,55 @@ def oracle_rows_per_second(wl, seconds: float, max_rows: int | None = None):
                 cache[key] = SequenceOracle(wl, L, b)
             cache[key].attend(r)
         done += 1
-    dt = time.perf_counter() - t0
-    return done, dt
+    return done
 
 
-def _cores() -> int:
-    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS"):
-        if os.environ.get(v, "").isdigit():
-            return int(os.environ[v])
-    return os.cpu_count() or 1
+class OraclePool:
+    """Single-threaded oracle workers, one per host core, started with spawn."""
+
+    def __init__(self, workers: int | None = None):
+        import multiprocessing as mp
+        self.workers = workers or (os.cpu_count() or 1)
+        saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+        for k in saved:
+            os.environ[k] = "1"  # inherited by the spawned workers: one thread each
+        try:
+            self.pool = mp.get_context("spawn").Pool(self.workers)
+        finally:
+            for k, v in saved.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+
+    def run(self, wl_idx: int, rows, deadline=None) -> int:
+        """Rows of `rows` answered; rows are dealt to workers by sequence, so each reuses its set-up."""
+        by_seq = {}
+        for b, r in rows:
+            by_seq.setdefault(b, []).append((b, r))
+        jobs = [[] for _ in range(self.workers)]
+        for i, seq_rows in enumerate(sorted(by_seq.values(), key=len, reverse=True)):
+            min(jobs, key=len).extend(seq_rows)
+        jobs = [(wl_idx, j, deadline) for j in jobs if j]
+        return sum(self.pool.map(_oracle_worker, jobs))
+
+    def close(self):
+        self.pool.terminate()
+        self.pool.join()
+
+
+def oracle_baseline(pool: OraclePool, wl_idx: int, seconds: float) -> dict:
+    """Rows per second of the oracle on the pool, over a bounded sample of the workload."""
+    import synth
+    wl = synth.workload(wl_idx)
+    rows = _sample_rows(wl, 64 * pool.workers)
+    t0 = time.time()
+    n = pool.run(wl_idx, rows, deadline=t0 + seconds)
+    dt = time.time() - t0
+    return {"value": n / dt, "unit": UNIT, "cores": pool.workers, "kind": "oracle",
+            "sample": f"{n} query rows of {wl.name} (every layer of each row; rows spread evenly over the "
+                      f"batch), fp64 numpy, {pool.workers} single-threaded worker processes, {dt:.1f} s",
+            "cpu": host_cpu()}
 
 
 # ---------------------------------------------------------------- reference arm
@@ -241,21 +393,30 @@ def run_reference(args):
         return
     import synth
     wl = synth.workload(args.workload)
-    for _ in range(args.warmup):
-        oracle_rows_per_second(wl, 0.0, max_rows=1)
-    t0 = time.perf_counter()
-    rows = 0
-    for _ in range(args.steps):
-        n, _ = oracle_rows_per_second(wl, 1e9, max_rows=1)
-        rows += n
-    dt = time.perf_counter() - t0
-    value = rows / dt
+    pool = OraclePool()
+    try:
+        rows = _sample_rows(wl, 64 * pool.workers)
+        per_step = pool.workers  # one row per worker and step
+        for i in range(args.warmup):
+            pool.run(args.workload, rows[(i * per_step) % len(rows):][:per_step])
+        t0 = time.time()
+        steps = n = 0
+        while steps < args.steps and time.time() - t0 < args.reference_seconds:
+            k = (steps * per_step) % len(rows)
+            n += pool.run(args.workload, (rows[k:] + rows[:k])[:per_step])
+            steps += 1
+        dt = time.time() - t0
+    finally:
+        pool.close()
+    value = n / dt
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": _config(wl, None),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": _cores(), "kind": "oracle",
-                             "sample": f"one query row (all layers) of {wl.name} per step, fp64 numpy"},
+            "steps": steps, "steps_requested": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * dt / max(steps, 1), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": _config(wl, None),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": pool.workers, "kind": "oracle",
+                             "sample": f"{n} query rows of {wl.name} in {steps} steps of {per_step} rows "
+                                       f"(every layer of each row), fp64 numpy, {pool.workers} single-threaded "
+                                       f"worker processes", "cpu": host_cpu()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 
@@ -266,9 +427,11 @@ def _config(wl, replicas):
     cfg = {"workload": wl.name, "batch": len(wl.seqs), "rows_per_step": wl.n_rows,
            "context": ctx[0] if len(ctx) == 1 else [ctx[0], ctx[-1]],
            "layers": [x.name for x in wl.layers], "dim": L.dim, "heads": L.heads, "cache": L.cache_dtype,
+           "indexer_cache": L.idx_dtype if L.has_indexer else None, "out": L.out_dtype,
            "topk": L.topk or "dense", "swa": L.swa}
     if replicas is not None:
-        cfg["l2"] = f"inputs larger than L2: {replicas} rotating cache replicas"
+        cfg["l2"] = (f"inputs larger than L2: {replicas} rotating cache replicas" if replicas > 1
+                     else "inputs larger than L2: the step's working set exceeds 2.5 x L2")
     return cfg
 
 
@@ -289,43 +452,75 @@ def _clone_layer(ld):
     return c
 
 
-def _launches_per_step(ld) -> int:
-    """Kernel launches of one layer step, following the library's dispatch rules."""
-    import compressed_sparse_long_c128a_gb300 as csa
-    L = ld.L
-    n = 2  # compress_insert: ingest + emit
+def graph_kernel_nodes(g) -> int | None:
+    """Kernel nodes of a captured torch CUDA graph (None if the graph handle is not exposed)."""
+    import ctypes
+    if not hasattr(g, "raw_cuda_graph"):
+        return None
+    try:
+        import torch
+        rt = None
+        for name in ("libcudart.so.13", "libcudart.so.12", "libcudart.so"):
+            try:
+                rt = ctypes.CDLL(name)
+                break
+            except OSError:
+                continue
+        if rt is None:
+            lib_dir = os.path.join(os.path.dirname(torch.__file__), "lib")
+            for f in sorted(os.listdir(lib_dir)):
+                if f.startswith("libcudart"):
+                    rt = ctypes.CDLL(os.path.join(lib_dir, f))
+                    break
+        if rt is None:
+            return None
+        graph = ctypes.c_void_p(g.raw_cuda_graph())
+        n = ctypes.c_size_t(0)
+        if rt.cudaGraphGetNodes(graph, None, ctypes.byref(n)) != 0:
+            return None
+        nodes = (ctypes.c_void_p * n.value)()
+        if rt.cudaGraphGetNodes(graph, nodes, ctypes.byref(n)) != 0:
+            return None
+        kernels = 0
+        for i in range(n.value):
+            t = ctypes.c_int(-1)
+            if rt.cudaGraphNodeGetType(ctypes.c_void_p(nodes[i]), ctypes.byref(t)) != 0:
+                return None
+            kernels += t.value == 0  # cudaGraphNodeTypeKernel
+        return kernels
+    except Exception:  # noqa: BLE001 -- a diagnostic count, never fatal
+        return None
+
+
+def _call_fns(ld, csa, stream):
+    """The step's calls of one layer, as (name, fn) in step order."""
+    L, io = ld.L, ld.io
+    fns = [("compress_insert", lambda: ld.compress_insert(io["kv"], io["gate"], io["seq_id"], io["pos"], stream))]
     if L.has_indexer:
-        n += 1  # scores (tensor-core or generic)
-        chunks = -(-max(ld.max_n, 1) // 16384)  # top-k chunks of 16384 scores
-        two_stage = 2 <= chunks <= 64 and 4 * (chunks * L.topk + chunks * L.topk // 32 + 1 + chunks * L.topk) <= 200 * 1024
-        n += 2 if two_stage else 1  # chunk select (+ merge)
-    tc = L.dim == 512 and L.heads == 64 and L.cache_dtype in ("bf16", "e4m3") and L.rope_dim <= 128
-    if tc:
-        n += 1  # one launch; split rows merge inside it
-    else:
-        kq = L.topk if L.has_indexer else ld.max_n
-        n += 2 if csa.sparse_attn_workspace_size(ld.c_layer, ld.n_rows, kq) > 0 else 1  # (+ split merge)
-    return n
+        fns.append(("indexer_topk", lambda: csa.indexer_topk(
+            io["q_idx"], io["w"], io["seq_id"], io["pos"], L.ratio, L.window, ld.idx, ld.tables["idx"], L.topk,
+            max(ld.max_n, 1), io["topk"], ld.ws_idx, ld.err, stream)))
+    attn = csa.sparse_attn_prefill if ld.prefill else csa.sparse_attn_decode
+    topk = io["topk"] if L.has_indexer else None
+    fns.append(("attention", lambda: attn(
+        ld.c_layer, io["q"], io["seq_id"], io["pos"], ld.comp, ld.tables["comp"], topk,
+        L.topk if L.has_indexer else 0, max(ld.max_n, 1), ld.swa, ld.tables["swa"], io["out"],
+        csa.DTYPES[L.out_dtype], io["out_scales"], ld.ws_attn, ld.err, stream)))
+    return fns
 
 
-def run_csa(args):
+def measure_workload(idx: int, args, steps: int, world: int, local: int, pool=None, headline=False) -> dict:
+    """Time one workload: K graph-replayed steps, each call alone, e2e, and the CPU baseline."""
     import torch
 
-    rank, world, local = _dist()
-    torch.cuda.set_device(local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     import compressed_sparse_long_c128a_gb300 as csa
-    from compressed_sparse_long_c128a_gb300 import build as csa_build
     import synth
     from harness import WorkloadDev
 
-    csa_build.build()
-    wl = synth.workload(args.workload)
+    hbm, tflops, peak_src = _peaks()
+    wl = synth.workload(idx)
     wd = WorkloadDev(wl)
     base = wd.layers
-
     step_bytes = sum(attention_bytes(ld) + indexer_bytes(ld) + compress_bytes(ld) for ld in base)
     replicas = 1 if step_bytes > 2.5 * L2_BYTES else int(math.ceil(2.5 * L2_BYTES / step_bytes)) + 1
     reps = [base] + [[_clone_layer(ld) for ld in base] for _ in range(replicas - 1)]
@@ -349,17 +544,17 @@ def run_csa(args):
             step(rep, stream)
         graphs.append(g)
     torch.cuda.synchronize()
+    nodes = [graph_kernel_nodes(g) for g in graphs]
 
     clocks = Clocks(local)
     clocks.start()
-    # keep the GPU loaded for a while so the clock sampler sees it under load
     t_load = time.perf_counter()
     i = 0
     with torch.cuda.stream(stream):  # a graph replays on the current stream
         while time.perf_counter() - t_load < args.load_seconds:
             graphs[i % replicas].replay()
             i += 1
-            if i % 256 == 0:
+            if i % 64 == 0:
                 stream.synchronize()
     stream.synchronize()
 
@@ -372,7 +567,7 @@ def run_csa(args):
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         t_start.record(stream)
-        for k in range(args.steps):
+        for k in range(steps):
             graphs[k % replicas].replay()
         t_end.record(stream)
     torch.cuda.synchronize()
@@ -380,82 +575,94 @@ def run_csa(args):
     clk = clocks.stop()
     ms_total = max_over_ranks(t_start.elapsed_time(t_end), world)
     rows_per_step = sum(ld.n_rows for ld in base)
-    value = weak_throughput(rows_per_step, args.steps, world, ms_total)
+    value = weak_throughput(rows_per_step, steps, world, ms_total)
     wd.check("timed steps")
 
-    # dominant kernel: sparse attention of the first layer, event-timed per launch
-    att_ms = []
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    with torch.cuda.stream(stream):
-        for k in range(args.steps):
-            ld = reps[k % replicas][0]
-            io = ld.io
-            L = ld.L
-            topk = io.get("topk") if L.has_indexer else None
-            attn = csa.sparse_attn_prefill if ld.prefill else csa.sparse_attn_decode
-            ev[k][0].record(stream)
-            attn(ld.c_layer, io["q"], io["seq_id"], io["pos"], ld.comp, ld.tables["comp"], topk,
-                 L.topk if L.has_indexer else 0, max(ld.max_n, 1), ld.swa, ld.tables["swa"], io["out"],
-                 csa.DTYPES[L.out_dtype], io["out_scales"], ld.ws_attn, ld.err, stream)
-            ev[k][1].record(stream)
-    torch.cuda.synchronize()
-    att_ms = [a.elapsed_time(b) for a, b in ev]
-    att_avg_ms = sum(att_ms) / len(att_ms)
-    att_bytes = attention_bytes(base[0])
-    peak, peak_src = _peaks()
-    achieved = att_bytes / (att_avg_ms / 1e3) / 1e9
+    # every call of every layer on its own, event-timed per launch over the same rotation
+    n_call = max(3, min(steps, 200))
+    calls = {}
+    for li in range(len(base)):
+        for ci, (name, _) in enumerate(_call_fns(base[li], csa, stream)):
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_call)]
+            with torch.cuda.stream(stream):
+                for k in range(n_call):
+                    fn = _call_fns(reps[k % replicas][li], csa, stream)[ci][1]
+                    ev[k][0].record(stream)
+                    fn()
+                    ev[k][1].record(stream)
+            torch.cuda.synchronize()
+            ms = sum(a.elapsed_time(b) for a, b in ev) / n_call
+            ld = base[li]
+            if name == "attention":
+                nb, fl = attention_bytes(ld), attention_flops(ld)
+            elif name == "indexer_topk":
+                nb, fl = indexer_bytes(ld), indexer_flops(ld)
+            else:
+                nb, fl = compress_bytes(ld), 0.0
+            key = f"{ld.L.name}.{name}" if len(base) > 1 else name
+            calls[key] = call_roofline(key, nb, fl, ms, hbm, tflops, measured_traffic(wl.name, name))
+    wd.check("per-call timing")
+    dominant = max(calls.values(), key=lambda c: c["avg_launch_ms"])
 
-    e2e = None
-    if not args.no_e2e:
-        e2e = _e2e(args, reps, graphs, stream, rows_per_step, world, step)
-
-    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_total / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": base[0].L.cache_dtype, "data": "synthetic",
-            "config": _config(wl, replicas),
-            "achieved_gbs_step": step_bytes / (ms_total / args.steps / 1e3) / 1e9,
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": _attn_traffic(wl.name), "kernel": "sparse attention",
-                         "algorithmic_bytes_per_launch": att_bytes, "avg_launch_ms": att_avg_ms,
-                         "peak_source": f"{peak_src} hbm_gbs (copy bandwidth, burst)"},
-            "clocks": clk,
-            "gpu_launches": sum(_launches_per_step(ld) for ld in base) * args.steps,
-            "e2e": e2e}
+    e2e = None if args.no_e2e else _e2e(min(steps, 200), reps, graphs, stream, rows_per_step, world, step)
+    res = {"value": value, "unit": UNIT, "steps": steps, "ms_per_step": ms_total / steps,
+           "dtype": base[0].L.cache_dtype, "config": _config(wl, replicas),
+           "achieved_gbs_step": step_bytes / (ms_total / steps / 1e3) / 1e9,
+           "algorithmic_bytes_per_step": step_bytes,
+           "roofline": dict(dominant, peak_source=f"{peak_src} (copy bandwidth / cuBLAS bf16, burst)"),
+           "calls": calls, "clocks": clk,
+           "gpu_launches": (sum(nodes[k % replicas] for k in range(steps))
+                            if all(n is not None for n in nodes) else None),
+           "kernels_per_step": nodes[0], "e2e": e2e}
     if side is not None:
-        line["config"]["indexer_stream"] = "side"
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        n, dt = oracle_rows_per_second(wl, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": n / dt, "unit": UNIT, "cores": _cores(), "kind": "oracle",
-                                "sample": f"{n} query rows of {wl.name} (all layers each), fp64 numpy, "
-                                          f"{dt:.1f} s"}
+        res["config"]["indexer_stream"] = "side"
+    if pool is not None:
+        res["cpu_baseline"] = oracle_baseline(pool, idx, args.cpu_seconds)
+    del graphs, reps, base, wd
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_csa(args):
+    import torch
+
+    rank, world, local = _dist()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from compressed_sparse_long_c128a_gb300 import build as csa_build
+
+    csa_build.build()
+    pool = OraclePool() if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
+    try:
+        head = measure_workload(args.workload, args, args.steps, world, local, pool, headline=True)
+        extra = {}
+        for idx in _extras(args):
+            r = measure_workload(idx, args, max(3, min(args.steps, args.extra_steps)), world, local, pool)
+            extra[r["config"]["workload"]] = r
+    finally:
+        if pool is not None:
+            pool.close()
+    line = {"metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": head["dtype"], "data": "synthetic",
+            "config": head["config"], "roofline": head["roofline"], "clocks": head["clocks"],
+            "gpu_launches": head["gpu_launches"], "e2e": head["e2e"],
+            "achieved_gbs_step": head["achieved_gbs_step"], "calls": head["calls"],
+            "kernels_per_step": head["kernels_per_step"]}
+    if "cpu_baseline" in head:
+        line["cpu_baseline"] = head["cpu_baseline"]
+    if extra:
+        line["configs"] = extra
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()
 
 
-# DRAM bytes (read + write) of one attention launch from an ncu capture, keyed by
-# workload, valid only for the kernel source it was taken on (sha256 of
-# k_attn_tc.cu); see profiles/attn_tc_c128a_decode_b32.md.
-ATTN_TRAFFIC = {
-    "c128a_decode_b32_128k": (40027392 + 768, "c2649c649246d32f996d462908a44e4a6c7dab5bb4b687a4794092a98d9c1985"),
-}
-
-
-def _attn_traffic(workload_name):
-    """Measured DRAM traffic per attention launch, or None when absent or taken on other source."""
-    import hashlib
-    entry = ATTN_TRAFFIC.get(workload_name)
-    if entry is None:
-        return None
-    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "compressed_sparse_long_c128a_gb300", "csrc",
-                       "k_attn_tc.cu")
-    with open(src, "rb") as f:
-        digest = hashlib.sha256(f.read()).hexdigest()
-    return float(entry[0]) if digest == entry[1] else None
-
-
-def _e2e(args, reps, graphs, stream, rows_per_step, world, step):
+def _e2e(k_steps, reps, graphs, stream, rows_per_step, world, step):
     """Same steps with inputs copied from pinned host memory and the output read back every step.
 
     Each replica's step is captured once more as one CUDA graph that also holds
@@ -502,7 +709,6 @@ def _e2e(args, reps, graphs, stream, rows_per_step, world, step):
     except RuntimeError:
         full = []
         torch.cuda.synchronize()
-    k_steps = min(args.steps, 200)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     t0.record(stream)

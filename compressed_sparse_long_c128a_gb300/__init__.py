@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_HERE, "libcsa.so")
 F32, BF16, E4M3, E2M1 = 0, 1, 2, 3
 DTYPES = {"f32": F32, "bf16": BF16, "e4m3": E4M3, "e2m1": E2M1}
 
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE_BOUNDS, ERR_WORKSPACE = 0, -1, -2, -3, -4, -5
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE_BOUNDS, ERR_WORKSPACE, ERR_TIMEOUT = 0, -1, -2, -3, -4, -5, -6
 
 
 class CsaError(RuntimeError):

@@ -80,6 +80,21 @@ EncodeTiled encode_tiled() {
 
 }  // namespace
 
+cudaError_t csa::sm_count(int* n) {
+  static PerDevice sms;
+  return with_device_slot(sms, [n](int dev, int64_t& v) {
+    if (!v) {
+      int c = 0;
+      const cudaError_t e = cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return e;
+      if (c <= 0) return cudaErrorInvalidDevice;
+      v = c;
+    }
+    *n = (int)v;
+    return cudaSuccess;
+  });
+}
+
 bool csa::encode_bf16_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t stride_bytes,
                           uint32_t box_cols, uint32_t box_rows) {
   const EncodeTiled fn = encode_tiled();
@@ -91,6 +106,38 @@ bool csa::encode_bf16_map(CUtensorMap* m, const void* base, uint64_t cols, uint6
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int csa::check_indexer_topk(const void* q_idx, int32_t q_dtype, const float* w, int32_t n_rows, int32_t idx_heads,
+                            int32_t idx_dim, const int32_t* seq_id, const int32_t* pos, int32_t ratio,
+                            int32_t window, const csa_paged* idx_cache, const csa_block_table* bt, int32_t k,
+                            int32_t max_n, const int32_t* out_idx, const int32_t* err) {
+  if (n_rows < 0 || k <= 0 || max_n < 0 || idx_heads <= 0 || idx_dim <= 0) return CSA_ERR_INVALID_ARG;
+  if (ratio <= 0 || window <= 0 || 256 % ratio) return CSA_ERR_INVALID_ARG;
+  if (n_rows == 0) return CSA_OK;
+  if (!q_idx || !w || !seq_id || !pos || !out_idx || !err) return CSA_ERR_INVALID_ARG;
+  if (q_dtype != CSA_F32 && q_dtype != CSA_BF16) return CSA_ERR_UNSUPPORTED;
+  int st = check_paged(idx_cache, idx_dim, 256 / ratio, kF32 | kBF16 | kE2M1);
+  if (st) return st;
+  if ((st = check_bt(bt))) return st;
+  if ((size_t)idx_heads * idx_dim > 32768 || idx_dim > 256) return CSA_ERR_UNSUPPORTED;
+  return CSA_OK;
+}
+
+int csa::enqueue_indexer_topk(const void* q_idx, int32_t q_dtype, const float* w, int32_t n_rows, int32_t idx_heads,
+                              int32_t idx_dim, const int32_t* seq_id, const int32_t* pos, int32_t ratio,
+                              int32_t window, const csa_paged* idx_cache, const csa_block_table* bt, int32_t k,
+                              int32_t max_n, int32_t* out_idx, float* scores, void* cand, int32_t* err,
+                              cudaStream_t stream) {
+  IndexerArgs ia{q_idx, q_dtype, w, seq_id, pos, *idx_cache, *bt, idx_heads, idx_dim, ratio, window, max_n,
+                 scores, err};
+  const bool tc = indexer_tc_eligible(ia);
+  cudaError_t e = tc ? launch_indexer_tc(ia, n_rows, stream) : launch_indexer_scores(ia, n_rows, stream);
+  if (e != cudaSuccess) return CSA_ERR_CUDA;
+  // the generic score kernel is not launched when no row can see an entry
+  const Order first = (tc || max_n > 0) ? kAfterOwnKernel : kStreamOrder;
+  TopkArgs ta{scores, pos, ratio, window, max_n, k, out_idx, err};
+  return cuda_status(launch_topk(ta, n_rows, cand, stream, first));
 }
 
 namespace {
@@ -207,28 +254,17 @@ int csa_indexer_topk(const void* q_idx, int32_t q_dtype, const float* w, int32_t
                      int32_t idx_dim, const int32_t* seq_id, const int32_t* pos, int32_t ratio, int32_t window,
                      const csa_paged* idx_cache, const csa_block_table* bt, int32_t k, int32_t max_n,
                      int32_t* out_idx, void* ws, size_t ws_bytes, int32_t* err, csa_stream_t stream) {
-  if (n_rows < 0 || k <= 0 || max_n < 0 || idx_heads <= 0 || idx_dim <= 0) return CSA_ERR_INVALID_ARG;
-  if (ratio <= 0 || window <= 0 || 256 % ratio) return CSA_ERR_INVALID_ARG;
-  if (n_rows == 0) return CSA_OK;
-  if (!q_idx || !w || !seq_id || !pos || !out_idx || !err) return CSA_ERR_INVALID_ARG;
-  if (q_dtype != CSA_F32 && q_dtype != CSA_BF16) return CSA_ERR_UNSUPPORTED;
-  int st = check_paged(idx_cache, idx_dim, 256 / ratio, kF32 | kBF16 | kE2M1);
-  if (st) return st;
-  if ((st = check_bt(bt))) return st;
-  if ((size_t)idx_heads * idx_dim > 32768 || idx_dim > 256) return CSA_ERR_UNSUPPORTED;
+  const int st = check_indexer_topk(q_idx, q_dtype, w, n_rows, idx_heads, idx_dim, seq_id, pos, ratio, window,
+                                    idx_cache, bt, k, max_n, out_idx, err);
+  if (st != CSA_OK || n_rows == 0) return st;
   const size_t need = csa_indexer_topk_workspace_size(n_rows, max_n, k);
   if (need && (!ws || ws_bytes < need)) return CSA_ERR_WORKSPACE;
   float* scores = reinterpret_cast<float*>(ws);
   void* cand = topk_candidate_bytes(n_rows, max_n, k)
                    ? reinterpret_cast<uint8_t*>(ws) + align_up(sizeof(float) * (size_t)n_rows * max_n)
                    : nullptr;
-  IndexerArgs ia{q_idx, q_dtype, w, seq_id, pos, *idx_cache, *bt, idx_heads, idx_dim, ratio, window, max_n,
-                 scores, err};
-  cudaError_t e = indexer_tc_eligible(ia) ? launch_indexer_tc(ia, n_rows, stream)
-                                           : launch_indexer_scores(ia, n_rows, stream);
-  if (e != cudaSuccess) return CSA_ERR_CUDA;
-  TopkArgs ta{scores, pos, ratio, window, max_n, k, out_idx, err};
-  return cuda_status(launch_topk(ta, n_rows, cand, stream));
+  return enqueue_indexer_topk(q_idx, q_dtype, w, n_rows, idx_heads, idx_dim, seq_id, pos, ratio, window, idx_cache,
+                              bt, k, max_n, out_idx, scores, cand, err, stream);
 }
 
 size_t csa_sparse_attn_workspace_size(const csa_layer* L, int32_t n_rows, int32_t k_or_max_n) {

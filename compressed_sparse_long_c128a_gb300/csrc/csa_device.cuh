@@ -23,15 +23,15 @@ struct RopeTab {
   int32_t rope_dim;
 };
 
-// Programmatic dependent launch.  Every kernel of the library is launched so
-// that it may start while the previous kernel of the stream is finishing:
-// pdl_trigger() lets the next kernel launch; pdl_wait() blocks until the
-// previous kernel has completed and its writes are visible.  A kernel calls
-// pdl_wait() before it touches a cache, a workspace or an output (anything an
-// earlier kernel may write or read); reading the caller's inputs before it is
-// safe, since those were complete before the library's first kernel started.
-// Every CTA passes pdl_wait() before it exits, so a grid completes only after
-// its predecessor did and completion stays transitive along the stream.
+// Programmatic dependent launch between the kernels of one call.  The first
+// kernel of an entry point is launched in plain stream order; each later one
+// may start while the call's previous kernel is finishing: pdl_trigger() lets
+// the next kernel launch; pdl_wait() blocks until the previous kernel has
+// completed and its writes are visible (it returns at once in a kernel
+// launched in plain stream order).  A kernel calls pdl_wait() before it
+// touches anything an earlier kernel of the call may write or read.  Every CTA
+// passes pdl_wait() before it exits, so a grid completes only after its
+// predecessor did and completion stays transitive along the call.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

@@ -4,15 +4,51 @@
 #include <cuda.h>  // CUtensorMap (type only; the encoder is fetched at run time)
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "csa_device.cuh"
 
 namespace csa {
 
-// Launch with programmatic stream serialization (see pdl_wait / pdl_trigger)
-// and, when cluster_y > 0, clusters of (1, cluster_y, 1) CTAs.
+// One-time set-up of a launcher, kept per device: function attributes set by
+// cudaFuncSetAttribute and device properties belong to the device that is
+// current when they are set or read, so each device ordinal has its own slot.
+constexpr int kMaxDevices = 64;
+struct PerDevice {
+  std::mutex mu;
+  int64_t value[kMaxDevices] = {};  // launcher-defined; 0 until the first set-up
+};
+
+// Runs f(device, slot) under the lock with the current device's slot.
+template <typename F>
+inline cudaError_t with_device_slot(PerDevice& pd, F f) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(pd.mu);
+  return f(dev, pd.value[dev]);
+}
+
+// Number of SMs of the current device (looked up once per device).
+cudaError_t sm_count(int* n);
+
+// How a launch is ordered after the work before it on the stream.
+//   kStreamOrder: plain stream order -- the kernel starts after everything
+//     enqueued before it has completed.  The first kernel of every entry point
+//     is launched this way, so a call never overlaps work the library did not
+//     enqueue (a caller's kernel that writes the call's inputs, or one that
+//     still reads its outputs).
+//   kAfterOwnKernel: programmatic stream serialization -- the kernel may start
+//     while the previous kernel of the same call is finishing (see pdl_wait /
+//     pdl_trigger); only for the second and later kernels of one call.
+enum Order : int { kStreamOrder = 0, kAfterOwnKernel = 1 };
+
+// Launch with the given ordering and, when cluster_y > 0, clusters of
+// (1, cluster_y, 1) CTAs.
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                           int cluster_y, Args... args) {
+                           Order order, int cluster_y, Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -20,9 +56,11 @@ inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, siz
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   int n = 0;
-  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[n].val.programmaticStreamSerializationAllowed = 1;
-  ++n;
+  if (order == kAfterOwnKernel) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
   if (cluster_y > 0) {
     attr[n].id = cudaLaunchAttributeClusterDimension;
     attr[n].val.clusterDim.x = 1;
@@ -120,7 +158,22 @@ struct TopkArgs {
 };
 // `cand`: topk_candidate_bytes() of scratch for the two-stage path (nullptr: one CTA per row)
 size_t topk_candidate_bytes(int32_t n_rows, int32_t max_n, int32_t k);
-cudaError_t launch_topk(const TopkArgs& a, int32_t n_rows, void* cand, cudaStream_t s);
+// `first`: kStreamOrder when no kernel of the call precedes the top-k launches
+cudaError_t launch_topk(const TopkArgs& a, int32_t n_rows, void* cand, cudaStream_t s, Order first);
+
+// Host validation and enqueue of indexer scores + top-k, shared by
+// csa_indexer_topk and csa_indexer_topk_noalloc so that both accept and refuse
+// the same calls (api.cu).  check_indexer_topk returns CSA_OK for n_rows == 0
+// before looking at any pointer; the caller then enqueues nothing.
+int check_indexer_topk(const void* q_idx, int32_t q_dtype, const float* w, int32_t n_rows, int32_t idx_heads,
+                       int32_t idx_dim, const int32_t* seq_id, const int32_t* pos, int32_t ratio, int32_t window,
+                       const csa_paged* idx_cache, const csa_block_table* bt, int32_t k, int32_t max_n,
+                       const int32_t* out_idx, const int32_t* err);
+// scores: n_rows * max_n floats; cand: topk_candidate_bytes(n_rows, max_n, k) bytes or nullptr when 0
+int enqueue_indexer_topk(const void* q_idx, int32_t q_dtype, const float* w, int32_t n_rows, int32_t idx_heads,
+                         int32_t idx_dim, const int32_t* seq_id, const int32_t* pos, int32_t ratio, int32_t window,
+                         const csa_paged* idx_cache, const csa_block_table* bt, int32_t k, int32_t max_n,
+                         int32_t* out_idx, float* scores, void* cand, int32_t* err, cudaStream_t stream);
 
 // ---- attention (k_attn.cu)
 struct AttnArgs {

@@ -317,10 +317,8 @@ __device__ __forceinline__ uint32_t rot_pack(float q0, float q1, int d, float qs
 // rounded to bf16, 128B-swizzled K-major (rows = heads).  bf16 rows arrive
 // raw as the CTA's first requests (eight TMA boxes of 64 dims x 64 heads, or
 // cp.async when the rows cannot be described by a tensor map), ahead of the
-// key lookups, which wait for the previous launch, and are then transformed
-// in place; fp32 rows go through registers.  The softmax threads then release the MMA issuer through q_full.
-// The query rows, seq_id and pos are inputs of the step, not written by the
-// library's preceding launches, so they are read before griddepcontrol.wait.
+// key lookups, and are then transformed in place; fp32 rows go through
+// registers.  The softmax threads then release the MMA issuer through q_full.
 __device__ __forceinline__ void fill_q_issue(const AttnArgs& a, uint8_t* smem, Misc& ms, int st) {
   if (a.q_dtype != CSA_BF16) return;
   if (a.q_tma) {
@@ -832,15 +830,17 @@ int32_t attn_tc_splits(int32_t n_rows, int32_t keys_per_row) {
 }
 
 cudaError_t launch_attn_tc(const AttnArgs& a, int32_t n_rows, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  return launch_k(attn_tc_kernel, dim3(n_rows, a.n_splits), dim3(kThreads), kSmemBytes, s, a.n_splits, a);
+  static PerDevice attrs;
+  cudaError_t e = with_device_slot(attrs, [](int, int64_t& done) {
+    if (done) return cudaSuccess;
+    cudaError_t r = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (r == cudaSuccess) r = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+    if (r == cudaSuccess) done = 1;
+    return r;
+  });
+  if (e != cudaSuccess) return e;
+  return launch_k(attn_tc_kernel, dim3(n_rows, a.n_splits), dim3(kThreads), kSmemBytes, s, kStreamOrder, a.n_splits,
+                  a);
 }
 
 }  // namespace csa

@@ -189,12 +189,12 @@ __global__ void __launch_bounds__(kThreads) emit_kernel(const EmitArgs a) {
 
 cudaError_t launch_ingest(const IngestArgs& a, int32_t n_tok, cudaStream_t s) {
   if (n_tok == 0) return cudaSuccess;
-  return launch_k(ingest_kernel, dim3(n_tok), dim3(kThreads), a.dim * sizeof(float), s, 0, a);
+  return launch_k(ingest_kernel, dim3(n_tok), dim3(kThreads), a.dim * sizeof(float), s, kStreamOrder, 0, a);
 }
 
 cudaError_t launch_emit(const EmitArgs& a, int32_t n_tok, cudaStream_t s) {
   if (n_tok == 0) return cudaSuccess;
-  return launch_k(emit_kernel, dim3(n_tok), dim3(kThreads), a.dim * sizeof(float), s, 0, a);
+  return launch_k(emit_kernel, dim3(n_tok), dim3(kThreads), a.dim * sizeof(float), s, kAfterOwnKernel, 0, a);
 }
 
 }  // namespace csa

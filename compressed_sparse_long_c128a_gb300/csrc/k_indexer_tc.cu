@@ -381,17 +381,17 @@ bool indexer_tc_eligible(const IndexerArgs& a) {
 }
 
 cudaError_t launch_indexer_tc(const IndexerArgs& args, int32_t n_rows, cudaStream_t s) {
-  static bool attr_set = false;
-  static int n_sm = 0;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm <= 0)
-      n_sm = 148;
-    attr_set = true;
-  }
+  static PerDevice attrs;
+  cudaError_t e = with_device_slot(attrs, [](int, int64_t& done) {
+    if (done) return cudaSuccess;
+    const cudaError_t r =
+        cudaFuncSetAttribute(indexer_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (r == cudaSuccess) done = 1;
+    return r;
+  });
+  if (e != cudaSuccess) return e;
+  int n_sm = 0;
+  if ((e = sm_count(&n_sm)) != cudaSuccess) return e;
   IndexerArgs a = args;
   a.k_tma = a.cache.dtype == CSA_BF16 &&
             encode_bf16_map(&a.k_map, a.cache.data, kDI, (uint64_t)a.cache.num_blocks * kRowsPerBlock, kDI * 2,
@@ -405,7 +405,7 @@ cudaError_t launch_indexer_tc(const IndexerArgs& args, int32_t n_rows, cudaStrea
   const int32_t min_splits = (tiles + tiles_per_cta_max - 1) / tiles_per_cta_max;
   if (splits < min_splits) splits = min_splits;
   if (splits < 1) splits = 1;
-  return launch_k(indexer_tc_kernel, dim3(n_rows, splits), dim3(kThreads), kSmemBytes, s, 0, a);
+  return launch_k(indexer_tc_kernel, dim3(n_rows, splits), dim3(kThreads), kSmemBytes, s, kStreamOrder, 0, a);
 }
 
 }  // namespace csa

@@ -375,35 +375,41 @@ size_t topk_candidate_bytes(int32_t n_rows, int32_t max_n, int32_t k) {
   return (size_t)n_rows * c * ((size_t)k * 8 + 4);
 }
 
-cudaError_t launch_topk(const TopkArgs& a, int32_t n_rows, void* cand, cudaStream_t s) {
+cudaError_t launch_topk(const TopkArgs& a, int32_t n_rows, void* cand, cudaStream_t s, Order first) {
   if (n_rows == 0 || a.k == 0) return cudaSuccess;
-  static bool chunk_attr = false;
-  if (!chunk_attr) {
-    cudaError_t e = cudaFuncSetAttribute(topk_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kChunkSmem);
-    if (e != cudaSuccess) return e;
-    chunk_attr = true;
-  }
+  static PerDevice chunk_attr;
+  cudaError_t e = with_device_slot(chunk_attr, [](int, int64_t& done) {
+    if (done) return cudaSuccess;
+    const cudaError_t r =
+        cudaFuncSetAttribute(topk_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kChunkSmem);
+    if (r == cudaSuccess) done = 1;
+    return r;
+  });
+  if (e != cudaSuccess) return e;
   const int32_t nc = topk_chunks(a.max_n);
   if (nc <= 1)
-    return launch_k(topk_chunk_kernel, dim3(n_rows, 1), dim3(kChunkThreads), kChunkSmem, s, 0, a,
+    return launch_k(topk_chunk_kernel, dim3(n_rows, 1), dim3(kChunkThreads), kChunkSmem, s, first, 0, a,
                     (uint32_t*)nullptr, (int32_t*)nullptr, (int32_t*)nullptr, 1);
   if (!topk_two_stage(a.max_n, a.k) || cand == nullptr)
-    return launch_k(topk_kernel, dim3(n_rows), dim3(kThreads), 0, s, 0, a);
+    return launch_k(topk_kernel, dim3(n_rows), dim3(kThreads), 0, s, first, 0, a);
   uint32_t* ck = reinterpret_cast<uint32_t*>(cand);
   int32_t* ci = reinterpret_cast<int32_t*>(ck + (size_t)n_rows * nc * a.k);
   int32_t* cc = ci + (size_t)n_rows * nc * a.k;
-  cudaError_t e = launch_k(topk_chunk_kernel, dim3(n_rows, nc), dim3(kChunkThreads), kChunkSmem, s, 0, a, ck, ci,
+  e = launch_k(topk_chunk_kernel, dim3(n_rows, nc), dim3(kChunkThreads), kChunkSmem, s, first, 0, a, ck, ci,
                            cc, nc);
   if (e != cudaSuccess) return e;
   const size_t smem = merge_smem(nc, a.k);
-  static size_t smem_set = 0;
-  if (smem > 48 * 1024 && smem > smem_set) {
-    e = cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    smem_set = smem;
-  }
-  return launch_k(topk_merge_kernel, dim3(n_rows), dim3(kMergeThreads), smem, s, 0, a, (const uint32_t*)ck,
+  static PerDevice merge_smem_set;  // the largest dynamic shared memory allowed so far
+  e = with_device_slot(merge_smem_set, [smem](int, int64_t& set) {
+    if (smem <= 48 * 1024 || (int64_t)smem <= set) return cudaSuccess;
+    const cudaError_t r = cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)smem);
+    if (r == cudaSuccess) set = (int64_t)smem;
+    return r;
+  });
+  if (e != cudaSuccess) return e;
+  return launch_k(topk_merge_kernel, dim3(n_rows), dim3(kMergeThreads), smem, s, kAfterOwnKernel, 0, a,
+                  (const uint32_t*)ck,
                   (const int32_t*)ci, (const int32_t*)cc, nc);
 }
 

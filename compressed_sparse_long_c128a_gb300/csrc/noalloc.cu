@@ -29,20 +29,19 @@
 namespace {
 
 constexpr size_t kScratchBytes = size_t(8) << 20;  // 8 MiB
-constexpr int kMaxDevices = 64;
 
 // The scratch itself.  In host code this name is only a stand-in symbol; the
 // device address comes from cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+void* g_scratch_addr[csa::kMaxDevices] = {};
 
 // Device address of g_scratch on the current device, looked up once per device.
 int scratch_for_current_device(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return CSA_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return CSA_ERR_UNSUPPORTED;
+  if (dev < 0 || dev >= csa::kMaxDevices) return CSA_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_mu);
   if (!g_scratch_addr[dev]) {
     void* p = nullptr;
@@ -64,37 +63,25 @@ int csa_indexer_topk_noalloc(const void* q_idx, int32_t q_dtype, const float* w,
                              int32_t window, const csa_paged* idx_cache, const csa_block_table* bt, int32_t k,
                              int32_t max_n, int32_t* out_idx, int32_t* err, csa_stream_t stream) {
   using namespace csa;
-  if (n_rows < 0 || k <= 0 || max_n < 0 || idx_heads <= 0 || idx_dim <= 0) return CSA_ERR_INVALID_ARG;
-  if (ratio <= 0 || window <= 0 || 256 % ratio) return CSA_ERR_INVALID_ARG;
-  if (n_rows == 0) return CSA_OK;
-  if (!q_idx || !w || !seq_id || !pos || !out_idx || !err || !idx_cache || !bt) return CSA_ERR_INVALID_ARG;
-  if (q_dtype != CSA_F32 && q_dtype != CSA_BF16) return CSA_ERR_UNSUPPORTED;
-  if (!idx_cache->data || idx_cache->num_blocks <= 0 || idx_cache->dim != idx_dim ||
-      idx_cache->rows_per_block != 256 / ratio)
-    return CSA_ERR_INVALID_ARG;
-  if (idx_cache->dtype != CSA_F32 && idx_cache->dtype != CSA_BF16 && idx_cache->dtype != CSA_E2M1)
-    return CSA_ERR_UNSUPPORTED;
-  if (idx_cache->dtype == CSA_E2M1 && (!idx_cache->scales || idx_dim % 16)) return CSA_ERR_INVALID_ARG;
-  if (!bt->table || bt->num_seqs <= 0 || bt->stride <= 0) return CSA_ERR_INVALID_ARG;
-  if ((size_t)idx_heads * idx_dim > 32768 || idx_dim > 256) return CSA_ERR_UNSUPPORTED;
+  const int st = check_indexer_topk(q_idx, q_dtype, w, n_rows, idx_heads, idx_dim, seq_id, pos, ratio, window,
+                                    idx_cache, bt, k, max_n, out_idx, err);
+  if (st != CSA_OK || n_rows == 0) return st;
 
-  const size_t score_bytes = align256(sizeof(float) * (size_t)n_rows * (max_n > 0 ? max_n : 1));
-  const size_t cand_bytes = align256(topk_candidate_bytes(n_rows, max_n > 0 ? max_n : 1, k));
+  // sized as csa_indexer_topk_workspace_size sizes a workspace (max_n >= 1 so
+  // that a request is never sized at zero); the kernels get max_n unchanged
+  const int32_t size_n = max_n > 0 ? max_n : 1;
+  const size_t score_bytes = align256(sizeof(float) * (size_t)n_rows * size_n);
+  const size_t cand_bytes = align256(topk_candidate_bytes(n_rows, max_n, k));
   if (score_bytes + cand_bytes > kScratchBytes) return CSA_ERR_WORKSPACE;
 
   void* scratch = nullptr;
-  const int st = scratch_for_current_device(&scratch);
-  if (st != CSA_OK) return st;
+  const int sst = scratch_for_current_device(&scratch);
+  if (sst != CSA_OK) return sst;
 
   float* scores = reinterpret_cast<float*>(scratch);
   void* cand = cand_bytes ? reinterpret_cast<uint8_t*>(scratch) + score_bytes : nullptr;
-  IndexerArgs ia{q_idx, q_dtype, w, seq_id, pos, *idx_cache, *bt, idx_heads, idx_dim, ratio, window,
-                 max_n > 0 ? max_n : 1, scores, err};
-  cudaError_t e = indexer_tc_eligible(ia) ? launch_indexer_tc(ia, n_rows, stream)
-                                          : launch_indexer_scores(ia, n_rows, stream);
-  if (e != cudaSuccess) return CSA_ERR_CUDA;
-  TopkArgs ta{scores, pos, ratio, window, max_n > 0 ? max_n : 1, k, out_idx, err};
-  return launch_topk(ta, n_rows, cand, stream) == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;
+  return enqueue_indexer_topk(q_idx, q_dtype, w, n_rows, idx_heads, idx_dim, seq_id, pos, ratio, window, idx_cache,
+                              bt, k, max_n, out_idx, scores, cand, err, stream);
 }
 
 }  // extern "C"

@@ -23,14 +23,12 @@
  *     atomicCAS from 0); the offending row or element is skipped, never read
  *     or written out of bounds.  No kernel traps or waits without a bound.
  *     csa_read_status() fetches and optionally clears the word.
- *   - Kernels are launched with programmatic dependent launch: a kernel may
- *     start while the previous launch on `stream` is still running, and waits
- *     for it to complete before it reads a cache, a block table, the selected
- *     indices or a scratch buffer.  The attention kernels read the query rows,
- *     seq_id and pos before that wait, so these inputs must be complete when the
- *     call is made, which holds for any producer except a kernel launched just
- *     before on the same stream that itself signals programmatic completion
- *     early.
+ *   - Every call is ordered after all work enqueued before it on `stream`, by
+ *     anyone: its first kernel is launched in plain stream order.  The later
+ *     kernels of one call use programmatic dependent launch among themselves
+ *     (a kernel may start while the call's previous kernel is finishing, and
+ *     waits for it before it reads what that kernel wrote).  Work enqueued after
+ *     a call starts after the call's last kernel has completed.
  *   - Positions are 0-based.  Compressed entry i of a layer with stride
  *     `ratio` and window `window` sums raw tokens [ratio*i, ratio*i+window-1]
  *     and is anchored (rotated) at ratio*i ([延迟] "KV 缓存压缩").  A query at

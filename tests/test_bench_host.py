@@ -3,15 +3,36 @@
 import bench
 
 
-def test_attention_traffic_only_for_the_captured_source(monkeypatch):
-    name = "c128a_decode_b32_128k"
-    assert name in bench.ATTN_TRAFFIC
-    nbytes, digest = bench.ATTN_TRAFFIC[name]
-    # the committed entry describes the kernel source as it stands
-    assert bench._attn_traffic(name) == float(nbytes)
-    monkeypatch.setitem(bench.ATTN_TRAFFIC, name, (nbytes, "0" * 64))
-    assert bench._attn_traffic(name) is None
-    assert bench._attn_traffic("no_such_workload") is None
+def test_traffic_only_for_the_captured_source(monkeypatch):
+    key = ("c4a_decode_b64_64k", "indexer_topk")
+    monkeypatch.setitem(bench.TRAFFIC, key, (123456.0, bench._kernel_digest("k_indexer_tc.cu")))
+    assert bench.measured_traffic(*key) == 123456.0
+    monkeypatch.setitem(bench.TRAFFIC, key, (123456.0, "0" * 64))
+    assert bench.measured_traffic(*key) is None
+    assert bench.measured_traffic("no_such_workload", "attention") is None
+
+
+def test_call_roofline_picks_the_longer_bound():
+    # 1 GB in 0.5 ms against 4000 GB/s: HBM-bound (0.25 ms at peak) at 2000 GB/s = half of peak
+    r = bench.call_roofline("x", 1e9, 1e9, 0.5, 4000.0, 1000.0)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert abs(r["achieved"] - 2000.0) < 1e-6 and abs(r["frac"] - 0.5) < 1e-9
+    # 10 TFLOP over 1 MB: tensor-bound; 10 TFLOP in 20 ms is 500 TFLOP/s of 1000
+    r = bench.call_roofline("y", 1e6, 1e13, 20.0, 4000.0, 1000.0)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert abs(r["achieved"] - 500.0) < 1e-6 and abs(r["frac"] - 0.5) < 1e-9
+
+
+def test_oracle_baseline_reports_the_workers_it_ran():
+    """The CPU baseline runs the oracle in single-threaded worker processes and
+    reports how many it used and what the host CPU is."""
+    pool = bench.OraclePool(workers=2)
+    try:
+        res = bench.oracle_baseline(pool, 0, seconds=3.0)
+    finally:
+        pool.close()
+    assert res["cores"] == 2 and res["kind"] == "oracle" and res["value"] > 0
+    assert res["cpu"]["logical_cpus"] >= 1 and res["cpu"]["model"]
 
 
 def test_weak_throughput_counts_all_ranks():
@@ -49,28 +70,3 @@ def test_indexer_bytes_count_every_visible_key():
     n = sum((int(p) - L.window) // L.ratio + 1 for p in pos)
     q = len(pos) * L.idx_heads * (L.idx_dim * 2 + 4)
     assert bench.indexer_bytes(ld) == n * L.idx_dim * 2 + q + len(pos) * L.topk * 4
-
-
-def _layer_stand_in(wl, L):
-    """What _launches_per_step reads of a device layer, without a device."""
-    import types
-
-    import compressed_sparse_long_c128a_gb300 as csa
-    from harness.device import n_visible
-
-    pos = [p for s in wl.seqs for p in range(s.first_new, s.end)]
-    return types.SimpleNamespace(L=L, n_rows=len(pos), max_n=max(n_visible(p, L.ratio, L.window) for p in pos),
-                                 c_layer=csa.make_layer(L.ratio, L.window, L.dim, L.rope_dim, L.heads, L.swa,
-                                                        L.theta, L.eps))
-
-
-def test_launch_count_matches_the_launch_lists():
-    """Kernel launches per step, from the dispatch rules, against what ncu listed per
-    step: c128a decode 3 (ingest, emit, attention), c4a decode 5 (+ indexer, one top-k
-    chunk launch), c4a at 2^20 with the fp4 indexer 6 (+ the top-k merge)."""
-    import synth
-
-    for idx, want in ((1, 3), (2, 5), (3, 6)):
-        wl = synth.workload(idx)
-        got = sum(bench._launches_per_step(_layer_stand_in(wl, L)) for L in wl.layers)
-        assert got == want, f"workload {idx}: {got} launches per step, the launch list shows {want}"

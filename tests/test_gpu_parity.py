@@ -269,40 +269,100 @@ def test_end_to_end(idx):
 
 
 
+def _snapshot(wd):
+    snap = []
+    for ld in wd.layers:
+        t = {"out": ld.io["out"].clone(), "comp": ld.comp.data.clone(), "swa": ld.swa.data.clone(),
+             "state": ld.state.data.clone()}
+        if ld.io["out_scales"] is not None:
+            t["out_scales"] = ld.io["out_scales"].clone()
+        if ld.comp.scales is not None:
+            t["comp_scales"] = ld.comp.scales.clone()
+        if "topk" in ld.io:
+            t["topk"] = ld.io["topk"].clone()
+        snap.append(t)
+    return snap
+
+
+def _describe_diff(name, key, a, b):
+    """Where two snapshots of one tensor differ (rows and heads for outputs)."""
+    if key != "out" or a.dim() != 3:
+        return f"{name}: {key} differs in {int((a != b).sum())} elements"
+    d = (a.float() - b.float()).abs().nan_to_num(nan=1e9).amax(dim=2) > 0
+    pairs = d.nonzero().cpu().numpy()
+    zero_a = int((a.float().abs().amax(dim=2) == 0).sum())
+    zero_b = int((b.float().abs().amax(dim=2) == 0).sum())
+    return (f"{name}: out differs at {len(pairs)} (row, head) pairs, first {pairs[:8].tolist()}; "
+            f"all-zero heads: {zero_a} before, {zero_b} after")
+
+
+def _assert_same(wd, a_snap, b_snap, what):
+    for ld, a, b in zip(wd.layers, a_snap, b_snap):
+        assert a.keys() == b.keys()
+        for key in a:
+            assert torch.equal(a[key], b[key]), f"{what}: " + _describe_diff(ld.L.name, key, a[key], b[key])
+
+
+def _run_step(wd, stream, side=None):
+    """One step on `stream` (outputs and selections poisoned first), checked for device errors."""
+    with torch.cuda.stream(stream):
+        for ld in wd.layers:
+            ld.io["out"].zero_()
+            if "topk" in ld.io:
+                ld.io["topk"].fill_(-2)
+        wd.step(stream, side_stream=side)
+    torch.cuda.synchronize()
+    wd.check("two-stream step" if side is not None else "one-stream step")
+    return _snapshot(wd)
+
+
+def _check_against_oracle(wd, what):
+    """Every checked row of every layer against the oracle (the end-to-end comparison)."""
+    wl = wd.wl
+    for ld in wd.layers:
+        L = ld.L
+        got_all, codes, scales = ld.output()
+        topk = _topk_sets(wd, ld) if L.has_indexer else None
+        for b, r in _rows_to_check(wl):
+            so = SequenceOracle(wl, L, b)
+            row = ld.row_index(b, r)
+            ids = None
+            if L.has_indexer:
+                ids = topk[row][topk[row] >= 0]
+                _check_topk_row(topk[row], so.scores(r), L.topk, f"{what}: {L.name} seq {b} row {r}")
+            res = so.attend(r, entry_ids=ids)
+            _compare_out(ld, got_all, codes, scales, row, res, f"{what}: {L.name} seq {b} row {r}")
+
+
 @pytest.mark.parametrize("idx", [4, 0, 2])  # 4 first: still resident from test_end_to_end
 def test_two_stream_step_matches_one_stream(idx):
     """A c4a layer's indexer and top-k on a second stream, beside compress_insert
-    on the first and joined before the attention, write the same bytes as the
-    one-stream step: the launches are the same, only the order of independent
-    ones changes (the indexer reads nothing compress_insert writes)."""
+    on the first and joined before the attention: each run is checked against
+    the oracle (stage-isolated on its own selection, which must be a valid
+    top-k), then the two runs must have written the same bytes -- the launches
+    are the same, only the order of independent ones changes (the indexer reads
+    nothing compress_insert writes)."""
     wd = _dev(idx)
     main, side = torch.cuda.Stream(), torch.cuda.Stream()
+    one = _run_step(wd, main)
+    _check_against_oracle(wd, "one stream")
+    two = _run_step(wd, main, side)
+    _check_against_oracle(wd, "two streams")
+    _assert_same(wd, one, two, "one vs two streams")
 
-    def run(side_stream):
-        with torch.cuda.stream(main):
-            for ld in wd.layers:
-                ld.io["out"].zero_()
-                if "topk" in ld.io:
-                    ld.io["topk"].fill_(-2)
-            wd.step(main, side_stream=side_stream)
-        torch.cuda.synchronize()
-        wd.check("two-stream step" if side_stream is not None else "one-stream step")
-        snap = []
-        for ld in wd.layers:
-            t = {"out": ld.io["out"].clone(), "comp": ld.comp.data.clone(), "swa": ld.swa.data.clone()}
-            if ld.io["out_scales"] is not None:
-                t["out_scales"] = ld.io["out_scales"].clone()
-            if "topk" in ld.io:
-                t["topk"] = ld.io["topk"].clone()
-            snap.append(t)
-        return snap
 
-    one = run(None)
-    two = run(side)
-    for ld, a, b in zip(wd.layers, one, two):
-        assert a.keys() == b.keys()
-        for key in a:
-            assert torch.equal(a[key], b[key]), f"{ld.L.name}: {key} differs between one and two streams"
+@pytest.mark.parametrize("idx", [4, 2, 3])
+def test_step_is_deterministic(idx):
+    """Re-running a step on one stream rewrites the same bytes into outputs,
+    selections and caches (a step is idempotent: it re-ingests the same tokens)."""
+    wd = _dev(idx)
+    s = torch.cuda.Stream()
+    first = _run_step(wd, s)
+    for rep in range(3):
+        _assert_same(wd, first, _run_step(wd, s), f"repeat {rep + 1}")
+    # and on the default stream, as the other tests run it
+    _assert_same(wd, first, _run_step(wd, torch.cuda.current_stream()), "default stream")
+
 
 def test_device_bounds_are_reported_not_faulted():
     """An unmapped block and an out-of-range selection set the error word; the kernels skip them."""

@@ -66,6 +66,31 @@ def test_noalloc_selects_what_the_workspace_entry_point_selects(idx):
         np.testing.assert_array_equal(np.sort(got, axis=1), np.sort(want, axis=1))
 
 
+def test_noalloc_matches_the_workspace_entry_point_when_max_n_is_zero():
+    """max_n = 0 declares that no row sees an entry: both entry points then
+    report every row that does see one as a device bounds error and select
+    nothing (all -1), the same way."""
+    import compressed_sparse_long_c128a_gb300 as csa
+
+    ld = _indexer_setup(0)
+    L, io = ld.L, ld.io
+    outs, status = [], []
+    for noalloc in (False, True):
+        out = torch.full((ld.n_rows, L.topk), 5, dtype=torch.int32, device="cuda")
+        if noalloc:
+            csa.indexer_topk_noalloc(io["q_idx"], io["w"], io["seq_id"], io["pos"], L.ratio, L.window, ld.idx,
+                                     ld.tables["idx"], L.topk, 0, out, ld.err)
+        else:
+            csa.indexer_topk(io["q_idx"], io["w"], io["seq_id"], io["pos"], L.ratio, L.window, ld.idx,
+                             ld.tables["idx"], L.topk, 0, out, None, ld.err)
+        torch.cuda.synchronize()
+        status.append(csa.read_status(ld.err))
+        outs.append(out.cpu().numpy())
+    assert status == [csa.ERR_DEVICE_BOUNDS, csa.ERR_DEVICE_BOUNDS]
+    np.testing.assert_array_equal(outs[0], outs[1])
+    assert np.all(outs[1] == -1)
+
+
 def test_noalloc_refuses_requests_beyond_its_scratch():
     import compressed_sparse_long_c128a_gb300 as csa
 
