@@ -25,8 +25,8 @@ rotate over R copies of every cache with R x (bytes a step touches) >
 event-timed on its own over the same rotation, for the per-call roofline; the
 dominant call's (the longest) is the line's `roofline`.  `e2e` repeats the
 step with its inputs copied from pinned host memory and its output read back
-to the host every step.  `gpu_launches` counts the kernel nodes of the
-captured step graphs times the steps replayed.
+to the host every step.  `gpu_launches` is the library's launches captured
+into the step graphs (its own host-side count) times the steps replayed.
 
 Under torchrun each rank runs its own replica of the workload on its own GPU
 (sequences are independent; no collective on the data path), so the scaling
@@ -452,46 +452,6 @@ def _clone_layer(ld):
     return c
 
 
-def graph_kernel_nodes(g) -> int | None:
-    """Kernel nodes of a captured torch CUDA graph (None if the graph handle is not exposed)."""
-    import ctypes
-    if not hasattr(g, "raw_cuda_graph"):
-        return None
-    try:
-        import torch
-        rt = None
-        for name in ("libcudart.so.13", "libcudart.so.12", "libcudart.so"):
-            try:
-                rt = ctypes.CDLL(name)
-                break
-            except OSError:
-                continue
-        if rt is None:
-            lib_dir = os.path.join(os.path.dirname(torch.__file__), "lib")
-            for f in sorted(os.listdir(lib_dir)):
-                if f.startswith("libcudart"):
-                    rt = ctypes.CDLL(os.path.join(lib_dir, f))
-                    break
-        if rt is None:
-            return None
-        graph = ctypes.c_void_p(g.raw_cuda_graph())
-        n = ctypes.c_size_t(0)
-        if rt.cudaGraphGetNodes(graph, None, ctypes.byref(n)) != 0:
-            return None
-        nodes = (ctypes.c_void_p * n.value)()
-        if rt.cudaGraphGetNodes(graph, nodes, ctypes.byref(n)) != 0:
-            return None
-        kernels = 0
-        for i in range(n.value):
-            t = ctypes.c_int(-1)
-            if rt.cudaGraphNodeGetType(ctypes.c_void_p(nodes[i]), ctypes.byref(t)) != 0:
-                return None
-            kernels += t.value == 0  # cudaGraphNodeTypeKernel
-        return kernels
-    except Exception:  # noqa: BLE001 -- a diagnostic count, never fatal
-        return None
-
-
 def _call_fns(ld, csa, stream):
     """The step's calls of one layer, as (name, fn) in step order."""
     L, io = ld.L, ld.io
@@ -537,14 +497,15 @@ def measure_workload(idx: int, args, steps: int, world: int, local: int, pool=No
     stream.synchronize()
     wd.check("warm-up")
 
-    graphs = []
+    graphs, nodes = [], []
     for rep in reps:
         g = torch.cuda.CUDAGraph()
+        n0 = csa.launch_count()
         with torch.cuda.graph(g, stream=stream):
             step(rep, stream)
+        nodes.append(csa.launch_count() - n0)  # the library's kernels in this step's graph
         graphs.append(g)
     torch.cuda.synchronize()
-    nodes = [graph_kernel_nodes(g) for g in graphs]
 
     clocks = Clocks(local)
     clocks.start()
@@ -578,20 +539,27 @@ def measure_workload(idx: int, args, steps: int, world: int, local: int, pool=No
     value = weak_throughput(rows_per_step, steps, world, ms_total)
     wd.check("timed steps")
 
-    # every call of every layer on its own, event-timed per launch over the same rotation
-    n_call = max(3, min(steps, 200))
+    # every call of every layer on its own: n_call launches of it over the same
+    # rotation, captured into one graph, replayed between two events (no host gaps)
+    n_call = max(3, min(steps, 200 if replicas > 1 else 20))
+    n_call = -(-n_call // replicas) * replicas
     calls = {}
     for li in range(len(base)):
         for ci, (name, _) in enumerate(_call_fns(base[li], csa, stream)):
-            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_call)]
-            with torch.cuda.stream(stream):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
                 for k in range(n_call):
-                    fn = _call_fns(reps[k % replicas][li], csa, stream)[ci][1]
-                    ev[k][0].record(stream)
-                    fn()
-                    ev[k][1].record(stream)
+                    _call_fns(reps[k % replicas][li], csa, stream)[ci][1]()
             torch.cuda.synchronize()
-            ms = sum(a.elapsed_time(b) for a, b in ev) / n_call
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                g.replay()  # warm
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / n_call
+            del g
             ld = base[li]
             if name == "attention":
                 nb, fl = attention_bytes(ld), attention_flops(ld)
@@ -611,8 +579,7 @@ def measure_workload(idx: int, args, steps: int, world: int, local: int, pool=No
            "algorithmic_bytes_per_step": step_bytes,
            "roofline": dict(dominant, peak_source=f"{peak_src} (copy bandwidth / cuBLAS bf16, burst)"),
            "calls": calls, "clocks": clk,
-           "gpu_launches": (sum(nodes[k % replicas] for k in range(steps))
-                            if all(n is not None for n in nodes) else None),
+           "gpu_launches": sum(nodes[k % replicas] for k in range(steps)),
            "kernels_per_step": nodes[0], "e2e": e2e}
     if side is not None:
         res["config"]["indexer_stream"] = "side"

@@ -18,8 +18,8 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libcsa.so")
 
-F32, BF16, E4M3, E2M1 = 0, 1, 2, 3
-DTYPES = {"f32": F32, "bf16": BF16, "e4m3": E4M3, "e2m1": E2M1}
+F32, BF16, E4M3, E2M1, E4M3R = 0, 1, 2, 3, 4
+DTYPES = {"f32": F32, "bf16": BF16, "e4m3": E4M3, "e2m1": E2M1, "e4m3r": E4M3R}
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE_BOUNDS, ERR_WORKSPACE, ERR_TIMEOUT = 0, -1, -2, -3, -4, -5, -6
 
@@ -32,7 +32,8 @@ class CsaError(RuntimeError):
 
 class Paged(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("dtype", ctypes.c_int32),
-                ("num_blocks", ctypes.c_int32), ("rows_per_block", ctypes.c_int32), ("dim", ctypes.c_int32)]
+                ("num_blocks", ctypes.c_int32), ("rows_per_block", ctypes.c_int32), ("dim", ctypes.c_int32),
+                ("tail_bf16", ctypes.c_int32)]
 
 
 class BlockTableC(ctypes.Structure):
@@ -67,6 +68,7 @@ _SIGS = {
     "csa_read_status": (_I32, [_VP, _I32, _VP]),
     "csa_status_string": (ctypes.c_char_p, [_I32]),
     "csa_version": (_I32, []),
+    "csa_launch_count": (ctypes.c_uint64, []),
 }
 
 EXPORTED = tuple(_SIGS)
@@ -94,6 +96,11 @@ def status_string(status: int) -> str:
 
 def version() -> int:
     return int(lib().csa_version())
+
+
+def launch_count() -> int:
+    """Kernel launches the library has enqueued in this process (host-side count)."""
+    return int(lib().csa_launch_count())
 
 
 def _check(status: int, what: str):
@@ -127,17 +134,20 @@ def _tdtype(t) -> int:
 @dataclass
 class PagedCache:
     """A paged cache in device memory: `data` [num_blocks, rows_per_block, row] and,
-    for quantised dtypes, `scales` (E4M3: float [num_blocks, rows_per_block];
-    E2M1: uint8 [num_blocks, rows_per_block, dim/16])."""
+    for quantised dtypes, `scales` (E4M3, E4M3R: float [num_blocks, rows_per_block];
+    E2M1: uint8 [num_blocks, rows_per_block, dim/16]).  An E4M3R row is
+    dim - tail_bf16 code bytes followed by tail_bf16 bf16 values."""
 
     data: torch.Tensor
     scales: torch.Tensor | None
     dtype: int
     rows_per_block: int
     dim: int
+    tail_bf16: int = 0
 
     @staticmethod
-    def empty(num_blocks: int, rows_per_block: int, dim: int, dtype: int, device="cuda") -> "PagedCache":
+    def empty(num_blocks: int, rows_per_block: int, dim: int, dtype: int, device="cuda",
+              tail_bf16: int = 0) -> "PagedCache":
         shape = (num_blocks, rows_per_block)
         scales = None
         if dtype == F32:
@@ -150,16 +160,20 @@ class PagedCache:
         elif dtype == E2M1:
             data = torch.zeros(*shape, dim // 2, dtype=torch.uint8, device=device)
             scales = torch.zeros(*shape, dim // 16, dtype=torch.uint8, device=device)
+        elif dtype == E4M3R:
+            data = torch.zeros(*shape, dim + tail_bf16, dtype=torch.uint8, device=device)
+            scales = torch.zeros(*shape, dtype=torch.float32, device=device)
         else:
             raise ValueError(dtype)
-        return PagedCache(data, scales, dtype, rows_per_block, dim)
+        return PagedCache(data, scales, dtype, rows_per_block, dim, tail_bf16 if dtype == E4M3R else 0)
 
     @property
     def num_blocks(self) -> int:
         return self.data.shape[0]
 
     def c(self) -> Paged:
-        return Paged(_ptr(self.data), _ptr(self.scales), self.dtype, self.num_blocks, self.rows_per_block, self.dim)
+        return Paged(_ptr(self.data), _ptr(self.scales), self.dtype, self.num_blocks, self.rows_per_block, self.dim,
+                     self.tail_bf16)
 
 
 def block_table(t: torch.Tensor) -> BlockTableC:

@@ -23,7 +23,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libcsa.so")
 
-SOURCES = ["api.cu", "k_compress.cu", "k_store.cu", "k_indexer.cu", "k_topk.cu", "k_attn.cu", "k_attn_tc.cu", "k_indexer_tc.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "k_compress.cu", "k_store.cu", "k_indexer.cu", "k_topk.cu", "k_attn.cu", "k_attn_tc.cu",
+           "k_indexer_tc.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          f"-I{INCLUDE}", f"-I{CSRC}"]

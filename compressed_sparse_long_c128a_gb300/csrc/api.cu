@@ -2,6 +2,7 @@
 // entry point validates on the host, enqueues its kernels on the caller's
 // stream and returns without synchronising or allocating.
 
+#include <atomic>
 #include <cmath>
 #include <cstring>
 
@@ -13,15 +14,22 @@ namespace {
 
 constexpr int32_t kVersion = 100;  // 0.1.0
 
-bool dtype_ok(int32_t dt) { return dt >= CSA_F32 && dt <= CSA_E2M1; }
+bool dtype_ok(int32_t dt) { return dt >= CSA_F32 && dt <= CSA_E4M3R; }
 
 int check_paged(const csa_paged* c, int32_t dim, int32_t rows_per_block, unsigned allowed_dtypes) {
   if (!c || !c->data || c->num_blocks <= 0) return CSA_ERR_INVALID_ARG;
   if (!dtype_ok(c->dtype)) return CSA_ERR_INVALID_ARG;
   if (!(allowed_dtypes & (1u << c->dtype))) return CSA_ERR_UNSUPPORTED;
   if (c->dim != dim || c->rows_per_block != rows_per_block) return CSA_ERR_INVALID_ARG;
-  if ((c->dtype == CSA_E4M3 || c->dtype == CSA_E2M1) && !c->scales) return CSA_ERR_INVALID_ARG;
+  if ((c->dtype == CSA_E4M3 || c->dtype == CSA_E4M3R || c->dtype == CSA_E2M1) && !c->scales)
+    return CSA_ERR_INVALID_ARG;
   if (c->dtype == CSA_E2M1 && dim % 16) return CSA_ERR_INVALID_ARG;
+  if (c->dtype == CSA_E4M3R) {
+    if (c->tail_bf16 <= 0 || c->tail_bf16 % 16 || c->tail_bf16 > dim || (dim - c->tail_bf16) % 16)
+      return CSA_ERR_INVALID_ARG;
+  } else if (c->tail_bf16 != 0) {
+    return CSA_ERR_INVALID_ARG;
+  }
   return CSA_OK;
 }
 
@@ -58,7 +66,7 @@ RopeTab make_rope(int32_t rope_dim, float theta) {
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA; }
 
 constexpr unsigned kF32 = 1u << CSA_F32, kBF16 = 1u << CSA_BF16, kE4M3 = 1u << CSA_E4M3,
-                   kE2M1 = 1u << CSA_E2M1;
+                   kE2M1 = 1u << CSA_E2M1, kE4M3R = 1u << CSA_E4M3R;
 
 size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -79,6 +87,12 @@ EncodeTiled encode_tiled() {
 }
 
 }  // namespace
+
+namespace {
+std::atomic<uint64_t> g_launches{0};
+}  // namespace
+
+void csa::count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 cudaError_t csa::sm_count(int* n) {
   static PerDevice sms;
@@ -127,12 +141,40 @@ int csa::check_indexer_topk(const void* q_idx, int32_t q_dtype, const float* w, 
 int csa::enqueue_indexer_topk(const void* q_idx, int32_t q_dtype, const float* w, int32_t n_rows, int32_t idx_heads,
                               int32_t idx_dim, const int32_t* seq_id, const int32_t* pos, int32_t ratio,
                               int32_t window, const csa_paged* idx_cache, const csa_block_table* bt, int32_t k,
-                              int32_t max_n, int32_t* out_idx, float* scores, void* cand, int32_t* err,
-                              cudaStream_t stream) {
-  IndexerArgs ia{q_idx, q_dtype, w, seq_id, pos, *idx_cache, *bt, idx_heads, idx_dim, ratio, window, max_n,
-                 scores, err};
+                              int32_t max_n, int32_t* out_idx, float* scores, void* cand, void* deal,
+                              int32_t* err, cudaStream_t stream) {
+  IndexerArgs ia{};
+  ia.q_idx = q_idx;
+  ia.q_dtype = q_dtype;
+  ia.w = w;
+  ia.seq_id = seq_id;
+  ia.pos = pos;
+  ia.cache = *idx_cache;
+  ia.bt = *bt;
+  ia.heads = idx_heads;
+  ia.dim = idx_dim;
+  ia.ratio = ratio;
+  ia.window = window;
+  ia.max_n = max_n;
+  ia.scores = scores;
+  ia.err = err;
   const bool tc = indexer_tc_eligible(ia);
-  cudaError_t e = tc ? launch_indexer_tc(ia, n_rows, stream) : launch_indexer_scores(ia, n_rows, stream);
+  int n_sm = 0;
+  if (sm_count(&n_sm) != cudaSuccess) return CSA_ERR_CUDA;
+  const int32_t G = n_sm < kDealMaxCtas ? n_sm : kDealMaxCtas;
+  // a balanced deal with the selection fused when the rows' tiles fit the CTAs' key stores
+  const int32_t bound = indexer_deal_bound(n_rows, max_n, G);
+  if (tc && deal && max_n > 0 && bound >= 0 && bound <= indexer_deal_capacity(idx_cache->dtype)) {
+    const DealCandidates dc = deal_candidates(deal, G, k);
+    ia.sel_k = k;
+    ia.cand_key = dc.key;
+    ia.cand_idx = dc.idx;
+    ia.cand_cnt = dc.cnt;
+    if (launch_indexer_tc(ia, n_rows, G, stream) != cudaSuccess) return CSA_ERR_CUDA;
+    TopkArgs ta{scores, pos, ratio, window, max_n, k, out_idx, err};
+    return cuda_status(launch_topk_deal_merge(ta, n_rows, dc, stream));
+  }
+  cudaError_t e = tc ? launch_indexer_tc(ia, n_rows, G, stream) : launch_indexer_scores(ia, n_rows, stream);
   if (e != cudaSuccess) return CSA_ERR_CUDA;
   // the generic score kernel is not launched when no row can see an entry
   const Order first = (tc || max_n > 0) ? kAfterOwnKernel : kStreamOrder;
@@ -161,8 +203,8 @@ int attn_common(const csa_layer* L, const void* q, int32_t q_dtype, int32_t n_ro
   if (q_dtype != CSA_F32 && q_dtype != CSA_BF16) return CSA_ERR_UNSUPPORTED;
   if (out_dtype != CSA_F32 && out_dtype != CSA_BF16 && out_dtype != CSA_E4M3) return CSA_ERR_UNSUPPORTED;
   if (out_dtype == CSA_E4M3 && !out_scales) return CSA_ERR_INVALID_ARG;
-  if ((st = check_paged(comp, L->dim, 256 / L->ratio, kF32 | kBF16 | kE4M3))) return st;
-  if ((st = check_paged(swa, L->dim, 256, kF32 | kBF16 | kE4M3))) return st;
+  if ((st = check_paged(comp, L->dim, 256 / L->ratio, kF32 | kBF16 | kE4M3 | kE4M3R))) return st;
+  if ((st = check_paged(swa, L->dim, 256, kF32 | kBF16 | kE4M3 | kE4M3R))) return st;
   if ((st = check_bt(comp_bt)) || (st = check_bt(swa_bt))) return st;
   if (L->dim % 32 || L->dim > 512 || L->heads % 8) return CSA_ERR_UNSUPPORTED;
   const int32_t keys = (topk ? k : max_n) + L->swa;
@@ -217,18 +259,19 @@ int csa_compress_insert(const csa_layer* L, const void* kv, const void* gate, in
   if (in_dtype != CSA_F32 && in_dtype != CSA_BF16) return CSA_ERR_UNSUPPORTED;
   if (L->dim > 4096) return CSA_ERR_UNSUPPORTED;
   if ((st = check_paged(state, 2 * L->dim, 256, 1u << in_dtype))) return st;
-  if (swa && (st = check_paged(swa, L->dim, 256, kF32 | kBF16 | kE4M3))) return st;
-  if ((st = check_paged(comp, L->dim, 256 / L->ratio, kF32 | kBF16 | kE4M3 | kE2M1))) return st;
+  if (swa && (st = check_paged(swa, L->dim, 256, kF32 | kBF16 | kE4M3 | kE4M3R))) return st;
+  if ((st = check_paged(comp, L->dim, 256 / L->ratio, kF32 | kBF16 | kE4M3 | kE4M3R | kE2M1))) return st;
   if ((st = check_bt(state_bt)) || (swa && (st = check_bt(swa_bt))) || (st = check_bt(comp_bt))) return st;
   const RopeTab rt = make_rope(L->rope_dim, L->rope_theta);
   const csa_paged no_swa{};
   const csa_block_table no_swa_bt{};
   IngestArgs ia{kv, gate, in_dtype, seq_id, pos, gamma_swa, *state, *state_bt, swa ? *swa : no_swa,
                 swa ? *swa_bt : no_swa_bt, L->dim, L->rms_eps, rt, err};
-  cudaError_t e = launch_ingest(ia, n_tok, stream);
-  if (e != cudaSuccess) return CSA_ERR_CUDA;
   EmitArgs ea{seq_id, pos, bias, gamma_c, *state, *state_bt, *comp, *comp_bt, L->dim, L->ratio, L->window,
               L->rms_eps, rt, err};
+  if (compress_fused_eligible(ia, ea, n_tok)) return cuda_status(launch_compress_fused(ia, ea, n_tok, stream));
+  cudaError_t e = launch_ingest(ia, n_tok, stream);
+  if (e != cudaSuccess) return CSA_ERR_CUDA;
   return cuda_status(launch_emit(ea, n_tok, stream));
 }
 
@@ -237,7 +280,7 @@ int csa_cache_store(const float* rows, int32_t n, const int32_t* seq_id, const i
   if (n < 0) return CSA_ERR_INVALID_ARG;
   if (n == 0) return CSA_OK;
   if (!rows || !seq_id || !row_idx || !err || !cache) return CSA_ERR_INVALID_ARG;
-  int st = check_paged(cache, cache->dim, cache->rows_per_block, kF32 | kBF16 | kE4M3 | kE2M1);
+  int st = check_paged(cache, cache->dim, cache->rows_per_block, kF32 | kBF16 | kE4M3 | kE4M3R | kE2M1);
   if (st) return st;
   if (cache->dim <= 0 || cache->rows_per_block <= 0 || cache->dim % 2) return CSA_ERR_INVALID_ARG;
   if ((st = check_bt(bt))) return st;
@@ -247,7 +290,12 @@ int csa_cache_store(const float* rows, int32_t n, const int32_t* seq_id, const i
 
 size_t csa_indexer_topk_workspace_size(int32_t n_rows, int32_t max_n, int32_t k) {
   if (n_rows <= 0 || max_n <= 0 || k <= 0) return 0;
-  return align_up(sizeof(float) * (size_t)n_rows * max_n) + align_up(topk_candidate_bytes(n_rows, max_n, k));
+  // the per-row path's scores and chunk candidates, plus (for batches a
+  // balanced deal may take) the deal's candidate lists for up to kDealMaxCtas CTAs
+  const size_t per_row = align_up(sizeof(float) * (size_t)n_rows * max_n) +
+                         align_up(topk_candidate_bytes(n_rows, max_n, k));
+  const size_t deal = n_rows < kDealMaxCtas ? align_up(deal_candidate_bytes(kDealMaxCtas, k)) : 0;
+  return per_row + deal;
 }
 
 int csa_indexer_topk(const void* q_idx, int32_t q_dtype, const float* w, int32_t n_rows, int32_t idx_heads,
@@ -260,11 +308,13 @@ int csa_indexer_topk(const void* q_idx, int32_t q_dtype, const float* w, int32_t
   const size_t need = csa_indexer_topk_workspace_size(n_rows, max_n, k);
   if (need && (!ws || ws_bytes < need)) return CSA_ERR_WORKSPACE;
   float* scores = reinterpret_cast<float*>(ws);
-  void* cand = topk_candidate_bytes(n_rows, max_n, k)
-                   ? reinterpret_cast<uint8_t*>(ws) + align_up(sizeof(float) * (size_t)n_rows * max_n)
+  uint8_t* after_scores = reinterpret_cast<uint8_t*>(ws) + align_up(sizeof(float) * (size_t)n_rows * max_n);
+  void* cand = topk_candidate_bytes(n_rows, max_n, k) ? after_scores : nullptr;
+  void* deal = n_rows < kDealMaxCtas && need
+                   ? after_scores + align_up(topk_candidate_bytes(n_rows, max_n, k))
                    : nullptr;
   return enqueue_indexer_topk(q_idx, q_dtype, w, n_rows, idx_heads, idx_dim, seq_id, pos, ratio, window, idx_cache,
-                              bt, k, max_n, out_idx, scores, cand, err, stream);
+                              bt, k, max_n, out_idx, scores, cand, deal, err, stream);
 }
 
 size_t csa_sparse_attn_workspace_size(const csa_layer* L, int32_t n_rows, int32_t k_or_max_n) {
@@ -322,5 +372,7 @@ const char* csa_status_string(int32_t s) {
 }
 
 int32_t csa_version(void) { return kVersion; }
+
+uint64_t csa_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 }  // extern "C"

@@ -60,6 +60,17 @@ __device__ __forceinline__ int64_t phys_row(const csa_block_table& bt, const csa
   return (int64_t)pb * c.rows_per_block + (lrow - lb * c.rows_per_block);
 }
 
+// Bytes of one row of a paged cache (see csa_paged in csa.h).
+__host__ __device__ __forceinline__ int64_t row_bytes(const csa_paged& c) {
+  switch (c.dtype) {
+    case CSA_F32: return (int64_t)c.dim * 4;
+    case CSA_BF16: return (int64_t)c.dim * 2;
+    case CSA_E4M3: return c.dim;
+    case CSA_E4M3R: return (int64_t)c.dim + c.tail_bf16;
+    default: return c.dim / 2;  // CSA_E2M1
+  }
+}
+
 // Number of compressed entries visible to a query at p: entries whose last raw
 // token ratio*i+window-1 lies before p.
 __host__ __device__ __forceinline__ int32_t n_visible(int32_t p, int32_t ratio, int32_t window) {

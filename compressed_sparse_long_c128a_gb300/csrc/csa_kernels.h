@@ -44,11 +44,15 @@ cudaError_t sm_count(int* n);
 //     pdl_trigger); only for the second and later kernels of one call.
 enum Order : int { kStreamOrder = 0, kAfterOwnKernel = 1 };
 
+// Kernel launches the library has issued (csa_launch_count); counted on the host.
+void count_launch();
+
 // Launch with the given ordering and, when cluster_y > 0, clusters of
 // (1, cluster_y, 1) CTAs.
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                            Order order, int cluster_y, Args... args) {
+  count_launch();
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -114,6 +118,9 @@ struct EmitArgs {
 
 cudaError_t launch_ingest(const IngestArgs& a, int32_t n_tok, cudaStream_t s);
 cudaError_t launch_emit(const EmitArgs& a, int32_t n_tok, cudaStream_t s);
+// one launch for calls of at most 1024 tokens (D % 8 == 0, D <= 512, 16-byte aligned rows)
+bool compress_fused_eligible(const IngestArgs& ia, const EmitArgs& ea, int32_t n_tok);
+cudaError_t launch_compress_fused(const IngestArgs& ia, const EmitArgs& ea, int32_t n_tok, cudaStream_t s);
 
 // ---- cache store (k_store.cu)
 struct StoreArgs {
@@ -140,14 +147,43 @@ struct IndexerArgs {
   float* scores;    // [n_rows][max_n]
   int32_t* err;
   // tensor-core path, bf16 cache: the cache as [blocks*64][128] rows, 64x64
-  // boxes, 128-byte swizzle (set by the launcher; k_tma = 0: cp.async gathers)
+  // boxes, 128-byte swizzle (set by the launcher)
   CUtensorMap k_map;
-  int32_t k_tma;
+  // balanced deal with the selection fused (sel_k > 0): the grid's CTAs share
+  // the rows' tiles in proportion to each row's length and each writes the
+  // top-sel_k of its range to the candidate lists, which the deal merge turns
+  // into the rows' selections; sel_k == 0: one CTA per row and split, every
+  // score written to `scores`
+  int32_t sel_k;
+  int32_t n_rows;
+  uint32_t* cand_key;  // [grid][sel_k] order-preserving keys of the scores
+  int32_t* cand_idx;   // [grid][sel_k] entry indices
+  int32_t* cand_cnt;   // [grid]
 };
 cudaError_t launch_indexer_scores(const IndexerArgs& a, int32_t n_rows, cudaStream_t s);
 // tensor-core scores, 64 heads x 128 dims, bf16 or e2m1 keys (k_indexer_tc.cu)
 bool indexer_tc_eligible(const IndexerArgs& a);
-cudaError_t launch_indexer_tc(const IndexerArgs& a, int32_t n_rows, cudaStream_t s);
+// Tiles (128 entries) a CTA of the balanced deal can hold for the fused
+// selection, by key format; 0 when the format has no tensor-core path.
+int32_t indexer_deal_capacity(int32_t cache_dtype);
+// The deal's largest per-CTA tile budget for n_rows rows of at most max_n
+// entries on G CTAs (an upper bound of what the device computes), or -1 when
+// a deal does not apply (more rows than CTAs).
+int32_t indexer_deal_bound(int32_t n_rows, int32_t max_n, int32_t G);
+// a.sel_k > 0: balanced deal on G CTAs; else one CTA per row and split
+cudaError_t launch_indexer_tc(const IndexerArgs& a, int32_t n_rows, int32_t G, cudaStream_t s);
+
+// Candidate lists of a balanced deal: G CTAs x k (key, index) pairs + counts;
+// a deal uses at most kDealMaxCtas CTAs.
+constexpr int32_t kDealMaxCtas = 256;
+struct DealCandidates {
+  uint32_t* key;
+  int32_t* idx;
+  int32_t* cnt;
+  int32_t ctas;
+};
+size_t deal_candidate_bytes(int32_t G, int32_t k);
+DealCandidates deal_candidates(void* base, int32_t G, int32_t k);
 
 struct TopkArgs {
   const float* scores;  // [n_rows][max_n]
@@ -160,6 +196,8 @@ struct TopkArgs {
 size_t topk_candidate_bytes(int32_t n_rows, int32_t max_n, int32_t k);
 // `first`: kStreamOrder when no kernel of the call precedes the top-k launches
 cudaError_t launch_topk(const TopkArgs& a, int32_t n_rows, void* cand, cudaStream_t s, Order first);
+// the rows' selections from the candidate lists of a balanced deal (after the indexer launch)
+cudaError_t launch_topk_deal_merge(const TopkArgs& a, int32_t n_rows, const DealCandidates& c, cudaStream_t s);
 
 // Host validation and enqueue of indexer scores + top-k, shared by
 // csa_indexer_topk and csa_indexer_topk_noalloc so that both accept and refuse
@@ -169,11 +207,14 @@ int check_indexer_topk(const void* q_idx, int32_t q_dtype, const float* w, int32
                        int32_t idx_dim, const int32_t* seq_id, const int32_t* pos, int32_t ratio, int32_t window,
                        const csa_paged* idx_cache, const csa_block_table* bt, int32_t k, int32_t max_n,
                        const int32_t* out_idx, const int32_t* err);
-// scores: n_rows * max_n floats; cand: topk_candidate_bytes(n_rows, max_n, k) bytes or nullptr when 0
+// scores: n_rows * max_n floats; cand: topk_candidate_bytes(n_rows, max_n, k)
+// bytes or nullptr when 0; deal: deal_candidate_bytes(kDealMaxCtas, k) bytes, or
+// nullptr (no balanced deal)
 int enqueue_indexer_topk(const void* q_idx, int32_t q_dtype, const float* w, int32_t n_rows, int32_t idx_heads,
                          int32_t idx_dim, const int32_t* seq_id, const int32_t* pos, int32_t ratio, int32_t window,
                          const csa_paged* idx_cache, const csa_block_table* bt, int32_t k, int32_t max_n,
-                         int32_t* out_idx, float* scores, void* cand, int32_t* err, cudaStream_t stream);
+                         int32_t* out_idx, float* scores, void* cand, void* deal, int32_t* err,
+                         cudaStream_t stream);
 
 // ---- attention (k_attn.cu)
 struct AttnArgs {

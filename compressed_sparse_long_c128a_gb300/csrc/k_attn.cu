@@ -27,8 +27,10 @@ constexpr int kMaxDim = 512;
 __device__ __forceinline__ float cache_elem(const csa_paged& c, int64_t prow, int d) {
   if (c.dtype == CSA_F32) return reinterpret_cast<const float*>(c.data)[prow * c.dim + d];
   if (c.dtype == CSA_BF16) return bf16_to_f32(reinterpret_cast<const uint16_t*>(c.data)[prow * c.dim + d]);
-  return e4m3_to_f32(reinterpret_cast<const uint8_t*>(c.data)[prow * c.dim + d]) *
-         reinterpret_cast<const float*>(c.scales)[prow];
+  const uint8_t* row = reinterpret_cast<const uint8_t*>(c.data) + prow * row_bytes(c);
+  const int Dq = c.dtype == CSA_E4M3R ? c.dim - c.tail_bf16 : c.dim;
+  if (d >= Dq) return bf16_to_f32(reinterpret_cast<const uint16_t*>(row + Dq)[d - Dq]);
+  return e4m3_to_f32(row[d]) * reinterpret_cast<const float*>(c.scales)[prow];
 }
 
 // Inverse rotation of o (lane holds dims lane + 32*i) at position p, in place.

@@ -142,17 +142,21 @@ __device__ __forceinline__ const uint8_t* key_row(const AttnArgs& a, const Geo& 
   }
   if (prow < 0) return nullptr;
   if (fp8) sc = reinterpret_cast<const float*>(c->scales)[prow];
-  return reinterpret_cast<const uint8_t*>(c->data) + prow * (int64_t)kD * (fp8 ? 1 : 2);
+  return reinterpret_cast<const uint8_t*>(c->data) + prow * row_bytes(*c);
 }
 
 // Producers: tile t goes to ring slot t & 1, one 16 KB chunk (128 dims) at a
 // time, each chunk as soon as O^T of tile t-2 has released it.  bf16 rows are copied with
 // cp.async, each thread's copies arriving on the chunk's barrier as they land
 // (the MMA issuer fences them into the async proxy); e4m3 rows are converted
-// through registers.  Keys past the slice are not loaded; the rest of the last
+// through registers (E4M3: codes to bf16 exactly, the row scale folded into the
+// logits and P; E4M3R: codes times the row scale rounded to bf16, the bf16
+// tail copied).  Keys past the slice are not loaded; the rest of the last
 // 16-key step of O^T is filled with zeros.
 __device__ void producer_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Misc& ms, int pt) {
-  const bool fp8 = a.comp.dtype == CSA_E4M3;
+  const bool fp8 = a.comp.dtype == CSA_E4M3 || a.comp.dtype == CSA_E4M3R;
+  const bool tail = a.comp.dtype == CSA_E4M3R;
+  const int Dq = tail ? kD - a.comp.tail_bf16 : kD;  // dims [Dq, kD) are bf16 in the row
   const int n = g.n_tiles;
   // bf16: thread pt copies 16-byte piece (pt & 15) of keys 6j + (pt >> 4)
   constexpr int kGroups = kProducers / 16, kPerThr = (kTile + kGroups - 1) / kGroups;
@@ -185,18 +189,26 @@ __device__ void producer_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mi
         cp_async_arrive_noinc(&ms.kfull[slot][c]);
       }
     } else {
-      // 8 consecutive threads per key row: 128 code bytes -> 128 bf16 (exact)
+      // 8 consecutive threads per key row, 16 dims each: 16 code bytes -> 16 bf16
+      // (a piece of the bf16 tail: 32 bytes copied)
       constexpr int kIters = (kTile * 8 + kProducers - 1) / kProducers;
       for (int c = 0; c < kChunks; ++c) {
         if (t >= 2) wait_or_abort(ms, &ms.kfree[slot][c], prev, a.err);
-        uint4 raw[kIters];
+        uint4 raw[kIters][2];
 #pragma unroll
         for (int it = 0; it < kIters; ++it) {
           const int x = pt + it * kProducers;
-          raw[it] = make_uint4(0, 0, 0, 0);
+          raw[it][0] = raw[it][1] = make_uint4(0, 0, 0, 0);
           if (x < lim * 8) {
             const uint8_t* rp = ms.rowptr[buf][x >> 3];
-            if (rp) raw[it] = __ldg(reinterpret_cast<const uint4*>(rp + c * 128 + (x & 7) * 16));
+            const int d0 = c * 128 + (x & 7) * 16;
+            if (rp && d0 < Dq) {
+              raw[it][0] = __ldg(reinterpret_cast<const uint4*>(rp + d0));
+            } else if (rp) {
+              const uint4* tp = reinterpret_cast<const uint4*>(rp + Dq + 2 * (d0 - Dq));
+              raw[it][0] = __ldg(tp);
+              raw[it][1] = __ldg(tp + 1);
+            }
           }
         }
 #pragma unroll
@@ -204,12 +216,19 @@ __device__ void producer_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mi
           const int x = pt + it * kProducers;
           if (x >= lim * 8) break;
           const uint32_t key = x >> 3, q8 = x & 7;
-          const uint32_t w[4] = {raw[it].x, raw[it].y, raw[it].z, raw[it].w};
+          const int d0 = c * 128 + q8 * 16;
           uint32_t outw[8];
+          if (d0 >= Dq) {
+            outw[0] = raw[it][0].x; outw[1] = raw[it][0].y; outw[2] = raw[it][0].z; outw[3] = raw[it][0].w;
+            outw[4] = raw[it][1].x; outw[5] = raw[it][1].y; outw[6] = raw[it][1].z; outw[7] = raw[it][1].w;
+          } else {
+            const uint32_t w[4] = {raw[it][0].x, raw[it][0].y, raw[it][0].z, raw[it][0].w};
+            const float rs = tail ? ms.kscale[buf][key] : 1.f;  // E4M3R: the row scale, applied here
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const uint32_t b0 = (w[e >> 1] >> ((e & 1) * 16)) & 0xFF, b1 = (w[e >> 1] >> ((e & 1) * 16 + 8)) & 0xFF;
-            outw[e] = f32x2_to_bf16x2(e4m3_to_f32((uint8_t)b0), e4m3_to_f32((uint8_t)b1));
+            for (int e = 0; e < 8; ++e) {
+              const uint32_t b0 = (w[e >> 1] >> ((e & 1) * 16)) & 0xFF, b1 = (w[e >> 1] >> ((e & 1) * 16 + 8)) & 0xFF;
+              outw[e] = f32x2_to_bf16x2(e4m3_to_f32((uint8_t)b0) * rs, e4m3_to_f32((uint8_t)b1) * rs);
+            }
           }
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
@@ -400,7 +419,7 @@ __device__ __forceinline__ void lookup_keys(const AttnArgs& a, const Geo& g, Mis
   const int b = u % kRowBufs;
   if (st < kTile) {
     float sc;
-    const uint8_t* rp = key_row(a, g, u, st, a.comp.dtype == CSA_E4M3, sc);
+    const uint8_t* rp = key_row(a, g, u, st, a.comp.dtype == CSA_E4M3 || a.comp.dtype == CSA_E4M3R, sc);
     ms.rowptr[b][st] = rp;
     ms.kvalid[b][st] = rp != nullptr;
     ms.kscale[b][st] = sc;
@@ -431,7 +450,7 @@ __device__ void softmax_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mis
   // lanes l and l+16 of warp w share head 16w + l (lanes 0-15 hold its TMEM row):
   // lane l takes keys [0, 32) of each tile, lane l+16 keys [32, 64)
   const int hf = l >> 4, h = 16 * w + (l & 15);
-  const bool fp8 = a.comp.dtype == CSA_E4M3;
+  const bool fp8 = a.comp.dtype == CSA_E4M3;  // per-key scales folded into the logits and P
   const uint32_t lane_addr = tmem + ((uint32_t)(w * 32) << 16);
   float m_run = -INFINITY, l_run = 0.f;  // the head's running max; this half's denominator
 
@@ -816,8 +835,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 }  // namespace
 
 bool attn_tc_eligible(const AttnArgs& a) {
-  return a.dim == kD && a.heads == kH && a.comp.dtype == a.swa.dtype &&
-         (a.comp.dtype == CSA_BF16 || a.comp.dtype == CSA_E4M3) && a.rope.rope_dim <= 128;
+  const uintptr_t al = reinterpret_cast<uintptr_t>(a.comp.data) | reinterpret_cast<uintptr_t>(a.swa.data);
+  return a.dim == kD && a.heads == kH && a.comp.dtype == a.swa.dtype && a.comp.tail_bf16 == a.swa.tail_bf16 &&
+         (a.comp.dtype == CSA_BF16 || a.comp.dtype == CSA_E4M3 || a.comp.dtype == CSA_E4M3R) &&
+         a.rope.rope_dim <= 128 && al % 16 == 0;
 }
 
 int32_t attn_tc_splits(int32_t n_rows, int32_t keys_per_row) {

@@ -26,7 +26,19 @@ __device__ __forceinline__ void store_elem(void* base, int32_t dtype, int64_t id
 // Write y[0..D) (shared memory) as physical row `prow` of cache c.  Called by
 // the whole block with a block-uniform prow >= 0.
 __device__ void store_row(const csa_paged& c, int64_t prow, const float* y, int D, float* red) {
-  if (c.dtype == CSA_E4M3) {
+  if (c.dtype == CSA_E4M3R) {  // e4m3 + per-row scale over [0, D - tail), bf16 tail
+    const int Dq = D - c.tail_bf16;
+    float am = 0.f;
+    for (int d = threadIdx.x; d < Dq; d += blockDim.x) am = fmaxf(am, fabsf(y[d]));
+    am = block_max(am, red);
+    const float inv = am > 0.f ? 448.0f / am : 0.0f;
+    uint8_t* row = reinterpret_cast<uint8_t*>(c.data) + prow * row_bytes(c);
+    for (int pr = threadIdx.x; pr < Dq / 2; pr += blockDim.x)
+      *reinterpret_cast<uint16_t*>(row + 2 * pr) = f32x2_to_e4m3x2(y[2 * pr] * inv, y[2 * pr + 1] * inv);
+    for (int pr = threadIdx.x; pr < c.tail_bf16 / 2; pr += blockDim.x)
+      *reinterpret_cast<uint32_t*>(row + Dq + 4 * pr) = f32x2_to_bf16x2(y[Dq + 2 * pr], y[Dq + 2 * pr + 1]);
+    if (threadIdx.x == 0) reinterpret_cast<float*>(c.scales)[prow] = am / 448.0f;
+  } else if (c.dtype == CSA_E4M3) {
     float am = 0.f;
     for (int d = threadIdx.x; d < D; d += blockDim.x) am = fmaxf(am, fabsf(y[d]));
     am = block_max(am, red);
@@ -185,7 +197,207 @@ __global__ void __launch_bounds__(kThreads) emit_kernel(const EmitArgs a) {
   store_row(a.comp, crow, y, D, red);
 }
 
+// ------------------------------------------------------------------ one launch for decode-sized calls
+
+constexpr int kFusedMaxTokens = 1024;  // the (seq, pos) scan of an emitting CTA stays cheap
+constexpr int kFusedMaxDim = 512;
+constexpr int kQuarters = 4;  // window rows split over four groups of threads per 8-channel group
+
+// Eight consecutive elements of a row in `dtype` (F32 or BF16) as floats; 16-byte (bf16) or
+// 2 x 16-byte (f32) loads, so `p` must be 16-byte aligned.
+__device__ __forceinline__ void load8(const void* base, int32_t dtype, int64_t idx, float* v) {
+  if (dtype == CSA_F32) {
+    const float4* p = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(base) + idx);
+    const float4 a = p[0], b = p[1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  } else {
+    const uint4 u = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(base) + idx);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      v[2 * e] = bf16_to_f32((uint16_t)(w[e] & 0xFFFF));
+      v[2 * e + 1] = bf16_to_f32((uint16_t)(w[e] >> 16));
+    }
+  }
+}
+
+__device__ __forceinline__ void store8(void* base, int32_t dtype, int64_t idx, const float* v) {
+  if (dtype == CSA_F32) {
+    float4* p = reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + idx);
+    p[0] = make_float4(v[0], v[1], v[2], v[3]);
+    p[1] = make_float4(v[4], v[5], v[6], v[7]);
+  } else {
+    *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(base) + idx) =
+        make_uint4(f32x2_to_bf16x2(v[0], v[1]), f32x2_to_bf16x2(v[2], v[3]), f32x2_to_bf16x2(v[4], v[5]),
+                   f32x2_to_bf16x2(v[6], v[7]));
+  }
+}
+
+// CTA j takes token j of the call: state row and window row as ingest_kernel
+// writes them; then, if a window closes at the token, the entry as emit_kernel
+// forms it, but with every window row that is one of the call's own tokens
+// read from the call's inputs (the state cache holds the rest, written by
+// earlier calls), so no CTA depends on another CTA's writes.
+__global__ void __launch_bounds__(kThreads) compress_fused_kernel(const IngestArgs ia, const EmitArgs ea,
+                                                                  int32_t n_tok) {
+  __shared__ float y[kFusedMaxDim];
+  __shared__ float red[32];
+  __shared__ float part[kQuarters][3][kFusedMaxDim];  // per row group: running max, denominator, weighted sum
+  __shared__ const void* src_kv[256];                  // window row o: kv and gate of the row
+  __shared__ const void* src_gate[256];
+  __shared__ int32_t src_dt[256];
+  __shared__ int in_call[256];
+  __shared__ int bad;
+  pdl_trigger();
+  pdl_wait();
+  const int j = blockIdx.x;
+  const int D = ia.dim, G8 = D / 8;
+  const int seq = ia.seq_id[j];
+  const int64_t p = ia.pos[j];
+  const int64_t srow = phys_row(ia.state_bt, ia.state, seq, p, ia.err);
+  const int64_t wrow = ia.swa.data ? phys_row(ia.swa_bt, ia.swa, seq, p, ia.err) : -1;
+
+  // ---- ingest
+  float ss = 0.f;
+  for (int g = threadIdx.x; g < G8; g += blockDim.x) {
+    float x[8], gt[8];
+    load8(ia.kv, ia.in_dtype, (int64_t)j * D + 8 * g, x);
+    if (srow >= 0) {
+      load8(ia.gate, ia.in_dtype, (int64_t)j * D + 8 * g, gt);
+      store8(ia.state.data, ia.state.dtype, srow * 2 * D + 8 * g, x);
+      store8(ia.state.data, ia.state.dtype, srow * 2 * D + D + 8 * g, gt);
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      y[8 * g + e] = x[e];
+      ss += x[e] * x[e];
+    }
+  }
+  ss = block_sum(ss, red);
+  if (wrow >= 0) {  // block-uniform
+    const float inv = 1.0f / sqrtf(ss / (float)D + ia.eps);
+    __syncthreads();
+    norm_rope_inplace(y, D, inv, ia.gamma_swa, ia.rope, p);
+    __syncthreads();
+    store_row(ia.swa, wrow, y, D, red);
+  }
+
+  // ---- emission of the entry whose window closes at this token
+  const int W = ea.window, Rt = ea.ratio;
+  if (p < W - 1 || (p - W + 1) % Rt) return;  // block-uniform
+  const int64_t i = (p - W + 1) / Rt;
+  const int64_t base = i * Rt;
+  __syncthreads();  // y and red are reused below
+  if (threadIdx.x == 0) bad = 0;
+  for (int o = threadIdx.x; o < W; o += blockDim.x) in_call[o] = -1;
+  __syncthreads();
+  for (int k = threadIdx.x; k < n_tok; k += blockDim.x) {
+    const int64_t q = ea.pos[k];
+    if (ea.seq_id[k] == seq && q >= base && q < base + W) in_call[q - base] = k;
+  }
+  __syncthreads();
+  for (int o = threadIdx.x; o < W; o += blockDim.x) {
+    const int k = in_call[o];
+    if (k >= 0) {
+      src_kv[o] = reinterpret_cast<const uint8_t*>(ia.kv) + (int64_t)k * D * (ia.in_dtype == CSA_F32 ? 4 : 2);
+      src_gate[o] = reinterpret_cast<const uint8_t*>(ia.gate) + (int64_t)k * D * (ia.in_dtype == CSA_F32 ? 4 : 2);
+      src_dt[o] = ia.in_dtype;
+    } else {
+      const int64_t r = phys_row(ea.state_bt, ea.state, seq, base + o, ea.err);
+      if (r < 0) {
+        bad = 1;
+        src_kv[o] = src_gate[o] = nullptr;
+      } else {
+        const size_t eb = ea.state.dtype == CSA_F32 ? 4 : 2;
+        src_kv[o] = reinterpret_cast<const uint8_t*>(ea.state.data) + r * 2 * D * eb;
+        src_gate[o] = reinterpret_cast<const uint8_t*>(ea.state.data) + (r * 2 * D + D) * eb;
+      }
+      src_dt[o] = ea.state.dtype;
+    }
+  }
+  const int64_t crow = phys_row(ea.comp_bt, ea.comp, seq, i, ea.err);
+  __syncthreads();
+  if (bad || crow < 0) return;
+
+  // online softmax over the window offsets, per channel: thread (g, qtr) takes
+  // channels [8g, 8g+8) and offsets qtr, qtr+4, ...; the four row groups merge below
+  for (int x = threadIdx.x; x < G8 * kQuarters; x += blockDim.x) {
+    const int g = x % G8, qtr = x / G8;
+    float m[8], sm[8], c[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      m[e] = -INFINITY;
+      sm[e] = 0.f;
+      c[e] = 0.f;
+    }
+    for (int o = qtr; o < W; o += kQuarters) {
+      float kv[8], gt[8];
+      load8(src_kv[o], src_dt[o], 8 * g, kv);
+      load8(src_gate[o], src_dt[o], 8 * g, gt);
+      const float4* b4 = reinterpret_cast<const float4*>(ea.bias + (int64_t)o * D + 8 * g);
+      const float4 b0 = b4[0], b1 = b4[1];
+      const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float z = gt[e] + bb[e];
+        if (z > m[e]) {
+          const float f = expf(m[e] - z);
+          sm[e] = sm[e] * f + 1.f;
+          c[e] = c[e] * f + kv[e];
+          m[e] = z;
+        } else {
+          const float ez = expf(z - m[e]);
+          sm[e] += ez;
+          c[e] += ez * kv[e];
+        }
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      part[qtr][0][8 * g + e] = m[e];
+      part[qtr][1][8 * g + e] = sm[e];
+      part[qtr][2][8 * g + e] = c[e];
+    }
+  }
+  __syncthreads();
+  float ss2 = 0.f;
+  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < kQuarters; ++q) mx = fmaxf(mx, part[q][0][d]);
+    float sm = 0.f, c = 0.f;
+#pragma unroll
+    for (int q = 0; q < kQuarters; ++q) {
+      const float mq = part[q][0][d];
+      if (mq == -INFINITY) continue;  // a row group with no offsets (W < 4)
+      const float f = expf(mq - mx);
+      sm += part[q][1][d] * f;
+      c += part[q][2][d] * f;
+    }
+    const float v = c / sm;
+    y[d] = v;
+    ss2 += v * v;
+  }
+  ss2 = block_sum(ss2, red);
+  const float inv = 1.0f / sqrtf(ss2 / (float)D + ea.eps);
+  __syncthreads();
+  norm_rope_inplace(y, D, inv, ea.gamma_c, ea.rope, base);
+  __syncthreads();
+  store_row(ea.comp, crow, y, D, red);
+}
+
 }  // namespace
+
+bool compress_fused_eligible(const IngestArgs& ia, const EmitArgs& ea, int32_t n_tok) {
+  const uintptr_t al = reinterpret_cast<uintptr_t>(ia.kv) | reinterpret_cast<uintptr_t>(ia.gate) |
+                       reinterpret_cast<uintptr_t>(ia.state.data) | reinterpret_cast<uintptr_t>(ea.bias);
+  return n_tok <= kFusedMaxTokens && ia.dim % 8 == 0 && ia.dim <= kFusedMaxDim && ea.window <= 256 && al % 16 == 0;
+}
+
+cudaError_t launch_compress_fused(const IngestArgs& ia, const EmitArgs& ea, int32_t n_tok, cudaStream_t s) {
+  if (n_tok == 0) return cudaSuccess;
+  return launch_k(compress_fused_kernel, dim3(n_tok), dim3(kThreads), 0, s, kStreamOrder, 0, ia, ea, n_tok);
+}
 
 cudaError_t launch_ingest(const IngestArgs& a, int32_t n_tok, cudaStream_t s) {
   if (n_tok == 0) return cudaSuccess;

@@ -7,17 +7,32 @@
 // contiguous range of 128-entry tiles.  Entries are the M dimension:
 //   S^T [128 entries x 64 heads] = K_idx [128 x 128] . Q_idx^T [128 x 64]
 // so thread t of the epilogue warps owns TMEM lane t = entry t, reads its 64
-// head dots, and writes one score.  Keys go into a 4-stage ring of
-// 128B-swizzled K-major tiles.  A tile is two 64-entry paged blocks, 16 KB
-// each and contiguous in a bf16 cache, so bf16 tiles arrive as four TMA boxes
-// (64 dims x 64 entries); e2m1 rows (64 code bytes + 8 e4m3 scale bytes) come
-// by cp.async into a raw ring and are dequantised to bf16 (exact: a 2-bit
-// e2m1 significand times a 4-bit e4m3 one fits bf16).
-// TMEM holds two S^T buffers so the epilogue of tile i overlaps the MMA of i+1.
+// head dots and forms one score.  TMEM holds two S^T buffers so the epilogue
+// of tile i overlaps the MMA of tile i+1.
 //
-// Warps 0-3: epilogue; warps 4-10: producers; warp 11: TMEM allocation + MMA issue.
+// Keys reach shared memory as 128B-swizzled K-major bf16 tiles.  A tile is two
+// 64-entry paged blocks; a bf16 block is 16 KB contiguous, so a bf16 tile
+// arrives as four TMA boxes (64 dims x 64 entries) issued by one thread.  An
+// e2m1 block is 4 KB of codes plus 512 B of e4m3 scales, each contiguous: one
+// thread issues four bulk copies per tile into a six-deep raw ring, and six
+// warps turn the codes into bf16 (exact: a 2-bit e2m1 significand times a
+// 4-bit e4m3 one fits bf16's 8 bits).
+//
+// Two ways to cut the work:
+//   * balanced deal (decode batches, IndexerArgs::sel_k > 0): the grid is one
+//     wave of G CTAs, and every CTA derives from the rows' positions the same
+//     deal of each row's tiles in proportion to its length (select.cuh), so
+//     short and long rows finish together.  The CTA keeps its scores in shared
+//     memory and, after its last tile, selects their top-k itself; the deal
+//     merge then combines each row's candidate lists.  No score reaches HBM.
+//   * one CTA per row and split (sel_k == 0, prefill-sized batches): every
+//     score goes to the caller's scratch for the top-k kernels.
+//
+// Warps 0-3: epilogue; warps 4-10: producers (bf16: one TMA thread; e2m1:
+// warp 4 issues the bulk copies, warps 5-10 convert); warp 11: TMEM
+// allocation + MMA issue.  After the last tile all 12 warps run the selection.
 
-#include "csa_kernels.h"
+#include "select.cuh"
 #include "tc_ptx.cuh"
 
 namespace csa {
@@ -25,30 +40,52 @@ namespace {
 
 using namespace tc;
 
-constexpr int kHI = 64, kDI = 128, kTile = 128, kStages = 4;
+constexpr int kHI = 64, kDI = 128, kTile = kDealTile;
 constexpr int kEpi = 128, kProd = 224;
 constexpr int kThreads = kEpi + kProd + 32;
 constexpr int kMmaWarp = (kEpi + kProd) / 32;
-constexpr uint32_t kQBytes = kHI * kDI * 2;         // 16 KB: 2 K-atoms of 64 rows x 128 B
-constexpr uint32_t kStageBytes = kTile * kDI * 2;   // 32 KB: 2 K-atoms of 128 rows x 128 B
-constexpr uint32_t kAtomBytes = kTile * 128;        // 16 KB
-constexpr uint32_t kRawCodes = kTile * kDI / 2;     // 8 KB of e2m1 codes per tile
-constexpr uint32_t kRawScales = kTile * kDI / 16;   // 1 KB of e4m3 scales per tile
-constexpr uint32_t kRawBytes = kRawCodes + kRawScales;
-constexpr uint32_t kOffQ = 0, kOffStage = kQBytes, kOffRaw = kOffStage + kStages * kStageBytes;
-constexpr uint32_t kOffMisc = kOffRaw + kStages * kRawBytes;
+constexpr int kConvThreads = kProd - 32;  // e2m1: warps 5-10 convert
+constexpr uint32_t kQBytes = kHI * kDI * 2;        // 16 KB: 2 K-atoms of 64 rows x 128 B
+constexpr uint32_t kStageBytes = kTile * kDI * 2;  // 32 KB: 2 K-atoms of 128 rows x 128 B
+constexpr uint32_t kAtomBytes = kTile * 128;       // 16 KB
+constexpr int kRowsPerBlock = 64;                  // entries per 256-position block (c4a)
+constexpr uint32_t kBlockCodes = kRowsPerBlock * kDI / 2;    // 4 KB of e2m1 codes per block
+constexpr uint32_t kBlockScales = kRowsPerBlock * kDI / 16;  // 512 B of e4m3 scales per block
+constexpr uint32_t kRawCodes = 2 * kBlockCodes;
+constexpr uint32_t kRawBytes = kRawCodes + 2 * kBlockScales;  // 9 KB per tile
 constexpr uint32_t kTmemCols = 128;
-constexpr int kRowsPerBlock = 64;  // entries per 256-position block (c4a)
-constexpr int kTblMax = 1024;      // block-table entries a CTA caches (= 512 tiles)
+constexpr int kTblMax = 1024;  // block-table entries a CTA caches (= 512 tiles)
+
+// Shared-memory plan per key format.
+template <bool kFp4>
+struct Plan {
+  static constexpr int kStages = kFp4 ? 3 : 4;       // bf16 tiles the MMA reads
+  static constexpr int kRaw = kFp4 ? 6 : 0;          // raw e2m1 tiles in flight
+  static constexpr int kCapTiles = kFp4 ? 64 : 128;  // tiles whose keys the fused selection holds
+  static constexpr uint32_t kOffQ = 0;
+  static constexpr uint32_t kOffStage = kQBytes;
+  static constexpr uint32_t kOffRaw = kOffStage + kStages * kStageBytes;
+  static constexpr uint32_t kOffKeys = kOffRaw + kRaw * kRawBytes;
+  static constexpr uint32_t kKeyBytes = ((uint32_t)padded_size(kCapTiles * kTile) * 4 + 1023) & ~1023u;
+  static constexpr uint32_t kOffMisc = kOffKeys + kKeyBytes;
+};
 
 struct Misc {
-  uint64_t full[kStages], empty[kStages], tfull[2], tempty[2];
+  uint64_t full[4], empty[4], raw_full[6], raw_empty[6], tfull[2], tempty[2], mma_done;
   uint32_t tmem_base;
   int32_t abort;
+  int32_t row, t0, nt;
   float w[kHI];
   int32_t tbl[kTblMax];  // physical blocks of the CTA's entry range (-1: unmapped / out of range)
 };
-constexpr uint32_t kSmemBytes = kOffMisc + sizeof(Misc) + 1024;
+
+template <bool kFp4>
+constexpr uint32_t smem_bytes() {
+  return Plan<kFp4>::kOffMisc + sizeof(Misc) + 1024;
+}
+static_assert(sizeof(DealShared) <= kStageBytes, "the deal is built in the idle stage ring");
+static_assert(sizeof(SelectScratch) <= kStageBytes, "the selection scratch reuses the drained stage ring");
+static_assert(smem_bytes<false>() <= 227 * 1024 && smem_bytes<true>() <= 227 * 1024, "shared memory");
 
 __device__ __forceinline__ bool wait_or_abort(Misc& ms, uint64_t* bar, uint32_t parity, int32_t* err) {
   if (*reinterpret_cast<volatile int32_t*>(&ms.abort)) return false;
@@ -59,24 +96,9 @@ __device__ __forceinline__ bool wait_or_abort(Misc& ms, uint64_t* bar, uint32_t 
 }
 
 struct Range {
-  int seq;
-  int32_t n, t0, nt;  // visible entries, first tile, tile count
+  int row, seq;
+  int32_t n, t0, nt;  // visible entries of the row, first tile, tile count
 };
-
-__device__ __forceinline__ Range row_range(const IndexerArgs& a, int r) {
-  Range g;
-  g.seq = a.seq_id[r];
-  g.n = n_visible(a.pos[r], a.ratio, a.window);
-  if (g.n > a.max_n) {
-    record_error(a.err, CSA_ERR_DEVICE_BOUNDS);
-    g.n = a.max_n;
-  }
-  const int32_t tiles = (g.n + kTile - 1) / kTile;
-  const int32_t per = (tiles + gridDim.y - 1) / gridDim.y;
-  g.t0 = min(tiles, (int32_t)blockIdx.y * per);
-  g.nt = min(tiles, g.t0 + per) - g.t0;
-  return g;
-}
 
 // High and low bytes of the bf16 bits of the e2m1 magnitudes 0, 0.5, 1, 1.5, 2,
 // 3, 4, 6, as byte-permute tables indexed by the 3-bit magnitude code.
@@ -115,33 +137,31 @@ __device__ __forceinline__ uint32_t e4m3_bf16x2(uint8_t v) {
   return b | (b << 16);
 }
 
-// Physical row of entry e of this CTA's range, from the cached block table; -1 if unmapped.
-__device__ __forceinline__ int64_t entry_row(const Misc& ms, int32_t blk0, int32_t e) {
-  const int32_t j = (e / kRowsPerBlock) - blk0;
-  if (j < 0 || j >= kTblMax) return -1;  // the launcher keeps every CTA's range inside the cache
-  const int32_t pb = ms.tbl[j];
-  return pb < 0 ? -1 : (int64_t)pb * kRowsPerBlock + (e % kRowsPerBlock);
+// Physical block of tile-half h (0, 1) of tile i of the range, or -1 when
+// unmapped or past the visible entries (then nothing is loaded).
+__device__ __forceinline__ int32_t tile_block(const Misc& ms, const Range& g, int i, int h) {
+  const int32_t e = (g.t0 + i) * kTile + h * kRowsPerBlock;
+  const int32_t j = 2 * i + h;  // the cached table starts at the range's first block
+  return (e < g.n && j < kTblMax) ? ms.tbl[j] : -1;
 }
 
-// bf16 with a tensor map: one thread issues each tile as up to four TMA boxes
-// (two blocks x two 64-dim atoms); a block that is unmapped or past the visible
-// entries is not loaded (its scores are not used).
-__device__ void producer_tma(const IndexerArgs& a, const Range& g, uint8_t* smem, Misc& ms) {
-  const int32_t blk0 = g.t0 * kTile / kRowsPerBlock;
+// bf16: one thread issues each tile as up to four TMA boxes (two blocks x two
+// 64-dim atoms).
+template <bool kFp4>
+__device__ void producer_bf16(const IndexerArgs& a, const Range& g, uint8_t* smem, Misc& ms) {
+  using P = Plan<kFp4>;
   for (int i = 0; i < g.nt; ++i) {
-    const int s = i % kStages;
-    if (i >= kStages) wait_or_abort(ms, &ms.empty[s], ((i / kStages) - 1) & 1, a.err);
-    const int32_t e0 = (g.t0 + i) * kTile;
+    const int s = i % P::kStages;
+    if (i >= P::kStages) wait_or_abort(ms, &ms.empty[s], ((i / P::kStages) - 1) & 1, a.err);
     int32_t pb[2];
     uint32_t bytes = 0;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const int32_t e = e0 + h * kRowsPerBlock, j = e / kRowsPerBlock - blk0;
-      pb[h] = (e < g.n && j >= 0 && j < kTblMax) ? ms.tbl[j] : -1;
+      pb[h] = tile_block(ms, g, i, h);
       if (pb[h] >= 0) bytes += kRowsPerBlock * kDI * 2;
     }
     mbar_arrive_expect_tx(&ms.full[s], bytes);
-    uint8_t* sb = smem + kOffStage + s * kStageBytes;
+    uint8_t* sb = smem + P::kOffStage + s * kStageBytes;
 #pragma unroll
     for (int h = 0; h < 2; ++h)
       if (pb[h] >= 0)
@@ -152,96 +172,77 @@ __device__ void producer_tma(const IndexerArgs& a, const Range& g, uint8_t* smem
   }
 }
 
-// Each thread derives its own rows' addresses from the cached table, so issuing
-// a tile needs no barrier; e2m1 tiles need one before the conversion reads
-// bytes other threads copied.
-__device__ void producer_role(const IndexerArgs& a, const Range& g, uint8_t* smem, Misc& ms, int pt) {
-  const bool fp4 = a.cache.dtype == CSA_E2M1;
-  const uint32_t stage0 = smem_u32(smem + kOffStage), raw0 = smem_u32(smem + kOffRaw);
-  const int32_t blk0 = g.t0 * kTile / kRowsPerBlock;
-  const uint8_t* base = reinterpret_cast<const uint8_t*>(a.cache.data);
-  const uint8_t* sbase = reinterpret_cast<const uint8_t*>(a.cache.scales);
-  for (int i = 0; i < g.nt + 2; ++i) {
-    if (i < g.nt) {
-      const int s = i % kStages;
-      if (i >= kStages) wait_or_abort(ms, &ms.empty[s], ((i / kStages) - 1) & 1, a.err);
-      const int32_t e0 = (g.t0 + i) * kTile;
-      if (!fp4) {
-        // 16 consecutive threads per 256-byte row
-        const uint32_t sb = stage0 + s * kStageBytes;
-        for (int x = pt; x < kTile * 16; x += kProd) {
-          const uint32_t key = x >> 4, piece = x & 15;
-          const int32_t e = e0 + (int32_t)key;
-          const int64_t pr = e < g.n ? entry_row(ms, blk0, e) : -1;
-          const uint32_t dst = sb + (piece >> 3) * kAtomBytes + (key >> 3) * 1024 + (key & 7) * 128 +
-                               (((piece & 7) ^ (key & 7)) << 4);
-          cp_async16(dst, pr >= 0 ? base + pr * (kDI * 2) + piece * 16 : base, pr >= 0 ? 16u : 0u);
-        }
-      } else {
-        // raw ring: [128 rows][64 code bytes] then [128 rows][8 scale bytes]
-        const uint32_t rb = raw0 + s * kRawBytes;
-        for (int x = pt; x < kTile * 4; x += kProd) {
-          const uint32_t key = x >> 2, piece = x & 3;
-          const int32_t e = e0 + (int32_t)key;
-          const int64_t pr = e < g.n ? entry_row(ms, blk0, e) : -1;
-          cp_async16(rb + key * 64 + piece * 16, pr >= 0 ? base + pr * (kDI / 2) + piece * 16 : base,
-                     pr >= 0 ? 16u : 0u);
-        }
-        // two entries' 8 scale bytes per 16-byte piece; entries 2x, 2x+1 share a block
-        for (int x = pt; x < kTile / 2; x += kProd) {
-          const int32_t e = e0 + 2 * x;
-          const int64_t pr = e < g.n ? entry_row(ms, blk0, e) : -1;
-          const bool both = e + 1 < g.n;
-          if (pr >= 0 && both) {
-            cp_async16(rb + kRawCodes + x * 16, sbase + pr * (kDI / 16), 16u);
-          } else {
-            const uint2 v0 = pr >= 0 ? *reinterpret_cast<const uint2*>(sbase + pr * (kDI / 16)) : make_uint2(0, 0);
-            *reinterpret_cast<uint4*>(smem + kOffRaw + s * kRawBytes + kRawCodes + x * 16) =
-                make_uint4(v0.x, v0.y, 0u, 0u);
-          }
-        }
-      }
-    }
-    cp_async_commit();
-    if (i >= 2) {
-      // the tile issued two groups ago has landed
-      cp_async_wait<2>();
-      const int ii = i - 2, s = ii % kStages;
-      if (fp4) {
-        named_bar(2, kProd);  // every producer's copies of tile ii are visible
-        const uint8_t* rb = smem + kOffRaw + s * kRawBytes;
-        uint8_t* sb = smem + kOffStage + s * kStageBytes;
-        // 16 bytes of codes = 32 values = 64 bytes of bf16 = 4 swizzled pieces
-        for (int x = pt; x < kTile * 4; x += kProd) {
-          const uint32_t key = x >> 2, q = x & 3;
-          const uint4 c4 = *reinterpret_cast<const uint4*>(rb + key * 64 + q * 16);
-          const uint8_t* sc = rb + kRawCodes + key * 8 + q * 2;
-          const uint32_t s0 = e4m3_bf16x2(sc[0]), s1 = e4m3_bf16x2(sc[1]);
-          const uint32_t cw[4] = {c4.x, c4.y, c4.z, c4.w};
+// e2m1, issuing thread: each tile's codes and scales as four bulk copies into
+// the raw ring (layout per tile: [128 entries][64 code bytes] then
+// [128 entries][8 scale bytes]).
+template <bool kFp4>
+__device__ void producer_raw(const IndexerArgs& a, const Range& g, uint8_t* smem, Misc& ms) {
+  using P = Plan<kFp4>;
+  const uint8_t* codes = reinterpret_cast<const uint8_t*>(a.cache.data);
+  const uint8_t* scales = reinterpret_cast<const uint8_t*>(a.cache.scales);
+  for (int i = 0; i < g.nt; ++i) {
+    const int rs = i % P::kRaw;
+    if (i >= P::kRaw) wait_or_abort(ms, &ms.raw_empty[rs], ((i / P::kRaw) - 1) & 1, a.err);
+    int32_t pb[2];
+    uint32_t bytes = 0;
 #pragma unroll
-          for (int half = 0; half < 4; ++half) {  // 8 values -> one 16-byte piece
-            uint32_t o[4];
-            e2m1x8_bf16x2(cw[half], half < 2 ? s0 : s1, o);
-            const uint32_t piece = q * 4 + half;  // 0..15 over the 128 dims
-            *reinterpret_cast<uint4*>(sb + (piece >> 3) * kAtomBytes + (key >> 3) * 1024 + (key & 7) * 128 +
-                                      (((piece & 7) ^ (key & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-          }
-        }
-        named_bar(2, kProd);  // the raw stage may be refilled only after everyone converted
-      }
-      fence_proxy_async();
-      mbar_arrive(&ms.full[s]);
+    for (int h = 0; h < 2; ++h) {
+      pb[h] = tile_block(ms, g, i, h);
+      if (pb[h] >= 0) bytes += kBlockCodes + kBlockScales;
     }
+    mbar_arrive_expect_tx(&ms.raw_full[rs], bytes);
+    uint8_t* rb = smem + P::kOffRaw + rs * kRawBytes;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      if (pb[h] >= 0) {
+        bulk_load(rb + h * kBlockCodes, codes + (int64_t)pb[h] * kBlockCodes, kBlockCodes, &ms.raw_full[rs]);
+        bulk_load(rb + kRawCodes + h * kBlockScales, scales + (int64_t)pb[h] * kBlockScales, kBlockScales,
+                  &ms.raw_full[rs]);
+      }
   }
-  cp_async_wait<0>();
 }
 
-__device__ void mma_role(const IndexerArgs& a, const Range& g, uint8_t* smem, Misc& ms, uint32_t tmem) {
-  constexpr uint32_t idesc = idesc_bf16(128, kHI, 0, 0);
-  const uint32_t stage0 = smem_u32(smem + kOffStage), qbase = smem_u32(smem + kOffQ);
+// e2m1, converting warps: raw tile -> bf16 tile of the stage ring.  A code of
+// an unloaded block is stale; its entry's score is not used.
+template <bool kFp4>
+__device__ void converter(const IndexerArgs& a, const Range& g, uint8_t* smem, Misc& ms, int ct) {
+  using P = Plan<kFp4>;
   for (int i = 0; i < g.nt; ++i) {
-    const int s = i % kStages, b = i & 1;
-    wait_or_abort(ms, &ms.full[s], (i / kStages) & 1, a.err);
+    const int rs = i % P::kRaw, s = i % P::kStages;
+    wait_or_abort(ms, &ms.raw_full[rs], (i / P::kRaw) & 1, a.err);
+    if (i >= P::kStages) wait_or_abort(ms, &ms.empty[s], ((i / P::kStages) - 1) & 1, a.err);
+    const uint8_t* rb = smem + P::kOffRaw + rs * kRawBytes;
+    uint8_t* sb = smem + P::kOffStage + s * kStageBytes;
+    // 16 bytes of codes = 32 values = 64 bytes of bf16 = 4 swizzled pieces
+    for (int x = ct; x < kTile * 4; x += kConvThreads) {
+      const uint32_t key = x >> 2, q = x & 3;
+      const uint4 c4 = *reinterpret_cast<const uint4*>(rb + key * 64 + q * 16);
+      const uint8_t* sc = rb + kRawCodes + key * 8 + q * 2;
+      const uint32_t s0 = e4m3_bf16x2(sc[0]), s1 = e4m3_bf16x2(sc[1]);
+      const uint32_t cw[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+      for (int half = 0; half < 4; ++half) {  // 8 values -> one 16-byte piece
+        uint32_t o[4];
+        e2m1x8_bf16x2(cw[half], half < 2 ? s0 : s1, o);
+        const uint32_t piece = q * 4 + half;  // 0..15 over the 128 dims
+        *reinterpret_cast<uint4*>(sb + (piece >> 3) * kAtomBytes + (key >> 3) * 1024 + (key & 7) * 128 +
+                                  (((piece & 7) ^ (key & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
+    fence_proxy_async();
+    mbar_arrive(&ms.full[s]);
+    mbar_arrive(&ms.raw_empty[rs]);
+  }
+}
+
+template <bool kFp4>
+__device__ void mma_role(const IndexerArgs& a, const Range& g, uint8_t* smem, Misc& ms, uint32_t tmem) {
+  using P = Plan<kFp4>;
+  constexpr uint32_t idesc = idesc_bf16(128, kHI, 0, 0);
+  const uint32_t stage0 = smem_u32(smem + P::kOffStage), qbase = smem_u32(smem + P::kOffQ);
+  for (int i = 0; i < g.nt; ++i) {
+    const int s = i % P::kStages, b = i & 1;
+    wait_or_abort(ms, &ms.full[s], (i / P::kStages) & 1, a.err);
     if (i >= 2) wait_or_abort(ms, &ms.tempty[b], ((i >> 1) - 1) & 1, a.err);
     tc_fence_after();
 #pragma unroll
@@ -253,15 +254,23 @@ __device__ void mma_role(const IndexerArgs& a, const Range& g, uint8_t* smem, Mi
     mma_commit(&ms.empty[s]);
     mma_commit(&ms.tfull[b]);
   }
+  // nothing may still write TMEM when it is released, even after a timeout
+  mma_commit(&ms.mma_done);
+  if (!mbar_wait(&ms.mma_done, 0)) record_error(a.err, CSA_ERR_TIMEOUT);
 }
 
-__device__ void epilogue_role(const IndexerArgs& a, const Range& g, Misc& ms, uint32_t tmem, int et) {
+// Scores of the range: to shared memory as order keys (fused selection) or to
+// the caller's score scratch.  An entry of an unmapped block scores -inf.
+template <bool kFp4>
+__device__ void epilogue_role(const IndexerArgs& a, const Range& g, uint8_t* smem, Misc& ms, uint32_t tmem,
+                              int et) {
+  using P = Plan<kFp4>;
   const uint32_t lane_addr = tmem + ((uint32_t)((et >> 5) * 32) << 16);
   float w[kHI];
 #pragma unroll
   for (int h = 0; h < kHI; ++h) w[h] = ms.w[h];
-  float* out = a.scores + (int64_t)blockIdx.x * a.max_n;
-  const int32_t blk0 = g.t0 * kTile / kRowsPerBlock;
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smem + P::kOffKeys);
+  float* out = a.scores + (int64_t)g.row * a.max_n;
   for (int i = 0; i < g.nt; ++i) {
     const int b = i & 1;
     wait_or_abort(ms, &ms.tfull[b], (i >> 1) & 1, a.err);
@@ -275,38 +284,85 @@ __device__ void epilogue_role(const IndexerArgs& a, const Range& g, Misc& ms, ui
     float s = 0.f;
 #pragma unroll
     for (int h = 0; h < kHI; ++h) s = fmaf(w[h], fmaxf(v[h], 0.f), s);
-    const int32_t e = (g.t0 + i) * kTile + et, j = e / kRowsPerBlock - blk0;
-    // an unmapped block (reported when the table was cached) scores 0
-    if (e < g.n) out[e] = (j >= 0 && j < kTblMax && ms.tbl[j] >= 0) ? s : 0.f;
+    const int32_t e = (g.t0 + i) * kTile + et, j = 2 * i + et / kRowsPerBlock;
+    if (e < g.n) {
+      const float sc = (j < kTblMax && ms.tbl[j] >= 0) ? s : -INFINITY;
+      if (a.sel_k > 0)
+        keys[padded(i * kTile + et)] = order_key(sc);
+      else
+        out[e] = sc;
+    }
   }
 }
 
+template <bool kFp4>
 __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(const __grid_constant__ IndexerArgs a) {
+  using P = Plan<kFp4>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Misc& ms = *reinterpret_cast<Misc*>(smem + kOffMisc);
+  Misc& ms = *reinterpret_cast<Misc*>(smem + P::kOffMisc);
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int r = blockIdx.x;
-  const Range g = row_range(a, r);
+  pdl_trigger();
+
+  // the CTA's row and tile range
+  if (a.sel_k > 0) {
+    DealShared& ds = *reinterpret_cast<DealShared*>(smem + P::kOffStage);
+    if (warp == 0) deal_compute(a.pos, a.n_rows, a.ratio, a.window, a.max_n, gridDim.x, ds);
+    __syncthreads();
+    if (tid == 0) {
+      const DealSlot sl = deal_slot(ds, a.n_rows, blockIdx.x);
+      ms.row = sl.row;
+      ms.t0 = sl.t0;
+      ms.nt = sl.nt;
+    }
+  } else if (tid == 0) {
+    // one row per blockIdx.x, its tiles split in equal parts over gridDim.y
+    const int r = blockIdx.x;
+    const int32_t tiles = deal_row_tiles(a.pos, r, a.ratio, a.window, a.max_n);
+    const int32_t per = (tiles + gridDim.y - 1) / gridDim.y;
+    ms.row = r;
+    ms.t0 = min(tiles, (int32_t)blockIdx.y * per);
+    ms.nt = min(tiles, ms.t0 + per) - ms.t0;
+  }
+  __syncthreads();
+  Range g;
+  g.row = ms.row;
+  g.t0 = ms.t0;
+  g.nt = ms.nt;
+  if (g.row < 0) return;  // a CTA the deal left without work
+  if (a.sel_k > 0 && g.nt > P::kCapTiles) {  // the launcher's bound rules this out; never overrun the key store
+    if (tid == 0) record_error(a.err, CSA_ERR_DEVICE_BOUNDS);
+    g.nt = P::kCapTiles;
+  }
+  g.seq = a.seq_id[g.row];
+  g.n = n_visible(a.pos[g.row], a.ratio, a.window);
+  if (g.n > a.max_n) {
+    if (tid == 0 && (a.sel_k > 0 ? g.t0 == 0 : blockIdx.y == 0)) record_error(a.err, CSA_ERR_DEVICE_BOUNDS);
+    g.n = a.max_n;
+  }
 
   if (tid == 0) {
-    const bool tma = a.k_tma && a.cache.dtype == CSA_BF16;
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&ms.full[s], tma ? 1 : kProd);
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&ms.full[s], kFp4 ? kConvThreads : 1);
       mbar_init(&ms.empty[s], 1);
+    }
+    for (int s = 0; s < 6; ++s) {
+      mbar_init(&ms.raw_full[s], 1);
+      mbar_init(&ms.raw_empty[s], kConvThreads);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&ms.tfull[b], 1);
       mbar_init(&ms.tempty[b], kEpi);
     }
+    mbar_init(&ms.mma_done, 1);
     mbar_init_fence();
     ms.abort = 0;
   }
-  if (tid < kHI) ms.w[tid] = a.w[(int64_t)r * kHI + tid];
+  if (tid < kHI) ms.w[tid] = a.w[(int64_t)g.row * kHI + tid];
   {
     // block-table slice of the CTA's entry range
-    const int32_t blk0 = g.t0 * kTile / kRowsPerBlock;
-    const int32_t nblk = min(kTblMax, (g.nt * kTile + kRowsPerBlock - 1) / kRowsPerBlock);
+    const int32_t blk0 = g.t0 * (kTile / kRowsPerBlock);
+    const int32_t nblk = min(kTblMax, g.nt * (kTile / kRowsPerBlock));
     for (int j = tid; j < nblk; j += kThreads) {
       const int32_t lb = blk0 + j;
       int32_t pb = -1;
@@ -328,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(const __grid_co
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
       const int x = min(tid + u * kThreads, kPieces - 1);  // clamped; stored below only when in range
-      const int64_t qb = (int64_t)r * kHI * kDI + 8 * x;
+      const int64_t qb = (int64_t)g.row * kHI * kDI + 8 * x;
       if (a.q_dtype == CSA_BF16) {
         const uint4 v = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q_idx) + qb));
         w[u][0] = v.x; w[u][1] = v.y; w[u][2] = v.z; w[u][3] = v.w;
@@ -346,24 +402,31 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(const __grid_co
       const int x = tid + u * kThreads;
       if (x >= kPieces) break;
       const int h = x / (kDI / 8), d0 = 8 * (x % (kDI / 8));
-      *reinterpret_cast<uint4*>(smem + kOffQ + sw128_offset(h, d0, kHI)) = make_uint4(w[u][0], w[u][1], w[u][2], w[u][3]);
+      *reinterpret_cast<uint4*>(smem + P::kOffQ + sw128_offset(h, d0, kHI)) =
+          make_uint4(w[u][0], w[u][1], w[u][2], w[u][3]);
     }
   }
   fence_proxy_async();
-  pdl_trigger();
-  pdl_wait();  // caches and the score scratch may be in use by the previous launch until here
+  pdl_wait();  // the score scratch and candidate lists may be in use by the previous launch until here
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ms.tmem_base;
 
   if (warp < 4) {
-    epilogue_role(a, g, ms, tmem, tid);
+    epilogue_role<kFp4>(a, g, smem, ms, tmem, tid);
   } else if (warp < kMmaWarp) {
-    if (!(a.k_tma && a.cache.dtype == CSA_BF16)) producer_role(a, g, smem, ms, tid - kEpi);
-    else if (tid == kEpi) producer_tma(a, g, smem, ms);
+    if constexpr (!kFp4) {
+      if (tid == kEpi) producer_bf16<kFp4>(a, g, smem, ms);
+    } else {
+      if (warp == kEpi / 32) {
+        if (tid == kEpi) producer_raw<kFp4>(a, g, smem, ms);
+      } else {
+        converter<kFp4>(a, g, smem, ms, tid - kEpi - 32);
+      }
+    }
   } else if ((tid & 31) == 0) {
-    mma_role(a, g, smem, ms, tmem);
+    mma_role<kFp4>(a, g, smem, ms, tmem);
   }
   tc_fence_before();
   __syncthreads();
@@ -371,41 +434,99 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(const __grid_co
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  if (a.sel_k <= 0) return;
+
+  // fused selection: the top-sel_k of the range's scores, in entry order of
+  // equal scores, as this CTA's candidate list (the stage ring is drained: every
+  // load landed before its MMA, every MMA completed before its scores were read)
+  const int32_t e0 = g.t0 * kTile;
+  const int n_local = max(0, min(g.n, (g.t0 + g.nt) * kTile) - e0);
+  const uint32_t* keys = reinterpret_cast<const uint32_t*>(smem + P::kOffKeys);
+  SelectScratch& sc = *reinterpret_cast<SelectScratch*>(smem + P::kOffStage);
+  const int64_t cta = blockIdx.x;
+  uint32_t* ck = a.cand_key + cta * a.sel_k;
+  int32_t* ci = a.cand_idx + cta * a.sel_k;
+  block_select<kThreads>(keys, n_local, a.sel_k, sc, [&](int pos, uint32_t rank) {
+    ck[rank] = keys[padded(pos)];
+    ci[rank] = e0 + pos;
+  });
+  if (tid == 0) a.cand_cnt[cta] = min(n_local, a.sel_k);
 }
 
 }  // namespace
 
-bool indexer_tc_eligible(const IndexerArgs& a) {
-  return a.heads == kHI && a.dim == kDI && a.cache.rows_per_block == kRowsPerBlock &&
-         (a.cache.dtype == CSA_BF16 || a.cache.dtype == CSA_E2M1);
+int32_t indexer_deal_capacity(int32_t cache_dtype) {
+  if (cache_dtype == CSA_BF16) return Plan<false>::kCapTiles;
+  if (cache_dtype == CSA_E2M1) return Plan<true>::kCapTiles;
+  return 0;
 }
 
-cudaError_t launch_indexer_tc(const IndexerArgs& args, int32_t n_rows, cudaStream_t s) {
+int32_t indexer_deal_bound(int32_t n_rows, int32_t max_n, int32_t G) {
+  if (n_rows <= 0 || n_rows >= G || n_rows > kDealMaxRows) return -1;
+  // the device picks the smallest feasible budget; ceil(T / (G - n_rows)) is
+  // always feasible (sum_r ceil(t_r / B) <= T / B + n_rows) and T <= n_rows * tiles(max_n)
+  const int64_t tiles = (max_n + kTile - 1) / kTile;
+  const int64_t T = (int64_t)n_rows * tiles;
+  const int64_t B = (T + (G - n_rows) - 1) / (G - n_rows);
+  return (int32_t)(B < tiles ? B : tiles);
+}
+
+size_t deal_candidate_bytes(int32_t G, int32_t k) {
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  return 2 * up((size_t)G * k * 4) + up((size_t)G * 4);
+}
+
+DealCandidates deal_candidates(void* base, int32_t G, int32_t k) {
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  uint8_t* p = reinterpret_cast<uint8_t*>(base);
+  DealCandidates c;
+  c.key = reinterpret_cast<uint32_t*>(p);
+  c.idx = reinterpret_cast<int32_t*>(p + up((size_t)G * k * 4));
+  c.cnt = reinterpret_cast<int32_t*>(p + 2 * up((size_t)G * k * 4));
+  c.ctas = G;
+  return c;
+}
+
+bool indexer_tc_eligible(const IndexerArgs& a) {
+  const uintptr_t d = reinterpret_cast<uintptr_t>(a.cache.data), s = reinterpret_cast<uintptr_t>(a.cache.scales);
+  return a.heads == kHI && a.dim == kDI && a.cache.rows_per_block == kRowsPerBlock &&
+         ((a.cache.dtype == CSA_BF16 && d % 16 == 0) || (a.cache.dtype == CSA_E2M1 && d % 16 == 0 && s % 16 == 0));
+}
+
+template <bool kFp4>
+static cudaError_t launch_indexer_tc_t(const IndexerArgs& args, int32_t n_rows, int32_t G, cudaStream_t s) {
   static PerDevice attrs;
   cudaError_t e = with_device_slot(attrs, [](int, int64_t& done) {
     if (done) return cudaSuccess;
-    const cudaError_t r =
-        cudaFuncSetAttribute(indexer_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    const cudaError_t r = cudaFuncSetAttribute(indexer_tc_kernel<kFp4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)smem_bytes<kFp4>());
     if (r == cudaSuccess) done = 1;
     return r;
   });
   if (e != cudaSuccess) return e;
-  int n_sm = 0;
-  if ((e = sm_count(&n_sm)) != cudaSuccess) return e;
   IndexerArgs a = args;
-  a.k_tma = a.cache.dtype == CSA_BF16 &&
-            encode_bf16_map(&a.k_map, a.cache.data, kDI, (uint64_t)a.cache.num_blocks * kRowsPerBlock, kDI * 2,
-                            64, kRowsPerBlock);
+  a.n_rows = n_rows;
+  if (!kFp4 && !encode_bf16_map(&a.k_map, a.cache.data, kDI, (uint64_t)a.cache.num_blocks * kRowsPerBlock, kDI * 2,
+                                64, kRowsPerBlock))
+    return cudaErrorInvalidValue;
+  if (a.sel_k > 0) return launch_k(indexer_tc_kernel<kFp4>, dim3(G), dim3(kThreads), smem_bytes<kFp4>(), s,
+                                   kStreamOrder, 0, a);
   const int32_t tiles = (a.max_n + kTile - 1) / kTile;
   // one CTA per SM: as many splits per row as fit in a single wave
-  int32_t splits = n_rows > 0 ? n_sm / n_rows : 1;
+  int32_t splits = n_rows > 0 ? G / n_rows : 1;
   if (splits > tiles) splits = tiles;
   // every CTA's range must fit the cached block-table slice (kTblMax blocks)
   const int32_t tiles_per_cta_max = kTblMax * kRowsPerBlock / kTile;
   const int32_t min_splits = (tiles + tiles_per_cta_max - 1) / tiles_per_cta_max;
   if (splits < min_splits) splits = min_splits;
   if (splits < 1) splits = 1;
-  return launch_k(indexer_tc_kernel, dim3(n_rows, splits), dim3(kThreads), kSmemBytes, s, kStreamOrder, 0, a);
+  return launch_k(indexer_tc_kernel<kFp4>, dim3(n_rows, splits), dim3(kThreads), smem_bytes<kFp4>(), s,
+                  kStreamOrder, 0, a);
+}
+
+cudaError_t launch_indexer_tc(const IndexerArgs& a, int32_t n_rows, int32_t G, cudaStream_t s) {
+  return a.cache.dtype == CSA_E2M1 ? launch_indexer_tc_t<true>(a, n_rows, G, s)
+                                   : launch_indexer_tc_t<false>(a, n_rows, G, s);
 }
 
 }  // namespace csa

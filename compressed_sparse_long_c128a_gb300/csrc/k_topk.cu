@@ -1,40 +1,162 @@
 // DSA top-k: the min(k, n) largest indexer scores of each row, equal scores
 // going to the lower entry index ("vLLM解密：DeepSeek-V4本地部署為何如此困難"
-// §二 item 3: k = 512 on c4a).
+// §二 item 3: k = 512 on c4a).  The radix select itself is in select.cuh.
 //
-// Exact radix select on an order-preserving 32-bit key of the fp32 score:
-// histogram passes over the key's bits (11, 11, 10) fix the k-th largest key T
-// and how many entries equal to T are still needed; a last pass in index order
-// takes every entry above T and the lowest-indexed entries equal to T.
-//
-// Scores are cut into chunks of 16384 held in shared memory by a 1024-thread
-// CTA.  A row of one chunk is selected and written out directly.  Longer rows
-// take two stages: (1) every chunk writes its own top-k as (key, index)
-// candidates in index order; (2) one CTA per row selects the top-k of the
-// row's candidates, which are in index order chunk after chunk, so ties still
-// resolve to the lower entry index.  The global top-k is a subset of the union
-// of the chunks' top-k sets because the order is total.  Rows whose candidates
-// would not fit in shared memory fall back to one CTA scanning the row.
+// Three ways in, by how the indexer left its results:
+//   * candidates of a balanced deal (decode batches): the indexer CTAs selected
+//     the top-k of their own tile ranges; topk_deal_merge_kernel merges each
+//     row's candidate lists (in entry order, so ties still go to the lower index).
+//   * a score row of at most 16384 entries (or several chunks of that size):
+//     topk_chunk_kernel selects each chunk in shared memory, writing the row's
+//     result directly when it is one chunk, else per-chunk candidates that
+//     topk_merge_kernel merges.  The global top-k is a subset of the union of
+//     the chunks' top-k sets because the order is total.
+//   * rows whose candidates would not fit in shared memory: topk_kernel, one
+//     CTA streaming the row's scores.
 
-#include "csa_kernels.h"
+#include "select.cuh"
 
 namespace csa {
 namespace {
 
-constexpr int kThreads = 1024;
-constexpr int kWarps = kThreads / 32;
+// ------------------------------------------------------------------ selection streamed from global memory
 
-__device__ __forceinline__ uint32_t order_key(float f) {
-  const uint32_t u = __float_as_uint(f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+struct StreamScratch {
+  uint32_t hist[4096];
+  uint32_t warp_cnt[32];
+  uint32_t digit, rem, eq_base, total;
+  int out_ctr;
+};
+
+// Exact top-min(k, V') of the V' valid keys among positions v in [0, V), read
+// through keyf(v, &key) -> valid, by one block of NT threads: three histogram
+// passes (12, 12, 8 bits) over the keys in L2, then one pass in position order.
+// out(v, slot) receives every selected v at a distinct slot in [0, kk): the keys
+// above the k-th key first, then those equal to it, each in position order;
+// returns kk.
+template <int NT, typename KeyFn, typename Out>
+__device__ int stream_select(int V, int k, KeyFn keyf, Out out, StreamScratch& ss) {
+  constexpr int kWarps = NT / 32;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    ss.total = 0;
+    ss.out_ctr = 0;
+    ss.eq_base = 0;
+  }
+  __syncthreads();
+  uint32_t cnt = 0;
+  for (int v = threadIdx.x; v < V; v += NT) {
+    uint32_t key;
+    cnt += keyf(v, key) ? 1u : 0u;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+  if (lane == 0) atomicAdd(&ss.total, cnt);
+  __syncthreads();
+  const int total = (int)ss.total;
+  const int kk = total < k ? total : k;
+  if (kk == total) {  // every valid key is selected: compact in position order
+    for (int v0 = 0; v0 < V; v0 += NT) {
+      const int v = v0 + threadIdx.x;
+      uint32_t key;
+      const bool ok = v < V && keyf(v, key);
+      const uint32_t bal = __ballot_sync(0xffffffffu, ok);
+      if (lane == 0) ss.warp_cnt[wid] = __popc(bal);
+      __syncthreads();
+      uint32_t off = 0, tot = 0;
+      for (int w = 0; w < kWarps; ++w) {
+        off += w < wid ? ss.warp_cnt[w] : 0u;
+        tot += ss.warp_cnt[w];
+      }
+      if (ok) out(v, (int)(ss.eq_base + off + __popc(bal & ((1u << lane) - 1u))));
+      __syncthreads();
+      if (threadIdx.x == 0) ss.eq_base += tot;
+      __syncthreads();
+    }
+    return kk;
+  }
+  uint32_t prefix = 0, mask = 0, rem = (uint32_t)kk;
+  const int shifts[3] = {20, 8, 0};
+  const int widths[3] = {12, 12, 8};
+  for (int pass = 0; pass < 3; ++pass) {
+    const int sh = shifts[pass], nb = 1 << widths[pass];
+    for (int b = threadIdx.x; b < nb; b += NT) ss.hist[b] = 0;
+    __syncthreads();
+    for (int v = threadIdx.x; v < V; v += NT) {
+      uint32_t key;
+      if (keyf(v, key) && (key & mask) == prefix) atomicAdd(&ss.hist[(key >> sh) & (nb - 1)], 1u);
+    }
+    __syncthreads();
+    if (wid == 0) {
+      const int per = nb / 32;
+      const int hi = nb - lane * per;  // this lane owns buckets [hi-per, hi), scanned downwards
+      uint32_t ls = 0;
+      for (int b = hi - 1; b >= hi - per; --b) ls += ss.hist[b];
+      uint32_t inc = ls;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+      }
+      const uint32_t exc = inc - ls;
+      if (exc < rem && rem <= inc) {
+        uint32_t cum = exc;
+        for (int b = hi - 1; b >= hi - per; --b) {
+          const uint32_t h = ss.hist[b];
+          if (cum + h >= rem) {
+            ss.digit = (uint32_t)b;
+            ss.rem = rem - cum;
+            break;
+          }
+          cum += h;
+        }
+      }
+    }
+    __syncthreads();
+    prefix |= ss.digit << sh;
+    mask |= (uint32_t)(nb - 1) << sh;
+    rem = ss.rem;
+    __syncthreads();
+  }
+  // keys above T go to slots [0, n_gt) and the first `rem` keys equal to T to
+  // [n_gt, kk), each group in position order (a deterministic output order)
+  const uint32_t T = prefix;
+  const uint32_t n_gt = (uint32_t)kk - rem;
+  for (int v0 = 0; v0 < V; v0 += NT) {
+    const int v = v0 + threadIdx.x;
+    uint32_t key = 0;
+    const bool ok = v < V && keyf(v, key);
+    const bool gt = ok && key > T, eq = ok && key == T;
+    const uint32_t bg = __ballot_sync(0xffffffffu, gt), be = __ballot_sync(0xffffffffu, eq);
+    if (lane == 0) ss.warp_cnt[wid] = __popc(bg) | ((uint32_t)__popc(be) << 16);
+    __syncthreads();
+    uint32_t off_g = 0, off_e = 0, tot_g = 0, tot_e = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      const uint32_t c = ss.warp_cnt[w];
+      off_g += w < wid ? (c & 0xFFFF) : 0u;
+      off_e += w < wid ? (c >> 16) : 0u;
+      tot_g += c & 0xFFFF;
+      tot_e += c >> 16;
+    }
+    const uint32_t below = (1u << lane) - 1u;
+    if (gt) out(v, (int)(ss.out_ctr + off_g + __popc(bg & below)));
+    const uint32_t rank = ss.eq_base + off_e + __popc(be & below);
+    if (eq && rank < rem) out(v, (int)(n_gt + rank));
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      ss.out_ctr += (int)tot_g;
+      ss.eq_base += tot_e;
+    }
+    __syncthreads();
+  }
+  return kk;
 }
 
-__global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
-  __shared__ uint32_t hist[4096];
-  __shared__ uint32_t warp_cnt[kWarps];
-  __shared__ uint32_t sh_digit, sh_rem, sh_eq_base;
-  __shared__ int out_ctr;
+constexpr int kThreads = 1024;
 
+// One CTA per row streaming the row's scores (rows too long for the chunked path).
+__global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
+  __shared__ StreamScratch ss;
   pdl_trigger();
   pdl_wait();
   const int r = blockIdx.x;
@@ -45,217 +167,47 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
   }
   const float* s = a.scores + (int64_t)r * a.max_n;
   int32_t* out = a.out + (int64_t)r * a.k;
-  const int kk = n < a.k ? n : a.k;
+  const int kk = stream_select<kThreads>(
+      n, a.k,
+      [&](int v, uint32_t& key) {
+        key = order_key(s[v]);
+        return true;
+      },
+      [&](int v, int slot) { out[slot] = v; }, ss);
   for (int i = kk + threadIdx.x; i < a.k; i += kThreads) out[i] = -1;
-  if (kk == n) {  // every visible entry is selected
-    for (int i = threadIdx.x; i < n; i += kThreads) out[i] = i;
-    return;
-  }
-
-  uint32_t prefix = 0, mask = 0, rem = (uint32_t)kk;
-  const int shifts[3] = {20, 8, 0};
-  const int widths[3] = {12, 12, 8};
-  for (int pass = 0; pass < 3; ++pass) {
-    const int sh = shifts[pass];
-    const int nb = 1 << widths[pass];
-    for (int b = threadIdx.x; b < nb; b += kThreads) hist[b] = 0;
-    __syncthreads();
-    for (int i = threadIdx.x; i < n; i += kThreads) {
-      const uint32_t key = order_key(s[i]);
-      if ((key & mask) == prefix) atomicAdd(&hist[(key >> sh) & (nb - 1)], 1u);
-    }
-    __syncthreads();
-    if (threadIdx.x < 32) {
-      const int lane = threadIdx.x;
-      const int per = nb / 32;
-      const int hi = nb - lane * per;  // this lane owns buckets [hi-per, hi), scanned downwards
-      uint32_t ls = 0;
-      for (int b = hi - 1; b >= hi - per; --b) ls += hist[b];
-      uint32_t inc = ls;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += v;
-      }
-      const uint32_t exc = inc - ls;
-      if (exc < rem && rem <= inc) {
-        uint32_t cum = exc;
-        for (int b = hi - 1; b >= hi - per; --b) {
-          const uint32_t h = hist[b];
-          if (cum + h >= rem) {
-            sh_digit = (uint32_t)b;
-            sh_rem = rem - cum;
-            break;
-          }
-          cum += h;
-        }
-      }
-    }
-    __syncthreads();
-    prefix |= sh_digit << sh;
-    mask |= (uint32_t)(nb - 1) << sh;
-    rem = sh_rem;
-    __syncthreads();
-  }
-
-  const uint32_t T = prefix;
-  const uint32_t n_gt = (uint32_t)kk - rem;
-  if (threadIdx.x == 0) {
-    out_ctr = 0;
-    sh_eq_base = 0;
-  }
-  __syncthreads();
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  for (int c0 = 0; c0 < n; c0 += kThreads) {
-    const int i = c0 + threadIdx.x;
-    const uint32_t key = i < n ? order_key(s[i]) : 0u;
-    const bool gt = i < n && key > T;
-    const bool eq = i < n && key == T;
-    if (gt) out[atomicAdd(&out_ctr, 1)] = i;
-    const uint32_t bal = __ballot_sync(0xffffffffu, eq);
-    if (lane == 0) warp_cnt[wid] = __popc(bal);
-    __syncthreads();
-    uint32_t off = 0, tot = 0;
-    for (int w = 0; w < kWarps; ++w) {
-      const uint32_t c = warp_cnt[w];
-      off += w < wid ? c : 0u;
-      tot += c;
-    }
-    const uint32_t rank = sh_eq_base + off + __popc(bal & ((1u << lane) - 1u));
-    if (eq && rank < rem) out[n_gt + rank] = i;
-    __syncthreads();
-    if (threadIdx.x == 0) sh_eq_base += tot;
-    __syncthreads();
-  }
 }
 
-// ------------------------------------------------------------------ two-stage select
+// ------------------------------------------------------------------ merge of a balanced deal's candidates
 
-// Exclusive prefix sum of v over the block; `total` receives the block sum.
-template <int NT>
-__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* wsum, uint32_t& total) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  uint32_t x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) wsum[wid] = x;
+constexpr int kDealMergeThreads = 512;
+
+// Row r: the candidate lists of its CTAs under the deal (each in entry order,
+// the CTAs' ranges ascending) merged into the row's top-k.
+__global__ void __launch_bounds__(kDealMergeThreads) topk_deal_merge_kernel(const TopkArgs a,
+                                                                            const uint32_t* cand_key,
+                                                                            const int32_t* cand_idx,
+                                                                            const int32_t* cand_cnt, int n_rows,
+                                                                            int G) {
+  __shared__ DealShared ds;
+  __shared__ StreamScratch ss;
+  pdl_trigger();
+  if (threadIdx.x < 32) deal_compute(a.pos, n_rows, a.ratio, a.window, a.max_n, G, ds);
+  pdl_wait();  // the candidates are complete only after the indexer launch
   __syncthreads();
-  if (wid == 0) {
-    uint32_t t = lane < NT / 32 ? wsum[lane] : 0u;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, t, o);
-      if (lane >= o) t += y;
-    }
-    if (lane < NT / 32) wsum[lane] = t;
-  }
-  __syncthreads();
-  const uint32_t base = wid ? wsum[wid - 1] : 0u;
-  total = wsum[NT / 32 - 1];
-  __syncthreads();
-  return base + x - v;
-}
-
-// Shared-memory key arrays are padded by one word per 32 (key i at i + i/32), so
-// that thread t reading element t*seg + j (a contiguous segment per thread, seg
-// = 16) hits 32 distinct banks.
-__device__ __forceinline__ int padded(int i) { return i + (i >> 5); }
-__host__ __device__ constexpr int padded_size(int n) { return n + (n >> 5) + 1; }
-
-// Histogram of digit (key >> sh) & (nb-1) over the keys matching prefix/mask.
-// With `aggregate`, lanes with the same digit are combined before the
-// shared-memory atomic (the leading digits of positive scores fall into a
-// handful of buckets; later passes see only the keys under the chosen prefix).
-template <int NT>
-__device__ __forceinline__ void digit_hist(const uint32_t* keys, int n, uint32_t prefix, uint32_t mask, int sh,
-                                           int nb, uint32_t* hist, bool aggregate) {
-  const int lane = threadIdx.x & 31;
-  for (int i0 = 0; i0 < n; i0 += NT) {
-    const int i = i0 + threadIdx.x;
-    const uint32_t key = i < n ? keys[padded(i)] : 0u;
-    const bool in = i < n && (key & mask) == prefix;
-    const uint32_t d = in ? (key >> sh) & (uint32_t)(nb - 1) : 0xFFFFFFFFu;
-    if (aggregate) {
-      const uint32_t peers = __match_any_sync(0xffffffffu, d);
-      if (in && lane == __ffs(peers) - 1) atomicAdd(&hist[d], (uint32_t)__popc(peers));
-    } else if (in) {
-      atomicAdd(&hist[d], 1u);
-    }
-  }
-}
-
-// Top min(k, n) of keys[0..n) (shared memory, padded as above, larger key =
-// better, equal keys: lower position first).  Calls emit(position, rank) for
-// every selected position, ranks 0.. in increasing position order.  Whole block.
-template <int NT, typename Emit>
-__device__ void block_select(const uint32_t* keys, int n, int k, Emit emit) {
-  __shared__ uint32_t hist[2048];
-  __shared__ uint32_t wsum[NT / 32];
-  __shared__ uint32_t sh_digit, sh_rem;
-  const int kk = n < k ? n : k;
-  if (kk == n) {
-    for (int i = threadIdx.x; i < n; i += NT) emit(i, (uint32_t)i);
-    return;
-  }
-  uint32_t prefix = 0, mask = 0, rem = (uint32_t)kk;
-  const int shifts[3] = {21, 10, 0};
-  const int widths[3] = {11, 11, 10};
-  for (int pass = 0; pass < 3; ++pass) {
-    const int sh = shifts[pass], nb = 1 << widths[pass];
-    for (int b = threadIdx.x; b < nb; b += NT) hist[b] = 0;
-    __syncthreads();
-    digit_hist<NT>(keys, n, prefix, mask, sh, nb, hist, pass == 0);
-    __syncthreads();
-    // the digit d with count(> d) < rem <= count(>= d): thread t owns buckets
-    // [nb - (t+1)*bpt, nb - t*bpt), scanned from the top
-    const int bpt = (nb + NT - 1) / NT, top = nb - threadIdx.x * bpt;
-    uint32_t local = 0;
-    for (int j = 0; j < bpt; ++j)
-      if (top - 1 - j >= 0) local += hist[top - 1 - j];
-    uint32_t tot;
-    const uint32_t above = block_excl_scan<NT>(local, wsum, tot);
-    if (above < rem && rem <= above + local) {
-      uint32_t cum = above;
-      for (int j = 0; j < bpt; ++j) {
-        const uint32_t h = hist[top - 1 - j];
-        if (cum + h >= rem) {
-          sh_digit = (uint32_t)(top - 1 - j);
-          sh_rem = rem - cum;
-          break;
-        }
-        cum += h;
-      }
-    }
-    __syncthreads();
-    prefix |= sh_digit << sh;
-    mask |= (uint32_t)(nb - 1) << sh;
-    rem = sh_rem;
-    __syncthreads();
-  }
-  // every key above T, and the first `rem` keys equal to T in position order.
-  // Thread t owns the contiguous segment [t*seg, t*seg+seg): one scan ranks the
-  // equal keys, one more places the selected ones.
-  const uint32_t T = prefix;
-  const int seg = (n + NT - 1) / NT;
-  const int lo = threadIdx.x * seg, hi = min(n, lo + seg);
-  uint32_t n_gt = 0, n_eq = 0;
-  for (int i = lo; i < hi; ++i) {
-    const uint32_t key = keys[padded(i)];
-    n_gt += key > T;
-    n_eq += key == T;
-  }
-  uint32_t tot;
-  const uint32_t eq0 = block_excl_scan<NT>(n_eq, wsum, tot);
-  const uint32_t take_eq = eq0 >= rem ? 0u : min(n_eq, rem - eq0);
-  uint32_t rank = block_excl_scan<NT>(n_gt + take_eq, wsum, tot);
-  uint32_t eq_seen = 0;
-  for (int i = lo; i < hi; ++i) {
-    const uint32_t key = keys[padded(i)];
-    if (key > T || (key == T && eq_seen++ < take_eq)) emit(i, rank++);
-  }
+  const int r = blockIdx.x;
+  const int first = ds.first[r], ctas = ds.ctas[r];
+  const int K = a.k;
+  int32_t* out = a.out + (int64_t)r * K;
+  const int kk = stream_select<kDealMergeThreads>(
+      ctas * K, K,
+      [&](int v, uint32_t& key) {
+        const int c = first + v / K, i = v % K;
+        if (i >= cand_cnt[c]) return false;
+        key = cand_key[(int64_t)c * K + i];
+        return true;
+      },
+      [&](int v, int slot) { out[slot] = cand_idx[(int64_t)(first + v / K) * K + v % K]; }, ss);
+  for (int i = kk + threadIdx.x; i < K; i += kDealMergeThreads) out[i] = -1;
 }
 
 constexpr int kChunk = 16384;
@@ -270,6 +222,7 @@ __global__ void __launch_bounds__(kChunkThreads) topk_chunk_kernel(const TopkArg
                                                                     int32_t* cand_idx, int32_t* cand_cnt,
                                                                     int n_chunks) {
   extern __shared__ uint32_t keys[];  // padded_size(kChunk)
+  __shared__ SelectScratch sc;
   pdl_trigger();
   pdl_wait();
   const int r = blockIdx.x, c = blockIdx.y;
@@ -305,12 +258,12 @@ __global__ void __launch_bounds__(kChunkThreads) topk_chunk_kernel(const TopkArg
   }
   __syncthreads();
   if (final_out) {
-    block_select<kChunkThreads>(keys, len, a.k, [&](int pos, uint32_t rank) { out[rank] = pos; });
+    block_select<kChunkThreads>(keys, len, a.k, sc, [&](int pos, uint32_t rank) { out[rank] = pos; });
     return;
   }
   uint32_t* ok = cand_key + slot * a.k;
   int32_t* oi = cand_idx + slot * a.k;
-  block_select<kChunkThreads>(keys, len, a.k, [&](int pos, uint32_t rank) {
+  block_select<kChunkThreads>(keys, len, a.k, sc, [&](int pos, uint32_t rank) {
     ok[rank] = keys[padded(pos)];
     oi[rank] = lo + pos;
   });
@@ -325,6 +278,7 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(const TopkArg
   uint32_t* keys = msm;                                             // padded_size(cap)
   int32_t* idx = reinterpret_cast<int32_t*>(msm + padded_size(cap));  // [cap]
   __shared__ int32_t off[65];
+  __shared__ SelectScratch sc;
   pdl_trigger();
   pdl_wait();
   const int r = blockIdx.x;
@@ -348,7 +302,7 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(const TopkArg
   }
   __syncthreads();
   int32_t* out = a.out + (int64_t)r * a.k;
-  block_select<kMergeThreads>(keys, total, a.k, [&](int pos, uint32_t rank) { out[rank] = idx[pos]; });
+  block_select<kMergeThreads>(keys, total, a.k, sc, [&](int pos, uint32_t rank) { out[rank] = idx[pos]; });
   const int kk = total < a.k ? total : a.k;
   for (int i = kk + threadIdx.x; i < a.k; i += kMergeThreads) out[i] = -1;
 }
@@ -411,6 +365,12 @@ cudaError_t launch_topk(const TopkArgs& a, int32_t n_rows, void* cand, cudaStrea
   return launch_k(topk_merge_kernel, dim3(n_rows), dim3(kMergeThreads), smem, s, kAfterOwnKernel, 0, a,
                   (const uint32_t*)ck,
                   (const int32_t*)ci, (const int32_t*)cc, nc);
+}
+
+cudaError_t launch_topk_deal_merge(const TopkArgs& a, int32_t n_rows, const DealCandidates& c, cudaStream_t s) {
+  if (n_rows == 0 || a.k == 0) return cudaSuccess;
+  return launch_k(topk_deal_merge_kernel, dim3(n_rows), dim3(kDealMergeThreads), 0, s, kAfterOwnKernel, 0, a,
+                  (const uint32_t*)c.key, (const int32_t*)c.idx, (const int32_t*)c.cnt, (int)n_rows, (int)c.ctas);
 }
 
 }  // namespace csa

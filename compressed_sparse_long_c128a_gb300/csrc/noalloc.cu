@@ -72,7 +72,8 @@ int csa_indexer_topk_noalloc(const void* q_idx, int32_t q_dtype, const float* w,
   const int32_t size_n = max_n > 0 ? max_n : 1;
   const size_t score_bytes = align256(sizeof(float) * (size_t)n_rows * size_n);
   const size_t cand_bytes = align256(topk_candidate_bytes(n_rows, max_n, k));
-  if (score_bytes + cand_bytes > kScratchBytes) return CSA_ERR_WORKSPACE;
+  const size_t deal_bytes = n_rows < kDealMaxCtas ? align256(deal_candidate_bytes(kDealMaxCtas, k)) : 0;
+  if (score_bytes + cand_bytes + deal_bytes > kScratchBytes) return CSA_ERR_WORKSPACE;
 
   void* scratch = nullptr;
   const int sst = scratch_for_current_device(&scratch);
@@ -80,8 +81,9 @@ int csa_indexer_topk_noalloc(const void* q_idx, int32_t q_dtype, const float* w,
 
   float* scores = reinterpret_cast<float*>(scratch);
   void* cand = cand_bytes ? reinterpret_cast<uint8_t*>(scratch) + score_bytes : nullptr;
+  void* deal = deal_bytes ? reinterpret_cast<uint8_t*>(scratch) + score_bytes + cand_bytes : nullptr;
   return enqueue_indexer_topk(q_idx, q_dtype, w, n_rows, idx_heads, idx_dim, seq_id, pos, ratio, window, idx_cache,
-                              bt, k, max_n, out_idx, scores, cand, err, stream);
+                              bt, k, max_n, out_idx, scores, cand, deal, err, stream);
 }
 
 }  // extern "C"

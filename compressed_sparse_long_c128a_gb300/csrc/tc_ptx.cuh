@@ -176,6 +176,16 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int32_t
 }
 
 // Bulk copy (copy engine) of `bytes` (multiple of 16, both ends 16-byte
+// aligned) from global memory into this CTA's shared memory; completion is
+// signalled as transaction bytes on the mbarrier.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+// Bulk copy (copy engine) of `bytes` (multiple of 16, both ends 16-byte
 // aligned) from this CTA's shared memory to a shared::cluster address in a
 // peer CTA; completion is signalled as transaction bytes on the peer's mbarrier.
 __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, const void* src, uint32_t bytes,

@@ -69,18 +69,25 @@ typedef enum {
   CSA_F32 = 0,  /* float */
   CSA_BF16 = 1, /* bfloat16 */
   CSA_E4M3 = 2, /* fp8 e4m3 (fn) codes + one fp32 scale per row: value = code * scale */
-  CSA_E2M1 = 3  /* fp4 e2m1 codes, two per byte (element 2j in the low nibble), plus one
+  CSA_E2M1 = 3, /* fp4 e2m1 codes, two per byte (element 2j in the low nibble), plus one
                    e4m3 scale byte per 16 elements: value = code * scale */
+  CSA_E4M3R = 4 /* "partial token-wise fp8" ([部署] §二: decode reads a partial
+                   token-wise fp8 cache): per row, the first dim - tail_bf16 elements
+                   as e4m3 codes with one fp32 scale per row (amax of those elements
+                   / 448), the last tail_bf16 elements (the rotary dims) as bf16 */
 } csa_dtype;
 
 /*
  * A paged cache: `num_blocks` physical blocks of `rows_per_block` rows of `dim`
  * elements, rows packed densely:
  *   row r of block b starts at data + (b*rows_per_block + r) * row_bytes,
- *   row_bytes = dim * sizeof(element)  (E2M1: dim/2).
- * scales: E4M3: float[num_blocks*rows_per_block], one per row;
+ *   row_bytes = dim * sizeof(element)  (E2M1: dim/2; E4M3R: dim + tail_bf16,
+ *   the codes of elements [0, dim - tail_bf16) then tail_bf16 bf16 values).
+ * scales: E4M3, E4M3R: float[num_blocks*rows_per_block], one per row;
  *         E2M1: uint8 e4m3 bytes [num_blocks*rows_per_block][dim/16];
  *         F32 / BF16: unused (may be NULL).
+ * tail_bf16: E4M3R only (a multiple of 16, dim - tail_bf16 a multiple of 16);
+ *         0 for every other dtype.
  * One logical block covers 256 native positions for every kind of cache
  * ([Support] "KV Cache Memory Management", item 1): a compressed cache has
  * 256/ratio rows per block (64 for c4a, 2 for c128a); a sliding-window cache
@@ -94,6 +101,7 @@ typedef struct {
   int32_t num_blocks;
   int32_t rows_per_block;
   int32_t dim;
+  int32_t tail_bf16;
 } csa_paged;
 
 /* Logical block j of sequence s lives in physical block table[s*stride + j]; -1 = unmapped. */
@@ -139,13 +147,13 @@ typedef struct {
  *   seq_id,pos [n_tok] int32; (seq, pos) pairs must be distinct within a call
  *   bias       [window][D] float; gamma_c, gamma_swa [D] float
  *   state      dtype == in_dtype, rows_per_block 256, dim 2*D
- *   swa        F32 / BF16 / E4M3, rows_per_block 256, dim D; or NULL, with
+ *   swa        F32 / BF16 / E4M3 / E4M3R, rows_per_block 256, dim D; or NULL, with
  *              swa_bt and gamma_swa unused (may be NULL): no window rows are
  *              written.  This is the indexer-key compressor ([部署] §3.2 first
  *              fusion: the indexer K cache keeps its own compress + norm + RoPE
  *              + insert), whose keys have no sliding window.
- *   comp       F32 / BF16 / E4M3 / E2M1, rows_per_block 256/ratio, dim D.
- *              E2M1 (D % 16 == 0) quantises as csa_cache_store does.
+ *   comp       F32 / BF16 / E4M3 / E4M3R / E2M1, rows_per_block 256/ratio, dim D.
+ *              E4M3R and E2M1 (D % 16 == 0) quantise as csa_cache_store does.
  *   err        device int32 error word
  */
 CSA_API int csa_compress_insert(const csa_layer* layer, const void* kv, const void* gate, int32_t in_dtype,
@@ -165,6 +173,7 @@ CSA_API int csa_compress_insert(const csa_layer* layer, const void* kv, const vo
  * E4M3: scale = amax/448, code = e4m3_rn_satfinite(x * (448/amax)), fp32 math.
  * E2M1: per 16 elements scale = e4m3_rn(amax16/6); code = e2m1_rn_satfinite(x/scale)
  *       (a zero scale gives zero codes).
+ * E4M3R: as E4M3 over elements [0, dim - tail_bf16), the rest rounded to bf16.
  *   rows [n][cache->dim] float; seq_id, row_idx [n] int32.
  */
 CSA_API int csa_cache_store(const float* rows, int32_t n, const int32_t* seq_id, const int32_t* row_idx,
@@ -273,6 +282,11 @@ CSA_API const char* csa_status_string(int32_t status);
 
 /* Library version: major*10000 + minor*100 + patch. */
 CSA_API int32_t csa_version(void);
+
+/* Kernel launches the library has enqueued in this process so far, over all
+ * entry points and devices (a host-side count, also advanced while a stream is
+ * being captured into a CUDA graph).  For measurement; not part of the method. */
+CSA_API uint64_t csa_launch_count(void);
 
 #ifdef __cplusplus
 }

@@ -40,6 +40,9 @@ What the pages fix, and the readings taken where they leave a step open:
     (amax / 448); e2m1 with one e4m3 scale per 16 elements (amax16 / 6, rounded
     to e4m3).  The codec's rounding decisions are taken in fp32, the precision
     the kernels take them in.
+  * decode reads a "partial token-wise fp8" cache ([部署] §二).  Reading: per
+    row, e4m3 codes with one fp32 scale (amax / 448) for the non-rotary dims and
+    bf16 for the rotary dims (`quantize_rows_e4m3_rope_bf16`).
   * the indexer K cache has its own compress + RMSNorm + RoPE + insert kernel
     ([部署] §3.2, first fusion).  Reading: the same compressor (c4a stride and
     window) over the indexer's own raw streams at its dim, with its own bias and
@@ -310,6 +313,35 @@ def quantize_rows_e4m3(x):
 
 def dequantize_rows_e4m3(codes, scale) -> np.ndarray:
     return e4m3_decode(codes) * np.asarray(scale, np.float64)[..., None]
+
+
+def round_bf16(x) -> np.ndarray:
+    """Round to the nearest bfloat16 value (8 significant bits, fp32's exponent
+    range), ties to even."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, ex = np.frexp(a)  # a = f * 2^ex, f in [0.5, 1)
+    step = np.ldexp(1.0, np.maximum(ex, -125) - 8)
+    r = np.rint(a / step) * step
+    return np.where(x < 0, -r, r)
+
+
+def quantize_rows_e4m3_rope_bf16(x, rope_dim: int):
+    """The decode cache's "partial token-wise fp8" ([部署] §二: the same
+    attention kernel reads a bf16 cache in prefill and a partial token-wise fp8
+    cache in decode).  Reading: per row (token-wise), the non-rotary dims
+    [0, D-r) as e4m3 with one fp32 scale = their amax / 448 (the e4m3 row codec
+    above on those dims alone); the r rotary dims kept in bf16.  Rounding
+    decisions in fp32, as the kernels take them.
+    Returns (codes uint8 [n, D-r], scale fp32 [n], rope fp64 [n, r] holding bf16 values)."""
+    x = np.asarray(x, dtype=np.float32)
+    d = x.shape[-1]
+    codes, scale = quantize_rows_e4m3(x[..., : d - rope_dim])
+    return codes, scale, round_bf16(x[..., d - rope_dim:])
+
+
+def dequantize_rows_e4m3_rope_bf16(codes, scale, rope) -> np.ndarray:
+    return np.concatenate([dequantize_rows_e4m3(codes, scale), np.asarray(rope, np.float64)], axis=-1)
 
 
 # ============================================================ e2m1 (fp4) codec

@@ -158,13 +158,18 @@ def test_workspace_checks(lib):
 
 def test_topk_scratch_sizes(lib):
     """Rows of one 16384-entry chunk need only the score scratch; longer rows also
-    need each chunk's top-k candidates (key and index) and a count."""
+    need each chunk's top-k candidates (key and index) and a count.  Batches of
+    fewer than 256 rows may instead be dealt over up to 256 CTAs that each keep
+    a top-k candidate list (key and index) and a count."""
     def aligned(x):
         return (x + 255) // 256 * 256
 
-    assert csa.indexer_topk_workspace_size(64, 16383, 512) == aligned(64 * 16383 * 4)
-    assert csa.indexer_topk_workspace_size(64, 16384, 512) == aligned(64 * 16384 * 4)
+    deal = 2 * aligned(256 * 512 * 4) + aligned(256 * 4)
+    assert csa.indexer_topk_workspace_size(64, 16383, 512) == aligned(64 * 16383 * 4) + deal
+    assert csa.indexer_topk_workspace_size(64, 16384, 512) == aligned(64 * 16384 * 4) + deal
     n = 262143
     chunks = (n + 16383) // 16384
-    assert csa.indexer_topk_workspace_size(4, n, 512) == aligned(4 * n * 4) + aligned(4 * chunks * (512 * 8 + 4))
+    assert csa.indexer_topk_workspace_size(4, n, 512) == (aligned(4 * n * 4) + aligned(4 * chunks * (512 * 8 + 4))
+                                                          + deal)
+    assert csa.indexer_topk_workspace_size(256, 1000, 512) == aligned(256 * 1000 * 4)
     assert csa.indexer_topk_workspace_size(0, n, 512) == 0

@@ -304,7 +304,10 @@ def _assert_same(wd, a_snap, b_snap, what):
 
 
 def _run_step(wd, stream, side=None):
-    """One step on `stream` (outputs and selections poisoned first), checked for device errors."""
+    """One step on `stream` (outputs and selections poisoned first), checked for
+    device errors.  The snapshot's copies run on the current (default) stream,
+    which a torch pool stream does not wait for, so they are complete before
+    this returns: the next step's poisoning must not overtake them."""
     with torch.cuda.stream(stream):
         for ld in wd.layers:
             ld.io["out"].zero_()
@@ -313,7 +316,9 @@ def _run_step(wd, stream, side=None):
         wd.step(stream, side_stream=side)
     torch.cuda.synchronize()
     wd.check("two-stream step" if side is not None else "one-stream step")
-    return _snapshot(wd)
+    snap = _snapshot(wd)
+    torch.cuda.synchronize()
+    return snap
 
 
 def _check_against_oracle(wd, what):

@@ -432,3 +432,39 @@ def test_kv_per_sequence_at_1m_matches_pages():
     # fp8 entries (512 B + fp32 scale) and fp4 indexer keys (64 B + 8 e4m3 scales)
     q = O.kv_bytes_per_sequence(ctx, 30, 31, 512, 128, entry_bytes=516, idx_entry_bytes=72) / gib
     assert 1.8 < v4 / q < 2.4 and round(v4 / q, 2) == 2.17
+
+
+# ------------------------------------------------------------ partial token-wise fp8 (e4m3 + bf16 rotary dims)
+
+
+def test_bf16_rounding_matches_torch_cast_incl_midpoints():
+    rng = np.random.default_rng(3)
+    x = np.concatenate([rng.standard_normal(4000) * 10.0 ** rng.integers(-30, 30, 4000),
+                        np.array([1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -(1.0 + 2.0 ** -8), 2.0 ** -130, 0.0])])
+    x32 = x.astype(np.float32)
+    want = torch.from_numpy(x32).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(O.round_bf16(x32), want)
+
+
+def test_partial_fp8_keeps_rotary_dims_in_bf16_and_scales_the_rest():
+    """Rotary dims come back as their bf16 rounding whatever their size; the
+    scale is the amax of the non-rotary dims only (large rotary values must not
+    coarsen the fp8 part); the fp8 part is torch's e4m3 cast of x * 448 / amax."""
+    rng = np.random.default_rng(4)
+    D, r = 512, 64
+    x = rng.standard_normal((6, D)).astype(np.float32)
+    x[:, D - r:] *= 50.0  # rotary dims far larger than the rest
+    codes, scale, rope = O.quantize_rows_e4m3_rope_bf16(x, r)
+    assert codes.shape == (6, D - r) and rope.shape == (6, r)
+    np.testing.assert_array_equal(rope, torch.from_numpy(x[:, D - r:]).to(torch.bfloat16).double().numpy())
+    np.testing.assert_allclose(scale, np.abs(x[:, : D - r]).max(axis=1) / 448.0, rtol=1e-7)
+    y = torch.from_numpy(x[:, : D - r] * (448.0 / np.abs(x[:, : D - r]).max(axis=1, keepdims=True)))
+    want_codes = y.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(codes, want_codes)
+    back = O.dequantize_rows_e4m3_rope_bf16(codes, scale, rope)
+    assert back.shape == (6, D)
+    # the fp8 part is within half an e4m3 step of x (relative 1/16 of the value's binade)
+    err = np.abs(back[:, : D - r] - x[:, : D - r])
+    assert np.all(err <= np.abs(x[:, : D - r]) / 16 + scale[:, None] * 2.0 ** -10)
+    assert np.all(back[:, D - r:] == rope)
+
