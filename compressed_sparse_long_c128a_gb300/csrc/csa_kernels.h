@@ -156,9 +156,10 @@ struct IndexerArgs {
   // score written to `scores`
   int32_t sel_k;
   int32_t n_rows;
-  uint32_t* cand_key;  // [grid][sel_k] order-preserving keys of the scores
-  int32_t* cand_idx;   // [grid][sel_k] entry indices
+  uint32_t* cand_key;  // [grid][2 sel_k] order-preserving keys of the scores
+  int32_t* cand_idx;   // [grid][2 sel_k] entry indices
   int32_t* cand_cnt;   // [grid]
+  uint32_t* cand_thr;  // [grid] every key of the CTA's range at or above it is in its list
 };
 cudaError_t launch_indexer_scores(const IndexerArgs& a, int32_t n_rows, cudaStream_t s);
 // tensor-core scores, 64 heads x 128 dims, bf16 or e2m1 keys (k_indexer_tc.cu)
@@ -173,14 +174,16 @@ int32_t indexer_deal_bound(int32_t n_rows, int32_t max_n, int32_t G);
 // a.sel_k > 0: balanced deal on G CTAs; else one CTA per row and split
 cudaError_t launch_indexer_tc(const IndexerArgs& a, int32_t n_rows, int32_t G, cudaStream_t s);
 
-// Candidate lists of a balanced deal: G CTAs x k (key, index) pairs + counts;
+// Candidate lists of a balanced deal: G CTAs x 2k (key, index) pairs, a count
+// and a threshold each;
 // a deal uses at most kDealMaxCtas CTAs.
 constexpr int32_t kDealMaxCtas = 256;
 struct DealCandidates {
-  uint32_t* key;
-  int32_t* idx;
-  int32_t* cnt;
-  int32_t ctas;
+  uint32_t* key;  // [ctas][cap]
+  int32_t* idx;   // [ctas][cap]
+  int32_t* cnt;   // [ctas]
+  uint32_t* thr;  // [ctas]
+  int32_t ctas, cap;
 };
 size_t deal_candidate_bytes(int32_t G, int32_t k);
 DealCandidates deal_candidates(void* base, int32_t G, int32_t k);

@@ -61,7 +61,7 @@ template <bool kFp4>
 struct Plan {
   static constexpr int kStages = kFp4 ? 3 : 4;       // bf16 tiles the MMA reads
   static constexpr int kRaw = kFp4 ? 6 : 0;          // raw e2m1 tiles in flight
-  static constexpr int kCapTiles = kFp4 ? 64 : 128;  // tiles whose keys the fused selection holds
+  static constexpr int kCapTiles = kFp4 ? 64 : 112;  // tiles whose keys the fused selection holds
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffStage = kQBytes;
   static constexpr uint32_t kOffRaw = kOffStage + kStages * kStageBytes;
@@ -77,6 +77,14 @@ struct Misc {
   int32_t row, t0, nt;
   float w[kHI];
   int32_t tbl[kTblMax];  // physical blocks of the CTA's entry range (-1: unmapped / out of range)
+  uint32_t hist0[2048];  // fused selection: counts of the keys' top 11 bits, built during the loop
+};
+
+// Scratch of the selection after the loop, in the drained stage ring.
+struct PickScratch {
+  uint32_t hist1[2048];
+  uint32_t wsum[32];
+  uint32_t digit, rem, above;
 };
 
 template <bool kFp4>
@@ -84,7 +92,8 @@ constexpr uint32_t smem_bytes() {
   return Plan<kFp4>::kOffMisc + sizeof(Misc) + 1024;
 }
 static_assert(sizeof(DealShared) <= kStageBytes, "the deal is built in the idle stage ring");
-static_assert(sizeof(SelectScratch) <= kStageBytes, "the selection scratch reuses the drained stage ring");
+static_assert(sizeof(SelectScratch) + sizeof(PickScratch) <= kStageBytes,
+              "the selection scratch reuses the drained stage ring");
 static_assert(smem_bytes<false>() <= 227 * 1024 && smem_bytes<true>() <= 227 * 1024, "shared memory");
 
 __device__ __forceinline__ bool wait_or_abort(Misc& ms, uint64_t* bar, uint32_t parity, int32_t* err) {
@@ -287,10 +296,13 @@ __device__ void epilogue_role(const IndexerArgs& a, const Range& g, uint8_t* sme
     const int32_t e = (g.t0 + i) * kTile + et, j = 2 * i + et / kRowsPerBlock;
     if (e < g.n) {
       const float sc = (j < kTblMax && ms.tbl[j] >= 0) ? s : -INFINITY;
-      if (a.sel_k > 0)
-        keys[padded(i * kTile + et)] = order_key(sc);
-      else
+      if (a.sel_k > 0) {
+        const uint32_t key = order_key(sc);
+        keys[padded(i * kTile + et)] = key;
+        atomicAdd(&ms.hist0[key >> 21], 1u);
+      } else {
         out[e] = sc;
+      }
     }
   }
 }
@@ -359,6 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(const __grid_co
     ms.abort = 0;
   }
   if (tid < kHI) ms.w[tid] = a.w[(int64_t)g.row * kHI + tid];
+  for (int b = tid; b < 2048; b += kThreads) ms.hist0[b] = 0;
   {
     // block-table slice of the CTA's entry range
     const int32_t blk0 = g.t0 * (kTile / kRowsPerBlock);
@@ -436,21 +449,102 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(const __grid_co
   }
   if (a.sel_k <= 0) return;
 
-  // fused selection: the top-sel_k of the range's scores, in entry order of
-  // equal scores, as this CTA's candidate list (the stage ring is drained: every
-  // load landed before its MMA, every MMA completed before its scores were read)
+  // fused selection.  The list this CTA hands to the merge is every key of its
+  // range at or above T22, the k-th largest key with its low 10 bits cleared
+  // (a superset of the range's top-k, in entry order), with T22 itself: the
+  // merge keeps only keys at or above the largest T22 of the row's CTAs, which
+  // is at most the row's own k-th key.  Radix digits: the top 11 bits were
+  // counted during the loop; one more pass fixes the next 11.
   const int32_t e0 = g.t0 * kTile;
   const int n_local = max(0, min(g.n, (g.t0 + g.nt) * kTile) - e0);
   const uint32_t* keys = reinterpret_cast<const uint32_t*>(smem + P::kOffKeys);
-  SelectScratch& sc = *reinterpret_cast<SelectScratch*>(smem + P::kOffStage);
+  PickScratch& pk = *reinterpret_cast<PickScratch*>(smem + P::kOffStage);
+  SelectScratch& sc = *reinterpret_cast<SelectScratch*>(smem + P::kOffStage + sizeof(PickScratch));
   const int64_t cta = blockIdx.x;
-  uint32_t* ck = a.cand_key + cta * a.sel_k;
-  int32_t* ci = a.cand_idx + cta * a.sel_k;
-  block_select<kThreads>(keys, n_local, a.sel_k, sc, [&](int pos, uint32_t rank) {
-    ck[rank] = keys[padded(pos)];
-    ci[rank] = e0 + pos;
-  });
-  if (tid == 0) a.cand_cnt[cta] = min(n_local, a.sel_k);
+  const int cap = 2 * a.sel_k;  // list capacity per CTA
+  uint32_t* ck = a.cand_key + cta * cap;
+  int32_t* ci = a.cand_idx + cta * cap;
+  uint32_t T = 0;  // every key qualifies when the range has at most k of them
+  if (n_local > a.sel_k) {
+    for (int b = tid; b < 2048; b += kThreads) pk.hist1[b] = 0;
+    uint32_t rem = (uint32_t)a.sel_k, d0 = 0, d1 = 0;
+    for (int pass = 0; pass < 2; ++pass) {
+      const uint32_t* hist = pass == 0 ? ms.hist0 : pk.hist1;
+      if (pass == 1) {
+        for (int i = tid; i < n_local; i += kThreads) {
+          const uint32_t key = keys[padded(i)];
+          if ((key >> 21) == d0) atomicAdd(&pk.hist1[(key >> 10) & 2047u], 1u);
+        }
+        __syncthreads();
+      }
+      // the digit d with count(> d) < rem <= count(>= d), buckets scanned from the top
+      constexpr int kBpt = (2048 + kThreads - 1) / kThreads;
+      const int top = 2048 - tid * kBpt;
+      uint32_t local = 0;
+      for (int j = 0; j < kBpt; ++j)
+        if (top - 1 - j >= 0) local += hist[top - 1 - j];
+      uint32_t tot;
+      const uint32_t above = block_excl_scan<kThreads>(local, pk.wsum, tot);
+      if (above < rem && rem <= above + local) {
+        uint32_t cum = above;
+        for (int j = 0; j < kBpt && top - 1 - j >= 0; ++j) {
+          const uint32_t h = hist[top - 1 - j];
+          if (cum + h >= rem) {
+            pk.digit = (uint32_t)(top - 1 - j);
+            pk.rem = rem - cum;
+            break;
+          }
+          cum += h;
+        }
+      }
+      __syncthreads();
+      if (pass == 0) d0 = pk.digit;
+      else d1 = pk.digit;
+      rem = pk.rem;
+      __syncthreads();
+    }
+    T = (d0 << 21) | (d1 << 10);
+  }
+  // keys at or above T, in entry order: one count per thread segment, one scan
+  const int seg = (n_local + kThreads - 1) / kThreads;
+  const int lo = tid * seg, hi = min(n_local, lo + seg);
+  uint32_t mine = 0;
+  for (int i = lo; i < hi; ++i) mine += keys[padded(i)] >= T;
+  uint32_t total;
+  uint32_t slot = block_excl_scan<kThreads>(mine, pk.wsum, total);
+  if ((int)total <= cap) {
+    for (int i = lo; i < hi; ++i) {
+      const uint32_t key = keys[padded(i)];
+      if (key >= T) {
+        ck[slot] = key;
+        ci[slot] = e0 + i;
+        ++slot;
+      }
+    }
+    if (tid == 0) {
+      a.cand_cnt[cta] = (int32_t)total;
+      a.cand_thr[cta] = T;
+    }
+  } else {
+    // many keys tie within T's 22-bit bucket: the exact top-k instead, with its
+    // k-th key as the threshold (still a lower bound of the row's k-th key)
+    if (tid == 0) pk.digit = 0xFFFFFFFFu;  // reused as the block minimum of the selected keys
+    __syncthreads();
+    uint32_t kth = 0xFFFFFFFFu;
+    block_select<kThreads>(keys, n_local, a.sel_k, sc, [&](int pos, uint32_t rank) {
+      const uint32_t key = keys[padded(pos)];
+      ck[rank] = key;
+      ci[rank] = e0 + pos;
+      kth = min(kth, key);
+    });
+    for (int o = 16; o > 0; o >>= 1) kth = min(kth, __shfl_xor_sync(0xffffffffu, kth, o));
+    if ((tid & 31) == 0) atomicMin(&pk.digit, kth);
+    __syncthreads();
+    if (tid == 0) {
+      a.cand_cnt[cta] = a.sel_k;
+      a.cand_thr[cta] = pk.digit;
+    }
+  }
 }
 
 }  // namespace
@@ -473,17 +567,20 @@ int32_t indexer_deal_bound(int32_t n_rows, int32_t max_n, int32_t G) {
 
 size_t deal_candidate_bytes(int32_t G, int32_t k) {
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
-  return 2 * up((size_t)G * k * 4) + up((size_t)G * 4);
+  return 2 * up((size_t)G * 2 * k * 4) + 2 * up((size_t)G * 4);
 }
 
 DealCandidates deal_candidates(void* base, int32_t G, int32_t k) {
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   uint8_t* p = reinterpret_cast<uint8_t*>(base);
+  const size_t lists = up((size_t)G * 2 * k * 4);
   DealCandidates c;
   c.key = reinterpret_cast<uint32_t*>(p);
-  c.idx = reinterpret_cast<int32_t*>(p + up((size_t)G * k * 4));
-  c.cnt = reinterpret_cast<int32_t*>(p + 2 * up((size_t)G * k * 4));
+  c.idx = reinterpret_cast<int32_t*>(p + lists);
+  c.cnt = reinterpret_cast<int32_t*>(p + 2 * lists);
+  c.thr = reinterpret_cast<uint32_t*>(p + 2 * lists + up((size_t)G * 4));
   c.ctas = G;
+  c.cap = 2 * k;
   return c;
 }
 

@@ -179,34 +179,108 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
 
 // ------------------------------------------------------------------ merge of a balanced deal's candidates
 
-constexpr int kDealMergeThreads = 512;
+constexpr int kDealMergeThreads = 1024;
+constexpr int kDealMergeCap = 20480;  // survivors of a row held in shared memory
+constexpr int kRankMax = 2048;        // survivors ranked by counting (beyond: radix select)
+constexpr size_t kDealMergeSmem = sizeof(uint32_t) * (padded_size(kDealMergeCap) + kDealMergeCap);
 
-// Row r: the candidate lists of its CTAs under the deal (each in entry order,
-// the CTAs' ranges ascending) merged into the row's top-k.
+// Row r: its CTAs' lists under the deal merged into the row's top-k.  CTA c's
+// list holds every key of its range at or above thr_c, and thr_c is at most
+// the row's k-th largest key, so the keys at or above max_c thr_c are all in
+// the lists and include the row's top-k.  Those survivors are gathered in
+// entry order (one warp per list, ballot compaction) and ranked: by counting
+// when there are few (rank = keys above + equal keys before, so equal scores
+// go to the lower entry index), else by radix select.
 __global__ void __launch_bounds__(kDealMergeThreads) topk_deal_merge_kernel(const TopkArgs a,
-                                                                            const uint32_t* cand_key,
-                                                                            const int32_t* cand_idx,
-                                                                            const int32_t* cand_cnt, int n_rows,
-                                                                            int G) {
+                                                                            const DealCandidates c, int n_rows) {
+  extern __shared__ uint32_t msm[];
+  uint32_t* keys = msm;                                                        // padded_size(cap)
+  int32_t* idx = reinterpret_cast<int32_t*>(msm + padded_size(kDealMergeCap));  // [cap]
   __shared__ DealShared ds;
+  __shared__ int32_t off[kDealMaxRows + 1];  // survivors before each of the row's lists
+  __shared__ uint32_t s_thr;
+  __shared__ SelectScratch sc;
   __shared__ StreamScratch ss;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   pdl_trigger();
-  if (threadIdx.x < 32) deal_compute(a.pos, n_rows, a.ratio, a.window, a.max_n, G, ds);
-  pdl_wait();  // the candidates are complete only after the indexer launch
+  if (warp == 0) deal_compute(a.pos, n_rows, a.ratio, a.window, a.max_n, c.ctas, ds);
+  pdl_wait();  // the lists are complete only after the indexer launch
   __syncthreads();
   const int r = blockIdx.x;
   const int first = ds.first[r], ctas = ds.ctas[r];
   const int K = a.k;
   int32_t* out = a.out + (int64_t)r * K;
-  const int kk = stream_select<kDealMergeThreads>(
-      ctas * K, K,
-      [&](int v, uint32_t& key) {
-        const int c = first + v / K, i = v % K;
-        if (i >= cand_cnt[c]) return false;
-        key = cand_key[(int64_t)c * K + i];
-        return true;
-      },
-      [&](int v, int slot) { out[slot] = cand_idx[(int64_t)(first + v / K) * K + v % K]; }, ss);
+  if (warp == 0) {
+    uint32_t t = 0;
+    for (int j = lane; j < ctas; j += 32) t = max(t, c.thr[first + j]);
+    for (int o = 16; o > 0; o >>= 1) t = max(t, __shfl_xor_sync(0xffffffffu, t, o));
+    if (lane == 0) s_thr = t;
+  }
+  __syncthreads();
+  const uint32_t thr = s_thr;
+  // survivors per list
+  for (int j = warp; j < ctas; j += kDealMergeThreads / 32) {
+    const int n = c.cnt[first + j];
+    const uint32_t* lk = c.key + (int64_t)(first + j) * c.cap;
+    int cnt = 0;
+    for (int i0 = 0; i0 < n; i0 += 32) {
+      const int i = i0 + lane;
+      cnt += __popc(__ballot_sync(0xffffffffu, i < n && lk[i] >= thr));
+    }
+    if (lane == 0) off[j + 1] = cnt;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    off[0] = 0;
+    for (int j = 0; j < ctas; ++j) off[j + 1] += off[j];
+  }
+  __syncthreads();
+  const int m = off[ctas];
+  int kk;
+  if (m <= kDealMergeCap) {
+    for (int j = warp; j < ctas; j += kDealMergeThreads / 32) {
+      const int n = c.cnt[first + j];
+      const int64_t base = (int64_t)(first + j) * c.cap;
+      int at = off[j];
+      for (int i0 = 0; i0 < n; i0 += 32) {
+        const int i = i0 + lane;
+        const uint32_t key = i < n ? c.key[base + i] : 0u;
+        const bool keep = i < n && key >= thr;
+        const uint32_t b = __ballot_sync(0xffffffffu, keep);
+        if (keep) {
+          const int q = at + __popc(b & ((1u << lane) - 1u));
+          keys[padded(q)] = key;
+          idx[q] = c.idx[base + i];
+        }
+        at += __popc(b);
+      }
+    }
+    __syncthreads();
+    if (m <= kRankMax) {
+      for (int i = threadIdx.x; i < m; i += kDealMergeThreads) {
+        const uint32_t ki = keys[padded(i)];
+        int rank = 0;
+        for (int j = 0; j < m; ++j) {
+          const uint32_t kj = keys[padded(j)];
+          rank += (kj > ki) || (kj == ki && j < i);
+        }
+        if (rank < K) out[rank] = idx[i];
+      }
+    } else {
+      block_select<kDealMergeThreads>(keys, m, K, sc, [&](int pos, uint32_t rank) { out[rank] = idx[pos]; });
+    }
+    kk = m < K ? m : K;
+  } else {
+    kk = stream_select<kDealMergeThreads>(
+        ctas * c.cap, K,
+        [&](int v, uint32_t& key) {
+          const int j = first + v / c.cap, i = v % c.cap;
+          if (i >= c.cnt[j]) return false;
+          key = c.key[(int64_t)j * c.cap + i];
+          return key >= thr;
+        },
+        [&](int v, int slot) { out[slot] = c.idx[(int64_t)(first + v / c.cap) * c.cap + v % c.cap]; }, ss);
+  }
   for (int i = kk + threadIdx.x; i < K; i += kDealMergeThreads) out[i] = -1;
 }
 
@@ -369,8 +443,17 @@ cudaError_t launch_topk(const TopkArgs& a, int32_t n_rows, void* cand, cudaStrea
 
 cudaError_t launch_topk_deal_merge(const TopkArgs& a, int32_t n_rows, const DealCandidates& c, cudaStream_t s) {
   if (n_rows == 0 || a.k == 0) return cudaSuccess;
-  return launch_k(topk_deal_merge_kernel, dim3(n_rows), dim3(kDealMergeThreads), 0, s, kAfterOwnKernel, 0, a,
-                  (const uint32_t*)c.key, (const int32_t*)c.idx, (const int32_t*)c.cnt, (int)n_rows, (int)c.ctas);
+  static PerDevice attr;
+  cudaError_t e = with_device_slot(attr, [](int, int64_t& done) {
+    if (done) return cudaSuccess;
+    const cudaError_t r = cudaFuncSetAttribute(topk_deal_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)kDealMergeSmem);
+    if (r == cudaSuccess) done = 1;
+    return r;
+  });
+  if (e != cudaSuccess) return e;
+  return launch_k(topk_deal_merge_kernel, dim3(n_rows), dim3(kDealMergeThreads), kDealMergeSmem, s,
+                  kAfterOwnKernel, 0, a, c, (int)n_rows);
 }
 
 }  // namespace csa

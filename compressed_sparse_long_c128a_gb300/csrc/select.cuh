@@ -169,6 +169,15 @@ struct DealShared {
   int32_t tiles[kDealMaxRows];
 };
 
+// ceil(t / m) for 0 <= t < 2^22 and 1 <= m, from a float reciprocal rm ~ 1/m:
+// the estimate is within one of the quotient and is corrected exactly.
+__device__ __forceinline__ int32_t ceil_div_small(int32_t t, int32_t m, float rm) {
+  int32_t q = __float2int_rn((float)t * rm);
+  if (q * m < t) ++q;
+  if (q > 0 && (q - 1) * m >= t) --q;
+  return q;
+}
+
 __device__ __forceinline__ int32_t deal_row_tiles(const int32_t* pos, int r, int32_t ratio, int32_t window,
                                                   int32_t max_n) {
   int32_t n = n_visible(pos[r], ratio, window);
@@ -202,9 +211,10 @@ __device__ __forceinline__ void deal_compute(const int32_t* pos, int n_rows, int
   if (hi < lo) hi = lo;
   while (lo < hi) {
     const int32_t mid = (lo + hi) >> 1;
+    const float rm = 1.0f / (float)mid;
     int32_t cnt = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) cnt += (t[i] + mid - 1) / mid;
+    for (int i = 0; i < 8; ++i) cnt += ceil_div_small(t[i], mid, rm);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
     if (cnt <= G) hi = mid;
@@ -212,9 +222,10 @@ __device__ __forceinline__ void deal_compute(const int32_t* pos, int n_rows, int
   }
   // CTAs per row and their prefix in row order
   int32_t k[8], mine = 0;
+  const float rlo = 1.0f / (float)lo;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    k[i] = (t[i] + lo - 1) / lo;
+    k[i] = ceil_div_small(t[i], lo, rlo);
     mine += k[i];
   }
   int32_t incl = mine;
