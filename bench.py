@@ -16,8 +16,9 @@ other full-size workloads are measured the same way and reported under
 attention cache and fp4 indexer cache; mixed chunked prefill + decode with a
 c4a and a c128a layer).
 
-Timing: W eager warm-up steps, then K steps replayed from CUDA graphs (one
-graph per step) on one stream, bracketed by CUDA events with a device
+Timing: W eager warm-up steps, then K steps replayed from CUDA graphs (a
+few consecutive steps per graph, as a serving loop captures consecutive
+layers) on one stream, bracketed by CUDA events with a device
 synchronise (and, under torchrun, a barrier) on both sides; the max over
 ranks is reported.  When a step's working set is smaller than L2 the steps
 rotate over R copies of every cache with R x (bytes a step touches) >
@@ -497,15 +498,24 @@ def measure_workload(idx: int, args, steps: int, world: int, local: int, pool=No
     stream.synchronize()
     wd.check("warm-up")
 
-    graphs, nodes = [], []
-    for rep in reps:
+    # consecutive steps are captured together (as a serving loop captures its
+    # layers), cycling over the replicas: `spg` steps per graph, and one more
+    # graph for the remainder so that exactly `steps` steps are timed
+    spg = replicas * max(1, -(-8 // replicas)) if step_bytes < 2 ** 30 else replicas
+
+    def capture(n_steps):
         g = torch.cuda.CUDAGraph()
         n0 = csa.launch_count()
         with torch.cuda.graph(g, stream=stream):
-            step(rep, stream)
-        nodes.append(csa.launch_count() - n0)  # the library's kernels in this step's graph
-        graphs.append(g)
+            for i in range(n_steps):
+                step(reps[i % replicas], stream)
+        return g, csa.launch_count() - n0  # the library's kernels in the graph
+
+    full, full_launches = capture(spg)
+    n_full, n_rest = divmod(steps, spg)
+    rest, rest_launches = capture(n_rest) if n_rest else (None, 0)
     torch.cuda.synchronize()
+    kernels_per_step = full_launches // spg
 
     clocks = Clocks(local)
     clocks.start()
@@ -513,9 +523,9 @@ def measure_workload(idx: int, args, steps: int, world: int, local: int, pool=No
     i = 0
     with torch.cuda.stream(stream):  # a graph replays on the current stream
         while time.perf_counter() - t_load < args.load_seconds:
-            graphs[i % replicas].replay()
+            full.replay()
             i += 1
-            if i % 64 == 0:
+            if i % 8 == 0:
                 stream.synchronize()
     stream.synchronize()
 
@@ -528,8 +538,10 @@ def measure_workload(idx: int, args, steps: int, world: int, local: int, pool=No
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         t_start.record(stream)
-        for k in range(steps):
-            graphs[k % replicas].replay()
+        for _ in range(n_full):
+            full.replay()
+        if rest is not None:
+            rest.replay()
         t_end.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -572,20 +584,21 @@ def measure_workload(idx: int, args, steps: int, world: int, local: int, pool=No
     wd.check("per-call timing")
     dominant = max(calls.values(), key=lambda c: c["avg_launch_ms"])
 
-    e2e = None if args.no_e2e else _e2e(min(steps, 200), reps, graphs, stream, rows_per_step, world, step)
+    del full, rest
+    e2e = None if args.no_e2e else _e2e(min(steps, 200), reps, stream, rows_per_step, world, step)
     res = {"value": value, "unit": UNIT, "steps": steps, "ms_per_step": ms_total / steps,
            "dtype": base[0].L.cache_dtype, "config": _config(wl, replicas),
            "achieved_gbs_step": step_bytes / (ms_total / steps / 1e3) / 1e9,
            "algorithmic_bytes_per_step": step_bytes,
            "roofline": dict(dominant, peak_source=f"{peak_src} (copy bandwidth / cuBLAS bf16, burst)"),
            "calls": calls, "clocks": clk,
-           "gpu_launches": sum(nodes[k % replicas] for k in range(steps)),
-           "kernels_per_step": nodes[0], "e2e": e2e}
+           "gpu_launches": n_full * full_launches + rest_launches,
+           "kernels_per_step": kernels_per_step, "steps_per_graph": spg, "e2e": e2e}
     if side is not None:
         res["config"]["indexer_stream"] = "side"
     if pool is not None:
         res["cpu_baseline"] = oracle_baseline(pool, idx, args.cpu_seconds)
-    del graphs, reps, base, wd
+    del reps, base, wd
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     return res
@@ -629,14 +642,14 @@ def run_csa(args):
         torch.distributed.destroy_process_group()
 
 
-def _e2e(k_steps, reps, graphs, stream, rows_per_step, world, step):
+def _e2e(k_steps, reps, stream, rows_per_step, world, step):
     """Same steps with inputs copied from pinned host memory and the output read back every step.
 
     Each replica's step is captured once more as one CUDA graph that also holds
     the host-to-device copies of the step's inputs and the device-to-host copy
     of its output, as a serving loop would launch it; the host waits for every
     step's result before launching the next.  If the copies cannot be captured,
-    they are issued around the replay of the kernel-only graph instead.
+    the step is issued eagerly between them instead.
     """
     import torch
     base = reps[0]
@@ -685,7 +698,7 @@ def _e2e(k_steps, reps, graphs, stream, rows_per_step, world, step):
                 full[k % len(full)].replay()
             else:
                 copy_in()
-                graphs[k % len(graphs)].replay()
+                step(reps[k % len(reps)], stream)
                 copy_out()
             stream.synchronize()  # the host reads the step's result
     t1.record(stream)

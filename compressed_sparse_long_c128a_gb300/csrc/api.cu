@@ -177,10 +177,8 @@ int csa::enqueue_indexer_topk(const void* q_idx, int32_t q_dtype, const float* w
   }
   cudaError_t e = tc ? launch_indexer_tc(ia, n_rows, G, stream) : launch_indexer_scores(ia, n_rows, stream);
   if (e != cudaSuccess) return CSA_ERR_CUDA;
-  // the generic score kernel is not launched when no row can see an entry
-  const Order first = (tc || max_n > 0) ? kAfterOwnKernel : kStreamOrder;
   TopkArgs ta{scores, pos, ratio, window, max_n, k, out_idx, err};
-  return cuda_status(launch_topk(ta, n_rows, cand, stream, first));
+  return cuda_status(launch_topk(ta, n_rows, cand, stream));
 }
 
 namespace {

@@ -23,15 +23,15 @@ struct RopeTab {
   int32_t rope_dim;
 };
 
-// Programmatic dependent launch between the kernels of one call.  The first
-// kernel of an entry point is launched in plain stream order; each later one
-// may start while the call's previous kernel is finishing: pdl_trigger() lets
-// the next kernel launch; pdl_wait() blocks until the previous kernel has
-// completed and its writes are visible (it returns at once in a kernel
-// launched in plain stream order).  A kernel calls pdl_wait() before it
-// touches anything an earlier kernel of the call may write or read.  Every CTA
-// passes pdl_wait() before it exits, so a grid completes only after its
-// predecessor did and completion stays transitive along the call.
+// Programmatic dependent launch.  Every kernel of the library is launched so
+// that it may start while the previous kernel of the stream (the library's or
+// anyone's) is finishing: pdl_trigger() lets the next kernel launch;
+// pdl_wait() blocks until the previous kernel has completed and its writes
+// are visible.  Every kernel calls pdl_wait() before its first access to
+// global memory -- only set-up that touches no memory (barrier init, TMEM
+// allocation) runs before it -- so a kernel is ordered after all work
+// enqueued before it exactly as in plain stream order, and every CTA passes
+// pdl_wait() before it exits, so completion stays transitive along the stream.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

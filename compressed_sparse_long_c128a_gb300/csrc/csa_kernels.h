@@ -33,25 +33,15 @@ inline cudaError_t with_device_slot(PerDevice& pd, F f) {
 // Number of SMs of the current device (looked up once per device).
 cudaError_t sm_count(int* n);
 
-// How a launch is ordered after the work before it on the stream.
-//   kStreamOrder: plain stream order -- the kernel starts after everything
-//     enqueued before it has completed.  The first kernel of every entry point
-//     is launched this way, so a call never overlaps work the library did not
-//     enqueue (a caller's kernel that writes the call's inputs, or one that
-//     still reads its outputs).
-//   kAfterOwnKernel: programmatic stream serialization -- the kernel may start
-//     while the previous kernel of the same call is finishing (see pdl_wait /
-//     pdl_trigger); only for the second and later kernels of one call.
-enum Order : int { kStreamOrder = 0, kAfterOwnKernel = 1 };
-
 // Kernel launches the library has issued (csa_launch_count); counted on the host.
 void count_launch();
 
-// Launch with the given ordering and, when cluster_y > 0, clusters of
-// (1, cluster_y, 1) CTAs.
+// Launch with programmatic stream serialization (see pdl_wait in
+// csa_device.cuh: every kernel waits for its predecessor before it touches
+// memory) and, when cluster_y > 0, clusters of (1, cluster_y, 1) CTAs.
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                           Order order, int cluster_y, Args... args) {
+                           int cluster_y, Args... args) {
   count_launch();
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
@@ -60,11 +50,9 @@ inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, siz
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   int n = 0;
-  if (order == kAfterOwnKernel) {
-    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[n].val.programmaticStreamSerializationAllowed = 1;
-    ++n;
-  }
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
   if (cluster_y > 0) {
     attr[n].id = cudaLaunchAttributeClusterDimension;
     attr[n].val.clusterDim.x = 1;
@@ -197,8 +185,7 @@ struct TopkArgs {
 };
 // `cand`: topk_candidate_bytes() of scratch for the two-stage path (nullptr: one CTA per row)
 size_t topk_candidate_bytes(int32_t n_rows, int32_t max_n, int32_t k);
-// `first`: kStreamOrder when no kernel of the call precedes the top-k launches
-cudaError_t launch_topk(const TopkArgs& a, int32_t n_rows, void* cand, cudaStream_t s, Order first);
+cudaError_t launch_topk(const TopkArgs& a, int32_t n_rows, void* cand, cudaStream_t s);
 // the rows' selections from the candidate lists of a balanced deal (after the indexer launch)
 cudaError_t launch_topk_deal_merge(const TopkArgs& a, int32_t n_rows, const DealCandidates& c, cudaStream_t s);
 

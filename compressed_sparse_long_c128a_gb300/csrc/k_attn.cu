@@ -254,14 +254,14 @@ cudaError_t launch_attn(const AttnArgs& a, int32_t n_rows, int32_t keys_per_row,
   const size_t smem = sizeof(float) * ((size_t)kHeadsPerCta * a.dim + (size_t)kKeyTile * (a.dim + 1));
   cudaError_t e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  e = launch_k(attn_kernel, dim3(n_rows, a.heads / kHeadsPerCta, a.n_splits), dim3(kThreads), smem, s, kStreamOrder, 0,
+  e = launch_k(attn_kernel, dim3(n_rows, a.heads / kHeadsPerCta, a.n_splits), dim3(kThreads), smem, s, 0,
                a);
   if (e != cudaSuccess || a.n_splits == 1) return e;
   return launch_attn_merge(a, n_rows, s);
 }
 
 cudaError_t launch_attn_merge(const AttnArgs& a, int32_t n_rows, cudaStream_t s) {
-  return launch_k(merge_kernel, dim3(n_rows, a.heads), dim3(32), 0, s, kAfterOwnKernel, 0, a);
+  return launch_k(merge_kernel, dim3(n_rows, a.heads), dim3(32), 0, s, 0, a);
 }
 
 }  // namespace csa

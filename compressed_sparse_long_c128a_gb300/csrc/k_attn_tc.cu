@@ -442,7 +442,6 @@ __device__ __forceinline__ void load_o_chunk(uint32_t taddr, bool any, float* o)
 
 __device__ void softmax_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Misc& ms, uint32_t tmem, int st) {
   fill_q_issue(a, smem, ms, st);
-  pdl_wait();  // selections and caches are complete only after the previous launch
   if (g.n_tiles > 0) lookup_keys(a, g, ms, 0, st);
   fill_q_finish(a, smem, ms, st);
   for (int u = 1; u < min(g.n_tiles, kRowBufs - 1); ++u) lookup_keys(a, g, ms, u, st);
@@ -770,7 +769,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   Misc& ms = *reinterpret_cast<Misc*>(smem + kOffMisc);
   const int tid = threadIdx.x, warp = tid >> 5;
   const int r = blockIdx.x;
-  const Geo g = row_geometry(a, r, blockIdx.y, gridDim.y);
   pdl_trigger();
 
   if (tid == 0) {
@@ -791,9 +789,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     mbar_init_fence();
     ms.abort = 0;
   }
+  if (warp == kMmaWarp) tmem_alloc(&ms.tmem_base, kTmemCols);
+  pdl_wait();  // before any access to memory: the previous kernel on the stream may still be running
+  const Geo g = row_geometry(a, r, blockIdx.y, gridDim.y);
   if (tid < kH) ms.M[tid] = -INFINITY;
   if (tid < a.rope.rope_dim / 2) rope_cs(a.rope, tid, g.p, ms.rc[tid], ms.rs[tid]);
-  if (warp == kMmaWarp) tmem_alloc(&ms.tmem_base, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -802,7 +802,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   if (warp < 4) {
     softmax_role(a, g, smem, ms, tmem, tid);
   } else if (warp < kMmaWarp) {
-    pdl_wait();  // caches and selections are complete only after the previous launch
     producer_role(a, g, smem, ms, tid - kSoftmax);
   } else if ((tid & 31) == 0) {
     mma_role(a, g, smem, ms, tmem);
@@ -860,7 +859,7 @@ cudaError_t launch_attn_tc(const AttnArgs& a, int32_t n_rows, cudaStream_t s) {
     return r;
   });
   if (e != cudaSuccess) return e;
-  return launch_k(attn_tc_kernel, dim3(n_rows, a.n_splits), dim3(kThreads), kSmemBytes, s, kStreamOrder, a.n_splits,
+  return launch_k(attn_tc_kernel, dim3(n_rows, a.n_splits), dim3(kThreads), kSmemBytes, s, a.n_splits,
                   a);
 }
 

@@ -126,14 +126,14 @@ __global__ void __launch_bounds__(kThreads) emit_kernel(const EmitArgs a) {
   __shared__ float red[32];
   __shared__ int64_t rows[256];
   __shared__ int bad;
-  const int j = blockIdx.x;
-  const int64_t t = a.pos[j];
-  const int W = a.window, Rt = a.ratio, D = a.dim;
   pdl_trigger();
   // every CTA waits, even one with nothing to emit: this grid may only complete
   // after the ingest launch has, so later launches that wait on this one also
   // see ingest's writes
   pdl_wait();
+  const int j = blockIdx.x;
+  const int64_t t = a.pos[j];
+  const int W = a.window, Rt = a.ratio, D = a.dim;
   if (t < W - 1 || (t - W + 1) % Rt) return;  // no window closes at this token
   const int64_t i = (t - W + 1) / Rt;
   const int64_t base = i * Rt;  // first raw position = anchor
@@ -396,17 +396,17 @@ bool compress_fused_eligible(const IngestArgs& ia, const EmitArgs& ea, int32_t n
 
 cudaError_t launch_compress_fused(const IngestArgs& ia, const EmitArgs& ea, int32_t n_tok, cudaStream_t s) {
   if (n_tok == 0) return cudaSuccess;
-  return launch_k(compress_fused_kernel, dim3(n_tok), dim3(kThreads), 0, s, kStreamOrder, 0, ia, ea, n_tok);
+  return launch_k(compress_fused_kernel, dim3(n_tok), dim3(kThreads), 0, s, 0, ia, ea, n_tok);
 }
 
 cudaError_t launch_ingest(const IngestArgs& a, int32_t n_tok, cudaStream_t s) {
   if (n_tok == 0) return cudaSuccess;
-  return launch_k(ingest_kernel, dim3(n_tok), dim3(kThreads), a.dim * sizeof(float), s, kStreamOrder, 0, a);
+  return launch_k(ingest_kernel, dim3(n_tok), dim3(kThreads), a.dim * sizeof(float), s, 0, a);
 }
 
 cudaError_t launch_emit(const EmitArgs& a, int32_t n_tok, cudaStream_t s) {
   if (n_tok == 0) return cudaSuccess;
-  return launch_k(emit_kernel, dim3(n_tok), dim3(kThreads), a.dim * sizeof(float), s, kAfterOwnKernel, 0, a);
+  return launch_k(emit_kernel, dim3(n_tok), dim3(kThreads), a.dim * sizeof(float), s, 0, a);
 }
 
 }  // namespace csa

@@ -97,7 +97,7 @@ cudaError_t launch_indexer_scores(const IndexerArgs& a, int32_t n_rows, cudaStre
   int gy = (2 * 152 * 2 + n_rows - 1) / n_rows;  // about four CTAs per SM in all
   if (gy > tiles) gy = tiles;
   if (gy < 1) gy = 1;
-  return launch_k(indexer_scores_kernel, dim3(n_rows, gy), dim3(kThreads), smem, s, kStreamOrder, 0, a);
+  return launch_k(indexer_scores_kernel, dim3(n_rows, gy), dim3(kThreads), smem, s, 0, a);
 }
 
 }  // namespace csa

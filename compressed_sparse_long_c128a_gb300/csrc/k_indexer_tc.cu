@@ -315,6 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(const __grid_co
   Misc& ms = *reinterpret_cast<Misc*>(smem + P::kOffMisc);
   const int tid = threadIdx.x, warp = tid >> 5;
   pdl_trigger();
+  pdl_wait();  // before any access to memory: the previous kernel on the stream may still be running
 
   // the CTA's row and tile range
   if (a.sel_k > 0) {
@@ -420,7 +421,6 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(const __grid_co
     }
   }
   fence_proxy_async();
-  pdl_wait();  // the score scratch and candidate lists may be in use by the previous launch until here
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -606,8 +606,8 @@ static cudaError_t launch_indexer_tc_t(const IndexerArgs& args, int32_t n_rows, 
   if (!kFp4 && !encode_bf16_map(&a.k_map, a.cache.data, kDI, (uint64_t)a.cache.num_blocks * kRowsPerBlock, kDI * 2,
                                 64, kRowsPerBlock))
     return cudaErrorInvalidValue;
-  if (a.sel_k > 0) return launch_k(indexer_tc_kernel<kFp4>, dim3(G), dim3(kThreads), smem_bytes<kFp4>(), s,
-                                   kStreamOrder, 0, a);
+  if (a.sel_k > 0) return launch_k(indexer_tc_kernel<kFp4>, dim3(G), dim3(kThreads), smem_bytes<kFp4>(), s, 0,
+                                   a);
   const int32_t tiles = (a.max_n + kTile - 1) / kTile;
   // one CTA per SM: as many splits per row as fit in a single wave
   int32_t splits = n_rows > 0 ? G / n_rows : 1;
@@ -617,8 +617,8 @@ static cudaError_t launch_indexer_tc_t(const IndexerArgs& args, int32_t n_rows, 
   const int32_t min_splits = (tiles + tiles_per_cta_max - 1) / tiles_per_cta_max;
   if (splits < min_splits) splits = min_splits;
   if (splits < 1) splits = 1;
-  return launch_k(indexer_tc_kernel<kFp4>, dim3(n_rows, splits), dim3(kThreads), smem_bytes<kFp4>(), s,
-                  kStreamOrder, 0, a);
+  return launch_k(indexer_tc_kernel<kFp4>, dim3(n_rows, splits), dim3(kThreads), smem_bytes<kFp4>(), s, 0,
+                  a);
 }
 
 cudaError_t launch_indexer_tc(const IndexerArgs& a, int32_t n_rows, int32_t G, cudaStream_t s) {

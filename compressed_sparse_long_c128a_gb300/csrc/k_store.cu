@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(kThreads) store_kernel(const StoreArgs a) {
 
 cudaError_t launch_store(const StoreArgs& a, int32_t n, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
-  return launch_k(store_kernel, dim3(n), dim3(kThreads), 0, s, kStreamOrder, 0, a);
+  return launch_k(store_kernel, dim3(n), dim3(kThreads), 0, s, 0, a);
 }
 
 }  // namespace csa

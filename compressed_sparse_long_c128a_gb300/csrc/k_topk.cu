@@ -15,6 +15,7 @@
 //     CTA streaming the row's scores.
 
 #include "select.cuh"
+#include "tc_ptx.cuh"
 
 namespace csa {
 namespace {
@@ -179,109 +180,200 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
 
 // ------------------------------------------------------------------ merge of a balanced deal's candidates
 
-constexpr int kDealMergeThreads = 1024;
-constexpr int kDealMergeCap = 20480;  // survivors of a row held in shared memory
-constexpr int kRankMax = 2048;        // survivors ranked by counting (beyond: radix select)
-constexpr size_t kDealMergeSmem = sizeof(uint32_t) * (padded_size(kDealMergeCap) + kDealMergeCap);
+constexpr int kDealMergeThreads = 256;
+constexpr int kMaxMergeCluster = 16;
+constexpr int kMergeKeep = 4096;  // survivors a member keeps in shared memory after its first read
 
-// Row r: its CTAs' lists under the deal merged into the row's top-k.  CTA c's
-// list holds every key of its range at or above thr_c, and thr_c is at most
-// the row's k-th largest key, so the keys at or above max_c thr_c are all in
-// the lists and include the row's top-k.  Those survivors are gathered in
-// entry order (one warp per list, ballot compaction) and ranked: by counting
-// when there are few (rank = keys above + equal keys before, so equal scores
-// go to the lower entry index), else by radix select.
+// Row r: its CTAs' lists under the deal merged into the row's top-k by one
+// cluster of Cs CTAs.  CTA c's list holds every key of its range at or above
+// thr_c, and thr_c is at most the row's k-th largest key, so the keys at or
+// above max_c thr_c ("survivors") are all in the lists and include the row's
+// top-k.  Member m of the cluster takes a contiguous run of the row's lists
+// (lists are in entry order) and streams its survivors from L2 in every pass:
+// a count, three radix-digit histograms (11, 11, 10 bits) summed into rank 0's
+// shared memory through the cluster (rank 0 picks each digit and hands it
+// back), and a last pass that places every survivor above the k-th key and
+// the first equal ones in entry order.
 __global__ void __launch_bounds__(kDealMergeThreads) topk_deal_merge_kernel(const TopkArgs a,
                                                                             const DealCandidates c, int n_rows) {
-  extern __shared__ uint32_t msm[];
-  uint32_t* keys = msm;                                                        // padded_size(cap)
-  int32_t* idx = reinterpret_cast<int32_t*>(msm + padded_size(kDealMergeCap));  // [cap]
+  constexpr int NT = kDealMergeThreads;
   __shared__ DealShared ds;
-  __shared__ int32_t off[kDealMaxRows + 1];  // survivors before each of the row's lists
-  __shared__ uint32_t s_thr;
-  __shared__ SelectScratch sc;
-  __shared__ StreamScratch ss;
+  __shared__ int32_t off[kDealMaxRows + 1];  // start of each of the row's lists in the flattened array
+  __shared__ uint32_t hloc[2048];            // this member's histogram of a pass
+  __shared__ uint32_t hsum[3][2048];         // rank 0: the cluster's histograms
+  __shared__ uint32_t wsum[32];
+  __shared__ uint32_t s_thr, s_total, s_digit[3], s_rem[3];
+  __shared__ uint32_t s_gt[kMaxMergeCluster], s_eq[kMaxMergeCluster];  // rank 0: members' counts
+  extern __shared__ uint32_t kept_key[];  // [kMergeKeep] this member's survivors in entry order, when they fit
+  int32_t* kept_idx = reinterpret_cast<int32_t*>(kept_key + kMergeKeep);  // [kMergeKeep]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int Cs = gridDim.y, me = (int)tc::cluster_rank();
+  for (int b = threadIdx.x; b < 3 * 2048; b += NT) (&hsum[0][0])[b] = 0;
+  if (threadIdx.x == 0) s_total = 0;
   pdl_trigger();
-  if (warp == 0) deal_compute(a.pos, n_rows, a.ratio, a.window, a.max_n, c.ctas, ds);
   pdl_wait();  // the lists are complete only after the indexer launch
-  __syncthreads();
+  if (warp == 0) deal_compute(a.pos, n_rows, a.ratio, a.window, a.max_n, c.ctas, ds);
+  tc::cluster_sync();  // rank 0's sums are zero before any member adds
   const int r = blockIdx.x;
   const int first = ds.first[r], ctas = ds.ctas[r];
   const int K = a.k;
   int32_t* out = a.out + (int64_t)r * K;
-  if (warp == 0) {
+  if (warp == 0) {  // lane l owns lists [8l, 8l+8): counts, thresholds, prefix
+    int32_t cnt[8], mine = 0;
     uint32_t t = 0;
-    for (int j = lane; j < ctas; j += 32) t = max(t, c.thr[first + j]);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int j = 8 * lane + i;
+      cnt[i] = j < ctas ? c.cnt[first + j] : 0;
+      t = j < ctas ? max(t, c.thr[first + j]) : t;
+      mine += cnt[i];
+    }
     for (int o = 16; o > 0; o >>= 1) t = max(t, __shfl_xor_sync(0xffffffffu, t, o));
+    int32_t incl = mine;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int32_t run = incl - mine;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int j = 8 * lane + i;
+      if (j <= ctas) off[j] = run;
+      run += cnt[i];
+    }
     if (lane == 0) s_thr = t;
   }
   __syncthreads();
   const uint32_t thr = s_thr;
-  // survivors per list
-  for (int j = warp; j < ctas; j += kDealMergeThreads / 32) {
-    const int n = c.cnt[first + j];
-    const uint32_t* lk = c.key + (int64_t)(first + j) * c.cap;
-    int cnt = 0;
-    for (int i0 = 0; i0 < n; i0 += 32) {
-      const int i = i0 + lane;
-      cnt += __popc(__ballot_sync(0xffffffffu, i < n && lk[i] >= thr));
-    }
-    if (lane == 0) off[j + 1] = cnt;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    off[0] = 0;
-    for (int j = 0; j < ctas; ++j) off[j + 1] += off[j];
-  }
-  __syncthreads();
-  const int m = off[ctas];
-  int kk;
-  if (m <= kDealMergeCap) {
-    for (int j = warp; j < ctas; j += kDealMergeThreads / 32) {
-      const int n = c.cnt[first + j];
-      const int64_t base = (int64_t)(first + j) * c.cap;
-      int at = off[j];
-      for (int i0 = 0; i0 < n; i0 += 32) {
-        const int i = i0 + lane;
-        const uint32_t key = i < n ? c.key[base + i] : 0u;
-        const bool keep = i < n && key >= thr;
-        const uint32_t b = __ballot_sync(0xffffffffu, keep);
-        if (keep) {
-          const int q = at + __popc(b & ((1u << lane) - 1u));
-          keys[padded(q)] = key;
-          idx[q] = c.idx[base + i];
+  // this member's lists and its thread's contiguous slice of their entries
+  const int per = (ctas + Cs - 1) / Cs, jb = min(ctas, me * per), je = min(ctas, jb + per);
+  const int vb = off[jb], ve = off[je];
+  const int seg = (ve - vb + NT - 1) / NT, v0 = min(ve, vb + (int)threadIdx.x * seg), v1 = min(ve, v0 + seg);
+  int j0 = jb;
+  while (j0 + 1 < je && off[j0 + 1] <= v0) ++j0;
+  // visit(key, idx_pos) over this thread's survivors in entry order, eight loads in flight
+  auto visit = [&](auto&& fn) {
+    int j = j0;
+    for (int v = v0; v < v1; v += 8) {
+      int64_t e[8];
+      uint32_t kb[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        e[u] = -1;
+        if (v + u < v1) {
+          while (j + 1 < je && off[j + 1] <= v + u) ++j;
+          e[u] = (int64_t)(first + j) * c.cap + (v + u - off[j]);
         }
-        at += __popc(b);
       }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) kb[u] = e[u] >= 0 ? c.key[e[u]] : 0u;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (e[u] >= 0 && kb[u] >= thr) fn(kb[u], e[u]);
     }
-    __syncthreads();
-    if (m <= kRankMax) {
-      for (int i = threadIdx.x; i < m; i += kDealMergeThreads) {
-        const uint32_t ki = keys[padded(i)];
-        int rank = 0;
-        for (int j = 0; j < m; ++j) {
-          const uint32_t kj = keys[padded(j)];
-          rank += (kj > ki) || (kj == ki && j < i);
-        }
-        if (rank < K) out[rank] = idx[i];
-      }
+  };
+  // survivors: counted, then (when this member's fit) copied to shared memory in
+  // entry order so that the later passes read them there
+  uint32_t n_mine = 0;
+  visit([&](uint32_t, int64_t) { ++n_mine; });
+  uint32_t n_member;
+  uint32_t at = block_excl_scan<NT>(n_mine, wsum, n_member);
+  const bool kept = n_member <= (uint32_t)kMergeKeep;
+  if (kept) visit([&](uint32_t key, int64_t e) {
+    kept_key[at] = key;
+    kept_idx[at] = c.idx[e];
+    ++at;
+  });
+  if (threadIdx.x == 0 && n_member) tc::cluster_red_add(tc::map_shared(&s_total, 0), n_member);
+  tc::cluster_sync();
+  // the survivors this thread visits in the later passes, in entry order
+  const int ks = (int)((n_member + NT - 1) / NT), k0 = min((int)n_member, (int)threadIdx.x * ks),
+            k1 = min((int)n_member, k0 + ks);
+  auto each = [&](auto&& fn) {
+    if (kept) {
+      for (int q = k0; q < k1; ++q) fn(kept_key[q], (int64_t)-1 - q);
     } else {
-      block_select<kDealMergeThreads>(keys, m, K, sc, [&](int pos, uint32_t rank) { out[rank] = idx[pos]; });
+      visit(fn);
     }
-    kk = m < K ? m : K;
-  } else {
-    kk = stream_select<kDealMergeThreads>(
-        ctas * c.cap, K,
-        [&](int v, uint32_t& key) {
-          const int j = first + v / c.cap, i = v % c.cap;
-          if (i >= c.cnt[j]) return false;
-          key = c.key[(int64_t)j * c.cap + i];
-          return key >= thr;
-        },
-        [&](int v, int slot) { out[slot] = c.idx[(int64_t)(first + v / c.cap) * c.cap + v % c.cap]; }, ss);
+  };
+  auto index_of = [&](int64_t e) { return e < 0 ? kept_idx[-1 - e] : c.idx[e]; };
+  const uint32_t total = tc::cluster_ld(tc::map_shared(&s_total, 0));
+  const uint32_t kk = total < (uint32_t)K ? total : (uint32_t)K;
+  uint32_t prefix = 0, mask = 0, rem = kk;
+  const int shifts[3] = {21, 10, 0}, widths[3] = {11, 11, 10};
+  for (int pass = 0; pass < 3 && kk > 0; ++pass) {
+    const int sh = shifts[pass], nb = 1 << widths[pass];
+    for (int b = threadIdx.x; b < nb; b += NT) hloc[b] = 0;
+    __syncthreads();
+    each([&](uint32_t key, int64_t) {
+      if ((key & mask) == prefix) atomicAdd(&hloc[(key >> sh) & (uint32_t)(nb - 1)], 1u);
+    });
+    __syncthreads();
+    for (int b = threadIdx.x; b < nb; b += NT)
+      if (hloc[b]) tc::cluster_red_add(tc::map_shared(&hsum[pass][b], 0), hloc[b]);
+    tc::cluster_sync();
+    if (me == 0) {  // the digit d with count(> d) < rem <= count(>= d)
+      const int bpt = (nb + NT - 1) / NT, top = nb - threadIdx.x * bpt;
+      uint32_t local = 0;
+      for (int q = 0; q < bpt; ++q)
+        if (top - 1 - q >= 0) local += hsum[pass][top - 1 - q];
+      uint32_t tot;
+      const uint32_t above = block_excl_scan<NT>(local, wsum, tot);
+      if (above < rem && rem <= above + local) {
+        uint32_t cum = above;
+        for (int q = 0; q < bpt && top - 1 - q >= 0; ++q) {
+          const uint32_t h = hsum[pass][top - 1 - q];
+          if (cum + h >= rem) {
+            s_digit[pass] = (uint32_t)(top - 1 - q);
+            s_rem[pass] = rem - cum;
+            break;
+          }
+          cum += h;
+        }
+      }
+    }
+    tc::cluster_sync();
+    prefix |= tc::cluster_ld(tc::map_shared(&s_digit[pass], 0)) << sh;
+    mask |= (uint32_t)(nb - 1) << sh;
+    rem = tc::cluster_ld(tc::map_shared(&s_rem[pass], 0));
   }
-  for (int i = kk + threadIdx.x; i < K; i += kDealMergeThreads) out[i] = -1;
+  // keys above T to slots [0, n_gt), the first `rem` keys equal to T to [n_gt, kk),
+  // each group in entry order: member prefixes through rank 0, thread prefixes by scans
+  const uint32_t T = prefix;
+  uint32_t n_gt = 0, n_eq = 0;
+  if (kk > 0) each([&](uint32_t key, int64_t) {
+    n_gt += key > T;
+    n_eq += key == T;
+  });
+  uint32_t m_gt, m_eq;
+  uint32_t t_gt = block_excl_scan<NT>(n_gt, wsum, m_gt);
+  uint32_t t_eq = block_excl_scan<NT>(n_eq, wsum, m_eq);
+  if (threadIdx.x == 0) {
+    tc::cluster_st(tc::map_shared(&s_gt[me], 0), m_gt);
+    tc::cluster_st(tc::map_shared(&s_eq[me], 0), m_eq);
+  }
+  tc::cluster_sync();
+  uint32_t gt_all = 0, gt_before = 0, eq_before = 0;
+  for (int q = 0; q < Cs; ++q) {
+    const uint32_t g = tc::cluster_ld(tc::map_shared(&s_gt[q], 0));
+    const uint32_t e = tc::cluster_ld(tc::map_shared(&s_eq[q], 0));
+    gt_all += g;
+    gt_before += q < me ? g : 0u;
+    eq_before += q < me ? e : 0u;
+  }
+  t_gt += gt_before;
+  t_eq += eq_before;
+  if (kk > 0) each([&](uint32_t key, int64_t e) {
+    if (key > T) {
+      out[t_gt++] = index_of(e);
+    } else if (key == T) {
+      if (t_eq < rem) out[gt_all + t_eq] = index_of(e);
+      ++t_eq;
+    }
+  });
+  if (me == 0)
+    for (int i = (int)kk + threadIdx.x; i < K; i += NT) out[i] = -1;
+  tc::cluster_sync();  // no member may leave while another still reads rank 0's shared memory
 }
 
 constexpr int kChunk = 16384;
@@ -403,7 +495,7 @@ size_t topk_candidate_bytes(int32_t n_rows, int32_t max_n, int32_t k) {
   return (size_t)n_rows * c * ((size_t)k * 8 + 4);
 }
 
-cudaError_t launch_topk(const TopkArgs& a, int32_t n_rows, void* cand, cudaStream_t s, Order first) {
+cudaError_t launch_topk(const TopkArgs& a, int32_t n_rows, void* cand, cudaStream_t s) {
   if (n_rows == 0 || a.k == 0) return cudaSuccess;
   static PerDevice chunk_attr;
   cudaError_t e = with_device_slot(chunk_attr, [](int, int64_t& done) {
@@ -416,14 +508,14 @@ cudaError_t launch_topk(const TopkArgs& a, int32_t n_rows, void* cand, cudaStrea
   if (e != cudaSuccess) return e;
   const int32_t nc = topk_chunks(a.max_n);
   if (nc <= 1)
-    return launch_k(topk_chunk_kernel, dim3(n_rows, 1), dim3(kChunkThreads), kChunkSmem, s, first, 0, a,
+    return launch_k(topk_chunk_kernel, dim3(n_rows, 1), dim3(kChunkThreads), kChunkSmem, s, 0, a,
                     (uint32_t*)nullptr, (int32_t*)nullptr, (int32_t*)nullptr, 1);
   if (!topk_two_stage(a.max_n, a.k) || cand == nullptr)
-    return launch_k(topk_kernel, dim3(n_rows), dim3(kThreads), 0, s, first, 0, a);
+    return launch_k(topk_kernel, dim3(n_rows), dim3(kThreads), 0, s, 0, a);
   uint32_t* ck = reinterpret_cast<uint32_t*>(cand);
   int32_t* ci = reinterpret_cast<int32_t*>(ck + (size_t)n_rows * nc * a.k);
   int32_t* cc = ci + (size_t)n_rows * nc * a.k;
-  e = launch_k(topk_chunk_kernel, dim3(n_rows, nc), dim3(kChunkThreads), kChunkSmem, s, first, 0, a, ck, ci,
+  e = launch_k(topk_chunk_kernel, dim3(n_rows, nc), dim3(kChunkThreads), kChunkSmem, s, 0, a, ck, ci,
                            cc, nc);
   if (e != cudaSuccess) return e;
   const size_t smem = merge_smem(nc, a.k);
@@ -436,7 +528,7 @@ cudaError_t launch_topk(const TopkArgs& a, int32_t n_rows, void* cand, cudaStrea
     return r;
   });
   if (e != cudaSuccess) return e;
-  return launch_k(topk_merge_kernel, dim3(n_rows), dim3(kMergeThreads), smem, s, kAfterOwnKernel, 0, a,
+  return launch_k(topk_merge_kernel, dim3(n_rows), dim3(kMergeThreads), smem, s, 0, a,
                   (const uint32_t*)ck,
                   (const int32_t*)ci, (const int32_t*)cc, nc);
 }
@@ -446,14 +538,21 @@ cudaError_t launch_topk_deal_merge(const TopkArgs& a, int32_t n_rows, const Deal
   static PerDevice attr;
   cudaError_t e = with_device_slot(attr, [](int, int64_t& done) {
     if (done) return cudaSuccess;
-    const cudaError_t r = cudaFuncSetAttribute(topk_deal_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)kDealMergeSmem);
+    cudaError_t r = cudaFuncSetAttribute(topk_deal_merge_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(topk_deal_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)(2 * kMergeKeep * sizeof(uint32_t)));
     if (r == cudaSuccess) done = 1;
     return r;
   });
   if (e != cudaSuccess) return e;
-  return launch_k(topk_deal_merge_kernel, dim3(n_rows), dim3(kDealMergeThreads), kDealMergeSmem, s,
-                  kAfterOwnKernel, 0, a, c, (int)n_rows);
+  // members per row: a power of two <= 16 keeping at least about four of the
+  // deal's lists per member (rows of a few lists merge in one CTA)
+  int32_t cs = 1;
+  while (cs < kMaxMergeCluster && 4 * cs * n_rows <= c.ctas) cs *= 2;
+  return launch_k(topk_deal_merge_kernel, dim3(n_rows, cs), dim3(kDealMergeThreads), 2 * kMergeKeep * sizeof(uint32_t),
+                  s, cs, a, c,
+                  (int)n_rows);
 }
 
 }  // namespace csa

@@ -178,9 +178,12 @@ __device__ __forceinline__ int32_t ceil_div_small(int32_t t, int32_t m, float rm
   return q;
 }
 
+// Tiles of row r; `ratio` divides 256, so it is a power of two and the
+// division is a shift.
 __device__ __forceinline__ int32_t deal_row_tiles(const int32_t* pos, int r, int32_t ratio, int32_t window,
                                                   int32_t max_n) {
-  int32_t n = n_visible(pos[r], ratio, window);
+  const int32_t p = pos[r];
+  int32_t n = p < window ? 0 : ((p - window) >> (__ffs(ratio) - 1)) + 1;
   n = n < max_n ? n : max_n;
   return (n + kDealTile - 1) / kDealTile;
 }
@@ -191,8 +194,7 @@ __device__ __forceinline__ void deal_compute(const int32_t* pos, int n_rows, int
                                              int32_t max_n, int G, DealShared& ds) {
   const int lane = threadIdx.x & 31;
   int32_t t[8];
-  int32_t tmax = 0;
-  long long tsum = 0;
+  int32_t tmax = 0, tsum = 0;  // at most 256 rows of 2^22 / 128 tiles
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int r = 8 * lane + i;

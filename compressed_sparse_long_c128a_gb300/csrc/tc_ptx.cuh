@@ -91,6 +91,25 @@ __device__ __forceinline__ uint32_t map_shared(const void* p, uint32_t rank) {
   return r;
 }
 
+// Add v to a 32-bit word of a peer CTA's shared memory (shared::cluster address).
+__device__ __forceinline__ void cluster_red_add(uint32_t addr, uint32_t v) {
+  asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void cluster_st(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_ld(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+// This CTA's rank in its cluster.
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
 // ---------------------------------------------------------------- TMEM
 
 // One full warp: allocate `ncols` TMEM columns (power of two >= 32); address written to *slot.

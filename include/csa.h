@@ -24,11 +24,10 @@
  *     or written out of bounds.  No kernel traps or waits without a bound.
  *     csa_read_status() fetches and optionally clears the word.
  *   - Every call is ordered after all work enqueued before it on `stream`, by
- *     anyone: its first kernel is launched in plain stream order.  The later
- *     kernels of one call use programmatic dependent launch among themselves
- *     (a kernel may start while the call's previous kernel is finishing, and
- *     waits for it before it reads what that kernel wrote).  Work enqueued after
- *     a call starts after the call's last kernel has completed.
+ *     anyone.  Kernels are launched with programmatic dependent launch: a
+ *     kernel may start while the previous kernel on the stream is finishing,
+ *     but it waits for that kernel to complete before it reads or writes any
+ *     memory, so only set-up that touches no memory overlaps.
  *   - Positions are 0-based.  Compressed entry i of a layer with stride
  *     `ratio` and window `window` sums raw tokens [ratio*i, ratio*i+window-1]
  *     and is anchored (rotated) at ratio*i ([延迟] "KV 缓存压缩").  A query at
