@@ -14,7 +14,7 @@ The headline workload is c4a DSA decode: 64 sequences at contexts uniform in
 other full-size workloads are measured the same way and reported under
 "configs" (c128a dense decode at 131072; c4a decode at 2^20 with the fp8
 attention cache and fp4 indexer cache; mixed chunked prefill + decode with a
-c4a and a c128a layer).
+c4a and a c128a layer; the c4a decode on the partial token-wise fp8 cache).
 
 Timing: W eager warm-up steps, then K steps replayed from CUDA graphs (a
 few consecutive steps per graph, as a serving loop captures consecutive
@@ -59,7 +59,7 @@ METRIC = "c4a/c128a sparse decode attention tokens/s; achieved HBM GB/s vs ~8 TB
 UNIT = "tokens/s"
 L2_BYTES = 129 * 2 ** 20
 HEADLINE = 2
-EXTRA = (1, 3, 4)
+EXTRA = (1, 3, 4, 5)
 
 
 def _args(argv=None):
@@ -129,7 +129,9 @@ def _elem_bytes(dt: str) -> float:
     return {"f32": 4.0, "bf16": 2.0, "e4m3": 1.0, "e2m1": 0.5}[dt]
 
 
-def _row_bytes(dt: str, dim: int) -> float:
+def _row_bytes(dt: str, dim: int, tail: int = 64) -> float:
+    if dt == "e4m3r":  # e4m3 codes + fp32 scale, the rotary tail in bf16
+        return (dim - tail) + 2 * tail + 4
     b = dim * _elem_bytes(dt)
     if dt == "e4m3":
         b += 4  # fp32 scale per row

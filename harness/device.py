@@ -55,8 +55,9 @@ class LayerDev:
             self.tables[kind] = _dev(t, device=device)
             self.n_blocks[kind] = n
         cd = csa.DTYPES[L.cache_dtype]
-        self.comp = csa.PagedCache.empty(self.n_blocks["comp"], L.entries_per_block, L.dim, cd, device)
-        self.swa = csa.PagedCache.empty(self.n_blocks["swa"], synth.BLOCK_POSITIONS, L.dim, cd, device)
+        tail = L.rope_dim if L.cache_dtype == "e4m3r" else 0  # rotary dims kept in bf16
+        self.comp = csa.PagedCache.empty(self.n_blocks["comp"], L.entries_per_block, L.dim, cd, device, tail)
+        self.swa = csa.PagedCache.empty(self.n_blocks["swa"], synth.BLOCK_POSITIONS, L.dim, cd, device, tail)
         self.state = csa.PagedCache.empty(self.n_blocks["state"], synth.BLOCK_POSITIONS, 2 * L.dim,
                                           csa.DTYPES[L.in_dtype], device)
         self.idx = None
@@ -245,6 +246,11 @@ class LayerDev:
         d = cache.data[bi, ri]
         if cache.dtype == csa.E4M3:
             v = d.view(torch.float8_e4m3fn).to(torch.float64) * cache.scales[bi, ri].to(torch.float64)[:, None]
+        elif cache.dtype == csa.E4M3R:
+            dq = cache.dim - cache.tail_bf16
+            head = d[:, :dq].view(torch.float8_e4m3fn).to(torch.float64) * cache.scales[bi, ri].to(torch.float64)[:, None]
+            tail = d[:, dq:].contiguous().view(torch.bfloat16).to(torch.float64)
+            v = torch.cat([head, tail], dim=1)
         elif cache.dtype == csa.E2M1:
             raise ValueError("use read_cache_bytes for e2m1")
         else:

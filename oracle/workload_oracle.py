@@ -11,8 +11,8 @@ csa_oracle.  What the caches are expected to hold:
   * sliding-window rows for positions [ingest_from, end) are RMSNorm -> RoPE of
     the raw kv row at its own position.
 
-A cache stored as e4m3 holds the codec's dequantised value of the fp32 form
-of the above; bf16 and fp32 caches are compared against the unrounded fp64
+A cache stored as e4m3 (or e4m3r: e4m3 non-rotary dims, bf16 rotary dims)
+holds the codec's dequantised value of the fp32 form of the above; bf16 and fp32 caches are compared against the unrounded fp64
 value, so the oracle never models the kernels' rounding.
 """
 
@@ -72,6 +72,9 @@ class SequenceOracle:
         if dtype == "e4m3":
             codes, scale = O.quantize_rows_e4m3(np.asarray(rows, np.float32))
             return O.dequantize_rows_e4m3(codes, scale)
+        if dtype == "e4m3r":
+            codes, scale, rope = O.quantize_rows_e4m3_rope_bf16(np.asarray(rows, np.float32), self.layer.rope_dim)
+            return O.dequantize_rows_e4m3_rope_bf16(codes, scale, rope)
         return np.asarray(rows, np.float64)
 
     def stored_entries(self, ids) -> np.ndarray:

@@ -18,6 +18,10 @@ Five workloads, each named by what it is:
   mixed_prefill_decode    8 prefill chunks of 2048 tokens over contexts
                           4k..1M with unaligned starts, plus 24 decode rows at
                           context 65536, for a c4a and a c128a layer, bf16.
+  c4a_decode_b64_64k_pfp8 the c4a sparse decode above with the "partial
+                          token-wise fp8" attention cache: per row, e4m3 codes
+                          with one fp32 scale for the non-rotary dims and the 64
+                          rotary dims in bf16 (cache dtype "e4m3r").
 
 How a sequence's history is given.  A step sees a sequence whose first
 `first_new` positions are already cached.  Drawing every raw token of a
@@ -72,7 +76,8 @@ def round_bf16(x) -> np.ndarray:
 
 
 def _stored(x: np.ndarray, dtype: str) -> np.ndarray:
-    """A draw as the caller hands it over: bf16 inputs are bf16 values, all others fp32."""
+    """A draw as the caller hands it over: bf16 inputs are bf16 values, all others
+    fp32 (quantised caches receive fp32 rows and quantise them on insert)."""
     if dtype == "bf16":
         return round_bf16(x)
     return np.ascontiguousarray(x, dtype=np.float32)
@@ -178,9 +183,18 @@ def _mixed_prefill_decode() -> Workload:
                     "8 prefill chunks of 2048 (contexts 4k..1M) + 24 decode rows at 64k")
 
 
-_BUILDERS = {0: _tiny, 1: _c128a_decode, 2: _c4a_decode, 3: _c4a_decode_1m_fp8, 4: _mixed_prefill_decode}
+def _c4a_decode_partial_fp8() -> Workload:
+    c4 = LayerSpec("c4a", 4, 8, dim=512, heads=64, cache_dtype="e4m3r", topk=512, idx_heads=64, idx_dim=128)
+    lens = _rng(5, _T_LENGTHS).integers(32768, 65536, size=64, endpoint=True)
+    return Workload("c4a_decode_b64_64k_pfp8", 5, (c4,),
+                    tuple(SeqSpec(int(n), 1, int(n) - SWA) for n in lens),
+                    "c4a sparse decode, partial token-wise fp8 cache (e4m3 + bf16 rotary dims), B=64")
+
+
+_BUILDERS = {0: _tiny, 1: _c128a_decode, 2: _c4a_decode, 3: _c4a_decode_1m_fp8, 4: _mixed_prefill_decode,
+             5: _c4a_decode_partial_fp8}
 WORKLOADS = {0: "tiny_c4a_f32", 1: "c128a_decode_b32_128k", 2: "c4a_decode_b64_64k",
-             3: "c4a_decode_b4_1m_fp8", 4: "mixed_prefill_decode"}
+             3: "c4a_decode_b4_1m_fp8", 4: "mixed_prefill_decode", 5: "c4a_decode_b64_64k_pfp8"}
 
 
 @lru_cache(maxsize=None)

@@ -11,7 +11,9 @@ GPU produced.  Per workload:
   * attention with a generator-drawn selection (one per row) against the
     oracle on the same selection;
   * end to end (the GPU's own selection): rows whose selection equals the
-    oracle's are compared element by element.
+    oracle's are compared element by element;
+  * one attention kernel reading a bf16 cache (a prefill call) and a partial
+    token-wise fp8 cache (a decode call) of the same entries.
 
 Tolerances: fp32 workload 1e-4 max-abs; bf16 2e-2 max-abs and 1e-2 rel-L2
 against the unrounded fp64 oracle; e4m3 caches within one e4m3 step of the
@@ -74,8 +76,13 @@ def _e4m3_step(v, scale):
     return np.ldexp(1.0, e - 3) * scale
 
 
-def _assert_values(got, want, dtype, what, scale=None):
+def _assert_values(got, want, dtype, what, scale=None, tail=0):
     got, want = np.asarray(got, np.float64), np.asarray(want, np.float64)
+    if dtype == "e4m3r":  # e4m3 over the non-rotary dims, bf16 over the `tail` rotary dims
+        dq = got.shape[-1] - tail
+        _assert_values(got[..., :dq], want[..., :dq], "e4m3", f"{what} (e4m3 dims)", scale)
+        _assert_values(got[..., dq:], want[..., dq:], "bf16", f"{what} (bf16 rotary dims)")
+        return
     assert got.shape == want.shape, what
     assert np.all(np.isfinite(got)), what
     diff = np.abs(got - want)
@@ -96,7 +103,7 @@ def _assert_values(got, want, dtype, what, scale=None):
         raise ValueError(dtype)
 
 
-WORKLOADS = [0, 1, 2, 3, 4]
+WORKLOADS = [0, 1, 2, 3, 4, 5]
 
 
 @pytest.mark.parametrize("idx", WORKLOADS)
@@ -118,8 +125,8 @@ def test_caches(idx):
             sw_pos = pos if len(pos) <= 300 else np.concatenate([pos[:150], pos[-150:]])
             got = ld.read_cache("swa", b, sw_pos)
             want = so.stored_swa(sw_pos)
-            sc = ld.read_cache_bytes("swa", b, sw_pos)[1] if L.cache_dtype == "e4m3" else None
-            _assert_values(got, want, L.cache_dtype, f"swa rows seq {b}", sc)
+            sc = ld.read_cache_bytes("swa", b, sw_pos)[1] if L.cache_dtype in ("e4m3", "e4m3r") else None
+            _assert_values(got, want, L.cache_dtype, f"swa rows seq {b}", sc, L.rope_dim)
             # entries emitted by ingest
             em = so.emitted()
             if len(em) > 200:
@@ -127,8 +134,8 @@ def test_caches(idx):
             if em:
                 got = ld.read_cache("comp", b, em)
                 want = so.stored_entries(em)
-                sc = ld.read_cache_bytes("comp", b, em)[1] if L.cache_dtype == "e4m3" else None
-                _assert_values(got, want, L.cache_dtype, f"emitted entries seq {b}", sc)
+                sc = ld.read_cache_bytes("comp", b, em)[1] if L.cache_dtype in ("e4m3", "e4m3r") else None
+                _assert_values(got, want, L.cache_dtype, f"emitted entries seq {b}", sc, L.rope_dim)
             # a few history entries: stored exactly as the oracle's codec stores the draw
             if s.ingest_from > 0:
                 hid = [0, 1, max(0, min(em) - 1) if em else 2]
@@ -179,7 +186,7 @@ def _check_topk_row(gpu_row, scores, k, what):
     return set(sel.tolist()) == set(ref.tolist())
 
 
-@pytest.mark.parametrize("idx", [0, 2, 3, 4])
+@pytest.mark.parametrize("idx", [0, 2, 3, 4, 5])
 def test_topk(idx):
     wd = _dev(idx)
     wl = wd.wl
@@ -395,3 +402,61 @@ def test_device_bounds_are_reported_not_faulted():
     ld.step()
     torch.cuda.synchronize()
     ld.check("restored step")
+
+
+def test_one_attention_kernel_reads_bf16_and_partial_fp8_caches():
+    """The same attention kernel serves a prefill call on a bf16 cache and a
+    decode call on a "partial token-wise fp8" cache (e4m3 non-rotary dims with
+    a row scale, bf16 rotary dims) holding the same entries; each output is
+    compared with the oracle attending over the values that cache stores."""
+    import compressed_sparse_long_c128a_gb300 as csa
+
+    from compressed_sparse_long_c128a_gb300 import build as csa_build
+
+    csa_build.build()
+    rng = np.random.default_rng(31)
+    D, r, H, n_ent, k = 512, 64, 64, 2048, 512
+    layer = csa.make_layer(4, 8, D, r, H)
+    entries = rng.standard_normal((n_ent, D)).astype(np.float32)
+    window = rng.standard_normal((256, D)).astype(np.float32)  # window rows of positions 0..255 of block 0
+    pos = np.array([8150, 8160, 8190, 8197], dtype=np.int32)    # queries see entries < n_visible(p)
+    n_rows = len(pos)
+    q = torch.from_numpy(synth.round_bf16(rng.standard_normal((n_rows, H, D)))).to(torch.bfloat16).cuda()
+    sel = np.stack([rng.choice(O.n_visible(int(p), 4, 8), size=k, replace=False) for p in pos]).astype(np.int32)
+    comp_bt = torch.arange(32, dtype=torch.int32).reshape(1, 32).cuda()
+    # the window rows of every position live in the SWA cache's block = position // 256
+    swa_bt = torch.zeros((1, 33), dtype=torch.int32).cuda()
+    seq = torch.zeros(n_rows, dtype=torch.int32).cuda()
+    err = torch.zeros(1, dtype=torch.int32).cuda()
+    results = {}
+    for dtype, tail, call in (("bf16", 0, csa.sparse_attn_prefill), ("e4m3r", r, csa.sparse_attn_decode)):
+        dt = csa.DTYPES[dtype]
+        comp = csa.PagedCache.empty(32, 64, D, dt, "cuda", tail)
+        swa = csa.PagedCache.empty(1, 256, D, dt, "cuda", tail)
+        csa.cache_store(torch.from_numpy(entries).cuda(), torch.zeros(n_ent, dtype=torch.int32).cuda(),
+                        torch.arange(n_ent, dtype=torch.int32).cuda(), comp, comp_bt, err)
+        swa_rows = torch.arange(256, dtype=torch.int32).cuda()
+        csa.cache_store(torch.from_numpy(window).cuda(), torch.zeros(256, dtype=torch.int32).cuda(), swa_rows, swa,
+                        swa_bt, err)
+        out = torch.zeros((n_rows, H, D), dtype=torch.bfloat16).cuda()
+        ws = torch.empty(max(1, csa.sparse_attn_workspace_size(layer, n_rows, k)), dtype=torch.uint8).cuda()
+        call(layer, q, seq, torch.from_numpy(pos).cuda(), comp, comp_bt, torch.from_numpy(sel).cuda(), k, n_ent, swa,
+             swa_bt, out, csa.BF16, None, ws, err)
+        torch.cuda.synchronize()
+        assert csa.read_status(err) == 0, dtype
+        results[dtype] = out.to(torch.float64).cpu().numpy()
+    qh = q.to(torch.float64).cpu().numpy()
+    for dtype, tail in (("bf16", 0), ("e4m3r", r)):
+        if dtype == "bf16":
+            stored_ent = synth.round_bf16(entries).astype(np.float64)
+            stored_win = synth.round_bf16(window).astype(np.float64)
+        else:
+            stored_ent = O.dequantize_rows_e4m3_rope_bf16(*O.quantize_rows_e4m3_rope_bf16(entries, r))
+            stored_win = O.dequantize_rows_e4m3_rope_bf16(*O.quantize_rows_e4m3_rope_bf16(window, r))
+        for i, p in enumerate(pos):
+            # window rows [p-127, p] are positions of block p // 256 -- all mapped to block 0 by swa_bt
+            wpos = np.asarray(O.swa_positions(int(p), 128))
+            keys = np.concatenate([stored_ent[sel[i]], stored_win[wpos % 256]])
+            want = O.attention(qh[i], int(p), keys, D ** -0.5, r, 10000.0)
+            _assert_values(results[dtype][i], want, "bf16", f"{dtype} cache, row {i}")
+
