@@ -40,6 +40,11 @@ class BlockTableC(ctypes.Structure):
     _fields_ = [("table", ctypes.c_void_p), ("num_seqs", ctypes.c_int32), ("stride", ctypes.c_int32)]
 
 
+class QueryNormC(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("q_dtype", ctypes.c_int32), ("heads", ctypes.c_int32),
+                ("gamma", ctypes.c_void_p), ("q_out", ctypes.c_void_p), ("out_dtype", ctypes.c_int32)]
+
+
 class Layer(ctypes.Structure):
     _fields_ = [("ratio", ctypes.c_int32), ("window", ctypes.c_int32), ("dim", ctypes.c_int32),
                 ("rope_dim", ctypes.c_int32), ("heads", ctypes.c_int32), ("swa", ctypes.c_int32),
@@ -50,10 +55,13 @@ _lib = None
 
 _VP, _I32, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
 _PP, _PB, _PL = ctypes.POINTER(Paged), ctypes.POINTER(BlockTableC), ctypes.POINTER(Layer)
+_PQ = ctypes.POINTER(QueryNormC)
 
 _SIGS = {
     "csa_compress_insert": (_I32, [_PL, _VP, _VP, _I32, _I32, _VP, _VP, _VP, _VP, _VP, _PP, _PB, _PP, _PB, _PP,
                                    _PB, _VP, _VP]),
+    "csa_compress_insert_qnorm": (_I32, [_PL, _VP, _VP, _I32, _I32, _VP, _VP, _VP, _VP, _VP, _PP, _PB, _PP, _PB,
+                                         _PP, _PB, _PQ, _VP, _VP]),
     "csa_cache_store": (_I32, [_VP, _I32, _VP, _VP, _PP, _PB, _VP, _VP]),
     "csa_indexer_topk": (_I32, [_VP, _I32, _VP, _I32, _I32, _I32, _VP, _VP, _I32, _I32, _PP, _PB, _I32, _I32, _VP,
                                 _VP, _SZ, _VP, _VP]),
@@ -205,6 +213,26 @@ def compress_insert(layer: Layer, kv, gate, seq_id, pos, bias, gamma_c, gamma_sw
                                    ctypes.byref(comp.c()), ctypes.byref(block_table(comp_bt)), _ptr(err),
                                    _stream(stream))
     _check(st, "csa_compress_insert")
+
+
+def compress_insert_qnorm(layer: Layer, kv, gate, seq_id, pos, bias, gamma_c, gamma_swa, state: PagedCache,
+                          state_bt, swa: PagedCache | None, swa_bt, comp: PagedCache, comp_bt, q, gamma_q, q_out,
+                          err, stream=None):
+    """compress_insert plus q_out[j, h] := RMSNorm(q[j, h]; gamma_q) in the same launch.
+    q, q_out: [n_tok, heads, D] (f32 or bf16; q_out may be q itself)."""
+    if q.dim() != 3 or q_out.shape != q.shape or q.shape[0] != kv.shape[0]:
+        raise ValueError("q and q_out must be [n_tok, heads, D] with n_tok rows of kv")
+    qn = QueryNormC(_ptr(q), _tdtype(q), q.shape[1], _ptr(gamma_q), _ptr(q_out), _tdtype(q_out))
+    no_swa = swa is None
+    st = lib().csa_compress_insert_qnorm(ctypes.byref(layer), _ptr(kv), _ptr(gate), _tdtype(kv), kv.shape[0],
+                                         _ptr(seq_id), _ptr(pos), _ptr(bias), _ptr(gamma_c),
+                                         None if no_swa else _ptr(gamma_swa),
+                                         ctypes.byref(state.c()), ctypes.byref(block_table(state_bt)),
+                                         None if no_swa else ctypes.byref(swa.c()),
+                                         None if no_swa else ctypes.byref(block_table(swa_bt)),
+                                         ctypes.byref(comp.c()), ctypes.byref(block_table(comp_bt)),
+                                         ctypes.byref(qn), _ptr(err), _stream(stream))
+    _check(st, "csa_compress_insert_qnorm")
 
 
 def cache_store(rows, seq_id, row_idx, cache: PagedCache, bt, err, stream=None):

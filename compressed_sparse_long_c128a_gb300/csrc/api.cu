@@ -244,11 +244,13 @@ int attn_common(const csa_layer* L, const void* q, int32_t q_dtype, int32_t n_ro
 
 extern "C" {
 
-int csa_compress_insert(const csa_layer* L, const void* kv, const void* gate, int32_t in_dtype, int32_t n_tok,
-                        const int32_t* seq_id, const int32_t* pos, const float* bias, const float* gamma_c,
-                        const float* gamma_swa, const csa_paged* state, const csa_block_table* state_bt,
-                        const csa_paged* swa, const csa_block_table* swa_bt, const csa_paged* comp,
-                        const csa_block_table* comp_bt, int32_t* err, csa_stream_t stream) {
+namespace {
+
+int compress_insert(const csa_layer* L, const void* kv, const void* gate, int32_t in_dtype, int32_t n_tok,
+                    const int32_t* seq_id, const int32_t* pos, const float* bias, const float* gamma_c,
+                    const float* gamma_swa, const csa_paged* state, const csa_block_table* state_bt,
+                    const csa_paged* swa, const csa_block_table* swa_bt, const csa_paged* comp,
+                    const csa_block_table* comp_bt, const csa_query_norm* qn, int32_t* err, csa_stream_t stream) {
   int st = check_layer(L);
   if (st) return st;
   if (n_tok < 0) return CSA_ERR_INVALID_ARG;
@@ -261,6 +263,17 @@ int csa_compress_insert(const csa_layer* L, const void* kv, const void* gate, in
   if (swa && (st = check_paged(swa, L->dim, 256, kF32 | kBF16 | kE4M3 | kE4M3R))) return st;
   if ((st = check_paged(comp, L->dim, 256 / L->ratio, kF32 | kBF16 | kE4M3 | kE4M3R | kE2M1))) return st;
   if ((st = check_bt(state_bt)) || (swa && (st = check_bt(swa_bt))) || (st = check_bt(comp_bt))) return st;
+  QNormArgs qa{};
+  if (qn) {
+    if (!qn->q || !qn->gamma || !qn->q_out) return CSA_ERR_INVALID_ARG;
+    if (qn->heads < 1 || qn->heads > 1024) return CSA_ERR_INVALID_ARG;
+    if ((qn->q_dtype != CSA_F32 && qn->q_dtype != CSA_BF16) || (qn->out_dtype != CSA_F32 && qn->out_dtype != CSA_BF16))
+      return CSA_ERR_UNSUPPORTED;
+    const uintptr_t al = reinterpret_cast<uintptr_t>(qn->q) | reinterpret_cast<uintptr_t>(qn->gamma) |
+                         reinterpret_cast<uintptr_t>(qn->q_out);
+    if (L->dim % 8 || L->dim > 512 || al % 16) return CSA_ERR_UNSUPPORTED;
+    qa = QNormArgs{qn->q, qn->q_dtype, qn->gamma, qn->q_out, qn->out_dtype, qn->heads, L->dim, L->rms_eps};
+  }
   const RopeTab rt = make_rope(L->rope_dim, L->rope_theta);
   const csa_paged no_swa{};
   const csa_block_table no_swa_bt{};
@@ -268,10 +281,32 @@ int csa_compress_insert(const csa_layer* L, const void* kv, const void* gate, in
                 swa ? *swa_bt : no_swa_bt, L->dim, L->rms_eps, rt, err};
   EmitArgs ea{seq_id, pos, bias, gamma_c, *state, *state_bt, *comp, *comp_bt, L->dim, L->ratio, L->window,
               L->rms_eps, rt, err};
-  if (compress_fused_eligible(ia, ea, n_tok)) return cuda_status(launch_compress_fused(ia, ea, n_tok, stream));
-  cudaError_t e = launch_ingest(ia, n_tok, stream);
+  if (compress_fused_eligible(ia, ea, n_tok)) return cuda_status(launch_compress_fused(ia, ea, qa, n_tok, stream));
+  cudaError_t e = launch_ingest(ia, qa, n_tok, stream);
   if (e != cudaSuccess) return CSA_ERR_CUDA;
   return cuda_status(launch_emit(ea, n_tok, stream));
+}
+
+}  // namespace
+
+int csa_compress_insert(const csa_layer* L, const void* kv, const void* gate, int32_t in_dtype, int32_t n_tok,
+                        const int32_t* seq_id, const int32_t* pos, const float* bias, const float* gamma_c,
+                        const float* gamma_swa, const csa_paged* state, const csa_block_table* state_bt,
+                        const csa_paged* swa, const csa_block_table* swa_bt, const csa_paged* comp,
+                        const csa_block_table* comp_bt, int32_t* err, csa_stream_t stream) {
+  return compress_insert(L, kv, gate, in_dtype, n_tok, seq_id, pos, bias, gamma_c, gamma_swa, state, state_bt, swa,
+                         swa_bt, comp, comp_bt, nullptr, err, stream);
+}
+
+int csa_compress_insert_qnorm(const csa_layer* L, const void* kv, const void* gate, int32_t in_dtype,
+                              int32_t n_tok, const int32_t* seq_id, const int32_t* pos, const float* bias,
+                              const float* gamma_c, const float* gamma_swa, const csa_paged* state,
+                              const csa_block_table* state_bt, const csa_paged* swa, const csa_block_table* swa_bt,
+                              const csa_paged* comp, const csa_block_table* comp_bt, const csa_query_norm* qn,
+                              int32_t* err, csa_stream_t stream) {
+  if (!qn) return CSA_ERR_INVALID_ARG;
+  return compress_insert(L, kv, gate, in_dtype, n_tok, seq_id, pos, bias, gamma_c, gamma_swa, state, state_bt, swa,
+                         swa_bt, comp, comp_bt, qn, err, stream);
 }
 
 int csa_cache_store(const float* rows, int32_t n, const int32_t* seq_id, const int32_t* row_idx,

@@ -104,11 +104,24 @@ struct EmitArgs {
   int32_t* err;
 };
 
-cudaError_t launch_ingest(const IngestArgs& a, int32_t n_tok, cudaStream_t s);
+// query RMSNorm of the call's tokens, run by eight extra warps of the ingest or
+// fused kernel (q == nullptr: none)
+struct QNormArgs {
+  const void* q;
+  int32_t q_dtype;
+  const float* gamma;
+  void* out;
+  int32_t out_dtype;
+  int32_t heads, dim;
+  float eps;
+};
+
+cudaError_t launch_ingest(const IngestArgs& a, const QNormArgs& q, int32_t n_tok, cudaStream_t s);
 cudaError_t launch_emit(const EmitArgs& a, int32_t n_tok, cudaStream_t s);
 // one launch for calls of at most 1024 tokens (D % 8 == 0, D <= 512, 16-byte aligned rows)
 bool compress_fused_eligible(const IngestArgs& ia, const EmitArgs& ea, int32_t n_tok);
-cudaError_t launch_compress_fused(const IngestArgs& ia, const EmitArgs& ea, int32_t n_tok, cudaStream_t s);
+cudaError_t launch_compress_fused(const IngestArgs& ia, const EmitArgs& ea, const QNormArgs& q, int32_t n_tok,
+                                  cudaStream_t s);
 
 // ---- cache store (k_store.cu)
 struct StoreArgs {

@@ -14,7 +14,32 @@
 namespace csa {
 namespace {
 
+// Threads of the key path: warps 0-7.  With the query norm fused in
+// (csa_compress_insert_qnorm), warps 8-15 of the same CTA normalise the
+// token's query heads meanwhile (static dispatch by warp ID), so the key path
+// synchronises on named barrier 1 over its own 256 threads only.
 constexpr int kThreads = 256;
+constexpr int kQThreads = 256;  // query-norm warps
+
+__device__ __forceinline__ void grp_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
+
+// Sum / max over the key path's 256 threads; `red` is shared scratch of >= 8 floats.
+__device__ __forceinline__ float group_sum(float v, float* red) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  v = warp_sum(v);
+  grp_sync();
+  if (lane == 0) red[wid] = v;
+  grp_sync();
+  return warp_sum(lane < kThreads / 32 ? red[lane] : 0.f);
+}
+__device__ __forceinline__ float group_max(float v, float* red) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  v = warp_max(v);
+  grp_sync();
+  if (lane == 0) red[wid] = v;
+  grp_sync();
+  return warp_max(lane < kThreads / 32 ? red[lane] : 0.f);
+}
 
 __device__ __forceinline__ void store_elem(void* base, int32_t dtype, int64_t idx, float v) {
   if (dtype == CSA_F32)
@@ -29,42 +54,42 @@ __device__ void store_row(const csa_paged& c, int64_t prow, const float* y, int 
   if (c.dtype == CSA_E4M3R) {  // e4m3 + per-row scale over [0, D - tail), bf16 tail
     const int Dq = D - c.tail_bf16;
     float am = 0.f;
-    for (int d = threadIdx.x; d < Dq; d += blockDim.x) am = fmaxf(am, fabsf(y[d]));
-    am = block_max(am, red);
+    for (int d = threadIdx.x; d < Dq; d += kThreads) am = fmaxf(am, fabsf(y[d]));
+    am = group_max(am, red);
     const float inv = am > 0.f ? 448.0f / am : 0.0f;
     uint8_t* row = reinterpret_cast<uint8_t*>(c.data) + prow * row_bytes(c);
-    for (int pr = threadIdx.x; pr < Dq / 2; pr += blockDim.x)
+    for (int pr = threadIdx.x; pr < Dq / 2; pr += kThreads)
       *reinterpret_cast<uint16_t*>(row + 2 * pr) = f32x2_to_e4m3x2(y[2 * pr] * inv, y[2 * pr + 1] * inv);
-    for (int pr = threadIdx.x; pr < c.tail_bf16 / 2; pr += blockDim.x)
+    for (int pr = threadIdx.x; pr < c.tail_bf16 / 2; pr += kThreads)
       *reinterpret_cast<uint32_t*>(row + Dq + 4 * pr) = f32x2_to_bf16x2(y[Dq + 2 * pr], y[Dq + 2 * pr + 1]);
     if (threadIdx.x == 0) reinterpret_cast<float*>(c.scales)[prow] = am / 448.0f;
   } else if (c.dtype == CSA_E4M3) {
     float am = 0.f;
-    for (int d = threadIdx.x; d < D; d += blockDim.x) am = fmaxf(am, fabsf(y[d]));
-    am = block_max(am, red);
+    for (int d = threadIdx.x; d < D; d += kThreads) am = fmaxf(am, fabsf(y[d]));
+    am = group_max(am, red);
     const float scale = am / 448.0f;
     const float inv = am > 0.f ? 448.0f / am : 0.0f;
     uint8_t* row = reinterpret_cast<uint8_t*>(c.data) + prow * (int64_t)D;
-    for (int pr = threadIdx.x; pr < D / 2; pr += blockDim.x)
+    for (int pr = threadIdx.x; pr < D / 2; pr += kThreads)
       *reinterpret_cast<uint16_t*>(row + 2 * pr) = f32x2_to_e4m3x2(y[2 * pr] * inv, y[2 * pr + 1] * inv);
     if (threadIdx.x == 0) reinterpret_cast<float*>(c.scales)[prow] = scale;
   } else if (c.dtype == CSA_E2M1) {  // one thread per group of 16 (D % 16 == 0)
     uint8_t* row = reinterpret_cast<uint8_t*>(c.data) + prow * (int64_t)(D / 2);
     uint8_t* srow = reinterpret_cast<uint8_t*>(c.scales) + prow * (int64_t)(D / 16);
-    for (int g = threadIdx.x; g < D / 16; g += blockDim.x) {
+    for (int g = threadIdx.x; g < D / 16; g += kThreads) {
       uint2 packed;
       srow[g] = quantize_e2m1_group(y + 16 * g, packed);
       *reinterpret_cast<uint2*>(row + g * 8) = packed;
     }
   } else if (c.dtype == CSA_BF16) {
     uint16_t* row = reinterpret_cast<uint16_t*>(c.data) + prow * (int64_t)D;
-    for (int pr = threadIdx.x; pr < D / 2; pr += blockDim.x) {
+    for (int pr = threadIdx.x; pr < D / 2; pr += kThreads) {
       uint32_t v = (uint32_t)f32_to_bf16(y[2 * pr]) | ((uint32_t)f32_to_bf16(y[2 * pr + 1]) << 16);
       *reinterpret_cast<uint32_t*>(row + 2 * pr) = v;
     }
   } else {
     float* row = reinterpret_cast<float*>(c.data) + prow * (int64_t)D;
-    for (int pr = threadIdx.x; pr < D / 2; pr += blockDim.x)
+    for (int pr = threadIdx.x; pr < D / 2; pr += kThreads)
       *reinterpret_cast<float2*>(row + 2 * pr) = make_float2(y[2 * pr], y[2 * pr + 1]);
   }
 }
@@ -73,7 +98,7 @@ __device__ void store_row(const csa_paged& c, int64_t prow, const float* y, int 
 __device__ void norm_rope_inplace(float* y, int D, float inv_rms, const float* gamma, const RopeTab& rt,
                                   int64_t pos) {
   const int R = rt.rope_dim;
-  for (int pr = threadIdx.x; pr < D / 2; pr += blockDim.x) {
+  for (int pr = threadIdx.x; pr < D / 2; pr += kThreads) {
     int d = 2 * pr;
     float y0 = y[d] * inv_rms * gamma[d];
     float y1 = y[d + 1] * inv_rms * gamma[d + 1];
@@ -89,11 +114,86 @@ __device__ void norm_rope_inplace(float* y, int D, float inv_rms, const float* g
   }
 }
 
-__global__ void __launch_bounds__(kThreads) ingest_kernel(const IngestArgs a) {
+// Eight consecutive elements of a row in `dtype` (F32 or BF16) as floats; 16-byte (bf16) or
+// 2 x 16-byte (f32) loads, so `p` must be 16-byte aligned.
+__device__ __forceinline__ void load8(const void* base, int32_t dtype, int64_t idx, float* v) {
+  if (dtype == CSA_F32) {
+    const float4* p = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(base) + idx);
+    const float4 a = p[0], b = p[1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  } else {
+    const uint4 u = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(base) + idx);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      v[2 * e] = bf16_to_f32((uint16_t)(w[e] & 0xFFFF));
+      v[2 * e + 1] = bf16_to_f32((uint16_t)(w[e] >> 16));
+    }
+  }
+}
+
+__device__ __forceinline__ void store8(void* base, int32_t dtype, int64_t idx, const float* v) {
+  if (dtype == CSA_F32) {
+    float4* p = reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + idx);
+    p[0] = make_float4(v[0], v[1], v[2], v[3]);
+    p[1] = make_float4(v[4], v[5], v[6], v[7]);
+  } else {
+    *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(base) + idx) =
+        make_uint4(f32x2_to_bf16x2(v[0], v[1]), f32x2_to_bf16x2(v[2], v[3]), f32x2_to_bf16x2(v[4], v[5]),
+                   f32x2_to_bf16x2(v[6], v[7]));
+  }
+}
+
+// Warps 8-15 of a CTA with the query norm fused in: the RMSNorm of each head of
+// query row j (the row of token j), RoPE left to the attention kernel.  Lane l
+// holds elements [8l, 8l+8) and [256+8l, 256+8l+8) of a head (D <= 512).
+__device__ void qnorm_role(const QNormArgs& q, int64_t j, int qt) {
+  const int lane = qt & 31, w = qt >> 5;
+  const int D = q.dim;
+  for (int h = w; h < q.heads; h += kQThreads / 32) {
+    const int64_t base = (j * q.heads + h) * D;
+    float x[2][8];
+    float ss = 0.f;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int d0 = 8 * lane + 256 * u;
+      if (d0 < D) {
+        load8(q.q, q.q_dtype, base + d0, x[u]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss += x[u][e] * x[u][e];
+      }
+    }
+    ss = warp_sum(ss);
+    const float inv = 1.0f / sqrtf(ss / (float)D + q.eps);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int d0 = 8 * lane + 256 * u;
+      if (d0 < D) {
+        const float4* g4 = reinterpret_cast<const float4*>(q.gamma + d0);
+        const float4 g0 = g4[0], g1 = g4[1];
+        const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = x[u][e] * inv * g[e];
+        store8(q.out, q.out_dtype, base + d0, y);
+      }
+    }
+  }
+}
+
+template <bool kQ>
+__global__ void __launch_bounds__(kQ ? kThreads + kQThreads : kThreads) ingest_kernel(const IngestArgs a,
+                                                                                     const QNormArgs qa) {
   extern __shared__ float y[];
   __shared__ float red[32];
   pdl_trigger();
   pdl_wait();
+  if constexpr (kQ) {
+    if (threadIdx.x >= kThreads) {  // warps 8-15: the query norm
+      qnorm_role(qa, blockIdx.x, threadIdx.x - kThreads);
+      return;
+    }
+  }
   const int j = blockIdx.x;
   const int D = a.dim;
   const int seq = a.seq_id[j];
@@ -102,7 +202,7 @@ __global__ void __launch_bounds__(kThreads) ingest_kernel(const IngestArgs a) {
   const int64_t wrow = a.swa.data ? phys_row(a.swa_bt, a.swa, seq, p, a.err) : -1;  // no window cache: state only
 
   float ss = 0.f;
-  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+  for (int d = threadIdx.x; d < D; d += kThreads) {
     float x = load_elem(a.kv, a.in_dtype, (int64_t)j * D + d);
     y[d] = x;
     ss += x * x;
@@ -112,12 +212,12 @@ __global__ void __launch_bounds__(kThreads) ingest_kernel(const IngestArgs a) {
       store_elem(a.state.data, a.state.dtype, srow * 2 * D + D + d, g);
     }
   }
-  ss = block_sum(ss, red);
+  ss = group_sum(ss, red);
   if (wrow < 0) return;  // block-uniform
   const float inv = 1.0f / sqrtf(ss / (float)D + a.eps);
-  __syncthreads();
+  grp_sync();
   norm_rope_inplace(y, D, inv, a.gamma_swa, a.rope, p);
-  __syncthreads();
+  grp_sync();
   store_row(a.swa, wrow, y, D, red);
 }
 
@@ -140,19 +240,19 @@ __global__ void __launch_bounds__(kThreads) emit_kernel(const EmitArgs a) {
   const int seq = a.seq_id[j];
 
   if (threadIdx.x == 0) bad = 0;
-  __syncthreads();
-  for (int o = threadIdx.x; o < W; o += blockDim.x) {
+  grp_sync();
+  for (int o = threadIdx.x; o < W; o += kThreads) {
     int64_t r = phys_row(a.state_bt, a.state, seq, base + o, a.err);
     rows[o] = r;
     if (r < 0) bad = 1;
   }
   const int64_t crow = phys_row(a.comp_bt, a.comp, seq, i, a.err);
-  __syncthreads();
+  grp_sync();
   if (bad || crow < 0) return;
 
   const int sdt = a.state.dtype;
   float ss = 0.f;
-  for (int pr = threadIdx.x; pr < D / 2; pr += blockDim.x) {
+  for (int pr = threadIdx.x; pr < D / 2; pr += kThreads) {
     const int d = 2 * pr;
     float m0 = -INFINITY, m1 = -INFINITY, s0 = 0.f, s1 = 0.f, c0 = 0.f, c1 = 0.f;
 #pragma unroll 4
@@ -189,11 +289,11 @@ __global__ void __launch_bounds__(kThreads) emit_kernel(const EmitArgs a) {
     y[d + 1] = v1;
     ss += v0 * v0 + v1 * v1;
   }
-  ss = block_sum(ss, red);
+  ss = group_sum(ss, red);
   const float inv = 1.0f / sqrtf(ss / (float)D + a.eps);
-  __syncthreads();
+  grp_sync();
   norm_rope_inplace(y, D, inv, a.gamma_c, a.rope, base);
-  __syncthreads();
+  grp_sync();
   store_row(a.comp, crow, y, D, red);
 }
 
@@ -203,43 +303,14 @@ constexpr int kFusedMaxTokens = 1024;  // the (seq, pos) scan of an emitting CTA
 constexpr int kFusedMaxDim = 512;
 constexpr int kQuarters = 4;  // window rows split over four groups of threads per 8-channel group
 
-// Eight consecutive elements of a row in `dtype` (F32 or BF16) as floats; 16-byte (bf16) or
-// 2 x 16-byte (f32) loads, so `p` must be 16-byte aligned.
-__device__ __forceinline__ void load8(const void* base, int32_t dtype, int64_t idx, float* v) {
-  if (dtype == CSA_F32) {
-    const float4* p = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(base) + idx);
-    const float4 a = p[0], b = p[1];
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-  } else {
-    const uint4 u = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(base) + idx);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      v[2 * e] = bf16_to_f32((uint16_t)(w[e] & 0xFFFF));
-      v[2 * e + 1] = bf16_to_f32((uint16_t)(w[e] >> 16));
-    }
-  }
-}
-
-__device__ __forceinline__ void store8(void* base, int32_t dtype, int64_t idx, const float* v) {
-  if (dtype == CSA_F32) {
-    float4* p = reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + idx);
-    p[0] = make_float4(v[0], v[1], v[2], v[3]);
-    p[1] = make_float4(v[4], v[5], v[6], v[7]);
-  } else {
-    *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(base) + idx) =
-        make_uint4(f32x2_to_bf16x2(v[0], v[1]), f32x2_to_bf16x2(v[2], v[3]), f32x2_to_bf16x2(v[4], v[5]),
-                   f32x2_to_bf16x2(v[6], v[7]));
-  }
-}
-
 // CTA j takes token j of the call: state row and window row as ingest_kernel
 // writes them; then, if a window closes at the token, the entry as emit_kernel
 // forms it, but with every window row that is one of the call's own tokens
 // read from the call's inputs (the state cache holds the rest, written by
 // earlier calls), so no CTA depends on another CTA's writes.
-__global__ void __launch_bounds__(kThreads) compress_fused_kernel(const IngestArgs ia, const EmitArgs ea,
-                                                                  int32_t n_tok) {
+template <bool kQ>
+__global__ void __launch_bounds__(kQ ? kThreads + kQThreads : kThreads)
+    compress_fused_kernel(const IngestArgs ia, const EmitArgs ea, int32_t n_tok, const QNormArgs qa) {
   __shared__ float y[kFusedMaxDim];
   __shared__ float red[32];
   __shared__ float part[kQuarters][3][kFusedMaxDim];  // per row group: running max, denominator, weighted sum
@@ -250,6 +321,12 @@ __global__ void __launch_bounds__(kThreads) compress_fused_kernel(const IngestAr
   __shared__ int bad;
   pdl_trigger();
   pdl_wait();
+  if constexpr (kQ) {
+    if (threadIdx.x >= kThreads) {  // warps 8-15: the query norm
+      qnorm_role(qa, blockIdx.x, threadIdx.x - kThreads);
+      return;
+    }
+  }
   const int j = blockIdx.x;
   const int D = ia.dim, G8 = D / 8;
   const int seq = ia.seq_id[j];
@@ -259,7 +336,7 @@ __global__ void __launch_bounds__(kThreads) compress_fused_kernel(const IngestAr
 
   // ---- ingest
   float ss = 0.f;
-  for (int g = threadIdx.x; g < G8; g += blockDim.x) {
+  for (int g = threadIdx.x; g < G8; g += kThreads) {
     float x[8], gt[8];
     load8(ia.kv, ia.in_dtype, (int64_t)j * D + 8 * g, x);
     if (srow >= 0) {
@@ -273,12 +350,12 @@ __global__ void __launch_bounds__(kThreads) compress_fused_kernel(const IngestAr
       ss += x[e] * x[e];
     }
   }
-  ss = block_sum(ss, red);
+  ss = group_sum(ss, red);
   if (wrow >= 0) {  // block-uniform
     const float inv = 1.0f / sqrtf(ss / (float)D + ia.eps);
-    __syncthreads();
+    grp_sync();
     norm_rope_inplace(y, D, inv, ia.gamma_swa, ia.rope, p);
-    __syncthreads();
+    grp_sync();
     store_row(ia.swa, wrow, y, D, red);
   }
 
@@ -287,16 +364,16 @@ __global__ void __launch_bounds__(kThreads) compress_fused_kernel(const IngestAr
   if (p < W - 1 || (p - W + 1) % Rt) return;  // block-uniform
   const int64_t i = (p - W + 1) / Rt;
   const int64_t base = i * Rt;
-  __syncthreads();  // y and red are reused below
+  grp_sync();  // y and red are reused below
   if (threadIdx.x == 0) bad = 0;
-  for (int o = threadIdx.x; o < W; o += blockDim.x) in_call[o] = -1;
-  __syncthreads();
-  for (int k = threadIdx.x; k < n_tok; k += blockDim.x) {
+  for (int o = threadIdx.x; o < W; o += kThreads) in_call[o] = -1;
+  grp_sync();
+  for (int k = threadIdx.x; k < n_tok; k += kThreads) {
     const int64_t q = ea.pos[k];
     if (ea.seq_id[k] == seq && q >= base && q < base + W) in_call[q - base] = k;
   }
-  __syncthreads();
-  for (int o = threadIdx.x; o < W; o += blockDim.x) {
+  grp_sync();
+  for (int o = threadIdx.x; o < W; o += kThreads) {
     const int k = in_call[o];
     if (k >= 0) {
       src_kv[o] = reinterpret_cast<const uint8_t*>(ia.kv) + (int64_t)k * D * (ia.in_dtype == CSA_F32 ? 4 : 2);
@@ -316,12 +393,12 @@ __global__ void __launch_bounds__(kThreads) compress_fused_kernel(const IngestAr
     }
   }
   const int64_t crow = phys_row(ea.comp_bt, ea.comp, seq, i, ea.err);
-  __syncthreads();
+  grp_sync();
   if (bad || crow < 0) return;
 
   // online softmax over the window offsets, per channel: thread (g, qtr) takes
   // channels [8g, 8g+8) and offsets qtr, qtr+4, ...; the four row groups merge below
-  for (int x = threadIdx.x; x < G8 * kQuarters; x += blockDim.x) {
+  for (int x = threadIdx.x; x < G8 * kQuarters; x += kThreads) {
     const int g = x % G8, qtr = x / G8;
     float m[8], sm[8], c[8];
 #pragma unroll
@@ -359,9 +436,9 @@ __global__ void __launch_bounds__(kThreads) compress_fused_kernel(const IngestAr
       part[qtr][2][8 * g + e] = c[e];
     }
   }
-  __syncthreads();
+  grp_sync();
   float ss2 = 0.f;
-  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+  for (int d = threadIdx.x; d < D; d += kThreads) {
     float mx = -INFINITY;
 #pragma unroll
     for (int q = 0; q < kQuarters; ++q) mx = fmaxf(mx, part[q][0][d]);
@@ -378,11 +455,11 @@ __global__ void __launch_bounds__(kThreads) compress_fused_kernel(const IngestAr
     y[d] = v;
     ss2 += v * v;
   }
-  ss2 = block_sum(ss2, red);
+  ss2 = group_sum(ss2, red);
   const float inv = 1.0f / sqrtf(ss2 / (float)D + ea.eps);
-  __syncthreads();
+  grp_sync();
   norm_rope_inplace(y, D, inv, ea.gamma_c, ea.rope, base);
-  __syncthreads();
+  grp_sync();
   store_row(ea.comp, crow, y, D, red);
 }
 
@@ -394,14 +471,18 @@ bool compress_fused_eligible(const IngestArgs& ia, const EmitArgs& ea, int32_t n
   return n_tok <= kFusedMaxTokens && ia.dim % 8 == 0 && ia.dim <= kFusedMaxDim && ea.window <= 256 && al % 16 == 0;
 }
 
-cudaError_t launch_compress_fused(const IngestArgs& ia, const EmitArgs& ea, int32_t n_tok, cudaStream_t s) {
+cudaError_t launch_compress_fused(const IngestArgs& ia, const EmitArgs& ea, const QNormArgs& q, int32_t n_tok,
+                                  cudaStream_t s) {
   if (n_tok == 0) return cudaSuccess;
-  return launch_k(compress_fused_kernel, dim3(n_tok), dim3(kThreads), 0, s, 0, ia, ea, n_tok);
+  if (q.q) return launch_k(compress_fused_kernel<true>, dim3(n_tok), dim3(kThreads + kQThreads), 0, s, 0, ia, ea, n_tok, q);
+  return launch_k(compress_fused_kernel<false>, dim3(n_tok), dim3(kThreads), 0, s, 0, ia, ea, n_tok, q);
 }
 
-cudaError_t launch_ingest(const IngestArgs& a, int32_t n_tok, cudaStream_t s) {
+cudaError_t launch_ingest(const IngestArgs& a, const QNormArgs& q, int32_t n_tok, cudaStream_t s) {
   if (n_tok == 0) return cudaSuccess;
-  return launch_k(ingest_kernel, dim3(n_tok), dim3(kThreads), a.dim * sizeof(float), s, 0, a);
+  const size_t smem = a.dim * sizeof(float);
+  if (q.q) return launch_k(ingest_kernel<true>, dim3(n_tok), dim3(kThreads + kQThreads), smem, s, 0, a, q);
+  return launch_k(ingest_kernel<false>, dim3(n_tok), dim3(kThreads), smem, s, 0, a, q);
 }
 
 cudaError_t launch_emit(const EmitArgs& a, int32_t n_tok, cudaStream_t s) {

@@ -68,6 +68,7 @@ class LayerDev:
         self.bias = _dev(prm["bias"], device=device)
         self.gamma_c = _dev(prm["gamma_c"], device=device)
         self.gamma_swa = _dev(prm["gamma_swa"], device=device)
+        self.gamma_q = _dev(prm["gamma_q"], device=device)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
 
     # ------------------------------------------------------------------ set-up
@@ -110,6 +111,12 @@ class LayerDev:
         csa.compress_insert(self.c_layer, kv, gate, seq_id, pos, self.bias, self.gamma_c, self.gamma_swa,
                             self.state, self.tables["state"], self.swa, self.tables["swa"], self.comp,
                             self.tables["comp"], self.err, stream)
+
+    def compress_insert_qnorm(self, kv, gate, seq_id, pos, q, q_out, stream=None):
+        """compress_insert with the query RMSNorm (gamma_q) of the same tokens in its launch."""
+        csa.compress_insert_qnorm(self.c_layer, kv, gate, seq_id, pos, self.bias, self.gamma_c, self.gamma_swa,
+                                  self.state, self.tables["state"], self.swa, self.tables["swa"], self.comp,
+                                  self.tables["comp"], q, self.gamma_q, q_out, self.err, stream)
 
     def setup_ingest(self):
         """Ingest [ingest_from, first_new) of every sequence in one call."""

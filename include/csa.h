@@ -163,6 +163,44 @@ CSA_API int csa_compress_insert(const csa_layer* layer, const void* kv, const vo
                         const csa_block_table* comp_bt, int32_t* err, csa_stream_t stream);
 
 /*
+ * csa_query_norm -- the query half of [部署] §3.2's third fusion (Q norm + KV
+ * RoPE + K insert, one kernel with warps statically given to query heads or to
+ * the key): per token j and head h,
+ *   q_out[j][h] := RMSNorm(q[j][h]; gamma_q)   (over the D dims of the head)
+ * RoPE of the query is not applied here: csa_sparse_attention rotates it.
+ *   q      [n_tok][heads][D] q_dtype (F32 or BF16), 16-byte aligned
+ *   gamma  [D] float, 16-byte aligned
+ *   q_out  [n_tok][heads][D] out_dtype (F32 or BF16), 16-byte aligned; may equal q
+ *          when the dtypes match (each element is read before it is written)
+ *   heads  1..1024; eps is the layer's rms_eps.  Requires D % 8 == 0, D <= 512.
+ */
+typedef struct {
+  const void* q;
+  int32_t q_dtype;
+  int32_t heads;
+  const float* gamma;
+  void* q_out;
+  int32_t out_dtype;
+} csa_query_norm;
+
+/*
+ * csa_compress_insert_qnorm -- csa_compress_insert with the query RMSNorm of
+ * the same tokens fused into its launch ([部署] §3.2 third fusion; [Support]
+ * "GPU Compute Saturation", kernel fusions).  The caches are written exactly as
+ * csa_compress_insert writes them; qn (required) describes the query rows,
+ * one per token.  Extra errors: CSA_ERR_UNSUPPORTED when D % 8, D > 512 or an
+ * alignment rule of csa_query_norm is not met.
+ */
+CSA_API int csa_compress_insert_qnorm(const csa_layer* layer, const void* kv, const void* gate,
+                                      int32_t in_dtype, int32_t n_tok, const int32_t* seq_id,
+                                      const int32_t* pos, const float* bias, const float* gamma_c,
+                                      const float* gamma_swa, const csa_paged* state,
+                                      const csa_block_table* state_bt, const csa_paged* swa,
+                                      const csa_block_table* swa_bt, const csa_paged* comp,
+                                      const csa_block_table* comp_bt, const csa_query_norm* qn,
+                                      int32_t* err, csa_stream_t stream);
+
+/*
  * csa_cache_store -- write fp32 rows into a paged cache, quantising to its
  * dtype: logical row row_idx[j] of sequence seq_id[j] := rows[j].  This is the
  * insert of the indexer key cache and the way a caller loads entries it

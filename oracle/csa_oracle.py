@@ -101,6 +101,14 @@ def rms_norm(x, gamma, eps: float) -> np.ndarray:
     return x / np.sqrt(ms + eps) * np.asarray(gamma, dtype=np.float64)
 
 
+def query_norm(q, gamma_q, eps: float) -> np.ndarray:
+    """RMSNorm of every query head on its own: q [..., H, D] -> same shape, each
+    [D] vector divided by its own root mean square and scaled by gamma_q [D].
+    The Q half of the third fusion of "vLLM解密" §3.2 (Q norm + KV RoPE + K
+    insert); no RoPE here, the attention rotates the query."""
+    return rms_norm(q, gamma_q, eps)
+
+
 # ============================================================ compressor geometry
 
 

@@ -61,6 +61,7 @@ CACHE_KINDS = ("comp", "idx", "swa", "state")
 _T_BIAS, _T_GAMMA_C, _T_GAMMA_SWA, _T_KV, _T_GATE, _T_HIST, _T_KIDX = 1, 2, 3, 4, 5, 6, 7
 _T_Q, _T_QIDX, _T_W, _T_LENGTHS, _T_TABLE, _T_SUBSET, _T_OFFSETS = 8, 9, 10, 11, 12, 13, 14
 _T_IK_KV, _T_IK_GATE, _T_IK_BIAS, _T_IK_GAMMA, _T_IK_TABLE = 15, 16, 17, 18, 19
+_T_GAMMA_Q = 20
 
 
 def _rng(*key) -> np.random.Generator:
@@ -215,7 +216,8 @@ def layer_params(wl: Workload, layer: LayerSpec) -> dict:
     bias = _rng(wl.seed, _T_BIAS, layer.tid).normal(0.0, 0.1, size=(layer.window, D)).astype(np.float32)
     gamma_c = (1.0 + _rng(wl.seed, _T_GAMMA_C, layer.tid).normal(0.0, 0.02, size=D)).astype(np.float32)
     gamma_swa = (1.0 + _rng(wl.seed, _T_GAMMA_SWA, layer.tid).normal(0.0, 0.02, size=D)).astype(np.float32)
-    return {"bias": bias, "gamma_c": gamma_c, "gamma_swa": gamma_swa}
+    gamma_q = (1.0 + _rng(wl.seed, _T_GAMMA_Q, layer.tid).normal(0.0, 0.02, size=D)).astype(np.float32)
+    return {"bias": bias, "gamma_c": gamma_c, "gamma_swa": gamma_swa, "gamma_q": gamma_q}
 
 
 def seq_raw(wl: Workload, layer: LayerSpec, b: int):

@@ -89,6 +89,18 @@ def test_rms_norm_unit_rms_and_scale_invariance():
     np.testing.assert_allclose(O.rms_norm(7.5 * x, np.ones(512), 1e-12), y, rtol=1e-9)
 
 
+def test_query_norm_is_per_head():
+    # heads are normalised one by one, not over H*D: scaling one head changes no other
+    # head's output, and a head of (3, 4) with gamma (1, 2) gives the hand value above
+    q = np.array([[[3.0, 4.0], [30.0, -40.0], [1.0, 1.0]]])  # [1, H=3, D=2]
+    y = O.query_norm(q, np.array([1.0, 2.0]), 0.0)
+    r = math.sqrt(12.5)
+    np.testing.assert_allclose(y[0, 0], [3.0 / r, 8.0 / r], rtol=1e-15)
+    np.testing.assert_allclose(y[0, 1], [3.0 / r, -8.0 / r], rtol=1e-15)
+    np.testing.assert_allclose(y[0, 2], [1.0, 2.0], rtol=1e-15)
+    assert y.shape == q.shape
+
+
 # ------------------------------------------------------------------ geometry (pages' figures)
 
 
