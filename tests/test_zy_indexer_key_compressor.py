@@ -8,8 +8,9 @@ span the calls.  Checked: every complete window's entry (e2m1: the band
 comparison of `fp4_band`; bf16: 2e-2 max-abs and 1e-2 rel-L2 against the fp64
 entry), and that the rows of entries whose window is not complete stay zero.
 
-The file name sorts after the other GPU tests, so that under -x a failure
-here stops none of them.
+The file name sorts after the parity tests, so that under -x a failure here
+stops none of them, and before the allocation-free entry point's test, which
+is collected last.
 """
 
 import numpy as np
