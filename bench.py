@@ -41,6 +41,7 @@ core, each answering whole query rows of the same workload.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -448,8 +449,7 @@ def _clone_layer(ld):
     def cl(pc):
         if pc is None:
             return None
-        return csa.PagedCache(pc.data.clone(), None if pc.scales is None else pc.scales.clone(), pc.dtype,
-                              pc.rows_per_block, pc.dim)
+        return dataclasses.replace(pc, data=pc.data.clone(), scales=None if pc.scales is None else pc.scales.clone())
 
     c.comp, c.swa, c.state, c.idx = cl(ld.comp), cl(ld.swa), cl(ld.state), cl(ld.idx)
     return c

@@ -121,6 +121,18 @@ __device__ __forceinline__ float e4m3_to_f32(uint8_t v) {
   return __uint_as_float(s | ((e + 120u) << 23) | (m << 20));
 }
 
+// Two e4m3 codes (bits 0-7: lo, 8-15: hi) to two floats through the hardware
+// e4m3x2 -> f16x2 conversion, exact (every e4m3 value is an f16 value).
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t two) {
+  uint32_t h2;
+  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(h2) : "r"(two));
+  float lo, hi;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h2));
+  return make_float2(lo, hi);
+}
+
 // Round-to-nearest-even to e4m3 with saturation to +-448 (hardware cvt).
 __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
   uint16_t r;

@@ -160,7 +160,9 @@ struct IndexerArgs {
   uint32_t* cand_key;  // [grid][2 sel_k] order-preserving keys of the scores
   int32_t* cand_idx;   // [grid][2 sel_k] entry indices
   int32_t* cand_cnt;   // [grid]
-  uint32_t* cand_thr;  // [grid] every key of the CTA's range at or above it is in its list
+  uint32_t* cand_thr;
+  int32_t* cand_row_first;
+  int32_t* cand_row_ctas;  // [grid] every key of the CTA's range at or above it is in its list
 };
 cudaError_t launch_indexer_scores(const IndexerArgs& a, int32_t n_rows, cudaStream_t s);
 // tensor-core scores, 64 heads x 128 dims, bf16 or e2m1 keys (k_indexer_tc.cu)
@@ -176,14 +178,17 @@ int32_t indexer_deal_bound(int32_t n_rows, int32_t max_n, int32_t G);
 cudaError_t launch_indexer_tc(const IndexerArgs& a, int32_t n_rows, int32_t G, cudaStream_t s);
 
 // Candidate lists of a balanced deal: G CTAs x 2k (key, index) pairs, a count
-// and a threshold each;
+// and a threshold each, and each row's first CTA and CTA count (written by the
+// indexer's CTA 0, so the merge does not compute the deal again);
 // a deal uses at most kDealMaxCtas CTAs.
 constexpr int32_t kDealMaxCtas = 256;
 struct DealCandidates {
-  uint32_t* key;  // [ctas][cap]
-  int32_t* idx;   // [ctas][cap]
-  int32_t* cnt;   // [ctas]
-  uint32_t* thr;  // [ctas]
+  uint32_t* key;        // [ctas][cap]
+  int32_t* idx;         // [ctas][cap]
+  int32_t* cnt;         // [ctas]
+  uint32_t* thr;        // [ctas]
+  int32_t* row_first;   // [kDealMaxRows]
+  int32_t* row_ctas;    // [kDealMaxRows]
   int32_t ctas, cap;
 };
 size_t deal_candidate_bytes(int32_t G, int32_t k);

@@ -158,6 +158,7 @@ __device__ void producer_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mi
   const bool tail = a.comp.dtype == CSA_E4M3R;
   const int Dq = tail ? kD - a.comp.tail_bf16 : kD;  // dims [Dq, kD) are bf16 in the row
   const int n = g.n_tiles;
+  const uint64_t pol = policy_evict_first();  // every key row is read once per call
   // bf16: thread pt copies 16-byte piece (pt & 15) of keys 6j + (pt >> 4)
   constexpr int kGroups = kProducers / 16, kPerThr = (kTile + kGroups - 1) / kGroups;
   const int kg = pt >> 4, piece = pt & 15;
@@ -183,34 +184,41 @@ __device__ void producer_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mi
           const int k = kGroups * j + kg;
           if (k < lim) {
             const uint32_t dst = cbase + (k >> 3) * 1024 + (k & 7) * 128 + (((piece & 7) ^ (k & 7)) << 4);
-            cp_async16(dst, rps[j] ? rps[j] + c * 256 + piece * 16 : a.comp.data, rps[j] ? 16u : 0u);
+            cp_async16_hint(dst, rps[j] ? rps[j] + c * 256 + piece * 16 : a.comp.data, rps[j] ? 16u : 0u, pol);
           }
         }
         cp_async_arrive_noinc(&ms.kfull[slot][c]);
       }
     } else {
       // 8 consecutive threads per key row, 16 dims each: 16 code bytes -> 16 bf16
-      // (a piece of the bf16 tail: 32 bytes copied)
+      // (a piece of the bf16 tail: 32 bytes copied).  The loads of all four
+      // chunks of the tile are issued first (they wait for no slot), so the
+      // tile costs one memory latency, not four; the tail (at most 128 dims)
+      // lies in the last chunk.
       constexpr int kIters = (kTile * 8 + kProducers - 1) / kProducers;
-      for (int c = 0; c < kChunks; ++c) {
-        if (t >= 2) wait_or_abort(ms, &ms.kfree[slot][c], prev, a.err);
-        uint4 raw[kIters][2];
+      uint4 raw[kChunks][kIters], tl[kIters];
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c)
 #pragma unroll
         for (int it = 0; it < kIters; ++it) {
           const int x = pt + it * kProducers;
-          raw[it][0] = raw[it][1] = make_uint4(0, 0, 0, 0);
+          raw[c][it] = make_uint4(0, 0, 0, 0);
+          if (c == kChunks - 1) tl[it] = make_uint4(0, 0, 0, 0);
           if (x < lim * 8) {
             const uint8_t* rp = ms.rowptr[buf][x >> 3];
             const int d0 = c * 128 + (x & 7) * 16;
             if (rp && d0 < Dq) {
-              raw[it][0] = __ldg(reinterpret_cast<const uint4*>(rp + d0));
-            } else if (rp) {
-              const uint4* tp = reinterpret_cast<const uint4*>(rp + Dq + 2 * (d0 - Dq));
-              raw[it][0] = __ldg(tp);
-              raw[it][1] = __ldg(tp + 1);
+              raw[c][it] = ldg16_hint(rp + d0, pol);
+            } else if (rp && c == kChunks - 1) {
+              const uint8_t* tp = rp + Dq + 2 * (d0 - Dq);
+              raw[c][it] = ldg16_hint(tp, pol);
+              tl[it] = ldg16_hint(tp + 16, pol);
             }
           }
         }
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) {
+        if (t >= 2) wait_or_abort(ms, &ms.kfree[slot][c], prev, a.err);
 #pragma unroll
         for (int it = 0; it < kIters; ++it) {
           const int x = pt + it * kProducers;
@@ -219,15 +227,15 @@ __device__ void producer_role(const AttnArgs& a, const Geo& g, uint8_t* smem, Mi
           const int d0 = c * 128 + q8 * 16;
           uint32_t outw[8];
           if (d0 >= Dq) {
-            outw[0] = raw[it][0].x; outw[1] = raw[it][0].y; outw[2] = raw[it][0].z; outw[3] = raw[it][0].w;
-            outw[4] = raw[it][1].x; outw[5] = raw[it][1].y; outw[6] = raw[it][1].z; outw[7] = raw[it][1].w;
+            outw[0] = raw[c][it].x; outw[1] = raw[c][it].y; outw[2] = raw[c][it].z; outw[3] = raw[c][it].w;
+            outw[4] = tl[it].x; outw[5] = tl[it].y; outw[6] = tl[it].z; outw[7] = tl[it].w;
           } else {
-            const uint32_t w[4] = {raw[it][0].x, raw[it][0].y, raw[it][0].z, raw[it][0].w};
+            const uint32_t w[4] = {raw[c][it].x, raw[c][it].y, raw[c][it].z, raw[c][it].w};
             const float rs = tail ? ms.kscale[buf][key] : 1.f;  // E4M3R: the row scale, applied here
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-              const uint32_t b0 = (w[e >> 1] >> ((e & 1) * 16)) & 0xFF, b1 = (w[e >> 1] >> ((e & 1) * 16 + 8)) & 0xFF;
-              outw[e] = f32x2_to_bf16x2(e4m3_to_f32((uint8_t)b0) * rs, e4m3_to_f32((uint8_t)b1) * rs);
+              const float2 v = e4m3x2_to_f32x2(w[e >> 1] >> ((e & 1) * 16));
+              outw[e] = f32x2_to_bf16x2(v.x * rs, v.y * rs);
             }
           }
 #pragma unroll
@@ -837,7 +845,7 @@ bool attn_tc_eligible(const AttnArgs& a) {
   const uintptr_t al = reinterpret_cast<uintptr_t>(a.comp.data) | reinterpret_cast<uintptr_t>(a.swa.data);
   return a.dim == kD && a.heads == kH && a.comp.dtype == a.swa.dtype && a.comp.tail_bf16 == a.swa.tail_bf16 &&
          (a.comp.dtype == CSA_BF16 || a.comp.dtype == CSA_E4M3 || a.comp.dtype == CSA_E4M3R) &&
-         a.rope.rope_dim <= 128 && al % 16 == 0;
+         a.comp.tail_bf16 <= kD / kChunks && a.rope.rope_dim <= 128 && al % 16 == 0;
 }
 
 int32_t attn_tc_splits(int32_t n_rows, int32_t keys_per_row) {

@@ -329,24 +329,54 @@ __global__ void __launch_bounds__(kQ ? kThreads + kQThreads : kThreads)
   }
   const int j = blockIdx.x;
   const int D = ia.dim, G8 = D / 8;
+  // every load that depends only on j first: the token's raw row with its
+  // position (one memory latency), then all block-table lookups of the CTA
+  // (a second), then the ingest's writes; the window rows of the emission
+  // are the third and last dependent read
+  float x[8], gt[8];
+  const bool has_g = threadIdx.x < G8;  // D <= 512: one 8-channel group per thread
+  if (has_g) {
+    load8(ia.kv, ia.in_dtype, (int64_t)j * D + 8 * threadIdx.x, x);
+    load8(ia.gate, ia.in_dtype, (int64_t)j * D + 8 * threadIdx.x, gt);
+  }
   const int seq = ia.seq_id[j];
   const int64_t p = ia.pos[j];
+  const int W = ea.window, Rt = ea.ratio;
+  const bool emits = p >= W - 1 && (p - W + 1) % Rt == 0;  // block-uniform
+  const int64_t i = emits ? (p - W + 1) / Rt : 0;
+  const int64_t base = i * Rt;
   const int64_t srow = phys_row(ia.state_bt, ia.state, seq, p, ia.err);
   const int64_t wrow = ia.swa.data ? phys_row(ia.swa_bt, ia.swa, seq, p, ia.err) : -1;
+  int64_t crow = -1;
+  if (emits) {
+    crow = phys_row(ea.comp_bt, ea.comp, seq, i, ea.err);
+    // window row o from the state cache unless it is one of the call's tokens
+    // (those are read from the inputs: another CTA writes their state rows)
+    for (int o = threadIdx.x; o < W; o += kThreads) {
+      in_call[o] = -1;
+      const int64_t r = phys_row(ea.state_bt, ea.state, seq, base + o, ea.err);
+      const size_t eb = ea.state.dtype == CSA_F32 ? 4 : 2;
+      src_kv[o] = r < 0 ? nullptr : reinterpret_cast<const uint8_t*>(ea.state.data) + r * 2 * D * eb;
+      src_gate[o] = r < 0 ? nullptr : reinterpret_cast<const uint8_t*>(ea.state.data) + (r * 2 * D + D) * eb;
+      src_dt[o] = ea.state.dtype;
+    }
+    grp_sync();
+    for (int k = threadIdx.x; k < n_tok; k += kThreads) {
+      const int64_t q = ea.pos[k];
+      if (ea.seq_id[k] == seq && q >= base && q < base + W) in_call[q - base] = k;
+    }
+  }
 
   // ---- ingest
   float ss = 0.f;
-  for (int g = threadIdx.x; g < G8; g += kThreads) {
-    float x[8], gt[8];
-    load8(ia.kv, ia.in_dtype, (int64_t)j * D + 8 * g, x);
+  if (has_g) {
     if (srow >= 0) {
-      load8(ia.gate, ia.in_dtype, (int64_t)j * D + 8 * g, gt);
-      store8(ia.state.data, ia.state.dtype, srow * 2 * D + 8 * g, x);
-      store8(ia.state.data, ia.state.dtype, srow * 2 * D + D + 8 * g, gt);
+      store8(ia.state.data, ia.state.dtype, srow * 2 * D + 8 * threadIdx.x, x);
+      store8(ia.state.data, ia.state.dtype, srow * 2 * D + D + 8 * threadIdx.x, gt);
     }
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      y[8 * g + e] = x[e];
+      y[8 * threadIdx.x + e] = x[e];
       ss += x[e] * x[e];
     }
   }
@@ -360,18 +390,9 @@ __global__ void __launch_bounds__(kQ ? kThreads + kQThreads : kThreads)
   }
 
   // ---- emission of the entry whose window closes at this token
-  const int W = ea.window, Rt = ea.ratio;
-  if (p < W - 1 || (p - W + 1) % Rt) return;  // block-uniform
-  const int64_t i = (p - W + 1) / Rt;
-  const int64_t base = i * Rt;
-  grp_sync();  // y and red are reused below
+  if (!emits) return;
+  grp_sync();  // y and red are reused below; in_call is complete
   if (threadIdx.x == 0) bad = 0;
-  for (int o = threadIdx.x; o < W; o += kThreads) in_call[o] = -1;
-  grp_sync();
-  for (int k = threadIdx.x; k < n_tok; k += kThreads) {
-    const int64_t q = ea.pos[k];
-    if (ea.seq_id[k] == seq && q >= base && q < base + W) in_call[q - base] = k;
-  }
   grp_sync();
   for (int o = threadIdx.x; o < W; o += kThreads) {
     const int k = in_call[o];
@@ -379,20 +400,10 @@ __global__ void __launch_bounds__(kQ ? kThreads + kQThreads : kThreads)
       src_kv[o] = reinterpret_cast<const uint8_t*>(ia.kv) + (int64_t)k * D * (ia.in_dtype == CSA_F32 ? 4 : 2);
       src_gate[o] = reinterpret_cast<const uint8_t*>(ia.gate) + (int64_t)k * D * (ia.in_dtype == CSA_F32 ? 4 : 2);
       src_dt[o] = ia.in_dtype;
-    } else {
-      const int64_t r = phys_row(ea.state_bt, ea.state, seq, base + o, ea.err);
-      if (r < 0) {
-        bad = 1;
-        src_kv[o] = src_gate[o] = nullptr;
-      } else {
-        const size_t eb = ea.state.dtype == CSA_F32 ? 4 : 2;
-        src_kv[o] = reinterpret_cast<const uint8_t*>(ea.state.data) + r * 2 * D * eb;
-        src_gate[o] = reinterpret_cast<const uint8_t*>(ea.state.data) + (r * 2 * D + D) * eb;
-      }
-      src_dt[o] = ea.state.dtype;
+    } else if (!src_kv[o]) {
+      bad = 1;
     }
   }
-  const int64_t crow = phys_row(ea.comp_bt, ea.comp, seq, i, ea.err);
   grp_sync();
   if (bad || crow < 0) return;
 

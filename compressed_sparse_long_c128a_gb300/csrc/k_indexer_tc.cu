@@ -159,6 +159,7 @@ __device__ __forceinline__ int32_t tile_block(const Misc& ms, const Range& g, in
 template <bool kFp4>
 __device__ void producer_bf16(const IndexerArgs& a, const Range& g, uint8_t* smem, Misc& ms) {
   using P = Plan<kFp4>;
+  const uint64_t pol = policy_evict_first();
   for (int i = 0; i < g.nt; ++i) {
     const int s = i % P::kStages;
     if (i >= P::kStages) wait_or_abort(ms, &ms.empty[s], ((i / P::kStages) - 1) & 1, a.err);
@@ -176,8 +177,8 @@ __device__ void producer_bf16(const IndexerArgs& a, const Range& g, uint8_t* sme
       if (pb[h] >= 0)
 #pragma unroll
         for (int at = 0; at < kDI / 64; ++at)
-          tma_load_2d(sb + at * kAtomBytes + h * (kRowsPerBlock * 128), &a.k_map, 64 * at, pb[h] * kRowsPerBlock,
-                      &ms.full[s]);
+          tma_load_2d_hint(sb + at * kAtomBytes + h * (kRowsPerBlock * 128), &a.k_map, 64 * at,
+                           pb[h] * kRowsPerBlock, &ms.full[s], pol);
   }
 }
 
@@ -189,6 +190,7 @@ __device__ void producer_raw(const IndexerArgs& a, const Range& g, uint8_t* smem
   using P = Plan<kFp4>;
   const uint8_t* codes = reinterpret_cast<const uint8_t*>(a.cache.data);
   const uint8_t* scales = reinterpret_cast<const uint8_t*>(a.cache.scales);
+  const uint64_t pol = policy_evict_first();
   for (int i = 0; i < g.nt; ++i) {
     const int rs = i % P::kRaw;
     if (i >= P::kRaw) wait_or_abort(ms, &ms.raw_empty[rs], ((i / P::kRaw) - 1) & 1, a.err);
@@ -204,9 +206,10 @@ __device__ void producer_raw(const IndexerArgs& a, const Range& g, uint8_t* smem
 #pragma unroll
     for (int h = 0; h < 2; ++h)
       if (pb[h] >= 0) {
-        bulk_load(rb + h * kBlockCodes, codes + (int64_t)pb[h] * kBlockCodes, kBlockCodes, &ms.raw_full[rs]);
-        bulk_load(rb + kRawCodes + h * kBlockScales, scales + (int64_t)pb[h] * kBlockScales, kBlockScales,
-                  &ms.raw_full[rs]);
+        bulk_load_hint(rb + h * kBlockCodes, codes + (int64_t)pb[h] * kBlockCodes, kBlockCodes, &ms.raw_full[rs],
+                       pol);
+        bulk_load_hint(rb + kRawCodes + h * kBlockScales, scales + (int64_t)pb[h] * kBlockScales, kBlockScales,
+                       &ms.raw_full[rs], pol);
       }
   }
 }
@@ -322,6 +325,11 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(const __grid_co
     DealShared& ds = *reinterpret_cast<DealShared*>(smem + P::kOffStage);
     if (warp == 0) deal_compute(a.pos, a.n_rows, a.ratio, a.window, a.max_n, gridDim.x, ds);
     __syncthreads();
+    if (blockIdx.x == 0)  // each row's CTAs, for the merge
+      for (int r = tid; r < a.n_rows; r += kThreads) {
+        a.cand_row_first[r] = ds.first[r];
+        a.cand_row_ctas[r] = ds.ctas[r];
+      }
     if (tid == 0) {
       const DealSlot sl = deal_slot(ds, a.n_rows, blockIdx.x);
       ms.row = sl.row;
@@ -567,7 +575,7 @@ int32_t indexer_deal_bound(int32_t n_rows, int32_t max_n, int32_t G) {
 
 size_t deal_candidate_bytes(int32_t G, int32_t k) {
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
-  return 2 * up((size_t)G * 2 * k * 4) + 2 * up((size_t)G * 4);
+  return 2 * up((size_t)G * 2 * k * 4) + 2 * up((size_t)G * 4) + 2 * up((size_t)kDealMaxRows * 4);
 }
 
 DealCandidates deal_candidates(void* base, int32_t G, int32_t k) {
@@ -579,6 +587,8 @@ DealCandidates deal_candidates(void* base, int32_t G, int32_t k) {
   c.idx = reinterpret_cast<int32_t*>(p + lists);
   c.cnt = reinterpret_cast<int32_t*>(p + 2 * lists);
   c.thr = reinterpret_cast<uint32_t*>(p + 2 * lists + up((size_t)G * 4));
+  c.row_first = reinterpret_cast<int32_t*>(p + 2 * lists + 2 * up((size_t)G * 4));
+  c.row_ctas = reinterpret_cast<int32_t*>(p + 2 * lists + 2 * up((size_t)G * 4) + up((size_t)kDealMaxRows * 4));
   c.ctas = G;
   c.cap = 2 * k;
   return c;

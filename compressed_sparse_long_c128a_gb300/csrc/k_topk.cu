@@ -183,6 +183,8 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
 constexpr int kDealMergeThreads = 256;
 constexpr int kMaxMergeCluster = 16;
 constexpr int kMergeKeep = 4096;  // survivors a member keeps in shared memory after its first read
+constexpr int kMergeKeyWords = (padded_size(kMergeKeep) + 3) & ~3;
+constexpr size_t kMergeSmem = sizeof(uint32_t) * (kMergeKeyWords + kMergeKeep);
 
 // Row r: its CTAs' lists under the deal merged into the row's top-k by one
 // cluster of Cs CTAs.  CTA c's list holds every key of its range at or above
@@ -194,28 +196,36 @@ constexpr int kMergeKeep = 4096;  // survivors a member keeps in shared memory a
 // shared memory through the cluster (rank 0 picks each digit and hands it
 // back), and a last pass that places every survivor above the k-th key and
 // the first equal ones in entry order.
+//
+// A row whose lists hold at most kMergeKeep entries in all, merged by a
+// single CTA, takes a shorter way: every list entry is loaded into shared
+// memory once (lists in CTA order, each in entry order: the row's entry
+// order) and block_select picks the top-k there.  That is exact without the
+// survivor filter: each CTA's list holds its range's top-k, which holds every
+// entry of the row's top-k that lies in the range.
 __global__ void __launch_bounds__(kDealMergeThreads) topk_deal_merge_kernel(const TopkArgs a,
                                                                             const DealCandidates c, int n_rows) {
   constexpr int NT = kDealMergeThreads;
-  __shared__ DealShared ds;
   __shared__ int32_t off[kDealMaxRows + 1];  // start of each of the row's lists in the flattened array
   __shared__ uint32_t hloc[2048];            // this member's histogram of a pass
   __shared__ uint32_t hsum[3][2048];         // rank 0: the cluster's histograms
   __shared__ uint32_t wsum[32];
   __shared__ uint32_t s_thr, s_total, s_digit[3], s_rem[3];
   __shared__ uint32_t s_gt[kMaxMergeCluster], s_eq[kMaxMergeCluster];  // rank 0: members' counts
-  extern __shared__ uint32_t kept_key[];  // [kMergeKeep] this member's survivors in entry order, when they fit
-  int32_t* kept_idx = reinterpret_cast<int32_t*>(kept_key + kMergeKeep);  // [kMergeKeep]
+  __shared__ int32_t s_all;
+  // [padded_size(kMergeKeep)] this member's survivors in entry order, when they fit
+  // (the short way: every list entry, padded as block_select reads them)
+  extern __shared__ uint32_t kept_key[];
+  int32_t* kept_idx = reinterpret_cast<int32_t*>(kept_key + kMergeKeyWords);  // [kMergeKeep]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int Cs = gridDim.y, me = (int)tc::cluster_rank();
   for (int b = threadIdx.x; b < 3 * 2048; b += NT) (&hsum[0][0])[b] = 0;
   if (threadIdx.x == 0) s_total = 0;
   pdl_trigger();
   pdl_wait();  // the lists are complete only after the indexer launch
-  if (warp == 0) deal_compute(a.pos, n_rows, a.ratio, a.window, a.max_n, c.ctas, ds);
   tc::cluster_sync();  // rank 0's sums are zero before any member adds
   const int r = blockIdx.x;
-  const int first = ds.first[r], ctas = ds.ctas[r];
+  const int first = c.row_first[r], ctas = min(c.row_ctas[r], kDealMaxRows);
   const int K = a.k;
   int32_t* out = a.out + (int64_t)r * K;
   if (warp == 0) {  // lane l owns lists [8l, 8l+8): counts, thresholds, prefix
@@ -242,8 +252,44 @@ __global__ void __launch_bounds__(kDealMergeThreads) topk_deal_merge_kernel(cons
       run += cnt[i];
     }
     if (lane == 0) s_thr = t;
+    if (lane == 31) s_all = incl;
   }
   __syncthreads();
+  if (Cs == 1 && s_all <= kMergeKeep) {  // the short way (block-uniform)
+    const int all = s_all;
+    SelectScratch& sc = *reinterpret_cast<SelectScratch*>(&hsum[0][0]);
+    for (int v0 = threadIdx.x; v0 < all; v0 += 8 * NT) {
+      uint32_t kb[8];
+      int32_t ib[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {  // eight independent loads in flight per thread
+        const int v = v0 + u * NT;
+        if (v < all) {
+          int lo = 0, hi = ctas - 1;  // the list holding flattened entry v
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (off[mid] <= v) lo = mid;
+            else hi = mid - 1;
+          }
+          const int64_t e = (int64_t)(first + lo) * c.cap + (v - off[lo]);
+          kb[u] = c.key[e];
+          ib[u] = c.idx[e];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int v = v0 + u * NT;
+        if (v < all) {
+          kept_key[padded(v)] = kb[u];
+          kept_idx[v] = ib[u];
+        }
+      }
+    }
+    __syncthreads();
+    block_select<NT>(kept_key, all, K, sc, [&](int pos, uint32_t rank) { out[rank] = kept_idx[pos]; });
+    for (int i = min(all, K) + threadIdx.x; i < K; i += NT) out[i] = -1;
+    return;
+  }
   const uint32_t thr = s_thr;
   // this member's lists and its thread's contiguous slice of their entries
   const int per = (ctas + Cs - 1) / Cs, jb = min(ctas, me * per), je = min(ctas, jb + per);
@@ -541,7 +587,7 @@ cudaError_t launch_topk_deal_merge(const TopkArgs& a, int32_t n_rows, const Deal
     cudaError_t r = cudaFuncSetAttribute(topk_deal_merge_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (r == cudaSuccess)
       r = cudaFuncSetAttribute(topk_deal_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)(2 * kMergeKeep * sizeof(uint32_t)));
+                               (int)kMergeSmem);
     if (r == cudaSuccess) done = 1;
     return r;
   });
@@ -550,8 +596,7 @@ cudaError_t launch_topk_deal_merge(const TopkArgs& a, int32_t n_rows, const Deal
   // deal's lists per member (rows of a few lists merge in one CTA)
   int32_t cs = 1;
   while (cs < kMaxMergeCluster && 4 * cs * n_rows <= c.ctas) cs *= 2;
-  return launch_k(topk_deal_merge_kernel, dim3(n_rows, cs), dim3(kDealMergeThreads), 2 * kMergeKeep * sizeof(uint32_t),
-                  s, cs, a, c,
+  return launch_k(topk_deal_merge_kernel, dim3(n_rows, cs), dim3(kDealMergeThreads), kMergeSmem, s, cs, a, c,
                   (int)n_rows);
 }
 

@@ -70,3 +70,19 @@ def test_indexer_bytes_count_every_visible_key():
     n = sum((int(p) - L.window) // L.ratio + 1 for p in pos)
     q = len(pos) * L.idx_heads * (L.idx_dim * 2 + 4)
     assert bench.indexer_bytes(ld) == n * L.idx_dim * 2 + q + len(pos) * L.topk * 4
+
+
+def test_cache_replicas_keep_every_field():
+    # a partial-fp8 cache's bf16 tail must survive the replica copy
+    import types
+
+    import torch
+
+    import compressed_sparse_long_c128a_gb300 as csa
+
+    pc = csa.PagedCache.empty(2, 4, 64, csa.E4M3R, "cpu", 16)
+    ld = types.SimpleNamespace(comp=pc, swa=pc, state=None, idx=None)
+    c = bench._clone_layer(ld)
+    assert c.comp.tail_bf16 == 16 and c.comp.dim == 64 and c.comp.dtype == csa.E4M3R
+    assert c.comp.data.data_ptr() != pc.data.data_ptr() and torch.equal(c.comp.data, pc.data)
+    assert c.state is None
