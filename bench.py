@@ -7,7 +7,10 @@
 One step is one pass of the hot path over one batch of a workload: for every
 layer, csa_compress_insert of the step's new tokens, csa_indexer_topk (c4a
 layers) and the sparse attention call.  A token is one query row that
-completes that pass for one layer.
+completes that pass for one layer.  On a c4a layer compress_insert runs on a
+second stream beside the indexer and top-k, joined before the attention (the
+multi-stream split of the decode path; --one-stream puts every call on one
+stream).
 
 The headline workload is c4a DSA decode: 64 sequences at contexts uniform in
 [32768, 65536], D=512, H=64, indexer 64 heads x 128 dims, top-512, bf16.  The
@@ -78,8 +81,9 @@ def _args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--reference-seconds", type=float, default=150.0,
                     help="the reference arm stops after this many seconds of timed steps")
-    ap.add_argument("--side-stream", action="store_true",
-                    help="run each c4a layer's indexer + top-k on a second stream, beside compress_insert")
+    ap.add_argument("--one-stream", action="store_true",
+                    help="run every call of a c4a layer on one stream (default: compress_insert on a second "
+                         "stream, beside the indexer + top-k)")
     ap.add_argument("--load-seconds", type=float, default=1.5,
                     help="untimed graph replays before the timed steps, so the clock sampler sees load")
     return ap.parse_args(argv)
@@ -488,7 +492,7 @@ def measure_workload(idx: int, args, steps: int, world: int, local: int, pool=No
     replicas = 1 if step_bytes > 2.5 * L2_BYTES else int(math.ceil(2.5 * L2_BYTES / step_bytes)) + 1
     reps = [base] + [[_clone_layer(ld) for ld in base] for _ in range(replicas - 1)]
     stream = torch.cuda.Stream()
-    side = torch.cuda.Stream() if args.side_stream else None
+    side = None if args.one_stream else torch.cuda.Stream()
 
     def step(rep, s=None):
         for ld in rep:
@@ -596,8 +600,8 @@ def measure_workload(idx: int, args, steps: int, world: int, local: int, pool=No
            "calls": calls, "clocks": clk,
            "gpu_launches": n_full * full_launches + rest_launches,
            "kernels_per_step": kernels_per_step, "steps_per_graph": spg, "e2e": e2e}
-    if side is not None:
-        res["config"]["indexer_stream"] = "side"
+    if side is not None and any(ld.L.has_indexer for ld in base):
+        res["config"]["streams"] = "compress_insert on a second stream, beside indexer_topk"
     if pool is not None:
         res["cpu_baseline"] = oracle_baseline(pool, idx, args.cpu_seconds)
     del reps, base, wd

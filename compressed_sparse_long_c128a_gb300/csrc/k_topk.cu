@@ -185,6 +185,7 @@ constexpr int kMaxMergeCluster = 16;
 constexpr int kMergeKeep = 4096;  // survivors a member keeps in shared memory after its first read
 constexpr int kMergeKeyWords = (padded_size(kMergeKeep) + 3) & ~3;
 constexpr size_t kMergeSmem = sizeof(uint32_t) * (kMergeKeyWords + kMergeKeep);
+constexpr int kMergeWarmK = 512;  // the warm-up's dummy selection: top 512 of 1025 keys
 
 // Row r: its CTAs' lists under the deal merged into the row's top-k by one
 // cluster of Cs CTAs.  CTA c's list holds every key of its range at or above
@@ -196,6 +197,14 @@ constexpr size_t kMergeSmem = sizeof(uint32_t) * (kMergeKeyWords + kMergeKeep);
 // shared memory through the cluster (rank 0 picks each digit and hands it
 // back), and a last pass that places every survivor above the k-th key and
 // the first equal ones in entry order.
+// The short way's selection (shared memory to `dst`): one out-of-line copy of
+// the code, run once on dummy keys before the PDL wait and once for real.
+__device__ __noinline__ void merge_select(const uint32_t* keys, const int32_t* idx, int n, int k, SelectScratch& sc,
+                                          int32_t* dst) {
+  block_select<kDealMergeThreads>(keys, n, k, sc, [&](int pos, uint32_t rank) { dst[rank] = idx[pos]; });
+  for (int i = min(n, k) + threadIdx.x; i < k; i += kDealMergeThreads) dst[i] = -1;
+}
+
 //
 // A row whose lists hold at most kMergeKeep entries in all, merged by a
 // single CTA, takes a shorter way: every list entry is loaded into shared
@@ -219,9 +228,23 @@ __global__ void __launch_bounds__(kDealMergeThreads) topk_deal_merge_kernel(cons
   int32_t* kept_idx = reinterpret_cast<int32_t*>(kept_key + kMergeKeyWords);  // [kMergeKeep]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int Cs = gridDim.y, me = (int)tc::cluster_rank();
+  pdl_trigger();
+  // The CTA is resident long before the indexer ends.  Meanwhile, touching
+  // nothing in global memory, it runs the selection once on dummy keys in
+  // shared memory, so that the selection's instructions are in this SM's
+  // instruction cache when the lists arrive (fetching them then, a line at a
+  // time, cost several microseconds).
+  {
+    const int n = 2 * kMergeWarmK + 1, k = kMergeWarmK;
+    for (int i = threadIdx.x; i < n; i += NT) kept_key[padded(i)] = (uint32_t)i * 2654435761u;
+    for (int i = threadIdx.x; i < n; i += NT) kept_idx[i] = i;
+    __syncthreads();
+    merge_select(kept_key, kept_idx, n, k, *reinterpret_cast<SelectScratch*>(&hsum[0][0]),
+                 reinterpret_cast<int32_t*>(hloc));
+    __syncthreads();
+  }
   for (int b = threadIdx.x; b < 3 * 2048; b += NT) (&hsum[0][0])[b] = 0;
   if (threadIdx.x == 0) s_total = 0;
-  pdl_trigger();
   pdl_wait();  // the lists are complete only after the indexer launch
   tc::cluster_sync();  // rank 0's sums are zero before any member adds
   const int r = blockIdx.x;
@@ -286,8 +309,7 @@ __global__ void __launch_bounds__(kDealMergeThreads) topk_deal_merge_kernel(cons
       }
     }
     __syncthreads();
-    block_select<NT>(kept_key, all, K, sc, [&](int pos, uint32_t rank) { out[rank] = kept_idx[pos]; });
-    for (int i = min(all, K) + threadIdx.x; i < K; i += NT) out[i] = -1;
+    merge_select(kept_key, kept_idx, all, K, sc, out);
     return;
   }
   const uint32_t thr = s_thr;

@@ -26,11 +26,15 @@ __device__ __forceinline__ int padded(int i) { return i + (i >> 5); }
 __host__ __device__ constexpr int padded_size(int n) { return n + (n >> 5) + 1; }
 
 // Scratch of one block_select (shared memory, any 4-byte aligned region).
+// hist holds 4096 bucket counts, bucket b at hist_slot(b): thread t < 256
+// owns buckets [16t, 16t+16), stored 256 words apart, so that its reads hit
+// distinct banks.
 struct SelectScratch {
-  uint32_t hist[2048];
+  uint32_t hist[4096];
   uint32_t wsum[32];
   uint32_t digit, rem;
 };
+__device__ __forceinline__ int hist_slot(uint32_t b) { return (int)((b & 15u) * 256u + (b >> 4)); }
 
 // Exclusive prefix sum of v over the block; `total` receives the block sum.
 template <int NT>
@@ -61,32 +65,60 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* wsum, 
   return base + x - v;
 }
 
-// Histogram of digit (key >> sh) & (nb-1) over the keys matching prefix/mask.
-// With `aggregate`, lanes with the same digit are combined before the
-// shared-memory atomic (the leading digits of positive scores fall into a
-// handful of buckets; later passes see only the keys under the chosen prefix).
+// The bucket of the 4096-bucket histogram sc.hist that holds the rem-th
+// largest key (buckets counted from the top; 1 <= rem <= the total) into
+// sc.digit, and how many keys of that bucket are still needed into sc.rem.
+// Threads 0-255 own 16 buckets each; one suffix scan over them finds the
+// owner, which walks its own buckets.  Whole block (NT >= 256).
 template <int NT>
-__device__ __forceinline__ void digit_hist(const uint32_t* keys, int n, uint32_t prefix, uint32_t mask, int sh,
-                                           int nb, uint32_t* hist, bool aggregate) {
-  const int lane = threadIdx.x & 31;
-  for (int i0 = 0; i0 < n; i0 += NT) {
-    const int i = i0 + threadIdx.x;
-    const uint32_t key = i < n ? keys[padded(i)] : 0u;
-    const bool in = i < n && (key & mask) == prefix;
-    const uint32_t d = in ? (key >> sh) & (uint32_t)(nb - 1) : 0xFFFFFFFFu;
-    if (aggregate) {
-      const uint32_t peers = __match_any_sync(0xffffffffu, d);
-      if (in && lane == __ffs(peers) - 1) atomicAdd(&hist[d], (uint32_t)__popc(peers));
-    } else if (in) {
-      atomicAdd(&hist[d], 1u);
+__device__ __forceinline__ void find_digit(uint32_t rem, SelectScratch& sc) {
+  static_assert(NT >= 256, "256 threads own the buckets");
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  uint32_t c[16], s = 0, x = 0;
+  if (t < 256) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      c[j] = sc.hist[j * 256 + t];
+      s += c[j];
+    }
+    x = s;  // becomes the sum over this warp's lanes at or above this one
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_down_sync(0xffffffffu, x, o);
+      if (lane + o < 32) x += y;
+    }
+    if (lane == 0) sc.wsum[warp] = x;
+  }
+  __syncthreads();
+  if (t < 256) {
+    uint32_t above = x - s;  // keys in the buckets of the threads above this one
+    for (int w = warp + 1; w < 8; ++w) above += sc.wsum[w];
+    if (above < rem && rem <= above + s) {  // exactly one thread
+      uint32_t cum = above;
+#pragma unroll
+      for (int j = 15; j >= 0; --j) {
+        if (cum + c[j] >= rem) {
+          sc.digit = (uint32_t)(16 * t + j);
+          sc.rem = rem - cum;
+          break;
+        }
+        cum += c[j];
+      }
     }
   }
+  __syncthreads();
 }
 
 // Top min(k, n) of keys[0..n) (shared memory, padded as above, larger key =
 // better, equal keys: lower position first).  Calls emit(position, rank) for
 // every selected position, ranks 0.. in increasing position order.  Whole
-// block of NT threads; `sc` is shared scratch.
+// block of NT >= 256 threads; `sc` is shared scratch.
+//
+// The k-th largest key T is found by histograms over the keys' own range
+// [min, max]: each pass splits the current range into at most 4096 buckets
+// (a power-of-two width each) and keeps the bucket holding the rank, so a
+// range of b bits takes ceil(b / 12) passes (two when the keys span less than
+// 2^24 key values, as the scores of one row usually do).
 template <int NT, typename Emit>
 __device__ void block_select(const uint32_t* keys, int n, int k, SelectScratch& sc, Emit emit) {
   const int kk = n < k ? n : k;
@@ -94,45 +126,82 @@ __device__ void block_select(const uint32_t* keys, int n, int k, SelectScratch& 
     for (int i = threadIdx.x; i < n; i += NT) emit(i, (uint32_t)i);
     return;
   }
-  uint32_t prefix = 0, mask = 0, rem = (uint32_t)kk;
-  const int shifts[3] = {21, 10, 0};
-  const int widths[3] = {11, 11, 10};
-  for (int pass = 0; pass < 3; ++pass) {
-    const int sh = shifts[pass], nb = 1 << widths[pass];
-    for (int b = threadIdx.x; b < nb; b += NT) sc.hist[b] = 0;
+  constexpr int kU = 4;  // keys loaded per thread before any is used
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t mn = 0xFFFFFFFFu, mx = 0u;
+  for (int i0 = 0; i0 < n; i0 += kU * NT) {
+    uint32_t kv[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i = i0 + u * NT + threadIdx.x;
+      kv[u] = i < n ? keys[padded(i)] : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+      if (i0 + u * NT + (int)threadIdx.x < n) {
+        mn = min(mn, kv[u]);
+        mx = max(mx, kv[u]);
+      }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  if (lane == 0) {
+    sc.hist[warp] = mn;
+    sc.hist[32 + warp] = mx;
+  }
+  __syncthreads();
+  mn = 0xFFFFFFFFu;
+  mx = 0u;
+  for (int w = 0; w < NT / 32; ++w) {
+    mn = min(mn, sc.hist[w]);
+    mx = max(mx, sc.hist[32 + w]);
+  }
+  __syncthreads();
+  uint32_t base = mn, rem = (uint32_t)kk;
+  uint64_t width = (uint64_t)(mx - mn) + 1;  // the keys still in play lie in [base, base + width)
+  while (width > 1) {
+    const uint32_t span = (uint32_t)(width - 1);
+    const int sh = span < 4096u ? 0 : (32 - __clz(span)) - 12;
+    for (int b = threadIdx.x; b < 4096; b += NT) sc.hist[b] = 0;
     __syncthreads();
-    digit_hist<NT>(keys, n, prefix, mask, sh, nb, sc.hist, pass == 0);
-    __syncthreads();
-    // the digit d with count(> d) < rem <= count(>= d): thread t owns buckets
-    // [nb - (t+1)*bpt, nb - t*bpt), scanned from the top
-    const int bpt = (nb + NT - 1) / NT, top = nb - threadIdx.x * bpt;
-    uint32_t local = 0;
-    for (int j = 0; j < bpt; ++j)
-      if (top - 1 - j >= 0) local += sc.hist[top - 1 - j];
-    uint32_t tot;
-    const uint32_t above = block_excl_scan<NT>(local, sc.wsum, tot);
-    if (above < rem && rem <= above + local) {
-      uint32_t cum = above;
-      for (int j = 0; j < bpt && top - 1 - j >= 0; ++j) {
-        const uint32_t h = sc.hist[top - 1 - j];
-        if (cum + h >= rem) {
-          sc.digit = (uint32_t)(top - 1 - j);
-          sc.rem = rem - cum;
-          break;
+    for (int i0 = 0; i0 < n; i0 += kU * NT) {
+      uint32_t kv[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = i0 + u * NT + threadIdx.x;
+        kv[u] = i < n ? keys[padded(i)] : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = i0 + u * NT + threadIdx.x;
+        const bool in = i < n && kv[u] >= base && (uint64_t)(kv[u] - base) < width;
+        const uint32_t d = in ? (kv[u] - base) >> sh : 0xFFFFFFFFu;
+        // a warp whose keys share one bucket adds once (keys crowd a few
+        // buckets when a few outliers stretch the range)
+        const uint32_t d0 = __shfl_sync(0xffffffffu, d, 0);
+        if (__all_sync(0xffffffffu, d == d0)) {
+          if (lane == 0 && d0 != 0xFFFFFFFFu) atomicAdd(&sc.hist[hist_slot(d0)], 32u);
+        } else if (d != 0xFFFFFFFFu) {
+          atomicAdd(&sc.hist[hist_slot(d)], 1u);
         }
-        cum += h;
       }
     }
     __syncthreads();
-    prefix |= sc.digit << sh;
-    mask |= (uint32_t)(nb - 1) << sh;
+    find_digit<NT>(rem, sc);
+    const uint32_t d = sc.digit;
     rem = sc.rem;
+    const uint64_t lo = (uint64_t)d << sh;
+    base += (uint32_t)lo;
+    width = min(width - lo, (uint64_t)1 << sh);
     __syncthreads();
   }
   // every key above T, and the first `rem` keys equal to T in position order.
-  // Thread t owns the contiguous segment [t*seg, t*seg+seg): one scan ranks the
-  // equal keys, one more places the selected ones.
-  const uint32_t T = prefix;
+  // Thread t owns the contiguous segment [t*seg, t*seg+seg); one scan of the
+  // packed counts (above T, equal to T) ranks everything.
+  const uint32_t T = base;
   const int seg = (n + NT - 1) / NT;
   const int lo = threadIdx.x * seg, hi = min(n, lo + seg);
   uint32_t n_gt = 0, n_eq = 0;
@@ -141,10 +210,18 @@ __device__ void block_select(const uint32_t* keys, int n, int k, SelectScratch& 
     n_gt += key > T;
     n_eq += key == T;
   }
-  uint32_t tot;
-  const uint32_t eq0 = block_excl_scan<NT>(n_eq, sc.wsum, tot);
+  uint32_t tot, gt0, eq0;
+  if (n < 65536) {
+    const uint32_t packed = block_excl_scan<NT>((n_gt << 16) | n_eq, sc.wsum, tot);
+    gt0 = packed >> 16;
+    eq0 = packed & 0xFFFFu;
+  } else {
+    gt0 = block_excl_scan<NT>(n_gt, sc.wsum, tot);
+    eq0 = block_excl_scan<NT>(n_eq, sc.wsum, tot);
+  }
+  // the equal keys before this segment that are taken: min(eq0, rem)
   const uint32_t take_eq = eq0 >= rem ? 0u : min(n_eq, rem - eq0);
-  uint32_t rank = block_excl_scan<NT>(n_gt + take_eq, sc.wsum, tot);
+  uint32_t rank = gt0 + min(eq0, rem);
   uint32_t eq_seen = 0;
   for (int i = lo; i < hi; ++i) {
     const uint32_t key = keys[padded(i)];

@@ -197,10 +197,14 @@ class LayerDev:
     def step(self, stream=None, topk_override=None, side_stream=None):
         """compress_insert -> (indexer_topk) -> sparse attention.
 
-        With `side_stream`, the indexer pipeline of a c4a layer runs on it in
-        parallel with compress_insert on `stream` and is joined before the
-        attention (the indexer reads only the indexer cache and the step's
-        indexer queries, nothing compress_insert writes)."""
+        With `side_stream`, a c4a layer's compress_insert runs on it in
+        parallel with the indexer pipeline on `stream`, and is joined before
+        the attention (the indexer reads only the indexer cache and the step's
+        indexer queries, nothing compress_insert writes).  The indexer stays
+        on `stream`, right behind the previous attention, so that it takes
+        every SM as soon as that ends; compress_insert, which waits for the
+        previous attention as a whole, fills the SMs the indexer's shorter
+        ranges leave."""
         L, io = self.L, self.io
         main = torch.cuda.current_stream() if stream is None else stream
         use_side = side_stream is not None and L.has_indexer and topk_override is None
@@ -208,6 +212,7 @@ class LayerDev:
             fork = torch.cuda.Event()
             fork.record(main)
             side_stream.wait_event(fork)
+            self.compress_insert(io["kv"], io["gate"], io["seq_id"], io["pos"], side_stream)
         else:
             self.compress_insert(io["kv"], io["gate"], io["seq_id"], io["pos"], main)
         topk, k = None, 0
@@ -217,19 +222,16 @@ class LayerDev:
                 topk = topk_override
             else:
                 csa.indexer_topk(io["q_idx"], io["w"], io["seq_id"], io["pos"], L.ratio, L.window, self.idx,
-                                 self.tables["idx"], k, max(self.max_n, 1), io["topk"], self.ws_idx, self.err,
-                                 side_stream if use_side else main)
+                                 self.tables["idx"], k, max(self.max_n, 1), io["topk"], self.ws_idx, self.err, main)
                 topk = io["topk"]
         if use_side:
-            self.compress_insert(io["kv"], io["gate"], io["seq_id"], io["pos"], main)
             join = torch.cuda.Event()
             join.record(side_stream)
             main.wait_event(join)
-        stream = main
         attn = csa.sparse_attn_prefill if self.prefill else csa.sparse_attn_decode
         attn(self.c_layer, io["q"], io["seq_id"], io["pos"], self.comp, self.tables["comp"], topk, k,
              max(self.max_n, 1), self.swa, self.tables["swa"], io["out"], csa.DTYPES[L.out_dtype],
-             io["out_scales"], self.ws_attn, self.err, stream)
+             io["out_scales"], self.ws_attn, self.err, main)
 
     def check(self, what: str):
         st = csa.read_status(self.err, reset=True)
