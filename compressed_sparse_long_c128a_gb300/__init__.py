@@ -260,7 +260,7 @@ def indexer_topk(q_idx, w, seq_id, pos, ratio: int, window: int, idx_cache: Page
 def indexer_topk_noalloc(q_idx, w, seq_id, pos, ratio: int, window: int, idx_cache: PagedCache, bt, k: int,
                          max_n: int, out_idx, err, stream=None):
     """indexer_topk without a workspace, for callers that cannot allocate device
-    memory: its scratch is a fixed 8 MiB array inside the library, shared by
+    memory: its scratch is a fixed 16 MiB array inside the library, shared by
     every call (calls that may overlap on the GPU race; the first call on a
     device should come before any stream capture)."""
     n_rows, heads, dim = q_idx.shape

@@ -173,6 +173,7 @@ int csa::enqueue_indexer_topk(const void* q_idx, int32_t q_dtype, const float* w
     ia.cand_thr = dc.thr;
     ia.cand_row_first = dc.row_first;
     ia.cand_row_ctas = dc.row_ctas;
+    ia.cand_row_seg = dc.row_seg;
     if (launch_indexer_tc(ia, n_rows, G, stream) != cudaSuccess) return CSA_ERR_CUDA;
     TopkArgs ta{scores, pos, ratio, window, max_n, k, out_idx, err};
     return cuda_status(launch_topk_deal_merge(ta, n_rows, dc, stream));

@@ -162,7 +162,8 @@ struct IndexerArgs {
   int32_t* cand_cnt;   // [grid]
   uint32_t* cand_thr;
   int32_t* cand_row_first;
-  int32_t* cand_row_ctas;  // [grid] every key of the CTA's range at or above it is in its list
+  int32_t* cand_row_ctas;
+  int32_t* cand_row_seg;  // [grid] every key of the CTA's range at or above it is in its list
 };
 cudaError_t launch_indexer_scores(const IndexerArgs& a, int32_t n_rows, cudaStream_t s);
 // tensor-core scores, 64 heads x 128 dims, bf16 or e2m1 keys (k_indexer_tc.cu)
@@ -177,18 +178,21 @@ int32_t indexer_deal_bound(int32_t n_rows, int32_t max_n, int32_t G);
 // a.sel_k > 0: balanced deal on G CTAs; else one CTA per row and split
 cudaError_t launch_indexer_tc(const IndexerArgs& a, int32_t n_rows, int32_t G, cudaStream_t s);
 
-// Candidate lists of a balanced deal: G CTAs x 2k (key, index) pairs, a count
-// and a threshold each, and each row's first CTA and CTA count (written by the
-// indexer's CTA 0, so the merge does not compute the deal again);
-// a deal uses at most kDealMaxCtas CTAs.
+// Candidate lists of a balanced deal: two list slots per CTA (2c and 2c + 1)
+// of 2k (key, index) pairs, a count and a threshold each, and each row's
+// first CTA, list count and first slot's segment (written by the indexer's
+// CTA 0, so the merge does not compute the deal again): the lists of row r
+// are slot 2 first + seg, then slots 2c for the next ctas - 1 CTAs.  A deal
+// uses at most kDealMaxCtas CTAs.
 constexpr int32_t kDealMaxCtas = 256;
 struct DealCandidates {
-  uint32_t* key;        // [ctas][cap]
-  int32_t* idx;         // [ctas][cap]
-  int32_t* cnt;         // [ctas]
-  uint32_t* thr;        // [ctas]
+  uint32_t* key;        // [2 ctas][cap]
+  int32_t* idx;         // [2 ctas][cap]
+  int32_t* cnt;         // [2 ctas]
+  uint32_t* thr;        // [2 ctas]
   int32_t* row_first;   // [kDealMaxRows]
   int32_t* row_ctas;    // [kDealMaxRows]
+  int32_t* row_seg;     // [kDealMaxRows]
   int32_t ctas, cap;
 };
 size_t deal_candidate_bytes(int32_t G, int32_t k);

@@ -61,7 +61,7 @@ template <bool kFp4>
 struct Plan {
   static constexpr int kStages = kFp4 ? 3 : 4;       // bf16 tiles the MMA reads
   static constexpr int kRaw = kFp4 ? 6 : 0;          // raw e2m1 tiles in flight
-  static constexpr int kCapTiles = kFp4 ? 64 : 112;  // tiles whose keys the fused selection holds
+  static constexpr int kCapTiles = kFp4 ? 64 : 104;  // tiles whose keys the fused selection holds
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffStage = kQBytes;
   static constexpr uint32_t kOffRaw = kOffStage + kStages * kStageBytes;
@@ -71,13 +71,13 @@ struct Plan {
 };
 
 struct Misc {
-  uint64_t full[4], empty[4], raw_full[6], raw_empty[6], tfull[2], tempty[2], mma_done;
+  uint64_t full[4], empty[4], raw_full[6], raw_empty[6], tfull[2], tempty[2], mma_done, qswap;
   uint32_t tmem_base;
   int32_t abort;
-  int32_t row, t0, nt;
-  float w[kHI];
-  int32_t tbl[kTblMax];  // physical blocks of the CTA's entry range (-1: unmapped / out of range)
-  uint32_t hist0[2048];  // fused selection: counts of the keys' top 11 bits, built during the loop
+  int32_t row[2], t0[2], nt[2];  // the CTA's segments (row -1: none)
+  float w[2][kHI];
+  int32_t tbl[kTblMax];     // physical blocks of the CTA's tiles (-1: unmapped / out of range)
+  uint32_t hist0[2][2048];  // fused selection: counts of each segment's keys' top 11 bits, built during the loop
 };
 
 // Scratch of the selection after the loop, in the drained stage ring.
@@ -104,9 +104,15 @@ __device__ __forceinline__ bool wait_or_abort(Misc& ms, uint64_t* bar, uint32_t 
   return false;
 }
 
+// The CTA's tiles: segment 0, then segment 1 (under the even deal, the head
+// of the next row).  Local tile i < nt[0] is tile t0[0] + i of row[0]; the
+// rest are tiles 0.. of row[1].
 struct Range {
-  int row, seq;
-  int32_t n, t0, nt;  // visible entries of the row, first tile, tile count
+  int nseg, nt_all;
+  int row[2], seq[2];
+  int32_t n[2], t0[2], nt[2];  // visible entries of the row, first tile, tile count
+  __device__ __forceinline__ int seg_of(int i) const { return i >= nt[0] ? 1 : 0; }
+  __device__ __forceinline__ int32_t tile_of(int i) const { return i >= nt[0] ? t0[1] + i - nt[0] : t0[0] + i; }
 };
 
 // High and low bytes of the bf16 bits of the e2m1 magnitudes 0, 0.5, 1, 1.5, 2,
@@ -149,9 +155,9 @@ __device__ __forceinline__ uint32_t e4m3_bf16x2(uint8_t v) {
 // Physical block of tile-half h (0, 1) of tile i of the range, or -1 when
 // unmapped or past the visible entries (then nothing is loaded).
 __device__ __forceinline__ int32_t tile_block(const Misc& ms, const Range& g, int i, int h) {
-  const int32_t e = (g.t0 + i) * kTile + h * kRowsPerBlock;
-  const int32_t j = 2 * i + h;  // the cached table starts at the range's first block
-  return (e < g.n && j < kTblMax) ? ms.tbl[j] : -1;
+  const int32_t e = g.tile_of(i) * kTile + h * kRowsPerBlock;
+  const int32_t j = 2 * i + h;  // the cached table follows the CTA's tiles
+  return (e < g.n[g.seg_of(i)] && j < kTblMax) ? ms.tbl[j] : -1;
 }
 
 // bf16: one thread issues each tile as up to four TMA boxes (two blocks x two
@@ -160,7 +166,7 @@ template <bool kFp4>
 __device__ void producer_bf16(const IndexerArgs& a, const Range& g, uint8_t* smem, Misc& ms) {
   using P = Plan<kFp4>;
   const uint64_t pol = policy_evict_first();
-  for (int i = 0; i < g.nt; ++i) {
+  for (int i = 0; i < g.nt_all; ++i) {
     const int s = i % P::kStages;
     if (i >= P::kStages) wait_or_abort(ms, &ms.empty[s], ((i / P::kStages) - 1) & 1, a.err);
     int32_t pb[2];
@@ -191,7 +197,7 @@ __device__ void producer_raw(const IndexerArgs& a, const Range& g, uint8_t* smem
   const uint8_t* codes = reinterpret_cast<const uint8_t*>(a.cache.data);
   const uint8_t* scales = reinterpret_cast<const uint8_t*>(a.cache.scales);
   const uint64_t pol = policy_evict_first();
-  for (int i = 0; i < g.nt; ++i) {
+  for (int i = 0; i < g.nt_all; ++i) {
     const int rs = i % P::kRaw;
     if (i >= P::kRaw) wait_or_abort(ms, &ms.raw_empty[rs], ((i / P::kRaw) - 1) & 1, a.err);
     int32_t pb[2];
@@ -219,7 +225,7 @@ __device__ void producer_raw(const IndexerArgs& a, const Range& g, uint8_t* smem
 template <bool kFp4>
 __device__ void converter(const IndexerArgs& a, const Range& g, uint8_t* smem, Misc& ms, int ct) {
   using P = Plan<kFp4>;
-  for (int i = 0; i < g.nt; ++i) {
+  for (int i = 0; i < g.nt_all; ++i) {
     const int rs = i % P::kRaw, s = i % P::kStages;
     wait_or_abort(ms, &ms.raw_full[rs], (i / P::kRaw) & 1, a.err);
     if (i >= P::kStages) wait_or_abort(ms, &ms.empty[s], ((i / P::kStages) - 1) & 1, a.err);
@@ -247,28 +253,81 @@ __device__ void converter(const IndexerArgs& a, const Range& g, uint8_t* smem, M
   }
 }
 
+// Q_idx^T of `row` into the Q area, by threads [t0, t0 + nthr) of the CTA:
+// bf16, 128B-swizzled K-major, rows = heads; 8 dims per 16-byte piece, each
+// thread's loads (up to eight) issued before its stores.
+__device__ __forceinline__ void load_q(const IndexerArgs& a, int row, uint8_t* q_smem, int t, int nthr) {
+  constexpr int kPieces = kHI * kDI / 8;
+  for (int x0 = t; x0 < kPieces; x0 += 8 * nthr) {
+    uint32_t w[8][4];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int x = x0 + u * nthr;
+      if (x >= kPieces) break;
+      const int64_t qb = (int64_t)row * kHI * kDI + 8 * x;
+      if (a.q_dtype == CSA_BF16) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q_idx) + qb));
+        w[u][0] = v.x; w[u][1] = v.y; w[u][2] = v.z; w[u][3] = v.w;
+      } else {
+        const float4* src = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.q_idx) + qb);
+        const float4 v0 = __ldg(src), v1 = __ldg(src + 1);
+        w[u][0] = f32x2_to_bf16x2(v0.x, v0.y);
+        w[u][1] = f32x2_to_bf16x2(v0.z, v0.w);
+        w[u][2] = f32x2_to_bf16x2(v1.x, v1.y);
+        w[u][3] = f32x2_to_bf16x2(v1.z, v1.w);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int x = x0 + u * nthr;
+      if (x >= kPieces) break;
+      const int h = x / (kDI / 8), d0 = 8 * (x % (kDI / 8));
+      *reinterpret_cast<uint4*>(q_smem + sw128_offset(h, d0, kHI)) = make_uint4(w[u][0], w[u][1], w[u][2], w[u][3]);
+    }
+  }
+}
+
+// The MMA warp: lane 0 issues every MMA.  At the start of a second segment the
+// whole warp waits for the first segment's MMAs to finish reading Q and loads
+// the second row's Q_idx in its place (the producers keep streaming tiles
+// meanwhile).
 template <bool kFp4>
-__device__ void mma_role(const IndexerArgs& a, const Range& g, uint8_t* smem, Misc& ms, uint32_t tmem) {
+__device__ void mma_role(const IndexerArgs& a, const Range& g, uint8_t* smem, Misc& ms, uint32_t tmem, int lane) {
   using P = Plan<kFp4>;
   constexpr uint32_t idesc = idesc_bf16(128, kHI, 0, 0);
   const uint32_t stage0 = smem_u32(smem + P::kOffStage), qbase = smem_u32(smem + P::kOffQ);
-  for (int i = 0; i < g.nt; ++i) {
+  for (int i = 0; i < g.nt_all; ++i) {
     const int s = i % P::kStages, b = i & 1;
+    if (g.nseg == 2 && i == g.nt[0]) {
+      if (lane == 0) mma_commit(&ms.qswap);
+      __syncwarp();
+      wait_or_abort(ms, &ms.qswap, 0, a.err);
+      load_q(a, g.row[1], smem + P::kOffQ, lane, 32);
+      fence_proxy_async();
+      __syncwarp();
+    }
     wait_or_abort(ms, &ms.full[s], (i / P::kStages) & 1, a.err);
     if (i >= 2) wait_or_abort(ms, &ms.tempty[b], ((i >> 1) - 1) & 1, a.err);
     tc_fence_after();
+    if (lane == 0) {
 #pragma unroll
-    for (int ks = 0; ks < kDI / 16; ++ks) {
-      const uint64_t ad = sdesc_sw128(stage0 + s * kStageBytes + (ks >> 2) * kAtomBytes + (ks & 3) * 32, 16, 1024);
-      const uint64_t bd = sdesc_sw128(qbase + (ks >> 2) * (kHI * 128) + (ks & 3) * 32, 16, 1024);
-      mma_bf16(tmem + 64 * b, ad, bd, idesc, ks > 0);
+      for (int ks = 0; ks < kDI / 16; ++ks) {
+        const uint64_t ad =
+            sdesc_sw128(stage0 + s * kStageBytes + (ks >> 2) * kAtomBytes + (ks & 3) * 32, 16, 1024);
+        const uint64_t bd = sdesc_sw128(qbase + (ks >> 2) * (kHI * 128) + (ks & 3) * 32, 16, 1024);
+        mma_bf16(tmem + 64 * b, ad, bd, idesc, ks > 0);
+      }
+      mma_commit(&ms.empty[s]);
+      mma_commit(&ms.tfull[b]);
     }
-    mma_commit(&ms.empty[s]);
-    mma_commit(&ms.tfull[b]);
+    __syncwarp();
   }
   // nothing may still write TMEM when it is released, even after a timeout
-  mma_commit(&ms.mma_done);
-  if (!mbar_wait(&ms.mma_done, 0)) record_error(a.err, CSA_ERR_TIMEOUT);
+  if (lane == 0) {
+    mma_commit(&ms.mma_done);
+    if (!mbar_wait(&ms.mma_done, 0)) record_error(a.err, CSA_ERR_TIMEOUT);
+  }
+  __syncwarp();
 }
 
 // Scores of the range: to shared memory as order keys (fused selection) or to
@@ -280,11 +339,17 @@ __device__ void epilogue_role(const IndexerArgs& a, const Range& g, uint8_t* sme
   const uint32_t lane_addr = tmem + ((uint32_t)((et >> 5) * 32) << 16);
   float w[kHI];
 #pragma unroll
-  for (int h = 0; h < kHI; ++h) w[h] = ms.w[h];
+  for (int h = 0; h < kHI; ++h) w[h] = ms.w[0][h];
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem + P::kOffKeys);
-  float* out = a.scores + (int64_t)g.row * a.max_n;
-  for (int i = 0; i < g.nt; ++i) {
+  float* out = a.scores + (int64_t)g.row[0] * a.max_n;
+  int seg = 0;
+  for (int i = 0; i < g.nt_all; ++i) {
     const int b = i & 1;
+    if (g.nseg == 2 && i == g.nt[0]) {  // the second row's weights
+      seg = 1;
+#pragma unroll
+      for (int h = 0; h < kHI; ++h) w[h] = ms.w[1][h];
+    }
     wait_or_abort(ms, &ms.tfull[b], (i >> 1) & 1, a.err);
     tc_fence_after();
     float v[kHI];
@@ -296,13 +361,13 @@ __device__ void epilogue_role(const IndexerArgs& a, const Range& g, uint8_t* sme
     float s = 0.f;
 #pragma unroll
     for (int h = 0; h < kHI; ++h) s = fmaf(w[h], fmaxf(v[h], 0.f), s);
-    const int32_t e = (g.t0 + i) * kTile + et, j = 2 * i + et / kRowsPerBlock;
-    if (e < g.n) {
+    const int32_t e = g.tile_of(i) * kTile + et, j = 2 * i + et / kRowsPerBlock;
+    if (e < g.n[seg]) {
       const float sc = (j < kTblMax && ms.tbl[j] >= 0) ? s : -INFINITY;
       if (a.sel_k > 0) {
         const uint32_t key = order_key(sc);
         keys[padded(i * kTile + et)] = key;
-        atomicAdd(&ms.hist0[key >> 21], 1u);
+        atomicAdd(&ms.hist0[seg][key >> 21], 1u);
       } else {
         out[e] = sc;
       }
@@ -320,46 +385,64 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(const __grid_co
   pdl_trigger();
   pdl_wait();  // before any access to memory: the previous kernel on the stream may still be running
 
-  // the CTA's row and tile range
+  // the CTA's rows and tile ranges
   if (a.sel_k > 0) {
     DealShared& ds = *reinterpret_cast<DealShared*>(smem + P::kOffStage);
-    if (warp == 0) deal_compute(a.pos, a.n_rows, a.ratio, a.window, a.max_n, gridDim.x, ds);
+    if (warp == 0) deal_compute(a.pos, a.n_rows, a.ratio, a.window, a.max_n, gridDim.x, P::kCapTiles, ds);
     __syncthreads();
-    if (blockIdx.x == 0)  // each row's CTAs, for the merge
+    if (blockIdx.x == 0)  // each row's list slots, for the merge
       for (int r = tid; r < a.n_rows; r += kThreads) {
         a.cand_row_first[r] = ds.first[r];
         a.cand_row_ctas[r] = ds.ctas[r];
+        a.cand_row_seg[r] = ds.seg[r];
       }
     if (tid == 0) {
-      const DealSlot sl = deal_slot(ds, a.n_rows, blockIdx.x);
-      ms.row = sl.row;
-      ms.t0 = sl.t0;
-      ms.nt = sl.nt;
+      const DealSlot sl = deal_slot(ds, a.n_rows, blockIdx.x, gridDim.x);
+      for (int q = 0; q < 2; ++q) {
+        ms.row[q] = sl.row[q];
+        ms.t0[q] = sl.t0[q];
+        ms.nt[q] = sl.nt[q];
+      }
     }
   } else if (tid == 0) {
     // one row per blockIdx.x, its tiles split in equal parts over gridDim.y
     const int r = blockIdx.x;
     const int32_t tiles = deal_row_tiles(a.pos, r, a.ratio, a.window, a.max_n);
     const int32_t per = (tiles + gridDim.y - 1) / gridDim.y;
-    ms.row = r;
-    ms.t0 = min(tiles, (int32_t)blockIdx.y * per);
-    ms.nt = min(tiles, ms.t0 + per) - ms.t0;
+    ms.row[0] = r;
+    ms.t0[0] = min(tiles, (int32_t)blockIdx.y * per);
+    ms.nt[0] = min(tiles, ms.t0[0] + per) - ms.t0[0];
+    ms.row[1] = -1;
+    ms.t0[1] = ms.nt[1] = 0;
   }
   __syncthreads();
   Range g;
-  g.row = ms.row;
-  g.t0 = ms.t0;
-  g.nt = ms.nt;
-  if (g.row < 0) return;  // a CTA the deal left without work
-  if (a.sel_k > 0 && g.nt > P::kCapTiles) {  // the launcher's bound rules this out; never overrun the key store
-    if (tid == 0) record_error(a.err, CSA_ERR_DEVICE_BOUNDS);
-    g.nt = P::kCapTiles;
+  g.nseg = ms.row[0] < 0 ? 0 : (ms.row[1] < 0 ? 1 : 2);
+  if (g.nseg == 0) return;  // a CTA the deal left without work
+  for (int q = 0; q < 2; ++q) {
+    g.row[q] = ms.row[q];
+    g.t0[q] = ms.t0[q];
+    g.nt[q] = q < g.nseg ? ms.nt[q] : 0;
   }
-  g.seq = a.seq_id[g.row];
-  g.n = n_visible(a.pos[g.row], a.ratio, a.window);
-  if (g.n > a.max_n) {
-    if (tid == 0 && (a.sel_k > 0 ? g.t0 == 0 : blockIdx.y == 0)) record_error(a.err, CSA_ERR_DEVICE_BOUNDS);
-    g.n = a.max_n;
+  if (a.sel_k > 0 && g.nt[0] + g.nt[1] > P::kCapTiles) {
+    // the launcher's bound and the deal rule this out; never overrun the key store
+    if (tid == 0) record_error(a.err, CSA_ERR_DEVICE_BOUNDS);
+    g.nt[0] = min(g.nt[0], P::kCapTiles);
+    g.nt[1] = min(g.nt[1], P::kCapTiles - g.nt[0]);
+    if (g.nt[1] == 0) g.nseg = 1;
+  }
+  g.nt_all = g.nt[0] + g.nt[1];
+  for (int q = 0; q < g.nseg; ++q) {
+    g.seq[q] = a.seq_id[g.row[q]];
+    g.n[q] = n_visible(a.pos[g.row[q]], a.ratio, a.window);
+    if (g.n[q] > a.max_n) {
+      if (tid == 0 && (a.sel_k > 0 ? g.t0[q] == 0 : blockIdx.y == 0)) record_error(a.err, CSA_ERR_DEVICE_BOUNDS);
+      g.n[q] = a.max_n;
+    }
+  }
+  if (g.nseg == 1) {
+    g.seq[1] = -1;
+    g.n[1] = 0;
   }
 
   if (tid == 0) {
@@ -376,58 +459,29 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(const __grid_co
       mbar_init(&ms.tempty[b], kEpi);
     }
     mbar_init(&ms.mma_done, 1);
+    mbar_init(&ms.qswap, 1);
     mbar_init_fence();
     ms.abort = 0;
   }
-  if (tid < kHI) ms.w[tid] = a.w[(int64_t)g.row * kHI + tid];
-  for (int b = tid; b < 2048; b += kThreads) ms.hist0[b] = 0;
+  if (tid < g.nseg * kHI) ms.w[tid / kHI][tid % kHI] = a.w[(int64_t)g.row[tid / kHI] * kHI + tid % kHI];
+  for (int b = tid; b < 2 * 2048; b += kThreads) (&ms.hist0[0][0])[b] = 0;
   {
-    // block-table slice of the CTA's entry range
-    const int32_t blk0 = g.t0 * (kTile / kRowsPerBlock);
-    const int32_t nblk = min(kTblMax, g.nt * (kTile / kRowsPerBlock));
+    // block-table entries of the CTA's tiles, two blocks a tile
+    const int32_t nblk = min(kTblMax, g.nt_all * (kTile / kRowsPerBlock));
     for (int j = tid; j < nblk; j += kThreads) {
-      const int32_t lb = blk0 + j;
+      const int i = j / (kTile / kRowsPerBlock), q = g.seg_of(i);
+      const int32_t lb = g.tile_of(i) * (kTile / kRowsPerBlock) + j % (kTile / kRowsPerBlock);
       int32_t pb = -1;
-      if (g.seq >= 0 && g.seq < a.bt.num_seqs && lb < a.bt.stride) {
-        pb = a.bt.table[(int64_t)g.seq * a.bt.stride + lb];
+      if (g.seq[q] >= 0 && g.seq[q] < a.bt.num_seqs && lb < a.bt.stride) {
+        pb = a.bt.table[(int64_t)g.seq[q] * a.bt.stride + lb];
         if (pb >= a.cache.num_blocks) pb = -1;
       }
-      if (pb < 0 && lb * kRowsPerBlock < g.n) record_error(a.err, CSA_ERR_DEVICE_BOUNDS);
+      if (pb < 0 && lb * kRowsPerBlock < g.n[q]) record_error(a.err, CSA_ERR_DEVICE_BOUNDS);
       ms.tbl[j] = pb;
     }
   }
   if (warp == kMmaWarp) tmem_alloc(&ms.tmem_base, kTmemCols);
-  // Q_idx^T: bf16, 128B-swizzled K-major, rows = heads; 8 dims per 16-byte
-  // piece, every thread's loads issued before its stores
-  {
-    constexpr int kPieces = kHI * kDI / 8;
-    constexpr int kPer = (kPieces + kThreads - 1) / kThreads;
-    uint32_t w[kPer][4];
-#pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-      const int x = min(tid + u * kThreads, kPieces - 1);  // clamped; stored below only when in range
-      const int64_t qb = (int64_t)g.row * kHI * kDI + 8 * x;
-      if (a.q_dtype == CSA_BF16) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q_idx) + qb));
-        w[u][0] = v.x; w[u][1] = v.y; w[u][2] = v.z; w[u][3] = v.w;
-      } else {
-        const float4* src = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.q_idx) + qb);
-        const float4 v0 = __ldg(src), v1 = __ldg(src + 1);
-        w[u][0] = (uint32_t)f32_to_bf16(v0.x) | ((uint32_t)f32_to_bf16(v0.y) << 16);
-        w[u][1] = (uint32_t)f32_to_bf16(v0.z) | ((uint32_t)f32_to_bf16(v0.w) << 16);
-        w[u][2] = (uint32_t)f32_to_bf16(v1.x) | ((uint32_t)f32_to_bf16(v1.y) << 16);
-        w[u][3] = (uint32_t)f32_to_bf16(v1.z) | ((uint32_t)f32_to_bf16(v1.w) << 16);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-      const int x = tid + u * kThreads;
-      if (x >= kPieces) break;
-      const int h = x / (kDI / 8), d0 = 8 * (x % (kDI / 8));
-      *reinterpret_cast<uint4*>(smem + P::kOffQ + sw128_offset(h, d0, kHI)) =
-          make_uint4(w[u][0], w[u][1], w[u][2], w[u][3]);
-    }
-  }
+  load_q(a, g.row[0], smem + P::kOffQ, tid, kThreads);
   fence_proxy_async();
   tc_fence_before();
   __syncthreads();
@@ -446,8 +500,8 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(const __grid_co
         converter<kFp4>(a, g, smem, ms, tid - kEpi - 32);
       }
     }
-  } else if ((tid & 31) == 0) {
-    mma_role<kFp4>(a, g, smem, ms, tmem);
+  } else {
+    mma_role<kFp4>(a, g, smem, ms, tmem, tid & 31);
   }
   tc_fence_before();
   __syncthreads();
@@ -457,101 +511,106 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(const __grid_co
   }
   if (a.sel_k <= 0) return;
 
-  // fused selection.  The list this CTA hands to the merge is every key of its
-  // range at or above T22, the k-th largest key with its low 10 bits cleared
-  // (a superset of the range's top-k, in entry order), with T22 itself: the
-  // merge keeps only keys at or above the largest T22 of the row's CTAs, which
-  // is at most the row's own k-th key.  Radix digits: the top 11 bits were
-  // counted during the loop; one more pass fixes the next 11.
-  const int32_t e0 = g.t0 * kTile;
-  const int n_local = max(0, min(g.n, (g.t0 + g.nt) * kTile) - e0);
-  const uint32_t* keys = reinterpret_cast<const uint32_t*>(smem + P::kOffKeys);
+  // fused selection, once per segment.  The list a segment hands to the merge
+  // is every key of its range at or above T22, the k-th largest key with its
+  // low 10 bits cleared (a superset of the range's top-k, in entry order), with
+  // T22 itself: the merge keeps only keys at or above the largest T22 of the
+  // row's lists, which is at most the row's own k-th key.  Radix digits: the
+  // top 11 bits were counted during the loop; one more pass fixes the next 11.
   PickScratch& pk = *reinterpret_cast<PickScratch*>(smem + P::kOffStage);
   SelectScratch& sc = *reinterpret_cast<SelectScratch*>(smem + P::kOffStage + sizeof(PickScratch));
-  const int64_t cta = blockIdx.x;
-  const int cap = 2 * a.sel_k;  // list capacity per CTA
-  uint32_t* ck = a.cand_key + cta * cap;
-  int32_t* ci = a.cand_idx + cta * cap;
-  uint32_t T = 0;  // every key qualifies when the range has at most k of them
-  if (n_local > a.sel_k) {
-    for (int b = tid; b < 2048; b += kThreads) pk.hist1[b] = 0;
-    uint32_t rem = (uint32_t)a.sel_k, d0 = 0, d1 = 0;
-    for (int pass = 0; pass < 2; ++pass) {
-      const uint32_t* hist = pass == 0 ? ms.hist0 : pk.hist1;
-      if (pass == 1) {
-        for (int i = tid; i < n_local; i += kThreads) {
-          const uint32_t key = keys[padded(i)];
-          if ((key >> 21) == d0) atomicAdd(&pk.hist1[(key >> 10) & 2047u], 1u);
+  const int cap = 2 * a.sel_k;  // list capacity per slot
+  for (int q = 0; q < g.nseg; ++q) {
+    const int i0 = q ? g.nt[0] : 0;  // the segment's first local tile; its keys start at i0 * kTile
+    const int32_t e0 = g.t0[q] * kTile;
+    const int n_local = max(0, min(g.n[q], (g.t0[q] + g.nt[q]) * kTile) - e0);
+    const uint32_t* keys = reinterpret_cast<const uint32_t*>(smem + P::kOffKeys) + padded(i0 * kTile);
+    const uint32_t* hist0 = ms.hist0[q];
+    const int64_t slot = 2 * (int64_t)blockIdx.x + q;
+    uint32_t* ck = a.cand_key + slot * cap;
+    int32_t* ci = a.cand_idx + slot * cap;
+    uint32_t T = 0;  // every key qualifies when the range has at most k of them
+    if (n_local > a.sel_k) {
+      for (int b = tid; b < 2048; b += kThreads) pk.hist1[b] = 0;
+      uint32_t rem = (uint32_t)a.sel_k, d0 = 0, d1 = 0;
+      for (int pass = 0; pass < 2; ++pass) {
+        const uint32_t* hist = pass == 0 ? hist0 : pk.hist1;
+        if (pass == 1) {
+          for (int i = tid; i < n_local; i += kThreads) {
+            const uint32_t key = keys[padded(i)];
+            if ((key >> 21) == d0) atomicAdd(&pk.hist1[(key >> 10) & 2047u], 1u);
+          }
+          __syncthreads();
+        }
+        // the digit d with count(> d) < rem <= count(>= d), buckets scanned from the top
+        constexpr int kBpt = (2048 + kThreads - 1) / kThreads;
+        const int top = 2048 - tid * kBpt;
+        uint32_t local = 0;
+        for (int jj = 0; jj < kBpt; ++jj)
+          if (top - 1 - jj >= 0) local += hist[top - 1 - jj];
+        uint32_t tot;
+        const uint32_t above = block_excl_scan<kThreads>(local, pk.wsum, tot);
+        if (above < rem && rem <= above + local) {
+          uint32_t cum = above;
+          for (int jj = 0; jj < kBpt && top - 1 - jj >= 0; ++jj) {
+            const uint32_t h = hist[top - 1 - jj];
+            if (cum + h >= rem) {
+              pk.digit = (uint32_t)(top - 1 - jj);
+              pk.rem = rem - cum;
+              break;
+            }
+            cum += h;
+          }
         }
         __syncthreads();
+        if (pass == 0) d0 = pk.digit;
+        else d1 = pk.digit;
+        rem = pk.rem;
+        __syncthreads();
       }
-      // the digit d with count(> d) < rem <= count(>= d), buckets scanned from the top
-      constexpr int kBpt = (2048 + kThreads - 1) / kThreads;
-      const int top = 2048 - tid * kBpt;
-      uint32_t local = 0;
-      for (int j = 0; j < kBpt; ++j)
-        if (top - 1 - j >= 0) local += hist[top - 1 - j];
-      uint32_t tot;
-      const uint32_t above = block_excl_scan<kThreads>(local, pk.wsum, tot);
-      if (above < rem && rem <= above + local) {
-        uint32_t cum = above;
-        for (int j = 0; j < kBpt && top - 1 - j >= 0; ++j) {
-          const uint32_t h = hist[top - 1 - j];
-          if (cum + h >= rem) {
-            pk.digit = (uint32_t)(top - 1 - j);
-            pk.rem = rem - cum;
-            break;
-          }
-          cum += h;
+      T = (d0 << 21) | (d1 << 10);
+    }
+    // keys at or above T, in entry order: one count per thread segment, one scan
+    const int seg = (n_local + kThreads - 1) / kThreads;
+    const int lo = tid * seg, hi = min(n_local, lo + seg);
+    uint32_t mine = 0;
+    for (int i = lo; i < hi; ++i) mine += keys[padded(i)] >= T;
+    uint32_t total;
+    uint32_t at = block_excl_scan<kThreads>(mine, pk.wsum, total);
+    if ((int)total <= cap) {
+      for (int i = lo; i < hi; ++i) {
+        const uint32_t key = keys[padded(i)];
+        if (key >= T) {
+          ck[at] = key;
+          ci[at] = e0 + i;
+          ++at;
         }
       }
+      if (tid == 0) {
+        a.cand_cnt[slot] = (int32_t)total;
+        a.cand_thr[slot] = T;
+      }
+    } else {
+      // many keys tie within T's 22-bit bucket: the exact top-k instead, with its
+      // k-th key as the threshold (still a lower bound of the row's k-th key)
+      if (tid == 0) pk.digit = 0xFFFFFFFFu;  // reused as the block minimum of the selected keys
       __syncthreads();
-      if (pass == 0) d0 = pk.digit;
-      else d1 = pk.digit;
-      rem = pk.rem;
+      uint32_t kth = 0xFFFFFFFFu;
+      block_select<kThreads>(keys, n_local, a.sel_k, sc, [&](int pos, uint32_t rank) {
+        const uint32_t key = keys[padded(pos)];
+        ck[rank] = key;
+        ci[rank] = e0 + pos;
+        kth = min(kth, key);
+      });
+      for (int o = 16; o > 0; o >>= 1) kth = min(kth, __shfl_xor_sync(0xffffffffu, kth, o));
+      if ((tid & 31) == 0) atomicMin(&pk.digit, kth);
       __syncthreads();
-    }
-    T = (d0 << 21) | (d1 << 10);
-  }
-  // keys at or above T, in entry order: one count per thread segment, one scan
-  const int seg = (n_local + kThreads - 1) / kThreads;
-  const int lo = tid * seg, hi = min(n_local, lo + seg);
-  uint32_t mine = 0;
-  for (int i = lo; i < hi; ++i) mine += keys[padded(i)] >= T;
-  uint32_t total;
-  uint32_t slot = block_excl_scan<kThreads>(mine, pk.wsum, total);
-  if ((int)total <= cap) {
-    for (int i = lo; i < hi; ++i) {
-      const uint32_t key = keys[padded(i)];
-      if (key >= T) {
-        ck[slot] = key;
-        ci[slot] = e0 + i;
-        ++slot;
+      if (tid == 0) {
+        a.cand_cnt[slot] = a.sel_k;
+        a.cand_thr[slot] = pk.digit;
       }
     }
-    if (tid == 0) {
-      a.cand_cnt[cta] = (int32_t)total;
-      a.cand_thr[cta] = T;
-    }
-  } else {
-    // many keys tie within T's 22-bit bucket: the exact top-k instead, with its
-    // k-th key as the threshold (still a lower bound of the row's k-th key)
-    if (tid == 0) pk.digit = 0xFFFFFFFFu;  // reused as the block minimum of the selected keys
-    __syncthreads();
-    uint32_t kth = 0xFFFFFFFFu;
-    block_select<kThreads>(keys, n_local, a.sel_k, sc, [&](int pos, uint32_t rank) {
-      const uint32_t key = keys[padded(pos)];
-      ck[rank] = key;
-      ci[rank] = e0 + pos;
-      kth = min(kth, key);
-    });
-    for (int o = 16; o > 0; o >>= 1) kth = min(kth, __shfl_xor_sync(0xffffffffu, kth, o));
-    if ((tid & 31) == 0) atomicMin(&pk.digit, kth);
-    __syncthreads();
-    if (tid == 0) {
-      a.cand_cnt[cta] = a.sel_k;
-      a.cand_thr[cta] = pk.digit;
-    }
+    __syncthreads();  // the scratch is reused by the next segment
   }
 }
 
@@ -573,22 +632,25 @@ int32_t indexer_deal_bound(int32_t n_rows, int32_t max_n, int32_t G) {
   return (int32_t)(B < tiles ? B : tiles);
 }
 
+// Two list slots per CTA (even deal: one per row the CTA meets).
 size_t deal_candidate_bytes(int32_t G, int32_t k) {
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
-  return 2 * up((size_t)G * 2 * k * 4) + 2 * up((size_t)G * 4) + 2 * up((size_t)kDealMaxRows * 4);
+  return 2 * up((size_t)2 * G * 2 * k * 4) + 2 * up((size_t)2 * G * 4) + 3 * up((size_t)kDealMaxRows * 4);
 }
 
 DealCandidates deal_candidates(void* base, int32_t G, int32_t k) {
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   uint8_t* p = reinterpret_cast<uint8_t*>(base);
-  const size_t lists = up((size_t)G * 2 * k * 4);
+  const size_t lists = up((size_t)2 * G * 2 * k * 4), words = up((size_t)2 * G * 4),
+               rows = up((size_t)kDealMaxRows * 4);
   DealCandidates c;
   c.key = reinterpret_cast<uint32_t*>(p);
   c.idx = reinterpret_cast<int32_t*>(p + lists);
   c.cnt = reinterpret_cast<int32_t*>(p + 2 * lists);
-  c.thr = reinterpret_cast<uint32_t*>(p + 2 * lists + up((size_t)G * 4));
-  c.row_first = reinterpret_cast<int32_t*>(p + 2 * lists + 2 * up((size_t)G * 4));
-  c.row_ctas = reinterpret_cast<int32_t*>(p + 2 * lists + 2 * up((size_t)G * 4) + up((size_t)kDealMaxRows * 4));
+  c.thr = reinterpret_cast<uint32_t*>(p + 2 * lists + words);
+  c.row_first = reinterpret_cast<int32_t*>(p + 2 * lists + 2 * words);
+  c.row_ctas = reinterpret_cast<int32_t*>(p + 2 * lists + 2 * words + rows);
+  c.row_seg = reinterpret_cast<int32_t*>(p + 2 * lists + 2 * words + 2 * rows);
   c.ctas = G;
   c.cap = 2 * k;
   return c;

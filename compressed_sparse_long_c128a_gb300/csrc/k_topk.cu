@@ -185,21 +185,20 @@ constexpr int kMaxMergeCluster = 16;
 constexpr int kMergeKeep = 4096;  // survivors a member keeps in shared memory after its first read
 constexpr int kMergeKeyWords = (padded_size(kMergeKeep) + 3) & ~3;
 constexpr size_t kMergeSmem = sizeof(uint32_t) * (kMergeKeyWords + kMergeKeep);
-constexpr int kMergeWarmK = 512;  // the warm-up's dummy selection: top 512 of 1025 keys
 
-// Row r: its CTAs' lists under the deal merged into the row's top-k by one
-// cluster of Cs CTAs.  CTA c's list holds every key of its range at or above
-// thr_c, and thr_c is at most the row's k-th largest key, so the keys at or
-// above max_c thr_c ("survivors") are all in the lists and include the row's
-// top-k.  Member m of the cluster takes a contiguous run of the row's lists
+// Row r: its lists under the deal (one per CTA range of the row, see
+// DealCandidates) merged into the row's top-k by one cluster of Cs CTAs.
+// List c holds every key of its range at or above thr_c, and thr_c is at most
+// the row's k-th largest key, so the keys at or above max_c thr_c
+// ("survivors") are all in the lists and include the row's top-k.  Member m of the cluster takes a contiguous run of the row's lists
 // (lists are in entry order) and streams its survivors from L2 in every pass:
 // a count, three radix-digit histograms (11, 11, 10 bits) summed into rank 0's
 // shared memory through the cluster (rank 0 picks each digit and hands it
 // back), and a last pass that places every survivor above the k-th key and
 // the first equal ones in entry order.
-// The short way's selection (shared memory to `dst`): one out-of-line copy of
-// the code, run once on dummy keys before the PDL wait and once for real.
-__device__ __noinline__ void merge_select(const uint32_t* keys, const int32_t* idx, int n, int k, SelectScratch& sc,
+//
+// The short way's selection (shared memory to `dst`).
+__device__ __forceinline__ void merge_select(const uint32_t* keys, const int32_t* idx, int n, int k, SelectScratch& sc,
                                           int32_t* dst) {
   block_select<kDealMergeThreads>(keys, n, k, sc, [&](int pos, uint32_t rank) { dst[rank] = idx[pos]; });
   for (int i = min(n, k) + threadIdx.x; i < k; i += kDealMergeThreads) dst[i] = -1;
@@ -228,27 +227,17 @@ __global__ void __launch_bounds__(kDealMergeThreads) topk_deal_merge_kernel(cons
   int32_t* kept_idx = reinterpret_cast<int32_t*>(kept_key + kMergeKeyWords);  // [kMergeKeep]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int Cs = gridDim.y, me = (int)tc::cluster_rank();
-  pdl_trigger();
-  // The CTA is resident long before the indexer ends.  Meanwhile, touching
-  // nothing in global memory, it runs the selection once on dummy keys in
-  // shared memory, so that the selection's instructions are in this SM's
-  // instruction cache when the lists arrive (fetching them then, a line at a
-  // time, cost several microseconds).
-  {
-    const int n = 2 * kMergeWarmK + 1, k = kMergeWarmK;
-    for (int i = threadIdx.x; i < n; i += NT) kept_key[padded(i)] = (uint32_t)i * 2654435761u;
-    for (int i = threadIdx.x; i < n; i += NT) kept_idx[i] = i;
-    __syncthreads();
-    merge_select(kept_key, kept_idx, n, k, *reinterpret_cast<SelectScratch*>(&hsum[0][0]),
-                 reinterpret_cast<int32_t*>(hloc));
-    __syncthreads();
-  }
+  // No early launch of the next kernel: the attention behind this one keeps
+  // its (large) CTAs waiting on the SMs, which would hold off the CTAs of this
+  // launch; it starts as this launch's CTAs exit.
   for (int b = threadIdx.x; b < 3 * 2048; b += NT) (&hsum[0][0])[b] = 0;
   if (threadIdx.x == 0) s_total = 0;
   pdl_wait();  // the lists are complete only after the indexer launch
   tc::cluster_sync();  // rank 0's sums are zero before any member adds
   const int r = blockIdx.x;
-  const int first = c.row_first[r], ctas = min(c.row_ctas[r], kDealMaxRows);
+  const int first = c.row_first[r], ctas = min(c.row_ctas[r], kDealMaxRows), seg0 = c.row_seg[r];
+  // list j of the row lives in slot 2 (first + j), plus seg0 for j = 0
+  auto slot = [&](int j) -> int64_t { return 2 * (int64_t)(first + j) + (j == 0 ? seg0 : 0); };
   const int K = a.k;
   int32_t* out = a.out + (int64_t)r * K;
   if (warp == 0) {  // lane l owns lists [8l, 8l+8): counts, thresholds, prefix
@@ -257,8 +246,8 @@ __global__ void __launch_bounds__(kDealMergeThreads) topk_deal_merge_kernel(cons
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int j = 8 * lane + i;
-      cnt[i] = j < ctas ? c.cnt[first + j] : 0;
-      t = j < ctas ? max(t, c.thr[first + j]) : t;
+      cnt[i] = j < ctas ? c.cnt[slot(j)] : 0;
+      t = j < ctas ? max(t, c.thr[slot(j)]) : t;
       mine += cnt[i];
     }
     for (int o = 16; o > 0; o >>= 1) t = max(t, __shfl_xor_sync(0xffffffffu, t, o));
@@ -294,7 +283,7 @@ __global__ void __launch_bounds__(kDealMergeThreads) topk_deal_merge_kernel(cons
             if (off[mid] <= v) lo = mid;
             else hi = mid - 1;
           }
-          const int64_t e = (int64_t)(first + lo) * c.cap + (v - off[lo]);
+          const int64_t e = slot(lo) * c.cap + (v - off[lo]);
           kb[u] = c.key[e];
           ib[u] = c.idx[e];
         }
@@ -330,7 +319,7 @@ __global__ void __launch_bounds__(kDealMergeThreads) topk_deal_merge_kernel(cons
         e[u] = -1;
         if (v + u < v1) {
           while (j + 1 < je && off[j + 1] <= v + u) ++j;
-          e[u] = (int64_t)(first + j) * c.cap + (v + u - off[j]);
+          e[u] = slot(j) * c.cap + (v + u - off[j]);
         }
       }
 #pragma unroll

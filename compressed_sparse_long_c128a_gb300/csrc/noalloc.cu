@@ -28,7 +28,7 @@
 
 namespace {
 
-constexpr size_t kScratchBytes = size_t(8) << 20;  // 8 MiB
+constexpr size_t kScratchBytes = size_t(16) << 20;  // 16 MiB
 
 // The scratch itself.  In host code this name is only a stand-in symbol; the
 // device address comes from cudaGetSymbolAddress below.

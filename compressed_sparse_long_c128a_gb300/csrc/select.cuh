@@ -231,19 +231,33 @@ __device__ void block_select(const uint32_t* keys, int n, int k, SelectScratch& 
 
 // ------------------------------------------------------------------ balanced deal
 
-// The indexer's work for a batch of rows dealt to G CTAs in proportion to each
-// row's key tiles: row r with t_r tiles (128 entries each) gets
-// k_r = ceil(t_r / B) CTAs, B the smallest tile budget with sum_r k_r <= G,
-// and its tiles are split into k_r contiguous ranges of equal size (+-1).
-// Rows get CTAs in row order.  Every CTA of the indexer and of the merge
-// computes the same deal from the rows' positions, so nothing is exchanged.
+// The indexer's work for a batch of rows dealt to G CTAs.  Every CTA of the
+// indexer computes the same deal from the rows' positions; its CTA 0 hands
+// each row's list slots to the merge.  Two forms:
+//
+//  * even deal: the rows' tiles (128 entries each) are laid end to end and
+//    CTA c takes tiles [floor(c T / G), floor((c+1) T / G)) of the T in all,
+//    so every CTA streams the same amount.  Used when every non-empty row has
+//    at least ceil(T / G) tiles (a CTA then meets at most two rows: the tail
+//    of one, the head of the next) and that many tiles fit the CTA.  A CTA
+//    keeps one list per row it meets, in list slot 2c (its first row) and
+//    2c + 1 (its second).
+//  * per-row deal, otherwise: row r with t_r tiles gets k_r = ceil(t_r / B)
+//    CTAs, B the smallest budget with sum_r k_r <= G, its tiles split into k_r
+//    contiguous ranges of equal size (+-1), one list each in slot 2c.
+//
+// Either way the lists of row r are, in entry order, slot 2 first_r + seg_r
+// and then slot 2c for c = first_r + 1 .. first_r + ctas_r - 1.
 constexpr int kDealTile = 128;
 constexpr int kDealMaxRows = 256;  // rows per deal (8 per lane)
 
 struct DealShared {
-  int32_t first[kDealMaxRows];  // first CTA of each row
-  int32_t ctas[kDealMaxRows];   // CTAs of each row (0 for a row with no tiles)
+  int32_t first[kDealMaxRows];  // the CTA holding the row's first list
+  int32_t ctas[kDealMaxRows];   // CTAs (lists) of each row (0 for a row with no tiles)
   int32_t tiles[kDealMaxRows];
+  int32_t seg[kDealMaxRows];    // even deal: 1 if the row is the second one of its first CTA
+  int32_t start[kDealMaxRows];  // even deal: the row's first tile in the concatenation
+  int32_t even, total;          // the even deal is in use; T
 };
 
 // ceil(t / m) for 0 <= t < 2^22 and 1 <= m, from a float reciprocal rm ~ 1/m:
@@ -265,27 +279,78 @@ __device__ __forceinline__ int32_t deal_row_tiles(const int32_t* pos, int r, int
   return (n + kDealTile - 1) / kDealTile;
 }
 
+// Under the even deal: the first tile of CTA c, and the CTA holding tile g.
+// 32-bit unsigned arithmetic is exact: c, G <= kDealMaxCtas + 1, and a deal
+// is launched only when T <= G x (the tiles a CTA holds) < 2^16, so every
+// product is below 2^32.
+__device__ __forceinline__ int32_t even_first_tile(int c, int32_t T, int G) {
+  return (int32_t)(((uint32_t)c * (uint32_t)T) / (uint32_t)G);
+}
+__device__ __forceinline__ int32_t even_cta_of(int32_t g, int32_t T, int G) {
+  return (int32_t)((((uint32_t)g + 1u) * (uint32_t)G - 1u) / (uint32_t)T);
+}
+
 // One warp (all 32 lanes): fills ds for n_rows <= kDealMaxRows rows dealt to
-// G >= n_rows CTAs.  Lane l owns rows [8l, 8l+8).
+// G >= n_rows CTAs; `cap` is the most tiles a CTA can take under the even
+// deal.  Lane l owns rows [8l, 8l+8).
 __device__ __forceinline__ void deal_compute(const int32_t* pos, int n_rows, int32_t ratio, int32_t window,
-                                             int32_t max_n, int G, DealShared& ds) {
+                                             int32_t max_n, int G, int32_t cap, DealShared& ds) {
   const int lane = threadIdx.x & 31;
   int32_t t[8];
-  int32_t tmax = 0, tsum = 0;  // at most 256 rows of 2^22 / 128 tiles
+  int32_t tmax = 0, tsum = 0, tmin = 0x7FFFFFFF;  // at most 256 rows of 2^22 / 128 tiles
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int r = 8 * lane + i;
     t[i] = r < n_rows ? deal_row_tiles(pos, r, ratio, window, max_n) : 0;
     tmax = max(tmax, t[i]);
     tsum += t[i];
+    if (t[i] > 0) tmin = min(tmin, t[i]);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
     tsum += __shfl_xor_sync(0xffffffffu, tsum, o);
+    tmin = min(tmin, __shfl_xor_sync(0xffffffffu, tmin, o));
+  }
+  const int32_t L = (tsum + G - 1) / G;  // the most tiles of a CTA under the even deal
+  if (tsum > 0 && tmin >= L && L <= cap) {
+    int32_t mine = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mine += t[i];
+    int32_t incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int32_t run = incl - mine;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = 8 * lane + i;
+      if (r < n_rows) {
+        ds.start[r] = run;
+        ds.tiles[r] = t[i];
+        if (t[i] > 0) {
+          const int32_t c1 = even_cta_of(run, tsum, G), c2 = even_cta_of(run + t[i] - 1, tsum, G);
+          ds.first[r] = c1;
+          ds.ctas[r] = c2 - c1 + 1;
+          ds.seg[r] = even_first_tile(c1, tsum, G) == run ? 0 : 1;
+        } else {
+          ds.first[r] = 0;
+          ds.ctas[r] = 0;
+          ds.seg[r] = 0;
+        }
+      }
+      run += t[i];
+    }
+    if (lane == 0) {
+      ds.even = 1;
+      ds.total = tsum;
+    }
+    return;
   }
   // smallest feasible budget in [ceil(T/G), tmax]; tmax is feasible as n_rows <= G
-  int32_t lo = (int32_t)((tsum + G - 1) / G), hi = tmax;
+  int32_t lo = L, hi = tmax;
   if (lo < 1) lo = 1;
   if (hi < lo) hi = lo;
   while (lo < hi) {
@@ -321,17 +386,52 @@ __device__ __forceinline__ void deal_compute(const int32_t* pos, int n_rows, int
       ds.first[r] = run;
       ds.ctas[r] = k[i];
       ds.tiles[r] = t[i];
+      ds.seg[r] = 0;
+      ds.start[r] = 0;
     }
     run += k[i];
   }
+  if (lane == 0) {
+    ds.even = 0;
+    ds.total = tsum;
+  }
 }
 
-// The row and tile range of CTA c under the deal (row -1: c has no work).
+// The rows and tile ranges of CTA c under the deal: up to two segments
+// (row -1: none), each a contiguous tile range [t0, t0 + nt) of one row.
 struct DealSlot {
-  int32_t row, t0, nt;
+  int32_t row[2], t0[2], nt[2];
 };
-__device__ __forceinline__ DealSlot deal_slot(const DealShared& ds, int n_rows, int c) {
-  DealSlot s{-1, 0, 0};
+__device__ __forceinline__ DealSlot deal_slot(const DealShared& ds, int n_rows, int c, int G) {
+  DealSlot s{{-1, -1}, {0, 0}, {0, 0}};
+  if (ds.even) {
+    const int32_t T = ds.total;
+    const int32_t g0 = even_first_tile(c, T, G), g1 = even_first_tile(c + 1, T, G);
+    if (g1 <= g0) return s;
+    // the row holding tile g0: the last row whose first tile is <= g0 (an empty
+    // row shares its first tile with the next row, which is the one kept)
+    int lo = 0, hi = n_rows - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (ds.start[mid] <= g0) lo = mid;
+      else hi = mid - 1;
+    }
+    const int ra = lo;
+    const int32_t end_a = ds.start[ra] + ds.tiles[ra];
+    s.row[0] = ra;
+    s.t0[0] = g0 - ds.start[ra];
+    s.nt[0] = min(end_a, g1) - g0;
+    if (g1 > end_a) {
+      int rb = ra + 1;
+      while (rb < n_rows && ds.tiles[rb] == 0) ++rb;
+      if (rb < n_rows) {
+        s.row[1] = rb;
+        s.t0[1] = 0;
+        s.nt[1] = g1 - ds.start[rb];
+      }
+    }
+    return s;
+  }
   // the last row whose first CTA is <= c (rows with no CTA share their successor's first)
   int lo = 0, hi = n_rows - 1;
   while (lo < hi) {
@@ -342,9 +442,9 @@ __device__ __forceinline__ DealSlot deal_slot(const DealShared& ds, int n_rows, 
   const int r = lo;
   const int32_t j = c - ds.first[r], k = ds.ctas[r], t = ds.tiles[r];
   if (j < 0 || j >= k) return s;
-  s.row = r;
-  s.t0 = (int32_t)(((long long)j * t) / k);
-  s.nt = (int32_t)(((long long)(j + 1) * t) / k) - s.t0;
+  s.row[0] = r;
+  s.t0[0] = (int32_t)(((uint32_t)j * (uint32_t)t) / (uint32_t)k);
+  s.nt[0] = (int32_t)(((uint32_t)(j + 1) * (uint32_t)t) / (uint32_t)k) - s.t0[0];
   return s;
 }
 

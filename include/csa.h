@@ -293,11 +293,11 @@ CSA_API size_t csa_sparse_attn_workspace_size(const csa_layer* layer, int32_t n_
  * loop that may not allocate on its hot path (an allocation can wait for the
  * whole device or fail under memory pressure).  This variant computes exactly
  * what csa_indexer_topk computes, with the same arguments minus the workspace,
- * and keeps its scratch in a fixed 8 MiB array of device memory defined inside
+ * and keeps its scratch in a fixed 16 MiB array of device memory defined inside
  * the library (held on every GPU that loads the library until the process
  * exits).  It calls no allocator.
  *   - A request whose scratch (csa_indexer_topk_workspace_size(n_rows, max_n,
- *     k)) exceeds 8 MiB returns CSA_ERR_WORKSPACE and enqueues nothing.
+ *     k)) exceeds 16 MiB returns CSA_ERR_WORKSPACE and enqueues nothing.
  *   - All calls share the one array: calls that can run at the same time on
  *     the GPU (different streams, no ordering between them) race.  Calls on one
  *     stream are safe; no scratch byte needs to start at zero.

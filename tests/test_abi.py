@@ -160,12 +160,12 @@ def test_topk_scratch_sizes(lib):
     """Rows of one 16384-entry chunk need only the score scratch; longer rows also
     need each chunk's top-k candidates (key and index) and a count.  Batches of
     fewer than 256 rows may instead be dealt over up to 256 CTAs that each keep
-    a candidate list of up to 2k (key, index) pairs, a count and a threshold, plus
-    each row's first CTA and CTA count."""
+    two candidate lists of up to 2k (key, index) pairs, a count and a threshold
+    each, plus each row's first CTA, list count and first list's slot."""
     def aligned(x):
         return (x + 255) // 256 * 256
 
-    deal = 2 * aligned(256 * 1024 * 4) + 2 * aligned(256 * 4) + 2 * aligned(256 * 4)
+    deal = 2 * aligned(2 * 256 * 1024 * 4) + 2 * aligned(2 * 256 * 4) + 3 * aligned(256 * 4)
     assert csa.indexer_topk_workspace_size(64, 16383, 512) == aligned(64 * 16383 * 4) + deal
     assert csa.indexer_topk_workspace_size(64, 16384, 512) == aligned(64 * 16384 * 4) + deal
     n = 262143

@@ -3,7 +3,7 @@
 That entry point serves callers that cannot allocate device memory -- a
 plugin inside a host runtime that owns every device byte and gives its
 extensions no allocator, or a serving loop that may not allocate on its hot
-path.  Instead of a caller-provided workspace it uses a fixed 8 MiB scratch
+path.  Instead of a caller-provided workspace it uses a fixed 16 MiB scratch
 array inside the library.
 
 These tests call it through the C ABI and check that two calls in a row
@@ -96,7 +96,7 @@ def test_noalloc_refuses_requests_beyond_its_scratch():
 
     lib = csa.lib()
     # 16408 rows over 262143 entries need far more than the fixed scratch
-    assert csa.indexer_topk_workspace_size(16408, 262143, 512) > 8 << 20
+    assert csa.indexer_topk_workspace_size(16408, 262143, 512) > 16 << 20
     cache = csa.Paged(0x1000, 0x2000, csa.E2M1, 10, 64, 128)
     bt = csa.BlockTableC(0x3000, 2, 4)
     st = lib.csa_indexer_topk_noalloc(0x10, csa.BF16, 0x10, 16408, 64, 128, 0x10, 0x10, 4, 8, ctypes.byref(cache),
