@@ -385,11 +385,15 @@ def oracle_baseline(pool: OraclePool, wl_idx: int, seconds: float) -> dict:
     wl = synth.workload(wl_idx)
     rows = _sample_rows(wl, 64 * pool.workers)
     t0 = time.time()
-    n = pool.run(wl_idx, rows, deadline=t0 + seconds)
+    n = passes = 0
+    while passes == 0 or time.time() - t0 < 0.9 * seconds:  # whole passes over the sample, about `seconds` long
+        n += pool.run(wl_idx, rows, deadline=t0 + seconds)
+        passes += 1
     dt = time.time() - t0
     return {"value": n / dt, "unit": UNIT, "cores": pool.workers, "kind": "oracle",
-            "sample": f"{n} query rows of {wl.name} (every layer of each row; rows spread evenly over the "
-                      f"batch), fp64 numpy, {pool.workers} single-threaded worker processes, {dt:.1f} s",
+            "sample": f"{n} query rows of {wl.name} ({passes} passes over {len(rows)} rows spread evenly over "
+                      f"the batch; every layer of each row), fp64 numpy, {pool.workers} single-threaded worker "
+                      f"processes, {dt:.1f} s",
             "cpu": host_cpu()}
 
 
