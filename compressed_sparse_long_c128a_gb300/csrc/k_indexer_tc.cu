@@ -28,9 +28,10 @@
 //   * one CTA per row and split (sel_k == 0, prefill-sized batches): every
 //     score goes to the caller's scratch for the top-k kernels.
 //
-// Warps 0-3: epilogue; warps 4-10: producers (bf16: one TMA thread; e2m1:
-// warp 4 issues the bulk copies, warps 5-10 convert); warp 11: TMEM
-// allocation + MMA issue.  After the last tile all 12 warps run the selection.
+// Warps 0-3: epilogue; then the producers (bf16: warps 4-10, one TMA thread;
+// e2m1: warps 4-14, warp 4 issues the bulk copies and ten warps convert); the
+// last warp: TMEM allocation + MMA issue.  After the last tile every warp runs
+// the selection.
 
 #include "select.cuh"
 #include "tc_ptx.cuh"
@@ -41,10 +42,7 @@ namespace {
 using namespace tc;
 
 constexpr int kHI = 64, kDI = 128, kTile = kDealTile;
-constexpr int kEpi = 128, kProd = 224;
-constexpr int kThreads = kEpi + kProd + 32;
-constexpr int kMmaWarp = (kEpi + kProd) / 32;
-constexpr int kConvThreads = kProd - 32;  // e2m1: warps 5-10 convert
+constexpr int kEpi = 128;
 constexpr uint32_t kQBytes = kHI * kDI * 2;        // 16 KB: 2 K-atoms of 64 rows x 128 B
 constexpr uint32_t kStageBytes = kTile * kDI * 2;  // 32 KB: 2 K-atoms of 128 rows x 128 B
 constexpr uint32_t kAtomBytes = kTile * 128;       // 16 KB
@@ -59,6 +57,13 @@ constexpr int kTblMax = 1024;  // block-table entries a CTA caches (= 512 tiles)
 // Shared-memory plan per key format.
 template <bool kFp4>
 struct Plan {
+  // warps 0-3 epilogue; then the producers (bf16: one TMA thread in warp 4;
+  // e2m1: warp 4 issues the bulk copies, the other ten convert); the last warp
+  // allocates TMEM and issues the MMAs
+  static constexpr int kProd = kFp4 ? 352 : 224;
+  static constexpr int kThreads = kEpi + kProd + 32;
+  static constexpr int kMmaWarp = (kEpi + kProd) / 32;
+  static constexpr int kConvThreads = kProd - 32;
   static constexpr int kStages = kFp4 ? 3 : 4;       // bf16 tiles the MMA reads
   static constexpr int kRaw = kFp4 ? 6 : 0;          // raw e2m1 tiles in flight
   static constexpr int kCapTiles = kFp4 ? 64 : 104;  // tiles whose keys the fused selection holds
@@ -232,7 +237,7 @@ __device__ void converter(const IndexerArgs& a, const Range& g, uint8_t* smem, M
     const uint8_t* rb = smem + P::kOffRaw + rs * kRawBytes;
     uint8_t* sb = smem + P::kOffStage + s * kStageBytes;
     // 16 bytes of codes = 32 values = 64 bytes of bf16 = 4 swizzled pieces
-    for (int x = ct; x < kTile * 4; x += kConvThreads) {
+    for (int x = ct; x < kTile * 4; x += P::kConvThreads) {
       const uint32_t key = x >> 2, q = x & 3;
       const uint4 c4 = *reinterpret_cast<const uint4*>(rb + key * 64 + q * 16);
       const uint8_t* sc = rb + kRawCodes + key * 8 + q * 2;
@@ -255,13 +260,13 @@ __device__ void converter(const IndexerArgs& a, const Range& g, uint8_t* smem, M
 
 // Q_idx^T of `row` into the Q area, by threads [t0, t0 + nthr) of the CTA:
 // bf16, 128B-swizzled K-major, rows = heads; 8 dims per 16-byte piece, each
-// thread's loads (up to eight) issued before its stores.
+// thread's loads (up to four) issued before its stores.
 __device__ __forceinline__ void load_q(const IndexerArgs& a, int row, uint8_t* q_smem, int t, int nthr) {
   constexpr int kPieces = kHI * kDI / 8;
-  for (int x0 = t; x0 < kPieces; x0 += 8 * nthr) {
-    uint32_t w[8][4];
+  for (int x0 = t; x0 < kPieces; x0 += 4 * nthr) {
+    uint32_t w[4][4];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+    for (int u = 0; u < 4; ++u) {
       const int x = x0 + u * nthr;
       if (x >= kPieces) break;
       const int64_t qb = (int64_t)row * kHI * kDI + 8 * x;
@@ -278,7 +283,7 @@ __device__ __forceinline__ void load_q(const IndexerArgs& a, int row, uint8_t* q
       }
     }
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+    for (int u = 0; u < 4; ++u) {
       const int x = x0 + u * nthr;
       if (x >= kPieces) break;
       const int h = x / (kDI / 8), d0 = 8 * (x % (kDI / 8));
@@ -352,15 +357,28 @@ __device__ void epilogue_role(const IndexerArgs& a, const Range& g, uint8_t* sme
     }
     wait_or_abort(ms, &ms.tfull[b], (i >> 1) & 1, a.err);
     tc_fence_after();
-    float v[kHI];
+    float s = 0.f;
+    if constexpr (kFp4) {
+      // the row's 64 head dots in two halves of 32 columns (registers for 512 threads)
 #pragma unroll
-    for (int q = 0; q < 4; ++q) tmem_ld16(lane_addr + 64 * b + 16 * q, v + 16 * q);
-    tmem_wait_ld();
+      for (int half = 0; half < 2; ++half) {
+        float v[kHI / 2];
+        tmem_ld16(lane_addr + 64 * b + 32 * half, v);
+        tmem_ld16(lane_addr + 64 * b + 32 * half + 16, v + 16);
+        tmem_wait_ld();
+#pragma unroll
+        for (int h = 0; h < kHI / 2; ++h) s = fmaf(w[32 * half + h], fmaxf(v[h], 0.f), s);
+      }
+    } else {
+      float v[kHI];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tmem_ld16(lane_addr + 64 * b + 16 * q, v + 16 * q);
+      tmem_wait_ld();
+#pragma unroll
+      for (int h = 0; h < kHI; ++h) s = fmaf(w[h], fmaxf(v[h], 0.f), s);
+    }
     tc_fence_before();
     mbar_arrive(&ms.tempty[b]);
-    float s = 0.f;
-#pragma unroll
-    for (int h = 0; h < kHI; ++h) s = fmaf(w[h], fmaxf(v[h], 0.f), s);
     const int32_t e = g.tile_of(i) * kTile + et, j = 2 * i + et / kRowsPerBlock;
     if (e < g.n[seg]) {
       const float sc = (j < kTblMax && ms.tbl[j] >= 0) ? s : -INFINITY;
@@ -376,7 +394,7 @@ __device__ void epilogue_role(const IndexerArgs& a, const Range& g, uint8_t* sme
 }
 
 template <bool kFp4>
-__global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(const __grid_constant__ IndexerArgs a) {
+__global__ void __launch_bounds__(Plan<kFp4>::kThreads, 1) indexer_tc_kernel(const __grid_constant__ IndexerArgs a) {
   using P = Plan<kFp4>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -391,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(const __grid_co
     if (warp == 0) deal_compute(a.pos, a.n_rows, a.ratio, a.window, a.max_n, gridDim.x, P::kCapTiles, ds);
     __syncthreads();
     if (blockIdx.x == 0)  // each row's list slots, for the merge
-      for (int r = tid; r < a.n_rows; r += kThreads) {
+      for (int r = tid; r < a.n_rows; r += P::kThreads) {
         a.cand_row_first[r] = ds.first[r];
         a.cand_row_ctas[r] = ds.ctas[r];
         a.cand_row_seg[r] = ds.seg[r];
@@ -447,12 +465,12 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(const __grid_co
 
   if (tid == 0) {
     for (int s = 0; s < 4; ++s) {
-      mbar_init(&ms.full[s], kFp4 ? kConvThreads : 1);
+      mbar_init(&ms.full[s], kFp4 ? P::kConvThreads : 1);
       mbar_init(&ms.empty[s], 1);
     }
     for (int s = 0; s < 6; ++s) {
       mbar_init(&ms.raw_full[s], 1);
-      mbar_init(&ms.raw_empty[s], kConvThreads);
+      mbar_init(&ms.raw_empty[s], P::kConvThreads);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&ms.tfull[b], 1);
@@ -464,11 +482,11 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(const __grid_co
     ms.abort = 0;
   }
   if (tid < g.nseg * kHI) ms.w[tid / kHI][tid % kHI] = a.w[(int64_t)g.row[tid / kHI] * kHI + tid % kHI];
-  for (int b = tid; b < 2 * 2048; b += kThreads) (&ms.hist0[0][0])[b] = 0;
+  for (int b = tid; b < 2 * 2048; b += P::kThreads) (&ms.hist0[0][0])[b] = 0;
   {
     // block-table entries of the CTA's tiles, two blocks a tile
     const int32_t nblk = min(kTblMax, g.nt_all * (kTile / kRowsPerBlock));
-    for (int j = tid; j < nblk; j += kThreads) {
+    for (int j = tid; j < nblk; j += P::kThreads) {
       const int i = j / (kTile / kRowsPerBlock), q = g.seg_of(i);
       const int32_t lb = g.tile_of(i) * (kTile / kRowsPerBlock) + j % (kTile / kRowsPerBlock);
       int32_t pb = -1;
@@ -480,8 +498,8 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(const __grid_co
       ms.tbl[j] = pb;
     }
   }
-  if (warp == kMmaWarp) tmem_alloc(&ms.tmem_base, kTmemCols);
-  load_q(a, g.row[0], smem + P::kOffQ, tid, kThreads);
+  if (warp == P::kMmaWarp) tmem_alloc(&ms.tmem_base, kTmemCols);
+  load_q(a, g.row[0], smem + P::kOffQ, tid, P::kThreads);
   fence_proxy_async();
   tc_fence_before();
   __syncthreads();
@@ -490,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(const __grid_co
 
   if (warp < 4) {
     epilogue_role<kFp4>(a, g, smem, ms, tmem, tid);
-  } else if (warp < kMmaWarp) {
+  } else if (warp < P::kMmaWarp) {
     if constexpr (!kFp4) {
       if (tid == kEpi) producer_bf16<kFp4>(a, g, smem, ms);
     } else {
@@ -505,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(const __grid_co
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == P::kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -531,25 +549,25 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(const __grid_co
     int32_t* ci = a.cand_idx + slot * cap;
     uint32_t T = 0;  // every key qualifies when the range has at most k of them
     if (n_local > a.sel_k) {
-      for (int b = tid; b < 2048; b += kThreads) pk.hist1[b] = 0;
+      for (int b = tid; b < 2048; b += P::kThreads) pk.hist1[b] = 0;
       uint32_t rem = (uint32_t)a.sel_k, d0 = 0, d1 = 0;
       for (int pass = 0; pass < 2; ++pass) {
         const uint32_t* hist = pass == 0 ? hist0 : pk.hist1;
         if (pass == 1) {
-          for (int i = tid; i < n_local; i += kThreads) {
+          for (int i = tid; i < n_local; i += P::kThreads) {
             const uint32_t key = keys[padded(i)];
             if ((key >> 21) == d0) atomicAdd(&pk.hist1[(key >> 10) & 2047u], 1u);
           }
           __syncthreads();
         }
         // the digit d with count(> d) < rem <= count(>= d), buckets scanned from the top
-        constexpr int kBpt = (2048 + kThreads - 1) / kThreads;
+        constexpr int kBpt = (2048 + P::kThreads - 1) / P::kThreads;
         const int top = 2048 - tid * kBpt;
         uint32_t local = 0;
         for (int jj = 0; jj < kBpt; ++jj)
           if (top - 1 - jj >= 0) local += hist[top - 1 - jj];
         uint32_t tot;
-        const uint32_t above = block_excl_scan<kThreads>(local, pk.wsum, tot);
+        const uint32_t above = block_excl_scan<P::kThreads>(local, pk.wsum, tot);
         if (above < rem && rem <= above + local) {
           uint32_t cum = above;
           for (int jj = 0; jj < kBpt && top - 1 - jj >= 0; ++jj) {
@@ -571,12 +589,12 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(const __grid_co
       T = (d0 << 21) | (d1 << 10);
     }
     // keys at or above T, in entry order: one count per thread segment, one scan
-    const int seg = (n_local + kThreads - 1) / kThreads;
+    const int seg = (n_local + P::kThreads - 1) / P::kThreads;
     const int lo = tid * seg, hi = min(n_local, lo + seg);
     uint32_t mine = 0;
     for (int i = lo; i < hi; ++i) mine += keys[padded(i)] >= T;
     uint32_t total;
-    uint32_t at = block_excl_scan<kThreads>(mine, pk.wsum, total);
+    uint32_t at = block_excl_scan<P::kThreads>(mine, pk.wsum, total);
     if ((int)total <= cap) {
       for (int i = lo; i < hi; ++i) {
         const uint32_t key = keys[padded(i)];
@@ -596,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_tc_kernel(const __grid_co
       if (tid == 0) pk.digit = 0xFFFFFFFFu;  // reused as the block minimum of the selected keys
       __syncthreads();
       uint32_t kth = 0xFFFFFFFFu;
-      block_select<kThreads>(keys, n_local, a.sel_k, sc, [&](int pos, uint32_t rank) {
+      block_select<P::kThreads>(keys, n_local, a.sel_k, sc, [&](int pos, uint32_t rank) {
         const uint32_t key = keys[padded(pos)];
         ck[rank] = key;
         ci[rank] = e0 + pos;
@@ -664,6 +682,7 @@ bool indexer_tc_eligible(const IndexerArgs& a) {
 
 template <bool kFp4>
 static cudaError_t launch_indexer_tc_t(const IndexerArgs& args, int32_t n_rows, int32_t G, cudaStream_t s) {
+  using P = Plan<kFp4>;
   static PerDevice attrs;
   cudaError_t e = with_device_slot(attrs, [](int, int64_t& done) {
     if (done) return cudaSuccess;
@@ -678,7 +697,7 @@ static cudaError_t launch_indexer_tc_t(const IndexerArgs& args, int32_t n_rows, 
   if (!kFp4 && !encode_bf16_map(&a.k_map, a.cache.data, kDI, (uint64_t)a.cache.num_blocks * kRowsPerBlock, kDI * 2,
                                 64, kRowsPerBlock))
     return cudaErrorInvalidValue;
-  if (a.sel_k > 0) return launch_k(indexer_tc_kernel<kFp4>, dim3(G), dim3(kThreads), smem_bytes<kFp4>(), s, 0,
+  if (a.sel_k > 0) return launch_k(indexer_tc_kernel<kFp4>, dim3(G), dim3(P::kThreads), smem_bytes<kFp4>(), s, 0,
                                    a);
   const int32_t tiles = (a.max_n + kTile - 1) / kTile;
   // one CTA per SM: as many splits per row as fit in a single wave
@@ -689,7 +708,7 @@ static cudaError_t launch_indexer_tc_t(const IndexerArgs& args, int32_t n_rows, 
   const int32_t min_splits = (tiles + tiles_per_cta_max - 1) / tiles_per_cta_max;
   if (splits < min_splits) splits = min_splits;
   if (splits < 1) splits = 1;
-  return launch_k(indexer_tc_kernel<kFp4>, dim3(n_rows, splits), dim3(kThreads), smem_bytes<kFp4>(), s, 0,
+  return launch_k(indexer_tc_kernel<kFp4>, dim3(n_rows, splits), dim3(P::kThreads), smem_bytes<kFp4>(), s, 0,
                   a);
 }
 

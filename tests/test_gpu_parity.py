@@ -157,7 +157,9 @@ def _compare_out(ld, got_all, codes, scales, row, res, what, e2e=False):
         rel = np.linalg.norm(got - want) / np.linalg.norm(want)
         assert diff.max() <= 6e-2 and rel <= 3e-2, f"{what}: max-abs {diff.max():.3g} rel {rel:.3g}"
         # one e4m3 step of rounding, plus the error of the bf16 operands the tensor
-        # cores take (q and p rounded to bf16): absolute, about 1% of the head's amax
+        # cores take (q and P rounded to bf16): P's rounding moves an element by at
+        # most 2^-9 x (a weighted mean of |K|, ~0.8), q's the weights by ~0.1%;
+        # with head amax ~0.25 for these inputs, 1% of the head's amax bounds both
         sc = scales[row][:, None]
         step = np.maximum(_e4m3_step(want, sc), _e4m3_step(got, sc))
         amax = np.abs(want).max(axis=1, keepdims=True)
