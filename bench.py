@@ -145,7 +145,52 @@ def _row_bytes(dt: str, dim: int, tail: int = 64) -> float:
     return b
 
 
+def _by_sequence(ld):
+    """Positions of the step's rows grouped by sequence (each row its own
+    sequence when the rows carry no sequence ids)."""
+    pos = [int(p) for p in ld.host["pos"]]
+    seq = ld.host.get("seq_id") if isinstance(ld.host, dict) else None
+    if seq is None:
+        return [[p] for p in pos]
+    groups = {}
+    for b, p in zip(seq, pos):
+        groups.setdefault(int(b), []).append(p)
+    return list(groups.values())
+
+
+def _union_len(intervals) -> int:
+    """Integers covered by closed intervals [lo, hi]."""
+    total, end = 0, None
+    for lo, hi in sorted(intervals):
+        if end is None or lo > end:
+            total += hi - lo + 1
+            end = hi
+        elif hi > end:
+            total += hi - end
+            end = hi
+    return total
+
+
 def _attended_keys(ld) -> int:
+    """Distinct key rows the attention must read: per sequence, its rows'
+    selected (c4a) or visible (c128a) entries, at most every visible entry, and
+    the union of its rows' windows.  One row per sequence (decode) gives each
+    row's selection + window."""
+    from harness import n_visible
+    L = ld.L
+    keys = 0
+    for ps in _by_sequence(ld):
+        n_max = max(n_visible(p, L.ratio, L.window) for p in ps)
+        if L.has_indexer:
+            keys += min(n_max, sum(min(L.topk, n_visible(p, L.ratio, L.window)) for p in ps))
+        else:
+            keys += n_max
+        keys += _union_len([(max(0, p - L.swa + 1), p) for p in ps])
+    return keys
+
+
+def _attended_pairs(ld) -> int:
+    """(row, key) pairs of the attention: the work of its contractions."""
     from harness import n_visible
     L = ld.L
     keys = 0
@@ -157,8 +202,8 @@ def _attended_keys(ld) -> int:
 
 
 def attention_bytes(ld) -> float:
-    """Algorithmic bytes of one sparse-attention launch: every key row read once,
-    queries read once, outputs written once."""
+    """Algorithmic bytes of one sparse-attention launch: every distinct key row
+    read once, queries read once, outputs written once."""
     L = ld.L
     q = ld.n_rows * L.heads * L.dim * _elem_bytes(L.in_dtype)
     out = ld.n_rows * L.heads * (L.dim * _elem_bytes(L.out_dtype) + (4 if L.out_dtype == "e4m3" else 0))
@@ -166,9 +211,9 @@ def attention_bytes(ld) -> float:
 
 
 def attention_flops(ld) -> float:
-    """q.k and p.v for every head over every attended key."""
+    """q.k and p.v for every head of every row over every key it attends."""
     L = ld.L
-    return 4.0 * L.heads * L.dim * _attended_keys(ld)
+    return 4.0 * L.heads * L.dim * _attended_pairs(ld)
 
 
 def _visible_sum(ld) -> int:
@@ -178,13 +223,16 @@ def _visible_sum(ld) -> int:
 
 
 def indexer_bytes(ld) -> float:
-    """Every visible indexer key read once, the indexer queries and weights read
-    once, the selection written once (score scratch not counted)."""
+    """Every visible indexer key of each sequence read once (the rows of one
+    sequence share theirs), the indexer queries and weights read once, the
+    selection written once (score scratch not counted)."""
+    from harness import n_visible
     L = ld.L
     if not L.has_indexer:
         return 0.0
+    keys = sum(max(n_visible(p, L.ratio, L.window) for p in ps) for ps in _by_sequence(ld))
     q = ld.n_rows * L.idx_heads * (L.idx_dim * _elem_bytes(L.in_dtype) + 4)
-    return _visible_sum(ld) * _row_bytes(L.idx_dtype, L.idx_dim) + q + ld.n_rows * L.topk * 4
+    return keys * _row_bytes(L.idx_dtype, L.idx_dim) + q + ld.n_rows * L.topk * 4
 
 
 def indexer_flops(ld) -> float:

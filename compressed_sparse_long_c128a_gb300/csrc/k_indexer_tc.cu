@@ -51,11 +51,10 @@ constexpr uint32_t kBlockCodes = kRowsPerBlock * kDI / 2;    // 4 KB of e2m1 cod
 constexpr uint32_t kBlockScales = kRowsPerBlock * kDI / 16;  // 512 B of e4m3 scales per block
 constexpr uint32_t kRawCodes = 2 * kBlockCodes;
 constexpr uint32_t kRawBytes = kRawCodes + 2 * kBlockScales;  // 9 KB per tile
-constexpr uint32_t kTmemCols = 128;
 constexpr int kTblMax = 1024;  // block-table entries a CTA caches (= 512 tiles)
 
 // Shared-memory plan per key format.
-template <bool kFp4>
+template <bool kFp4, int kR = 1>
 struct Plan {
   // warps 0-3 epilogue; then the producers (bf16: one TMA thread in warp 4;
   // e2m1: warp 4 issues the bulk copies, the other ten convert); the last warp
@@ -66,9 +65,12 @@ struct Plan {
   static constexpr int kConvThreads = kProd - 32;
   static constexpr int kStages = kFp4 ? 3 : 4;       // bf16 tiles the MMA reads
   static constexpr int kRaw = kFp4 ? 6 : 0;          // raw e2m1 tiles in flight
-  static constexpr int kCapTiles = kFp4 ? 64 : 104;  // tiles whose keys the fused selection holds
+  // kR query rows share every key tile (prefill: four rows of one sequence as
+  // N = 256 of the MMA); the fused selection is for single rows only
+  static constexpr int kCapTiles = kR > 1 ? 0 : (kFp4 ? 64 : 104);  // tiles whose keys the fused selection holds
+  static constexpr uint32_t kTmemCols = 2 * 64 * kR;  // two S^T buffers of 64 kR columns
   static constexpr uint32_t kOffQ = 0;
-  static constexpr uint32_t kOffStage = kQBytes;
+  static constexpr uint32_t kOffStage = kR * kQBytes;
   static constexpr uint32_t kOffRaw = kOffStage + kStages * kStageBytes;
   static constexpr uint32_t kOffKeys = kOffRaw + kRaw * kRawBytes;
   static constexpr uint32_t kKeyBytes = ((uint32_t)padded_size(kCapTiles * kTile) * 4 + 1023) & ~1023u;
@@ -80,7 +82,8 @@ struct Misc {
   uint32_t tmem_base;
   int32_t abort;
   int32_t row[2], t0[2], nt[2];  // the CTA's segments (row -1: none)
-  float w[2][kHI];
+  int32_t nr, rr[4], rn[4];      // multi-row CTA: its rows and their visible entries
+  alignas(16) float w[4][kHI];
   int32_t tbl[kTblMax];     // physical blocks of the CTA's tiles (-1: unmapped / out of range)
   uint32_t hist0[2][2048];  // fused selection: counts of each segment's keys' top 11 bits, built during the loop
 };
@@ -92,14 +95,15 @@ struct PickScratch {
   uint32_t digit, rem, above;
 };
 
-template <bool kFp4>
+template <bool kFp4, int kR = 1>
 constexpr uint32_t smem_bytes() {
-  return Plan<kFp4>::kOffMisc + sizeof(Misc) + 1024;
+  return Plan<kFp4, kR>::kOffMisc + sizeof(Misc) + 1024;
 }
 static_assert(sizeof(DealShared) <= kStageBytes, "the deal is built in the idle stage ring");
 static_assert(sizeof(SelectScratch) + sizeof(PickScratch) <= kStageBytes,
               "the selection scratch reuses the drained stage ring");
-static_assert(smem_bytes<false>() <= 227 * 1024 && smem_bytes<true>() <= 227 * 1024, "shared memory");
+static_assert(smem_bytes<false>() <= 227 * 1024 && smem_bytes<true>() <= 227 * 1024 &&
+                  smem_bytes<false, 4>() <= 227 * 1024, "shared memory");
 
 __device__ __forceinline__ bool wait_or_abort(Misc& ms, uint64_t* bar, uint32_t parity, int32_t* err) {
   if (*reinterpret_cast<volatile int32_t*>(&ms.abort)) return false;
@@ -114,6 +118,8 @@ __device__ __forceinline__ bool wait_or_abort(Misc& ms, uint64_t* bar, uint32_t 
 // rest are tiles 0.. of row[1].
 struct Range {
   int nseg, nt_all;
+  int nr, rr[4];
+  int32_t rn[4];  // multi-row CTA: rows sharing the tiles (one sequence) and their visible entries
   int row[2], seq[2];
   int32_t n[2], t0[2], nt[2];  // visible entries of the row, first tile, tile count
   __device__ __forceinline__ int seg_of(int i) const { return i >= nt[0] ? 1 : 0; }
@@ -167,9 +173,9 @@ __device__ __forceinline__ int32_t tile_block(const Misc& ms, const Range& g, in
 
 // bf16: one thread issues each tile as up to four TMA boxes (two blocks x two
 // 64-dim atoms).
-template <bool kFp4>
+template <bool kFp4, int kR>
 __device__ void producer_bf16(const IndexerArgs& a, const Range& g, uint8_t* smem, Misc& ms) {
-  using P = Plan<kFp4>;
+  using P = Plan<kFp4, kR>;
   const uint64_t pol = policy_evict_first();
   for (int i = 0; i < g.nt_all; ++i) {
     const int s = i % P::kStages;
@@ -196,9 +202,9 @@ __device__ void producer_bf16(const IndexerArgs& a, const Range& g, uint8_t* sme
 // e2m1, issuing thread: each tile's codes and scales as four bulk copies into
 // the raw ring (layout per tile: [128 entries][64 code bytes] then
 // [128 entries][8 scale bytes]).
-template <bool kFp4>
+template <bool kFp4, int kR>
 __device__ void producer_raw(const IndexerArgs& a, const Range& g, uint8_t* smem, Misc& ms) {
-  using P = Plan<kFp4>;
+  using P = Plan<kFp4, kR>;
   const uint8_t* codes = reinterpret_cast<const uint8_t*>(a.cache.data);
   const uint8_t* scales = reinterpret_cast<const uint8_t*>(a.cache.scales);
   const uint64_t pol = policy_evict_first();
@@ -227,9 +233,9 @@ __device__ void producer_raw(const IndexerArgs& a, const Range& g, uint8_t* smem
 
 // e2m1, converting warps: raw tile -> bf16 tile of the stage ring.  A code of
 // an unloaded block is stale; its entry's score is not used.
-template <bool kFp4>
+template <bool kFp4, int kR>
 __device__ void converter(const IndexerArgs& a, const Range& g, uint8_t* smem, Misc& ms, int ct) {
-  using P = Plan<kFp4>;
+  using P = Plan<kFp4, kR>;
   for (int i = 0; i < g.nt_all; ++i) {
     const int rs = i % P::kRaw, s = i % P::kStages;
     wait_or_abort(ms, &ms.raw_full[rs], (i / P::kRaw) & 1, a.err);
@@ -259,9 +265,11 @@ __device__ void converter(const IndexerArgs& a, const Range& g, uint8_t* smem, M
 }
 
 // Q_idx^T of `row` into the Q area, by threads [t0, t0 + nthr) of the CTA:
-// bf16, 128B-swizzled K-major, rows = heads; 8 dims per 16-byte piece, each
-// thread's loads (up to four) issued before its stores.
-__device__ __forceinline__ void load_q(const IndexerArgs& a, int row, uint8_t* q_smem, int t, int nthr) {
+// bf16, 128B-swizzled K-major, rows = heads (at N rows n_off.. of an operand
+// of n_all rows); 8 dims per 16-byte piece, each thread's loads (up to four)
+// issued before its stores.
+__device__ __forceinline__ void load_q(const IndexerArgs& a, int row, uint8_t* q_smem, int t, int nthr,
+                                       int n_off = 0, uint32_t n_all = kHI) {
   constexpr int kPieces = kHI * kDI / 8;
   for (int x0 = t; x0 < kPieces; x0 += 4 * nthr) {
     uint32_t w[4][4];
@@ -287,7 +295,8 @@ __device__ __forceinline__ void load_q(const IndexerArgs& a, int row, uint8_t* q
       const int x = x0 + u * nthr;
       if (x >= kPieces) break;
       const int h = x / (kDI / 8), d0 = 8 * (x % (kDI / 8));
-      *reinterpret_cast<uint4*>(q_smem + sw128_offset(h, d0, kHI)) = make_uint4(w[u][0], w[u][1], w[u][2], w[u][3]);
+      *reinterpret_cast<uint4*>(q_smem + sw128_offset(n_off + h, d0, n_all)) =
+          make_uint4(w[u][0], w[u][1], w[u][2], w[u][3]);
     }
   }
 }
@@ -296,14 +305,14 @@ __device__ __forceinline__ void load_q(const IndexerArgs& a, int row, uint8_t* q
 // whole warp waits for the first segment's MMAs to finish reading Q and loads
 // the second row's Q_idx in its place (the producers keep streaming tiles
 // meanwhile).
-template <bool kFp4>
+template <bool kFp4, int kR>
 __device__ void mma_role(const IndexerArgs& a, const Range& g, uint8_t* smem, Misc& ms, uint32_t tmem, int lane) {
-  using P = Plan<kFp4>;
-  constexpr uint32_t idesc = idesc_bf16(128, kHI, 0, 0);
+  using P = Plan<kFp4, kR>;
+  constexpr uint32_t idesc = idesc_bf16(128, kHI * kR, 0, 0);
   const uint32_t stage0 = smem_u32(smem + P::kOffStage), qbase = smem_u32(smem + P::kOffQ);
   for (int i = 0; i < g.nt_all; ++i) {
     const int s = i % P::kStages, b = i & 1;
-    if (g.nseg == 2 && i == g.nt[0]) {
+    if (kR == 1 && g.nseg == 2 && i == g.nt[0]) {
       if (lane == 0) mma_commit(&ms.qswap);
       __syncwarp();
       wait_or_abort(ms, &ms.qswap, 0, a.err);
@@ -319,8 +328,8 @@ __device__ void mma_role(const IndexerArgs& a, const Range& g, uint8_t* smem, Mi
       for (int ks = 0; ks < kDI / 16; ++ks) {
         const uint64_t ad =
             sdesc_sw128(stage0 + s * kStageBytes + (ks >> 2) * kAtomBytes + (ks & 3) * 32, 16, 1024);
-        const uint64_t bd = sdesc_sw128(qbase + (ks >> 2) * (kHI * 128) + (ks & 3) * 32, 16, 1024);
-        mma_bf16(tmem + 64 * b, ad, bd, idesc, ks > 0);
+        const uint64_t bd = sdesc_sw128(qbase + (ks >> 2) * (kR * kHI * 128) + (ks & 3) * 32, 16, 1024);
+        mma_bf16(tmem + kR * kHI * b, ad, bd, idesc, ks > 0);
       }
       mma_commit(&ms.empty[s]);
       mma_commit(&ms.tfull[b]);
@@ -337,16 +346,47 @@ __device__ void mma_role(const IndexerArgs& a, const Range& g, uint8_t* smem, Mi
 
 // Scores of the range: to shared memory as order keys (fused selection) or to
 // the caller's score scratch.  An entry of an unmapped block scores -inf.
-template <bool kFp4>
+template <bool kFp4, int kR>
 __device__ void epilogue_role(const IndexerArgs& a, const Range& g, uint8_t* smem, Misc& ms, uint32_t tmem,
                               int et) {
-  using P = Plan<kFp4>;
+  using P = Plan<kFp4, kR>;
   const uint32_t lane_addr = tmem + ((uint32_t)((et >> 5) * 32) << 16);
   float w[kHI];
 #pragma unroll
   for (int h = 0; h < kHI; ++h) w[h] = ms.w[0][h];
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem + P::kOffKeys);
   float* out = a.scores + (int64_t)g.row[0] * a.max_n;
+  if constexpr (kR > 1) {
+    // every row of the CTA reads the same tile: row j's 64 head dots are TMEM
+    // columns 64 kR b + 64 j of this thread's lane
+    for (int i = 0; i < g.nt_all; ++i) {
+      const int b = i & 1;
+      wait_or_abort(ms, &ms.tfull[b], (i >> 1) & 1, a.err);
+      tc_fence_after();
+      const int32_t e = g.tile_of(i) * kTile + et, jt = 2 * i + et / kRowsPerBlock;
+      const bool mapped = jt < kTblMax && ms.tbl[jt] >= 0;
+      for (int j = 0; j < g.nr; ++j) {
+        float v[kHI];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_ld16(lane_addr + kR * kHI * b + kHI * j + 16 * q, v + 16 * q);
+        tmem_wait_ld();
+        const float4* w4 = reinterpret_cast<const float4*>(ms.w[j]);
+        float s = 0.f;
+#pragma unroll
+        for (int q = 0; q < kHI / 4; ++q) {
+          const float4 ww = w4[q];
+          s = fmaf(ww.x, fmaxf(v[4 * q], 0.f), s);
+          s = fmaf(ww.y, fmaxf(v[4 * q + 1], 0.f), s);
+          s = fmaf(ww.z, fmaxf(v[4 * q + 2], 0.f), s);
+          s = fmaf(ww.w, fmaxf(v[4 * q + 3], 0.f), s);
+        }
+        if (e < g.rn[j]) a.scores[(int64_t)g.rr[j] * a.max_n + e] = mapped ? s : -INFINITY;
+      }
+      tc_fence_before();
+      mbar_arrive(&ms.tempty[b]);
+    }
+    return;
+  }
   int seg = 0;
   for (int i = 0; i < g.nt_all; ++i) {
     const int b = i & 1;
@@ -393,9 +433,9 @@ __device__ void epilogue_role(const IndexerArgs& a, const Range& g, uint8_t* sme
   }
 }
 
-template <bool kFp4>
-__global__ void __launch_bounds__(Plan<kFp4>::kThreads, 1) indexer_tc_kernel(const __grid_constant__ IndexerArgs a) {
-  using P = Plan<kFp4>;
+template <bool kFp4, int kR>
+__global__ void __launch_bounds__(Plan<kFp4, kR>::kThreads, 1) indexer_tc_kernel(const __grid_constant__ IndexerArgs a) {
+  using P = Plan<kFp4, kR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Misc& ms = *reinterpret_cast<Misc*>(smem + P::kOffMisc);
@@ -423,11 +463,30 @@ __global__ void __launch_bounds__(Plan<kFp4>::kThreads, 1) indexer_tc_kernel(con
       }
     }
   } else if (tid == 0) {
-    // one row per blockIdx.x, its tiles split in equal parts over gridDim.y
+    // one row per blockIdx.x, its tiles split in equal parts over gridDim.y.
+    // With kR rows a CTA, blockIdx.x = 4q leads rows 4q..4q+3: it takes every
+    // one of them in the sequence of row 4q (they then share every key tile);
+    // the others exit, unless their own sequence differs, when they take
+    // their row alone.
     const int r = blockIdx.x;
-    const int32_t tiles = deal_row_tiles(a.pos, r, a.ratio, a.window, a.max_n);
+    int nr = 1;
+    ms.rr[0] = r;
+    if constexpr (kR > 1) {
+      const int lead = r & ~(kR - 1);
+      const int lead_seq = a.seq_id[lead];
+      if (r != lead && a.seq_id[r] == lead_seq) {
+        nr = 0;
+      } else if (r == lead) {
+        nr = 0;
+        for (int j = 0; j < kR && lead + j < a.n_rows; ++j)
+          if (a.seq_id[lead + j] == lead_seq) ms.rr[nr++] = lead + j;
+      }
+    }
+    int32_t tiles = 0;
+    for (int j = 0; j < nr; ++j) tiles = max(tiles, deal_row_tiles(a.pos, ms.rr[j], a.ratio, a.window, a.max_n));
     const int32_t per = (tiles + gridDim.y - 1) / gridDim.y;
-    ms.row[0] = r;
+    ms.nr = nr;
+    ms.row[0] = nr ? ms.rr[0] : -1;
     ms.t0[0] = min(tiles, (int32_t)blockIdx.y * per);
     ms.nt[0] = min(tiles, ms.t0[0] + per) - ms.t0[0];
     ms.row[1] = -1;
@@ -462,6 +521,22 @@ __global__ void __launch_bounds__(Plan<kFp4>::kThreads, 1) indexer_tc_kernel(con
     g.seq[1] = -1;
     g.n[1] = 0;
   }
+  g.nr = 0;
+  if constexpr (kR > 1) {
+    // the CTA's rows (one sequence): each row's visible entries; the tiles
+    // cover the longest (g.n[0] is its count)
+    g.nr = ms.nr;
+    g.n[0] = 0;
+    for (int j = 0; j < g.nr; ++j) {
+      g.rr[j] = ms.rr[j];
+      g.rn[j] = n_visible(a.pos[g.rr[j]], a.ratio, a.window);
+      if (g.rn[j] > a.max_n) {
+        if (tid == 0 && blockIdx.y == 0) record_error(a.err, CSA_ERR_DEVICE_BOUNDS);
+        g.rn[j] = a.max_n;
+      }
+      g.n[0] = max(g.n[0], g.rn[j]);
+    }
+  }
 
   if (tid == 0) {
     for (int s = 0; s < 4; ++s) {
@@ -481,7 +556,11 @@ __global__ void __launch_bounds__(Plan<kFp4>::kThreads, 1) indexer_tc_kernel(con
     mbar_init_fence();
     ms.abort = 0;
   }
-  if (tid < g.nseg * kHI) ms.w[tid / kHI][tid % kHI] = a.w[(int64_t)g.row[tid / kHI] * kHI + tid % kHI];
+  if constexpr (kR > 1) {
+    if (tid < g.nr * kHI) ms.w[tid / kHI][tid % kHI] = a.w[(int64_t)g.rr[tid / kHI] * kHI + tid % kHI];
+  } else {
+    if (tid < g.nseg * kHI) ms.w[tid / kHI][tid % kHI] = a.w[(int64_t)g.row[tid / kHI] * kHI + tid % kHI];
+  }
   for (int b = tid; b < 2 * 2048; b += P::kThreads) (&ms.hist0[0][0])[b] = 0;
   {
     // block-table entries of the CTA's tiles, two blocks a tile
@@ -498,8 +577,12 @@ __global__ void __launch_bounds__(Plan<kFp4>::kThreads, 1) indexer_tc_kernel(con
       ms.tbl[j] = pb;
     }
   }
-  if (warp == P::kMmaWarp) tmem_alloc(&ms.tmem_base, kTmemCols);
-  load_q(a, g.row[0], smem + P::kOffQ, tid, P::kThreads);
+  if (warp == P::kMmaWarp) tmem_alloc(&ms.tmem_base, P::kTmemCols);
+  if constexpr (kR > 1) {
+    for (int j = 0; j < g.nr; ++j) load_q(a, g.rr[j], smem + P::kOffQ, tid, P::kThreads, kHI * j, kR * kHI);
+  } else {
+    load_q(a, g.row[0], smem + P::kOffQ, tid, P::kThreads);
+  }
   fence_proxy_async();
   tc_fence_before();
   __syncthreads();
@@ -507,27 +590,27 @@ __global__ void __launch_bounds__(Plan<kFp4>::kThreads, 1) indexer_tc_kernel(con
   const uint32_t tmem = ms.tmem_base;
 
   if (warp < 4) {
-    epilogue_role<kFp4>(a, g, smem, ms, tmem, tid);
+    epilogue_role<kFp4, kR>(a, g, smem, ms, tmem, tid);
   } else if (warp < P::kMmaWarp) {
     if constexpr (!kFp4) {
-      if (tid == kEpi) producer_bf16<kFp4>(a, g, smem, ms);
+      if (tid == kEpi) producer_bf16<kFp4, kR>(a, g, smem, ms);
     } else {
       if (warp == kEpi / 32) {
-        if (tid == kEpi) producer_raw<kFp4>(a, g, smem, ms);
+        if (tid == kEpi) producer_raw<kFp4, kR>(a, g, smem, ms);
       } else {
-        converter<kFp4>(a, g, smem, ms, tid - kEpi - 32);
+        converter<kFp4, kR>(a, g, smem, ms, tid - kEpi - 32);
       }
     }
   } else {
-    mma_role<kFp4>(a, g, smem, ms, tmem, tid & 31);
+    mma_role<kFp4, kR>(a, g, smem, ms, tmem, tid & 31);
   }
   tc_fence_before();
   __syncthreads();
   if (warp == P::kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, P::kTmemCols);
   }
-  if (a.sel_k <= 0) return;
+  if (kR > 1 || a.sel_k <= 0) return;
 
   // fused selection, once per segment.  The list a segment hands to the merge
   // is every key of its range at or above T22, the k-th largest key with its
@@ -680,14 +763,14 @@ bool indexer_tc_eligible(const IndexerArgs& a) {
          ((a.cache.dtype == CSA_BF16 && d % 16 == 0) || (a.cache.dtype == CSA_E2M1 && d % 16 == 0 && s % 16 == 0));
 }
 
-template <bool kFp4>
+template <bool kFp4, int kR>
 static cudaError_t launch_indexer_tc_t(const IndexerArgs& args, int32_t n_rows, int32_t G, cudaStream_t s) {
-  using P = Plan<kFp4>;
+  using P = Plan<kFp4, kR>;
   static PerDevice attrs;
   cudaError_t e = with_device_slot(attrs, [](int, int64_t& done) {
     if (done) return cudaSuccess;
-    const cudaError_t r = cudaFuncSetAttribute(indexer_tc_kernel<kFp4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)smem_bytes<kFp4>());
+    const cudaError_t r = cudaFuncSetAttribute(indexer_tc_kernel<kFp4, kR>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<kFp4, kR>());
     if (r == cudaSuccess) done = 1;
     return r;
   });
@@ -697,8 +780,8 @@ static cudaError_t launch_indexer_tc_t(const IndexerArgs& args, int32_t n_rows, 
   if (!kFp4 && !encode_bf16_map(&a.k_map, a.cache.data, kDI, (uint64_t)a.cache.num_blocks * kRowsPerBlock, kDI * 2,
                                 64, kRowsPerBlock))
     return cudaErrorInvalidValue;
-  if (a.sel_k > 0) return launch_k(indexer_tc_kernel<kFp4>, dim3(G), dim3(P::kThreads), smem_bytes<kFp4>(), s, 0,
-                                   a);
+  if (a.sel_k > 0)
+    return launch_k(indexer_tc_kernel<kFp4, kR>, dim3(G), dim3(P::kThreads), smem_bytes<kFp4, kR>(), s, 0, a);
   const int32_t tiles = (a.max_n + kTile - 1) / kTile;
   // one CTA per SM: as many splits per row as fit in a single wave
   int32_t splits = n_rows > 0 ? G / n_rows : 1;
@@ -708,13 +791,16 @@ static cudaError_t launch_indexer_tc_t(const IndexerArgs& args, int32_t n_rows, 
   const int32_t min_splits = (tiles + tiles_per_cta_max - 1) / tiles_per_cta_max;
   if (splits < min_splits) splits = min_splits;
   if (splits < 1) splits = 1;
-  return launch_k(indexer_tc_kernel<kFp4>, dim3(n_rows, splits), dim3(P::kThreads), smem_bytes<kFp4>(), s, 0,
-                  a);
+  return launch_k(indexer_tc_kernel<kFp4, kR>, dim3(n_rows, splits), dim3(P::kThreads), smem_bytes<kFp4, kR>(), s,
+                  0, a);
 }
 
 cudaError_t launch_indexer_tc(const IndexerArgs& a, int32_t n_rows, int32_t G, cudaStream_t s) {
-  return a.cache.dtype == CSA_E2M1 ? launch_indexer_tc_t<true>(a, n_rows, G, s)
-                                   : launch_indexer_tc_t<false>(a, n_rows, G, s);
+  if (a.cache.dtype == CSA_E2M1) return launch_indexer_tc_t<true, 1>(a, n_rows, G, s);
+  // score-scratch batches of many rows (prefill chunks): four rows of a
+  // sequence share every key tile
+  if (a.sel_k <= 0 && n_rows >= 2 * G) return launch_indexer_tc_t<false, 4>(a, n_rows, G, s);
+  return launch_indexer_tc_t<false, 1>(a, n_rows, G, s);
 }
 
 }  // namespace csa

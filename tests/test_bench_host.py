@@ -86,3 +86,26 @@ def test_cache_replicas_keep_every_field():
     assert c.comp.tail_bf16 == 16 and c.comp.dim == 64 and c.comp.dtype == csa.E4M3R
     assert c.comp.data.data_ptr() != pc.data.data_ptr() and torch.equal(c.comp.data, pc.data)
     assert c.state is None
+
+
+def test_prefill_rows_of_one_sequence_share_their_keys():
+    # four rows of one sequence at consecutive positions read the keys of the
+    # longest once; two rows of other sequences read their own
+    import types
+
+    import numpy as np
+
+    import synth
+    L = synth.workload(4).layers[0]
+    pos = np.array([4000, 4001, 4002, 4003, 9000, 9000], dtype=np.int64)
+    seq = np.array([0, 0, 0, 0, 1, 2], dtype=np.int32)
+    ld = types.SimpleNamespace(L=L, n_rows=6, host={"pos": pos, "seq_id": seq})
+    nv = lambda p: (p - L.window) // L.ratio + 1
+    keys = nv(4003) + 2 * nv(9000)
+    q = 6 * L.idx_heads * (L.idx_dim * 2 + 4)
+    assert bench.indexer_bytes(ld) == keys * L.idx_dim * 2 + q + 6 * L.topk * 4
+    # attention: selections capped by the visible entries, windows as a union
+    att = min(nv(4003), 4 * L.topk) + (4003 - (4000 - L.swa + 1) + 1) + 2 * (L.topk + L.swa)
+    q_out = 6 * L.heads * L.dim * 2 * 2
+    assert bench.attention_bytes(ld) == att * L.dim * 2 + q_out
+    assert bench.attention_flops(ld) == 4.0 * L.heads * L.dim * (4 * (L.topk + L.swa) + 2 * (L.topk + L.swa))
