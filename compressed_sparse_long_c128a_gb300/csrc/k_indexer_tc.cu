@@ -348,7 +348,7 @@ __device__ void mma_role(const IndexerArgs& a, const Range& g, uint8_t* smem, Mi
 // the caller's score scratch.  An entry of an unmapped block scores -inf.
 template <bool kFp4, int kR>
 __device__ void epilogue_role(const IndexerArgs& a, const Range& g, uint8_t* smem, Misc& ms, uint32_t tmem,
-                              int et) {
+                              int et, int j0 = 0, int j1 = 0) {
   using P = Plan<kFp4, kR>;
   const uint32_t lane_addr = tmem + ((uint32_t)((et >> 5) * 32) << 16);
   float w[kHI];
@@ -358,28 +358,31 @@ __device__ void epilogue_role(const IndexerArgs& a, const Range& g, uint8_t* sme
   float* out = a.scores + (int64_t)g.row[0] * a.max_n;
   if constexpr (kR > 1) {
     // every row of the CTA reads the same tile: row j's 64 head dots are TMEM
-    // columns 64 kR b + 64 j of this thread's lane
+    // columns 64 kR b + 64 j of this thread's lane.  This thread takes rows
+    // [j0, j1) of entry et; four partial sums keep the dependent chain short.
+    j1 = min(j1, g.nr);
     for (int i = 0; i < g.nt_all; ++i) {
       const int b = i & 1;
       wait_or_abort(ms, &ms.tfull[b], (i >> 1) & 1, a.err);
       tc_fence_after();
       const int32_t e = g.tile_of(i) * kTile + et, jt = 2 * i + et / kRowsPerBlock;
       const bool mapped = jt < kTblMax && ms.tbl[jt] >= 0;
-      for (int j = 0; j < g.nr; ++j) {
+      for (int j = j0; j < j1; ++j) {
         float v[kHI];
 #pragma unroll
         for (int q = 0; q < 4; ++q) tmem_ld16(lane_addr + kR * kHI * b + kHI * j + 16 * q, v + 16 * q);
         tmem_wait_ld();
         const float4* w4 = reinterpret_cast<const float4*>(ms.w[j]);
-        float s = 0.f;
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int q = 0; q < kHI / 4; ++q) {
           const float4 ww = w4[q];
-          s = fmaf(ww.x, fmaxf(v[4 * q], 0.f), s);
-          s = fmaf(ww.y, fmaxf(v[4 * q + 1], 0.f), s);
-          s = fmaf(ww.z, fmaxf(v[4 * q + 2], 0.f), s);
-          s = fmaf(ww.w, fmaxf(v[4 * q + 3], 0.f), s);
+          s4[0] = fmaf(ww.x, fmaxf(v[4 * q], 0.f), s4[0]);
+          s4[1] = fmaf(ww.y, fmaxf(v[4 * q + 1], 0.f), s4[1]);
+          s4[2] = fmaf(ww.z, fmaxf(v[4 * q + 2], 0.f), s4[2]);
+          s4[3] = fmaf(ww.w, fmaxf(v[4 * q + 3], 0.f), s4[3]);
         }
+        const float s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
         if (e < g.rn[j]) a.scores[(int64_t)g.rr[j] * a.max_n + e] = mapped ? s : -INFINITY;
       }
       tc_fence_before();
@@ -549,7 +552,7 @@ __global__ void __launch_bounds__(Plan<kFp4, kR>::kThreads, 1) indexer_tc_kernel
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&ms.tfull[b], 1);
-      mbar_init(&ms.tempty[b], kEpi);
+      mbar_init(&ms.tempty[b], kR > 1 ? 2 * kEpi : kEpi);
     }
     mbar_init(&ms.mma_done, 1);
     mbar_init(&ms.qswap, 1);
@@ -590,7 +593,11 @@ __global__ void __launch_bounds__(Plan<kFp4, kR>::kThreads, 1) indexer_tc_kernel
   const uint32_t tmem = ms.tmem_base;
 
   if (warp < 4) {
-    epilogue_role<kFp4, kR>(a, g, smem, ms, tmem, tid);
+    epilogue_role<kFp4, kR>(a, g, smem, ms, tmem, tid, 0, kR / 2);
+  } else if (kR > 1 && warp >= 5 && warp < 9) {
+    // multi-row: warps 5-8 (idle producers of the bf16 plan) take the other
+    // half of the rows; warp w reads TMEM lanes 32 (w mod 4) ..
+    epilogue_role<kFp4, kR>(a, g, smem, ms, tmem, 32 * (warp & 3) + (tid & 31), kR / 2, kR);
   } else if (warp < P::kMmaWarp) {
     if constexpr (!kFp4) {
       if (tid == kEpi) producer_bf16<kFp4, kR>(a, g, smem, ms);
