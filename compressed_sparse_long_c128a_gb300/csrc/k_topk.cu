@@ -448,49 +448,54 @@ __global__ void __launch_bounds__(kChunkThreads) topk_chunk_kernel(const TopkArg
   __shared__ SelectScratch sc;
   pdl_trigger();
   pdl_wait();
-  const int r = blockIdx.x, c = blockIdx.y;
+  const int r = blockIdx.x;
   int n = n_visible(a.pos[r], a.ratio, a.window);
   if (n > a.max_n) {
-    if (threadIdx.x == 0 && c == 0) record_error(a.err, CSA_ERR_DEVICE_BOUNDS);
+    if (threadIdx.x == 0 && blockIdx.y == 0) record_error(a.err, CSA_ERR_DEVICE_BOUNDS);
     n = a.max_n;
   }
-  const int lo = c * kChunk;
-  const int len = max(0, min(kChunk, n - lo));
   const bool final_out = n_chunks == 1;
   int32_t* out = a.out + (int64_t)r * a.k;
-  if (final_out)
-    for (int i = min(len, a.k) + threadIdx.x; i < a.k; i += kChunkThreads) out[i] = -1;
-  const int64_t slot = (int64_t)r * n_chunks + c;
-  if (len <= 0) {
-    if (threadIdx.x == 0 && !final_out) cand_cnt[slot] = 0;
-    return;
-  }
-  const float* s = a.scores + (int64_t)r * a.max_n + lo;
-  // all of a thread's loads are issued before any is stored
-  constexpr int kLoads = kChunk / kChunkThreads;
-  float v[kLoads];
+  // CTA (r, y) takes chunks y, y + gridDim.y, ... of row r: a row's chunks past
+  // its visible entries cost no CTA of their own
+  for (int c = blockIdx.y; c < n_chunks; c += gridDim.y) {
+    const int lo = c * kChunk;
+    const int len = max(0, min(kChunk, n - lo));
+    if (final_out)
+      for (int i = min(len, a.k) + threadIdx.x; i < a.k; i += kChunkThreads) out[i] = -1;
+    const int64_t slot = (int64_t)r * n_chunks + c;
+    if (len <= 0) {
+      if (threadIdx.x == 0 && !final_out) cand_cnt[slot] = 0;
+      continue;  // block-uniform
+    }
+    const float* s = a.scores + (int64_t)r * a.max_n + lo;
+    // all of a thread's loads are issued before any is stored
+    constexpr int kLoads = kChunk / kChunkThreads;
+    float v[kLoads];
 #pragma unroll
-  for (int u = 0; u < kLoads; ++u) {
-    const int i = threadIdx.x + u * kChunkThreads;
-    v[u] = i < len ? s[i] : 0.f;
-  }
+    for (int u = 0; u < kLoads; ++u) {
+      const int i = threadIdx.x + u * kChunkThreads;
+      v[u] = i < len ? s[i] : 0.f;
+    }
 #pragma unroll
-  for (int u = 0; u < kLoads; ++u) {
-    const int i = threadIdx.x + u * kChunkThreads;
-    if (i < len) keys[padded(i)] = order_key(v[u]);
+    for (int u = 0; u < kLoads; ++u) {
+      const int i = threadIdx.x + u * kChunkThreads;
+      if (i < len) keys[padded(i)] = order_key(v[u]);
+    }
+    __syncthreads();
+    if (final_out) {
+      block_select<kChunkThreads>(keys, len, a.k, sc, [&](int pos, uint32_t rank) { out[rank] = pos; });
+    } else {
+      uint32_t* ok = cand_key + slot * a.k;
+      int32_t* oi = cand_idx + slot * a.k;
+      block_select<kChunkThreads>(keys, len, a.k, sc, [&](int pos, uint32_t rank) {
+        ok[rank] = keys[padded(pos)];
+        oi[rank] = lo + pos;
+      });
+      if (threadIdx.x == 0) cand_cnt[slot] = min(len, a.k);
+    }
+    __syncthreads();  // the keys are read by the emission before the next chunk overwrites them
   }
-  __syncthreads();
-  if (final_out) {
-    block_select<kChunkThreads>(keys, len, a.k, sc, [&](int pos, uint32_t rank) { out[rank] = pos; });
-    return;
-  }
-  uint32_t* ok = cand_key + slot * a.k;
-  int32_t* oi = cand_idx + slot * a.k;
-  block_select<kChunkThreads>(keys, len, a.k, sc, [&](int pos, uint32_t rank) {
-    ok[rank] = keys[padded(pos)];
-    oi[rank] = lo + pos;
-  });
-  if (threadIdx.x == 0) cand_cnt[slot] = min(len, a.k);
 }
 
 __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(const TopkArgs a, const uint32_t* cand_key,
@@ -572,8 +577,9 @@ cudaError_t launch_topk(const TopkArgs& a, int32_t n_rows, void* cand, cudaStrea
   uint32_t* ck = reinterpret_cast<uint32_t*>(cand);
   int32_t* ci = reinterpret_cast<int32_t*>(ck + (size_t)n_rows * nc * a.k);
   int32_t* cc = ci + (size_t)n_rows * nc * a.k;
-  e = launch_k(topk_chunk_kernel, dim3(n_rows, nc), dim3(kChunkThreads), kChunkSmem, s, 0, a, ck, ci,
-                           cc, nc);
+  // up to four CTAs a row, each looping over its chunks
+  e = launch_k(topk_chunk_kernel, dim3(n_rows, nc < 4 ? nc : 4), dim3(kChunkThreads), kChunkSmem, s, 0, a, ck, ci,
+               cc, nc);
   if (e != cudaSuccess) return e;
   const size_t smem = merge_smem(nc, a.k);
   static PerDevice merge_smem_set;  // the largest dynamic shared memory allowed so far
