@@ -266,15 +266,16 @@ __device__ void converter(const IndexerArgs& a, const Range& g, uint8_t* smem, M
 
 // Q_idx^T of `row` into the Q area, by threads [t0, t0 + nthr) of the CTA:
 // bf16, 128B-swizzled K-major, rows = heads (at N rows n_off.. of an operand
-// of n_all rows); 8 dims per 16-byte piece, each thread's loads (up to four)
-// issued before its stores.
+// of n_all rows); 8 dims per 16-byte piece, each thread's loads (kB at a
+// time) issued before its stores.
+template <int kB>
 __device__ __forceinline__ void load_q(const IndexerArgs& a, int row, uint8_t* q_smem, int t, int nthr,
                                        int n_off = 0, uint32_t n_all = kHI) {
   constexpr int kPieces = kHI * kDI / 8;
-  for (int x0 = t; x0 < kPieces; x0 += 4 * nthr) {
-    uint32_t w[4][4];
+  for (int x0 = t; x0 < kPieces; x0 += kB * nthr) {
+    uint32_t w[kB][4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kB; ++u) {
       const int x = x0 + u * nthr;
       if (x >= kPieces) break;
       const int64_t qb = (int64_t)row * kHI * kDI + 8 * x;
@@ -291,7 +292,7 @@ __device__ __forceinline__ void load_q(const IndexerArgs& a, int row, uint8_t* q
       }
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kB; ++u) {
       const int x = x0 + u * nthr;
       if (x >= kPieces) break;
       const int h = x / (kDI / 8), d0 = 8 * (x % (kDI / 8));
@@ -316,7 +317,7 @@ __device__ void mma_role(const IndexerArgs& a, const Range& g, uint8_t* smem, Mi
       if (lane == 0) mma_commit(&ms.qswap);
       __syncwarp();
       wait_or_abort(ms, &ms.qswap, 0, a.err);
-      load_q(a, g.row[1], smem + P::kOffQ, lane, 32);
+      load_q<kFp4 ? 4 : 8>(a, g.row[1], smem + P::kOffQ, lane, 32);  // L2-warm: prefetched at the start
       fence_proxy_async();
       __syncwarp();
     }
@@ -582,9 +583,16 @@ __global__ void __launch_bounds__(Plan<kFp4, kR>::kThreads, 1) indexer_tc_kernel
   }
   if (warp == P::kMmaWarp) tmem_alloc(&ms.tmem_base, P::kTmemCols);
   if constexpr (kR > 1) {
-    for (int j = 0; j < g.nr; ++j) load_q(a, g.rr[j], smem + P::kOffQ, tid, P::kThreads, kHI * j, kR * kHI);
+    for (int j = 0; j < g.nr; ++j) load_q<4>(a, g.rr[j], smem + P::kOffQ, tid, P::kThreads, kHI * j, kR * kHI);
   } else {
-    load_q(a, g.row[0], smem + P::kOffQ, tid, P::kThreads);
+    load_q<4>(a, g.row[0], smem + P::kOffQ, tid, P::kThreads);
+    // the second row's Q_idx (swapped in by the MMA warp mid-loop) into L2 now
+    if (g.nseg == 2 && tid < kHI * kDI * 2 / 128) {
+      const char* q1 = reinterpret_cast<const char*>(a.q_idx) +
+                       (int64_t)g.row[1] * kHI * kDI * (a.q_dtype == CSA_BF16 ? 2 : 4);
+      for (int o = tid * 128; o < kHI * kDI * (a.q_dtype == CSA_BF16 ? 2 : 4); o += kHI * kDI * 2)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(q1 + o));
+    }
   }
   fence_proxy_async();
   tc_fence_before();
