@@ -271,7 +271,14 @@ def call_roofline(name: str, nbytes: float, flops: float, ms: float, hbm_gbs: fl
 # DRAM bytes (read + write) per launch of a call from an ncu capture, keyed by
 # (workload, call); valid only for the kernel source it was taken on (sha256 of
 # the call's kernel file).
-TRAFFIC = {}
+TRAFFIC = {
+    # ncu --set full --clock-control none, one launch of indexer_tc_kernel on the workload
+    ("c4a_decode_b64_64k", "indexer_topk"): (199313920.0 + 5145344.0, "fe4c3295e7a072e78f961bd38cb71df3da34e45b3ecb7d051c5bbc4ba9797f3c"),
+    # the same for one launch of attn_tc_kernel
+    ("c128a_decode_b32_128k", "attention"): (40029696.0 + 3328.0, "4fdeee2cb2e6e8999e370c0ccbcd24f37fdcc26d1980a1d01873efd6f1f68d19"),
+    # the same for one launch of the e2m1 indexer_tc_kernel
+    ("c4a_decode_b4_1m_fp8", "indexer_topk"): (75728896.0 + 1843968.0, "fe4c3295e7a072e78f961bd38cb71df3da34e45b3ecb7d051c5bbc4ba9797f3c"),
+}
 _CALL_SOURCE = {"attention": "k_attn_tc.cu", "indexer_topk": "k_indexer_tc.cu", "compress_insert": "k_compress.cu"}
 
 
