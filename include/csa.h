@@ -230,9 +230,12 @@ CSA_API int csa_cache_store(const float* rows, int32_t n, const int32_t* seq_id,
  *   idx_cache F32 / BF16 / E2M1, rows_per_block 256/ratio, dim idx_dim
  *   out_idx   [n_rows][k] int32
  *   ws        workspace of at least csa_indexer_topk_workspace_size(n_rows, max_n, k)
- *             bytes, max_n >= every row's n.  Contents are scratch (the rows'
- *             scores, and when max_n > 16384 each 16384-entry chunk's top-k
- *             candidates).
+ *             bytes, max_n >= every row's n.  Contents are scratch: the rows'
+ *             scores and, when max_n > 16384, each 16384-entry chunk's top-k
+ *             candidates; for batches of fewer than 256 rows, the candidate
+ *             lists of the CTAs the rows' tiles are dealt to (two lists of up
+ *             to 2k (key, index) pairs a CTA, with a count and a threshold
+ *             each, and each row's first list).  Nothing needs to start at zero.
  */
 CSA_API int csa_indexer_topk(const void* q_idx, int32_t q_dtype, const float* w, int32_t n_rows,
                      int32_t idx_heads, int32_t idx_dim, const int32_t* seq_id, const int32_t* pos,
