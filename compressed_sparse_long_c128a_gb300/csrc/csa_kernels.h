@@ -157,13 +157,14 @@ struct IndexerArgs {
   // score written to `scores`
   int32_t sel_k;
   int32_t n_rows;
-  uint32_t* cand_key;  // [grid][2 sel_k] order-preserving keys of the scores
-  int32_t* cand_idx;   // [grid][2 sel_k] entry indices
-  int32_t* cand_cnt;   // [grid]
-  uint32_t* cand_thr;
-  int32_t* cand_row_first;
-  int32_t* cand_row_ctas;
-  int32_t* cand_row_seg;  // [grid] every key of the CTA's range at or above it is in its list
+  // two list slots per CTA (2c, 2c + 1: one per row the CTA meets), see DealCandidates
+  uint32_t* cand_key;       // [2 grid][2 sel_k] order-preserving keys of the scores
+  int32_t* cand_idx;        // [2 grid][2 sel_k] entry indices
+  int32_t* cand_cnt;        // [2 grid]
+  uint32_t* cand_thr;       // [2 grid] every key of the slot's range at or above it is in its list
+  int32_t* cand_row_first;  // [rows] the CTA holding the row's first list
+  int32_t* cand_row_ctas;   // [rows] the row's lists
+  int32_t* cand_row_seg;    // [rows] the slot of the row's first list within its CTA
 };
 cudaError_t launch_indexer_scores(const IndexerArgs& a, int32_t n_rows, cudaStream_t s);
 // tensor-core scores, 64 heads x 128 dims, bf16 or e2m1 keys (k_indexer_tc.cu)
