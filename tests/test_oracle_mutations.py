@@ -8,7 +8,8 @@ method is prone to: RoPE sign, pairing, frequency exponent, rotated dims and
 angle precision; softmax axis and bias indexing of the compressor; anchor and
 order of norm and RoPE; RMSNorm epsilon and gain; the attention's inverse
 RoPE, scale and split merge; tie order and visibility of the selection; relu
-and weights of the indexer; the e4m3 and e2m1 codecs; geometry constants.
+and weights of the indexer; the e4m3, e2m1 and bf16 codecs; the partial fp8
+row scale; the query norm's extent; geometry constants.
 """
 
 import numpy as np
@@ -130,7 +131,36 @@ def _round_e4m3_truncate(x):
     return np.where(x < 0, -r, r)
 
 
+def _query_norm_joint(q, gamma_q, eps):
+    """One RMS over all heads of a row instead of one per head."""
+    q = np.asarray(q, np.float64)
+    ms = np.mean(q * q, axis=(-2, -1), keepdims=True)
+    return q / np.sqrt(ms + eps) * np.asarray(gamma_q, np.float64)
+
+
+def _partial_fp8_scale_all_dims(x, rope_dim):
+    """The row scale taken over every dim, rotary ones included."""
+    x = np.asarray(x, dtype=np.float32)
+    d = x.shape[-1]
+    am = np.abs(x).max(axis=-1)
+    inv = np.where(am > 0, 448.0 / np.where(am > 0, am, 1.0), 0.0).astype(np.float32)
+    codes = O.e4m3_encode(x[..., : d - rope_dim] * inv[..., None])
+    return codes, (am / 448.0).astype(np.float32), O.round_bf16(x[..., d - rope_dim:])
+
+
+def _round_bf16_truncate(x):
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, ex = np.frexp(a)
+    step = np.ldexp(1.0, np.maximum(ex, -125) - 8)
+    r = np.floor(a / step) * step
+    return np.where(x < 0, -r, r)
+
+
 MUTATIONS = {
+    "query_norm_over_all_heads": {"query_norm": _query_norm_joint},
+    "partial_fp8_scale_over_all_dims": {"quantize_rows_e4m3_rope_bf16": _partial_fp8_scale_all_dims},
+    "bf16_truncating_round": {"round_bf16": _round_bf16_truncate},
     "rope_sign": {"rope": lambda x, pos, r, th, inverse=False: _rope(x, pos, r, th, not inverse)},
     "rope_pairing_rotate_half": {"rope": _rope_half},
     "rope_frequency_exponent": {"rope_inv_freq": lambda r, th: np.power(float(th), -np.arange(r // 2) / r)},
