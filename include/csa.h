@@ -167,7 +167,8 @@ CSA_API int csa_compress_insert(const csa_layer* layer, const void* kv, const vo
  * RoPE + K insert, one kernel with warps statically given to query heads or to
  * the key): per token j and head h,
  *   q_out[j][h] := RMSNorm(q[j][h]; gamma_q)   (over the D dims of the head)
- * RoPE of the query is not applied here: csa_sparse_attention rotates it.
+ * RoPE of the query is not applied here: csa_sparse_attn_decode / _prefill
+ * rotate it.
  *   q      [n_tok][heads][D] q_dtype (F32 or BF16), 16-byte aligned
  *   gamma  [D] float, 16-byte aligned
  *   q_out  [n_tok][heads][D] out_dtype (F32 or BF16), 16-byte aligned; may equal q
@@ -188,8 +189,10 @@ typedef struct {
  * the same tokens fused into its launch ([部署] §3.2 third fusion; [Support]
  * "GPU Compute Saturation", kernel fusions).  The caches are written exactly as
  * csa_compress_insert writes them; qn (required) describes the query rows,
- * one per token.  Extra errors: CSA_ERR_UNSUPPORTED when D % 8, D > 512 or an
- * alignment rule of csa_query_norm is not met.
+ * one per token.  Extra errors: CSA_ERR_INVALID_ARG when qn, or one of its
+ * pointers, is null or heads is outside 1..1024; CSA_ERR_UNSUPPORTED for a
+ * dtype other than F32 / BF16, D % 8, D > 512 or a pointer not 16-byte
+ * aligned.  With n_tok == 0 the call is a no-op: only qn != NULL is checked.
  */
 CSA_API int csa_compress_insert_qnorm(const csa_layer* layer, const void* kv, const void* gate,
                                       int32_t in_dtype, int32_t n_tok, const int32_t* seq_id,

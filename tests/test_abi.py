@@ -133,6 +133,46 @@ def test_indexer_key_compressor_validation(lib):
                                 ctypes.byref(B), None, None)
     assert r == csa.OK
 
+def test_query_norm_validation(lib):
+    """csa_compress_insert_qnorm: the checks of the query rows that stop a call
+    before any launch (null or out-of-range fields, dtypes, D and alignment)."""
+    L = csa.make_layer(4, 8, 512, 64, 64)
+    P, B = _paged(), _bt()
+    st, sw = _paged(csa.BF16, 256, 1024), _paged(csa.BF16, 256, 512)
+
+    def call(qn, layer=L, state=st, swa=sw, comp=P, n_tok=4):
+        return lib.csa_compress_insert_qnorm(ctypes.byref(layer), 0x10, 0x10, csa.BF16, n_tok, 0x10, 0x10,
+                                             0x10, 0x10, 0x10, ctypes.byref(state), ctypes.byref(B),
+                                             ctypes.byref(swa), ctypes.byref(B), ctypes.byref(comp),
+                                             ctypes.byref(B), qn, 0x10, None)
+
+    def qn(q=0x1000, q_dtype=csa.BF16, heads=64, gamma=0x2000, q_out=0x3000, out_dtype=csa.BF16):
+        return ctypes.byref(csa.QueryNormC(q, q_dtype, heads, gamma, q_out, out_dtype))
+
+    assert call(None) == csa.ERR_INVALID_ARG                      # qn is required
+    assert call(None, n_tok=0) == csa.ERR_INVALID_ARG             # even for no tokens
+    assert call(qn(q=None)) == csa.ERR_INVALID_ARG
+    assert call(qn(gamma=None)) == csa.ERR_INVALID_ARG
+    assert call(qn(q_out=None)) == csa.ERR_INVALID_ARG
+    assert call(qn(heads=0)) == csa.ERR_INVALID_ARG
+    assert call(qn(heads=1025)) == csa.ERR_INVALID_ARG
+    assert call(qn(q_dtype=csa.E4M3)) == csa.ERR_UNSUPPORTED
+    assert call(qn(out_dtype=csa.E2M1)) == csa.ERR_UNSUPPORTED
+    for field in ("q", "gamma", "q_out"):                          # 16-byte alignment
+        assert call(qn(**{field: 0x1008})) == csa.ERR_UNSUPPORTED
+    # D above 512, and D not a multiple of 8
+    L1k = csa.make_layer(4, 8, 1024, 64, 64)
+    r = call(qn(), layer=L1k, state=_paged(csa.BF16, 256, 2048), swa=_paged(csa.BF16, 256, 1024),
+             comp=_paged(csa.BF16, 64, 1024))
+    assert r == csa.ERR_UNSUPPORTED
+    L20 = csa.make_layer(4, 8, 20, 8, 8)
+    r = call(qn(), layer=L20, state=_paged(csa.BF16, 256, 40), swa=_paged(csa.BF16, 256, 20),
+             comp=_paged(csa.BF16, 64, 20))
+    assert r == csa.ERR_UNSUPPORTED
+    # no tokens: a no-op once qn is given, whatever it holds
+    assert call(qn(heads=0), n_tok=0) == csa.OK
+
+
 def test_workspace_checks(lib):
     L = csa.make_layer(4, 8, 512, 64, 64)
     need = csa.indexer_topk_workspace_size(4, 262143, 512)
