@@ -173,6 +173,101 @@ def test_query_norm_validation(lib):
     assert call(qn(heads=0), n_tok=0) == csa.OK
 
 
+def test_cache_store_validation(lib):
+    """csa_cache_store: checks of the count, the pointers, the cache's dtype,
+    dims and scales, and the block table, answered before any launch."""
+    B = _bt()
+
+    def call(cache, n=4, rows=0x10, bt=B):
+        return lib.csa_cache_store(rows, n, 0x10, 0x10, ctypes.byref(cache) if cache else None,
+                                   ctypes.byref(bt) if bt else None, 0x10, None)
+
+    assert call(_paged(), n=-1) == csa.ERR_INVALID_ARG
+    assert lib.csa_cache_store(None, 0, None, None, None, None, None, None) == csa.OK   # no rows: a no-op
+    assert call(_paged(), rows=None) == csa.ERR_INVALID_ARG
+    assert call(None) == csa.ERR_INVALID_ARG
+    assert call(_paged(), bt=None) == csa.ERR_INVALID_ARG
+    assert call(_paged(), bt=csa.BlockTableC(0x3000, 0, 4)) == csa.ERR_INVALID_ARG     # no sequences
+    assert call(csa.Paged(0x1000, 0x2000, 7, 10, 64, 512)) == csa.ERR_INVALID_ARG       # no such dtype
+    assert call(csa.Paged(0x1000, 0x2000, csa.BF16, 0, 64, 512)) == csa.ERR_INVALID_ARG  # no blocks
+    assert call(csa.Paged(0x1000, 0x2000, csa.BF16, 10, 64, 511)) == csa.ERR_INVALID_ARG  # odd dim
+    # quantised rows need their scales; e2m1 groups of 16
+    assert call(csa.Paged(0x1000, None, csa.E4M3, 10, 64, 512)) == csa.ERR_INVALID_ARG
+    assert call(csa.Paged(0x1000, None, csa.E2M1, 10, 64, 128)) == csa.ERR_INVALID_ARG
+    assert call(_paged(csa.E2M1, 64, 120)) == csa.ERR_INVALID_ARG
+    # the partial fp8 tail: required, a multiple of 16, no larger than the row;
+    # every other dtype has none
+    for tail in (0, 8, 520):
+        assert call(csa.Paged(0x1000, 0x2000, csa.E4M3R, 10, 64, 512, tail)) == csa.ERR_INVALID_ARG
+    assert call(csa.Paged(0x1000, 0x2000, csa.BF16, 10, 64, 512, 64)) == csa.ERR_INVALID_ARG
+
+
+def test_sparse_attention_validation(lib):
+    """csa_sparse_attn_prefill (the decode entry shares its checks): layer,
+    counts, dtypes of query, output and caches, cache geometry and the shapes
+    the kernels take, all answered before any launch."""
+    L = csa.make_layer(4, 8, 512, 64, 64)
+    B = _bt()
+    C, S = _paged(csa.BF16, 64, 512), _paged(csa.BF16, 256, 512)
+
+    def call(layer=L, n_rows=4, q_dtype=csa.BF16, comp=C, swa=S, topk=0x10, k=512, max_n=1000,
+             out_dtype=csa.BF16, out_scales=None, q=0x10):
+        return lib.csa_sparse_attn_prefill(ctypes.byref(layer), q, q_dtype, n_rows, 0x10, 0x10,
+                                           ctypes.byref(comp), ctypes.byref(B), topk, k, max_n,
+                                           ctypes.byref(swa), ctypes.byref(B), 0x10, out_dtype, out_scales,
+                                           0x10, 1 << 40, 0x10, None)
+
+    assert call(n_rows=0) == csa.OK
+    assert call(n_rows=-1) == csa.ERR_INVALID_ARG
+    assert call(max_n=-1) == csa.ERR_INVALID_ARG
+    assert call(k=0) == csa.ERR_INVALID_ARG                      # a selection needs k >= 1
+    assert call(q=None) == csa.ERR_INVALID_ARG
+    assert call(layer=csa.make_layer(4, 0, 512, 64, 64)) == csa.ERR_INVALID_ARG
+    assert call(q_dtype=csa.E4M3) == csa.ERR_UNSUPPORTED
+    assert call(out_dtype=csa.E2M1) == csa.ERR_UNSUPPORTED
+    assert call(out_dtype=csa.E4M3) == csa.ERR_INVALID_ARG      # e4m3 output without its scales
+    assert call(comp=_paged(csa.E2M1, 64, 512)) == csa.ERR_UNSUPPORTED   # attention reads no e2m1
+    assert call(comp=_paged(csa.BF16, 32, 512)) == csa.ERR_INVALID_ARG   # 256 / ratio rows a block
+    assert call(swa=_paged(csa.BF16, 64, 512)) == csa.ERR_INVALID_ARG    # 256 window rows a block
+    # the kernels take D a multiple of 32 up to 512 and heads a multiple of 8
+    L48 = csa.make_layer(4, 8, 48, 16, 64)
+    assert call(layer=L48, comp=_paged(csa.BF16, 64, 48), swa=_paged(csa.BF16, 256, 48)) == csa.ERR_UNSUPPORTED
+    L1k = csa.make_layer(4, 8, 1024, 64, 64)
+    assert call(layer=L1k, comp=_paged(csa.BF16, 64, 1024), swa=_paged(csa.BF16, 256, 1024)) == csa.ERR_UNSUPPORTED
+    assert call(layer=csa.make_layer(4, 8, 512, 64, 12)) == csa.ERR_UNSUPPORTED
+
+
+def test_indexer_validation_and_noalloc_refusal(lib):
+    """csa_indexer_topk and csa_indexer_topk_noalloc share their argument
+    checks; the allocation-free entry refuses a request larger than its fixed
+    scratch before it looks the scratch up."""
+    B = _bt()
+    idx = _paged(csa.BF16, 64, 128)
+
+    def call(fn, n_rows=4, q_dtype=csa.BF16, heads=64, dim=128, ratio=4, cache=idx, k=512, max_n=1000,
+             q=0x10):
+        args = [q, q_dtype, 0x10, n_rows, heads, dim, 0x10, 0x10, ratio, 8, ctypes.byref(cache),
+                ctypes.byref(B), k, max_n, 0x10]
+        if fn == "ws":
+            return lib.csa_indexer_topk(*args, 0x10, 1 << 40, 0x10, None)
+        return lib.csa_indexer_topk_noalloc(*args, 0x10, None)
+
+    for fn in ("ws", "noalloc"):
+        assert call(fn, n_rows=0) == csa.OK
+        assert call(fn, n_rows=-1) == csa.ERR_INVALID_ARG
+        assert call(fn, k=0) == csa.ERR_INVALID_ARG
+        assert call(fn, max_n=-1) == csa.ERR_INVALID_ARG
+        assert call(fn, ratio=3) == csa.ERR_INVALID_ARG          # the stride divides 256
+        assert call(fn, q=None) == csa.ERR_INVALID_ARG
+        assert call(fn, q_dtype=csa.E2M1) == csa.ERR_UNSUPPORTED
+        assert call(fn, cache=_paged(csa.E4M3, 64, 128)) == csa.ERR_UNSUPPORTED   # keys: f32, bf16, e2m1
+        assert call(fn, cache=_paged(csa.BF16, 32, 128)) == csa.ERR_INVALID_ARG
+        assert call(fn, dim=512, cache=_paged(csa.BF16, 64, 512)) == csa.ERR_UNSUPPORTED  # dim <= 256
+        assert call(fn, heads=512) == csa.ERR_UNSUPPORTED     # heads x dim <= 32768
+    # 64 rows of 2^20 scores are 256 MiB, far beyond the fixed 16 MiB scratch
+    assert call("noalloc", n_rows=64, max_n=1 << 20) == csa.ERR_WORKSPACE
+
+
 def test_workspace_checks(lib):
     L = csa.make_layer(4, 8, 512, 64, 64)
     need = csa.indexer_topk_workspace_size(4, 262143, 512)
